@@ -1,0 +1,166 @@
+"""Seeded synthetic payload generators for packed quantized weights.
+
+This module only draws random field values and lays them out as bytes; it
+contains none of the decode arithmetic.  It is shared by the tests (which
+feed the same bytes to the CPU oracle and the CUDA library) and by the
+benchmark.  Every generator is a pure function of (shape, seed).
+
+Field distributions follow the benchmark workloads:
+  * gguf:q8_0  -- per block one binary16 scale drawn log-uniform in
+    [1e-3, 1e-1], 32 signed bytes uniform in [-127, 127];
+  * gguf:q4_0, q4_g64_fp16, gguf:iq4_nl -- binary16 scales |N(0,0.02)|+1e-4,
+    code bytes uniform (every nibble value 0..15 equally likely);
+  * gguf:q4_k, gguf:q6_k -- binary16 d/dmin |N(0,0.01)|, every other byte
+    (packed 6-bit sub-scales and minima, signed 8-bit sub-scales, quant
+    nibbles and 2-bit planes) uniform;
+  * gguf:mxfp4 -- exponent byte uniform in [118, 130], code bytes uniform;
+  * nvfp4 -- E4M3FN scale bytes uniform over 0x00..0x7e (every valid
+    nonnegative finite word), code bytes uniform, one FP32 divisor
+    d_w = binary32(2688 / binary32(amax)) with amax = 0.1 (448*6/amax);
+  * gguf:nvfp4 -- scale bytes uniform over 0x00..0x7e, codes uniform;
+  * "bytes" -- every byte uniform over 0..255 (exercises special scales:
+    binary16 infinities/NaNs, E4M3FN NaN words, E8M0 extremes).
+
+Blocks are row-contiguous along the last dimension (row-major shapes).
+"""
+from __future__ import annotations
+
+import hashlib
+from dataclasses import dataclass
+
+import numpy as np
+
+# (B, S) of the formats generated here.  Geometry only; no decode rules.
+GEOMETRY = {
+    "gguf:q8_0": (32, 34), "q8_g32_fp16": (32, 34), "gguf:q4_0": (32, 18),
+    "gguf:iq4_nl": (32, 18), "q4_g64_fp16": (64, 34), "gguf:q4_k": (256, 144),
+    "gguf:q6_k": (256, 210), "gguf:mxfp4": (32, 17), "gguf:nvfp4": (64, 36),
+    "nvfp4": (64, 36),
+}
+
+NVFP4_AMAX = 0.1
+
+
+def _nblocks(fmt: str, shape) -> int:
+    B, _ = GEOMETRY[fmt]
+    n = 1
+    for s in shape[:-1]:
+        n *= int(s)
+    K = int(shape[-1])
+    if K % B:
+        raise ValueError(f"{fmt}: last dim {K} not a multiple of {B}")
+    return n * (K // B)
+
+
+def _u8(rng, shape) -> np.ndarray:
+    return rng.integers(0, 256, size=shape, dtype=np.uint8)
+
+
+def _f16_bytes(values: np.ndarray) -> np.ndarray:
+    """binary16 (numpy RNE conversion) as little-endian byte pairs, shape [n, 2]."""
+    return values.astype(np.float16).astype("<f2").view(np.uint8).reshape(-1, 2)
+
+
+def nvfp4_divisor(amax: float = NVFP4_AMAX) -> np.float32:
+    """The global FP32 divisor of the workload: binary32(448*6 / binary32(amax))."""
+    return np.float32(np.float32(2688.0) / np.float32(amax))
+
+
+def nvfp4_divisors(ndiv: int, seed: int) -> np.ndarray:
+    """`ndiv` FP32 divisors: the workload's d_w first, then 2688/U(0.01, 1)."""
+    rng = np.random.default_rng(seed + 7919)
+    extra = np.float32(2688.0) / rng.uniform(0.01, 1.0, size=max(0, ndiv - 1)).astype(np.float32)
+    return np.concatenate([np.array([nvfp4_divisor()], np.float32), extra.astype(np.float32)])
+
+
+def payload(fmt: str, shape, seed: int, dist: str = "workload", ndiv: int = 1) -> np.ndarray:
+    """Packed payload bytes (uint8, flat) for `fmt` with logical `shape`.
+
+    dist="workload" uses the benchmark field distributions above;
+    dist="bytes" draws every byte uniformly (including scale fields).
+    For nvfp4, `ndiv` FP32 divisors follow the blocks (none when empty).
+    """
+    rng = np.random.default_rng(seed)
+    nb = _nblocks(fmt, shape)
+    B, S = GEOMETRY[fmt]
+    blk = _u8(rng, (nb, S))
+    if dist == "bytes":
+        out = blk.reshape(-1)
+        if fmt == "nvfp4" and nb:
+            out = np.concatenate([out, nvfp4_divisors(ndiv, seed).astype("<f4").view(np.uint8)])
+        return out
+    if dist != "workload":
+        raise ValueError(dist)
+    if fmt in ("gguf:q8_0", "q8_g32_fp16"):
+        d = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), size=nb))
+        blk[:, 0:2] = _f16_bytes(d)
+        blk[:, 2:34] = rng.integers(-127, 128, size=(nb, 32), dtype=np.int8).view(np.uint8)
+    elif fmt in ("gguf:q4_0", "gguf:iq4_nl", "q4_g64_fp16"):
+        d = np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4
+        blk[:, 0:2] = _f16_bytes(d)
+    elif fmt == "gguf:q4_k":
+        d = np.abs(rng.normal(0.0, 0.01, size=(nb, 2)))
+        blk[:, 0:4] = _f16_bytes(d.reshape(-1)).reshape(nb, 4)
+    elif fmt == "gguf:q6_k":
+        d = np.abs(rng.normal(0.0, 0.01, size=nb))
+        blk[:, 208:210] = _f16_bytes(d)
+    elif fmt == "gguf:mxfp4":
+        blk[:, 0] = rng.integers(118, 131, size=nb, dtype=np.uint8)
+    elif fmt in ("gguf:nvfp4", "nvfp4"):
+        blk[:, 0:4] = rng.integers(0, 0x7F, size=(nb, 4), dtype=np.uint8)
+    else:
+        raise ValueError(fmt)
+    out = blk.reshape(-1)
+    if fmt == "nvfp4" and nb:
+        out = np.concatenate([out, nvfp4_divisors(ndiv, seed).astype("<f4").view(np.uint8)])
+    return out
+
+
+def sha256(a: np.ndarray) -> str:
+    return hashlib.sha256(np.ascontiguousarray(a).view(np.uint8).data).hexdigest()
+
+
+# --------------------------------------------------------------------------
+# Benchmark workloads.
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class TensorSpec:
+    name: str
+    fmt: str
+    shape: tuple
+    seed: int
+    out_dtype: str
+
+
+def llama3_8b_tensors() -> list[TensorSpec]:
+    """Whole-model decode: Llama-3-8B-shaped weights.
+
+    32 layers of attention q/o [4096,4096] and k/v [1024,4096] in gguf:q4_k,
+    FFN gate/up [14336,4096] and down [4096,14336] in gguf:q6_k, and one
+    embedding [128256,4096] in gguf:q8_0; 225 tensors, all decoded to bf16.
+    Tensor i uses seed 1000 + i.
+    """
+    specs = []
+    i = 0
+    for layer in range(32):
+        for nm, shp in (("q", (4096, 4096)), ("k", (1024, 4096)), ("v", (1024, 4096)), ("o", (4096, 4096))):
+            specs.append(TensorSpec(f"layers.{layer}.attn.{nm}", "gguf:q4_k", shp, 1000 + i, "bfloat16"))
+            i += 1
+        for nm, shp in (("gate", (14336, 4096)), ("up", (14336, 4096)), ("down", (4096, 14336))):
+            specs.append(TensorSpec(f"layers.{layer}.ffn.{nm}", "gguf:q6_k", shp, 1000 + i, "bfloat16"))
+            i += 1
+    specs.append(TensorSpec("embed", "gguf:q8_0", (128256, 4096), 1000 + i, "bfloat16"))
+    return specs
+
+
+# Single-format workloads: (label, format, shape, seed, output dtype).
+WORKLOADS = [
+    ("q8_0[256,4096]->f32", "gguf:q8_0", (256, 4096), 0, "float32"),
+    ("q4_0[4096,4096]->bf16", "gguf:q4_0", (4096, 4096), 1, "bfloat16"),
+    ("q4_g64_fp16[4096,4096]->bf16", "q4_g64_fp16", (4096, 4096), 2, "bfloat16"),
+    ("q4_k[14336,4096]->f16", "gguf:q4_k", (14336, 4096), 3, "float16"),
+    ("q6_k[14336,4096]->f16", "gguf:q6_k", (14336, 4096), 4, "float16"),
+    ("nvfp4[8192,28672]->bf16", "nvfp4", (8192, 28672), 5, "bfloat16"),
+    ("mxfp4[8192,28672]->bf16", "gguf:mxfp4", (8192, 28672), 6, "bfloat16"),
+    ("iq4_nl[8192,28672]->bf16", "gguf:iq4_nl", (8192, 28672), 7, "bfloat16"),
+]
