@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Decode-throughput benchmark of the GB300 packed quantized-weight decoder.
+
+One step = one batched launch decoding a whole Llama-3-8B-shaped model
+(225 tensors: attention q/k/v/o in gguf:q4_k, FFN gate/up/down in gguf:q6_k,
+the [128256,4096] embedding in gguf:q8_0) from HBM-resident payloads into
+bf16, i.e. every row of the decode path: validation, block staging, scale
+decode, code unpack, FP32 arithmetic, RNE cast and the batched launcher.
+
+Printed (rank 0, one JSON line on stdout):
+  value         dequant GB/s = (payload bytes + output bytes) / step time,
+                whole job (all ranks), inputs resident in HBM;
+  e2e           the same metric through the public API with host buffers:
+                each step copies the payloads host->device from pinned memory,
+                decodes, and copies the decoded bf16 weights device->host;
+  roofline      the decode kernel against the measured HBM copy bandwidth;
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload;
+  per_workload  the single-format workloads (q8_0, q4_0, q4_g64, q4_k, q6_k,
+                nvfp4, mxfp4, iq4_nl), each timed with an L2 flush between
+                repetitions.
+
+`--impl reference` times the CPU oracle (the parity reference) on the host
+cores instead, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD_NAME = ("whole-model batched decode: Llama-3-8B-shaped weights, 225 tensors "
+                 "(q/k/v/o gguf:q4_k, gate/up/down gguf:q6_k, embedding [128256,4096] gguf:q8_0) -> bf16, "
+                 "one launch per step")
+METRIC = "dequant GB/s (bytes in+out) and elements/s per format vs 8 TB/s HBM peak"
+ALIGN = 256
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-workloads", action="store_true", help="skip the single-format workload table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-fraction", type=int, default=1,
+                    help="CPU baseline decodes 1/N of every tensor's blocks")
+    return ap.parse_args()
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# workload layout
+# --------------------------------------------------------------------------
+class ModelWorkload:
+    def __init__(self, specs):
+        self.specs = specs
+        self.x_off, self.y_off, self.x_len, self.nel = [], [], [], []
+        xo = yo = 0
+        for s in specs:
+            B, S = synth.GEOMETRY[s.fmt]
+            nb = synth._nblocks(s.fmt, s.shape)
+            n = int(np.prod(s.shape))
+            self.x_off.append(xo)
+            self.y_off.append(yo)
+            self.x_len.append(nb * S)
+            self.nel.append(n)
+            xo += (nb * S + ALIGN - 1) // ALIGN * ALIGN
+            yo += (n * 2 + ALIGN - 1) // ALIGN * ALIGN
+        self.x_total, self.y_total = xo, yo
+        self.bytes_in = sum(self.x_len)
+        self.bytes_out = 2 * sum(self.nel)
+        self.elements = sum(self.nel)
+
+    def fill_host(self, x_host_np):
+        t0 = time.time()
+        for i, s in enumerate(self.specs):
+            x_host_np[self.x_off[i]:self.x_off[i] + self.x_len[i]] = synth.payload(s.fmt, s.shape, s.seed)
+        return time.time() - t0
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [c.strip() for c in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline
+# --------------------------------------------------------------------------
+def cpu_oracle_sample(work: ModelWorkload, x_host_np, fraction: int, cores: int):
+    """Decode the first 1/fraction of every tensor's blocks with the oracle,
+    one piece per thread (the oracle itself is single-threaded C; ctypes
+    releases the GIL).  Returns (seconds, bytes in+out, elements)."""
+    import oracle
+
+    oracle.build()
+    pieces = []
+    for i, s in enumerate(work.specs):
+        B, S = synth.GEOMETRY[s.fmt]
+        nb = work.x_len[i] // S
+        take = max(1, nb // fraction)
+        x = x_host_np[work.x_off[i]:work.x_off[i] + work.x_len[i]]
+        step = max(1, take // 4)
+        for b0 in range(0, take, step):
+            pieces.append((s.fmt, s.shape, x, b0, min(take, b0 + step), B, S))
+    nbytes = sum((b1 - b0) * (S + 2 * B) for (_, _, _, b0, b1, B, S) in pieces)
+    nel = sum((b1 - b0) * B for (_, _, _, b0, b1, B, S) in pieces)
+
+    def run(p):
+        fmt, shape, x, b0, b1, B, S = p
+        oracle.decode_range(fmt, shape, x, b0, b1, "bfloat16")
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(cores) as ex:
+        list(ex.map(run, pieces))
+    return time.perf_counter() - t0, nbytes, nel
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def kernel_source_sha() -> str:
+    p = os.path.join(ROOT, "quantized_weight_block_gb300", "csrc", "ndq_kernels.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+
+
+def profiled_traffic(profile_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_src_sha256") == kernel_source_sha():
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def time_single_workloads(torch, ndq, stream, peak):
+    """Single-format workloads, L2 flushed before every repetition."""
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}
+    for label, fmt, shape, seed, od in synth.WORKLOADS:
+        x_np = synth.payload(fmt, shape, seed)
+        x = torch.from_numpy(x_np).cuda()
+        y = torch.empty(shape, dtype=tdt[od], device="cuda")
+        for _ in range(3):
+            ndq.dequantize_packed(fmt, shape, x, tdt[od], y=y)
+        times = []
+        for _ in range(20):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ndq.dequantize_packed(fmt, shape, x, tdt[od], y=y)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        nbytes = x_np.size + y.numel() * y.element_size()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[label] = {"ms": round(ms, 5), "ms_best": round(min(times), 5), "GB/s": round(gbs, 1),
+                      "elements/s": float(f"{y.numel() / (ms * 1e-3):.4g}"),
+                      "frac_of_8TBs": round(gbs / 8000.0, 4), "frac_of_measured": round(gbs / peak, 4),
+                      "bytes": nbytes, "l2": "flushed (512 MB write) before each repetition"}
+        del x, y
+    del flush
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import quantized_weight_block_gb300 as ndq
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    peak, peak_src = measured_peaks()
+    work = ModelWorkload(synth.llama3_8b_tensors())
+
+    # host payloads (pinned, for the end-to-end leg and the CPU baseline)
+    x_host = torch.empty(work.x_total, dtype=torch.uint8, pin_memory=True)
+    gen_s = work.fill_host(x_host.numpy())
+    log(f"[bench] generated {work.bytes_in / 1e9:.2f} GB of payloads in {gen_s:.1f}s")
+
+    x_dev = torch.empty(work.x_total, dtype=torch.uint8, device="cuda")
+    y_dev = torch.empty(work.y_total // 2, dtype=torch.bfloat16, device="cuda")
+    x_dev.copy_(x_host)
+    items = []
+    for i, s in enumerate(work.specs):
+        xv = x_dev[work.x_off[i]:work.x_off[i] + work.x_len[i]]
+        yv = y_dev[work.y_off[i] // 2:work.y_off[i] // 2 + work.nel[i]].view(s.shape)
+        items.append(ndq.make_desc(s.fmt, s.shape, xv, yv))
+    descs = (ndq.ndq_tensor_desc * len(items))(*items)
+    ws_bytes = ndq.ndq_batched_workspace_bytes(len(items))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    lib = ndq._lib
+
+    def step():
+        rc = lib.ndq_dequantize_packed_batched(descs, len(items), ws.data_ptr(), ws_bytes, sh)
+        if rc:
+            raise ndq.NdqError(rc)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(local_rank)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(("GPU-" + str(uuid)) if uuid else None)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    step_bytes = work.bytes_in + work.bytes_out
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    if ndq.get_device_fault():
+        raise RuntimeError("device fault word set during the timed region")
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        y_host = torch.empty(work.y_total // 2, dtype=torch.bfloat16, pin_memory=True)
+        e_steps = max(1, args.e2e_steps)
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            step()
+            y_host.copy_(y_dev, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms = a.elapsed_time(b) / e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda", dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 3), "steps": e_steps,
+               "h2d_bytes_per_step": work.x_total, "d2h_bytes_per_step": work.y_total,
+               "path": "pinned host payloads -> H2D copy -> ndq_dequantize_packed_batched -> D2H copy "
+                       "of the bf16 weights, one stream"}
+        del y_host
+
+    per_workload = None
+    if not args.no_workloads and rank == 0:
+        per_workload = time_single_workloads(torch, ndq, stream, peak)
+
+    cpu = None
+    if not args.no_cpu and rank == 0:
+        cores = os.cpu_count() or 1
+        secs, nbytes, nel = cpu_oracle_sample(work, x_host.numpy(), args.cpu_fraction, cores)
+        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "elements/s": float(f"{nel / secs:.4g}"), "seconds": round(secs, 2),
+               "sample": f"first 1/{args.cpu_fraction} of every tensor's blocks of the same whole-model "
+                         f"payloads ({nel} elements, {nbytes / 1e9:.3f} GB in+out), decoded to bf16, "
+                         f"{cores} threads over disjoint block ranges"}
+
+    traffic = profiled_traffic("k_decode_whole_model.json")
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded payloads, recipe in synth/)",
+        "config": {"workload": WORKLOAD_NAME, "tensors": len(work.specs), "elements": work.elements,
+                   "bytes_in": work.bytes_in, "bytes_out": work.bytes_out, "out_dtype": "bf16",
+                   "elements/s": float(f"{world * work.elements / (ms * 1e-3):.4g}"),
+                   "frac_of_8TBs": round(value / world / 8000.0, 4),
+                   "l2": "inputs larger than L2 (20.9 GB moved per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+                     "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "k_decode (batched; step time includes the 2 KB descriptor-table upload kernel)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "per_workload": per_workload,
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# --------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    fraction = 4096
+    specs = synth.llama3_8b_tensors()
+    # a bounded sample with the same field distributions: for every tensor,
+    # 1/fraction of its rows (at least one), generated from the tensor's seed
+    sample = []
+    for s in specs:
+        rows = max(1, s.shape[0] // fraction)
+        shp = (rows,) + tuple(s.shape[1:])
+        sample.append((s.fmt, shp, synth.payload(s.fmt, shp, s.seed)))
+    nbytes = sum(x.size + 2 * int(np.prod(shp)) for (_, shp, x) in sample)
+    nel = sum(int(np.prod(shp)) for (_, shp, _) in sample)
+    cores = os.cpu_count() or 1
+
+    def one(item):
+        fmt, shp, x = item
+        oracle.decode(fmt, shp, x, "bfloat16")
+
+    ex = cf.ThreadPoolExecutor(cores)
+
+    def step():
+        list(ex.map(one, sample))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = (time.perf_counter() - t0) / args.steps
+    ex.shutdown()
+    value = nbytes / secs / 1e9
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded payloads, recipe in synth/)",
+        "config": {"workload": WORKLOAD_NAME, "tensors": len(specs), "elements": nel, "bytes": nbytes,
+                   "out_dtype": "bf16"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"1/{fraction} of every tensor's rows (same field distributions and seeds), "
+                                   f"{nel} elements per step, {cores} threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * ndq.h -- C ABI of the GB300 (sm_103a) packed quantized-weight decoder.
+ *
+ * The library decodes packed quantized weight payloads into float tensors
+ * under the contract of the ONNX "DequantizePacked decoding specification"
+ * (opset 29), section "Signature and storage":
+ *
+ *     y = DequantizePacked<format, shape, output_dtype>(x)
+ *
+ * x is the exact payload bytes; blocks are decoded in input order to binary32
+ * with the specification's rounding points ("Decoding algorithms": every
+ * multiplication, addition and subtraction rounded separately, no fusion),
+ * the values are laid out in `shape` (row-major) and converted once to the
+ * output type (FLOAT16 / BFLOAT16 by round-to-nearest-even; DOUBLE exactly).
+ *
+ * Everything runs on the caller's CUDA device and stream.  The header pulls in
+ * no CUDA or framework header: streams are passed as `void*` (a cudaStream_t;
+ * NULL means the legacy default stream) and buffers as plain pointers.
+ *
+ * Thread safety: all entry points may be called from several host threads.
+ * Calls are asynchronous with respect to the host unless stated otherwise.
+ */
+#ifndef NDQ_H
+#define NDQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Status codes.  Every entry point returns one of these (0 = success).      */
+/* Validation errors are returned synchronously before anything is launched. */
+/* ------------------------------------------------------------------------ */
+#define NDQ_OK 0
+#define NDQ_ERR_NULL 1               /* a required pointer is NULL */
+#define NDQ_ERR_UNKNOWN_FORMAT 2     /* not one of the registered identifiers */
+#define NDQ_ERR_UNSUPPORTED_FORMAT 3 /* registered, but this build has no decoder */
+#define NDQ_ERR_BAD_RANK 4           /* ndim < 1 or ndim > NDQ_MAX_RANK */
+#define NDQ_ERR_NEGATIVE_DIM 5       /* a dimension is negative */
+#define NDQ_ERR_NOT_BLOCK_ALIGNED 6  /* shape[-1] % B != 0 */
+#define NDQ_ERR_LENGTH_MISMATCH 7    /* x_len violates the length rule */
+#define NDQ_ERR_OVERFLOW 8           /* an element or byte count overflows */
+#define NDQ_ERR_BAD_DTYPE 9          /* out_dtype is not one of NDQ_FLOAT.. */
+#define NDQ_ERR_WORKSPACE 10         /* batched workspace NULL or too small */
+#define NDQ_ERR_CUDA 11              /* a CUDA runtime call or launch failed */
+#define NDQ_ERR_DEVICE_FAULT 12      /* a kernel gave up on a bounded wait */
+#define NDQ_ERR_BAD_COUNT 13         /* batched tensor count < 0 */
+
+/* Output element types: the ONNX TensorProto data-type numbers of the four
+ * output types DequantizePacked supports ("Signature and storage"). */
+#define NDQ_FLOAT 1
+#define NDQ_FLOAT16 10
+#define NDQ_DOUBLE 11
+#define NDQ_BFLOAT16 16
+
+/* Format identifiers: a closed enumeration.  0..26 are the 27 fixed GGUF
+ * profiles of "Quantization formats", in the specification's table order;
+ * 27..29 are formats of the NInfer "tensor-formats" registry. */
+#define NDQ_GGUF_Q4_0 0
+#define NDQ_GGUF_Q4_1 1
+#define NDQ_GGUF_Q5_0 2
+#define NDQ_GGUF_Q5_1 3
+#define NDQ_GGUF_Q8_0 4
+#define NDQ_GGUF_Q8_1 5
+#define NDQ_GGUF_Q2_K 6
+#define NDQ_GGUF_Q3_K 7
+#define NDQ_GGUF_Q4_K 8
+#define NDQ_GGUF_Q5_K 9
+#define NDQ_GGUF_Q6_K 10
+#define NDQ_GGUF_Q8_K 11
+#define NDQ_GGUF_IQ2_XXS 12
+#define NDQ_GGUF_IQ2_XS 13
+#define NDQ_GGUF_IQ3_XXS 14
+#define NDQ_GGUF_IQ1_S 15
+#define NDQ_GGUF_IQ4_NL 16
+#define NDQ_GGUF_IQ3_S 17
+#define NDQ_GGUF_IQ2_S 18
+#define NDQ_GGUF_IQ4_XS 19
+#define NDQ_GGUF_IQ1_M 20
+#define NDQ_GGUF_TQ1_0 21
+#define NDQ_GGUF_TQ2_0 22
+#define NDQ_GGUF_MXFP4 23
+#define NDQ_GGUF_NVFP4 24
+#define NDQ_GGUF_Q1_0 25
+#define NDQ_GGUF_Q2_0 26
+/* nvfp4 (NInfer section 3.3): E2M1 codes, one E4M3FN scale per 16 values and
+ * FP32 weight divisors.  Byte layout (a reading: the NInfer page gives the
+ * semantics, not the bytes): 64-value blocks of 36 bytes laid out as
+ * gguf:nvfp4 (4 scale bytes, then 32 code bytes; group g's codes in bytes
+ * 4+8g..11+8g, low nibbles then high nibbles), followed after the last block
+ * by D >= 1 little-endian FP32 divisors d_w; row r of the N = prod(shape[:-1])
+ * rows uses divisor floor(r / (N / D)), so D must divide N.  Each element is
+ * decode_e2m1(c) * decode_e4m3fn(s) rounded once after division by d_w. */
+#define NDQ_NVFP4 27
+/* q4_g64_fp16 (NInfer sections 4-6.2): 64-value blocks of 34 bytes: a
+ * binary16 scale, then 32 bytes holding element k in bits 4*(k mod 2) of byte
+ * floor(k/2) as a 4-bit two's-complement code (a layout reading). */
+#define NDQ_Q4_G64_FP16 28
+/* q8_g32_fp16 (NInfer sections 4-6.2): 32-value blocks of 34 bytes: a
+ * binary16 scale then 32 signed bytes (byte-identical to gguf:q8_0). */
+#define NDQ_Q8_G32_FP16 29
+#define NDQ_NUM_FORMATS 30
+
+#define NDQ_MAX_RANK 8
+
+/* Map an identifier to its format id ("Format identifiers": case-sensitive,
+ * exact; parameterised spellings are unknown).  Returns -1 when unknown or
+ * when `id` is NULL. */
+int ndq_format_from_name(const char *id);
+
+/* Canonical identifier of a format id ("gguf:q4_k", "nvfp4", ...), or NULL.
+ * The string is static and owned by the library. */
+const char *ndq_format_name(int format_id);
+
+/* Block geometry of a format: B decoded elements and S packed bytes per block
+ * ("Quantization formats" table; NInfer formats as described above).
+ * Returns NDQ_ERR_UNKNOWN_FORMAT for an unregistered id, NDQ_ERR_NULL for NULL
+ * outputs.  Works for every registered id, decodable or not. */
+int ndq_format_geometry(int format_id, int *B, int *S);
+
+/* 1 if this build decodes the format on the GPU, 0 if it is registered but
+ * unsupported, -1 if the id is unknown. */
+int ndq_format_supported(int format_id);
+
+/* Static, human-readable name of a status code. */
+const char *ndq_status_string(int status);
+
+/* Host-only validation of one payload under the length rule of "Signature
+ * and storage": rank >= 1, nonnegative dims, shape[-1] % B == 0 and
+ * x_len == prod(shape[:-1]) * (shape[-1] / B) * S (for nvfp4 plus 4*D bytes of
+ * divisors, D >= 1 dividing the row count, none when the tensor is empty).
+ * On success writes the block count, the element count and the number of
+ * nvfp4 divisors (0 otherwise); any output pointer may be NULL.  Does not
+ * touch the GPU. */
+int ndq_payload_geometry(int format_id, const int64_t *shape, int ndim, uint64_t x_len,
+                         uint64_t *nblocks, uint64_t *nelements, uint64_t *ndivisors);
+
+/* Decode one payload.
+ *   format_id  one of NDQ_* format ids (must be supported by this build)
+ *   shape      host array of ndim logical dimensions (ONNX order: the last
+ *              dimension is contiguous and is the block axis)
+ *   out_dtype  NDQ_FLOAT, NDQ_FLOAT16, NDQ_BFLOAT16 or NDQ_DOUBLE
+ *   x_u8       device pointer to x_len payload bytes (any alignment; a
+ *              16-byte-aligned payload takes the bulk-copy path)
+ *   y          device pointer receiving prod(shape) elements of out_dtype,
+ *              row-major (any alignment; 16-byte alignment takes the vector
+ *              store path)
+ *   stream     cudaStream_t to enqueue on (NULL = legacy default stream)
+ * The caller owns x and y and keeps them alive until the stream has passed
+ * the call.  The call allocates nothing and is asynchronous; validation
+ * errors return before any launch; an empty tensor returns NDQ_OK without a
+ * launch; a launch failure returns NDQ_ERR_CUDA.  No payload byte is
+ * rejected: every bit pattern decodes to a defined value (NaN/inf scales
+ * propagate by IEEE rules).  x and y must not overlap. */
+int ndq_dequantize_packed(int format_id, const int64_t *shape, int ndim, int out_dtype,
+                          const uint8_t *x_u8, size_t x_len, void *y, void *stream);
+
+/* One tensor of a batched decode (same meaning as the single call's
+ * arguments; x and y are device pointers). */
+typedef struct ndq_tensor_desc {
+    int32_t format_id;
+    int32_t ndim;
+    int64_t shape[NDQ_MAX_RANK];
+    int32_t out_dtype;
+    int32_t reserved; /* ignored; set to 0 */
+    const uint8_t *x;
+    uint64_t x_len;
+    void *y;
+} ndq_tensor_desc;
+
+/* Device workspace bytes the batched call needs for n tensors (a table of
+ * per-tensor launch descriptors), or 0 when n < 0. */
+size_t ndq_batched_workspace_bytes(int n);
+
+/* Decode n tensors (for example every weight of a model) in ONE kernel
+ * launch.  This is not part of the DequantizePacked specification: it is a
+ * launcher over the same per-tensor decode.
+ *   descs      host array of n descriptors; read during the call only
+ *   workspace  device buffer of at least ndq_batched_workspace_bytes(n) bytes,
+ *              16-byte aligned; the call writes the launch table into it with
+ *              one cudaMemcpyAsync on `stream` and the kernel reads it, so the
+ *              caller keeps it alive and unmodified until the stream has
+ *              passed the call, and does not share it between calls that may
+ *              run concurrently
+ *   stream     as for the single call
+ * Every descriptor is validated before anything is enqueued: one bad entry
+ * rejects the whole batch with that entry's status.  Outputs of different
+ * tensors must not overlap each other or any payload.  n == 0, or a batch
+ * whose tensors are all empty, returns NDQ_OK without a launch. */
+int ndq_dequantize_packed_batched(const ndq_tensor_desc *descs, int n, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
+/* Read and clear the library's device fault word on the current device.
+ * A kernel sets a nonzero bit when one of its bounded waits for staged
+ * payload data gives up (it then stops decoding instead of hanging the GPU).
+ * This call synchronizes the device.  *flags == 0 means no fault occurred
+ * since the last call.  Returns NDQ_ERR_CUDA if the device cannot be read. */
+int ndq_get_device_fault(uint32_t *flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NDQ_H */

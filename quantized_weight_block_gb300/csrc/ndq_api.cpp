@@ -1,0 +1,270 @@
+// ndq_api.cpp -- the C ABI declared in include/ndq.h: format registry, host
+// validation under the DequantizePacked length rule, and launches.
+//
+// Validation follows the ONNX "DequantizePacked decoding specification",
+// sections "Format identifiers" (closed, case-sensitive identifiers) and
+// "Signature and storage" (len(x) == prod(shape[:-1]) * (shape[-1]/B) * S,
+// shape[-1] % B == 0, rank >= 1, nonnegative dims, zero dims give empty
+// outputs); the nvfp4 divisor words follow NInfer tensor-formats section 3.3
+// (one FP32 divisor per stacked source matrix, covering N / D rows).
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "ndq.h"
+#include "ndq_internal.h"
+
+namespace {
+
+struct FormatRow {
+    const char* name;
+    int B;
+    int S;
+    int kfmt;  // ndq::KFmt, or -1 when this build has no decoder
+};
+
+// "Quantization formats" table (order = NDQ_GGUF_* ids), then the NInfer
+// formats.
+const FormatRow kFormats[NDQ_NUM_FORMATS] = {
+    {"gguf:q4_0", 32, 18, ndq::KF_Q4_0},
+    {"gguf:q4_1", 32, 20, -1},
+    {"gguf:q5_0", 32, 22, -1},
+    {"gguf:q5_1", 32, 24, -1},
+    {"gguf:q8_0", 32, 34, ndq::KF_Q8_0},
+    {"gguf:q8_1", 32, 36, -1},
+    {"gguf:q2_k", 256, 84, -1},
+    {"gguf:q3_k", 256, 110, -1},
+    {"gguf:q4_k", 256, 144, ndq::KF_Q4_K},
+    {"gguf:q5_k", 256, 176, -1},
+    {"gguf:q6_k", 256, 210, ndq::KF_Q6_K},
+    {"gguf:q8_k", 256, 292, -1},
+    {"gguf:iq2_xxs", 256, 66, -1},
+    {"gguf:iq2_xs", 256, 74, -1},
+    {"gguf:iq3_xxs", 256, 98, -1},
+    {"gguf:iq1_s", 256, 50, -1},
+    {"gguf:iq4_nl", 32, 18, ndq::KF_IQ4_NL},
+    {"gguf:iq3_s", 256, 110, -1},
+    {"gguf:iq2_s", 256, 82, -1},
+    {"gguf:iq4_xs", 256, 136, -1},
+    {"gguf:iq1_m", 256, 56, -1},
+    {"gguf:tq1_0", 256, 54, -1},
+    {"gguf:tq2_0", 256, 66, -1},
+    {"gguf:mxfp4", 32, 17, ndq::KF_MXFP4},
+    {"gguf:nvfp4", 64, 36, ndq::KF_GGUF_NVFP4},
+    {"gguf:q1_0", 128, 18, -1},
+    {"gguf:q2_0", 64, 18, -1},
+    {"nvfp4", 64, 36, ndq::KF_NVFP4},
+    {"q4_g64_fp16", 64, 34, ndq::KF_Q4_G64},
+    {"q8_g32_fp16", 32, 34, ndq::KF_Q8_0},
+};
+
+bool valid_id(int id) { return id >= 0 && id < NDQ_NUM_FORMATS; }
+
+int out_code(int out_dtype, int* size) {
+    switch (out_dtype) {
+        case NDQ_FLOAT: *size = 4; return ndq::KO_F32;
+        case NDQ_FLOAT16: *size = 2; return ndq::KO_F16;
+        case NDQ_BFLOAT16: *size = 2; return ndq::KO_BF16;
+        case NDQ_DOUBLE: *size = 8; return ndq::KO_F64;
+        default: return -1;
+    }
+}
+
+bool mul_ovf(uint64_t a, uint64_t b, uint64_t* r) { return __builtin_mul_overflow(a, b, r); }
+
+struct Geometry {
+    uint64_t nblocks = 0;
+    uint64_t nelements = 0;
+    uint64_t rows = 0;
+    uint64_t ndiv = 0;
+};
+
+int geometry(int id, const int64_t* shape, int ndim, uint64_t x_len, Geometry* g) {
+    if (!valid_id(id)) return NDQ_ERR_UNKNOWN_FORMAT;
+    if (ndim < 1 || ndim > NDQ_MAX_RANK) return NDQ_ERR_BAD_RANK;
+    if (!shape) return NDQ_ERR_NULL;
+    for (int i = 0; i < ndim; ++i)
+        if (shape[i] < 0) return NDQ_ERR_NEGATIVE_DIM;
+    const uint64_t B = static_cast<uint64_t>(kFormats[id].B), S = static_cast<uint64_t>(kFormats[id].S);
+    const uint64_t K = static_cast<uint64_t>(shape[ndim - 1]);
+    if (K % B != 0) return NDQ_ERR_NOT_BLOCK_ALIGNED;
+    uint64_t N = 1;
+    for (int i = 0; i < ndim - 1; ++i)
+        if (mul_ovf(N, static_cast<uint64_t>(shape[i]), &N)) return NDQ_ERR_OVERFLOW;
+    uint64_t nb = 0, bytes = 0, elems = 0, out8 = 0;
+    if (mul_ovf(N, K / B, &nb) || mul_ovf(nb, S, &bytes) || mul_ovf(N, K, &elems) || mul_ovf(elems, 8, &out8))
+        return NDQ_ERR_OVERFLOW;
+    if (bytes > static_cast<uint64_t>(INT64_MAX) || out8 > static_cast<uint64_t>(INT64_MAX)) return NDQ_ERR_OVERFLOW;
+    uint64_t D = 0;
+    if (id == NDQ_NVFP4 && nb > 0) {
+        if (x_len < bytes || (x_len - bytes) % 4 != 0) return NDQ_ERR_LENGTH_MISMATCH;
+        D = (x_len - bytes) / 4;
+        if (D < 1 || N % D != 0) return NDQ_ERR_LENGTH_MISMATCH;
+    } else if (x_len != bytes) {
+        return NDQ_ERR_LENGTH_MISMATCH;
+    }
+    g->nblocks = nb;
+    g->nelements = elems;
+    g->rows = N;
+    g->ndiv = D;
+    return NDQ_OK;
+}
+
+// Full validation of one tensor and its kernel descriptor (tile_begin unset).
+int prepare(int id, const int64_t* shape, int ndim, int out_dtype, const uint8_t* x, uint64_t x_len, void* y,
+            ndq::DevTensor* t, Geometry* g) {
+    if (!valid_id(id)) return NDQ_ERR_UNKNOWN_FORMAT;
+    int osize = 0;
+    const int oc = out_code(out_dtype, &osize);
+    int rc = geometry(id, shape, ndim, x_len, g);
+    if (rc != NDQ_OK) return rc;
+    if (kFormats[id].kfmt < 0) return NDQ_ERR_UNSUPPORTED_FORMAT;
+    if (oc < 0) return NDQ_ERR_BAD_DTYPE;
+    if (g->nblocks == 0) return NDQ_OK;
+    if (!x || !y) return NDQ_ERR_NULL;
+    std::memset(t, 0, sizeof(*t));
+    t->x = x;
+    t->y = y;
+    t->nblocks = g->nblocks;
+    t->fmt = kFormats[id].kfmt;
+    t->out = oc;
+    t->S = static_cast<uint16_t>(kFormats[id].S);
+    t->B = static_cast<uint16_t>(kFormats[id].B);
+    t->bpt = static_cast<uint16_t>(ndq::kTileElems / kFormats[id].B);
+    t->yvec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
+    if (id == NDQ_NVFP4) {
+        const uint64_t bpr = static_cast<uint64_t>(shape[ndim - 1]) / 64u;
+        t->divs = x + g->nblocks * 36u;
+        t->blocks_per_div = bpr * (g->rows / g->ndiv);
+    }
+    return NDQ_OK;
+}
+
+uint64_t tiles_of(const ndq::DevTensor& t) { return (t.nblocks + t.bpt - 1) / t.bpt; }
+
+constexpr size_t kWorkspaceAlign = 16;
+
+}  // namespace
+
+extern "C" {
+
+int ndq_format_from_name(const char* id) {
+    if (!id) return -1;
+    for (int i = 0; i < NDQ_NUM_FORMATS; ++i)
+        if (std::strcmp(kFormats[i].name, id) == 0) return i;
+    return -1;
+}
+
+const char* ndq_format_name(int format_id) { return valid_id(format_id) ? kFormats[format_id].name : nullptr; }
+
+int ndq_format_geometry(int format_id, int* B, int* S) {
+    if (!valid_id(format_id)) return NDQ_ERR_UNKNOWN_FORMAT;
+    if (!B || !S) return NDQ_ERR_NULL;
+    *B = kFormats[format_id].B;
+    *S = kFormats[format_id].S;
+    return NDQ_OK;
+}
+
+int ndq_format_supported(int format_id) {
+    if (!valid_id(format_id)) return -1;
+    return kFormats[format_id].kfmt >= 0 ? 1 : 0;
+}
+
+const char* ndq_status_string(int status) {
+    switch (status) {
+        case NDQ_OK: return "ok";
+        case NDQ_ERR_NULL: return "null pointer";
+        case NDQ_ERR_UNKNOWN_FORMAT: return "unknown format";
+        case NDQ_ERR_UNSUPPORTED_FORMAT: return "format not supported by this build";
+        case NDQ_ERR_BAD_RANK: return "bad rank";
+        case NDQ_ERR_NEGATIVE_DIM: return "negative dimension";
+        case NDQ_ERR_NOT_BLOCK_ALIGNED: return "last dimension not a multiple of the block size";
+        case NDQ_ERR_LENGTH_MISMATCH: return "payload length does not match shape";
+        case NDQ_ERR_OVERFLOW: return "element or byte count overflows";
+        case NDQ_ERR_BAD_DTYPE: return "unsupported output dtype";
+        case NDQ_ERR_WORKSPACE: return "workspace missing or too small";
+        case NDQ_ERR_CUDA: return "CUDA error";
+        case NDQ_ERR_DEVICE_FAULT: return "device fault (bounded wait expired)";
+        case NDQ_ERR_BAD_COUNT: return "bad tensor count";
+        default: return "unknown status";
+    }
+}
+
+int ndq_payload_geometry(int format_id, const int64_t* shape, int ndim, uint64_t x_len, uint64_t* nblocks,
+                         uint64_t* nelements, uint64_t* ndivisors) {
+    Geometry g;
+    const int rc = geometry(format_id, shape, ndim, x_len, &g);
+    if (rc != NDQ_OK) return rc;
+    if (nblocks) *nblocks = g.nblocks;
+    if (nelements) *nelements = g.nelements;
+    if (ndivisors) *ndivisors = g.ndiv;
+    return NDQ_OK;
+}
+
+int ndq_dequantize_packed(int format_id, const int64_t* shape, int ndim, int out_dtype, const uint8_t* x_u8,
+                          size_t x_len, void* y, void* stream) {
+    ndq::KParams p;
+    std::memset(&p, 0, sizeof(p));
+    Geometry g;
+    const int rc = prepare(format_id, shape, ndim, out_dtype, x_u8, x_len, y, &p.single, &g);
+    if (rc != NDQ_OK) return rc;
+    if (g.nblocks == 0) return NDQ_OK;
+    p.single.tile_begin = 0;
+    p.table = nullptr;
+    p.n = 1;
+    p.any_nvfp4 = p.single.fmt == ndq::KF_NVFP4;
+    p.total_tiles = tiles_of(p.single);
+    return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+}
+
+size_t ndq_batched_workspace_bytes(int n) {
+    if (n < 0) return 0;
+    return (static_cast<size_t>(n) * sizeof(ndq::DevTensor) + kWorkspaceAlign - 1) / kWorkspaceAlign *
+           kWorkspaceAlign;
+}
+
+int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* workspace, size_t ws_bytes,
+                                  void* stream) {
+    if (n < 0) return NDQ_ERR_BAD_COUNT;
+    if (n == 0) return NDQ_OK;
+    if (!descs) return NDQ_ERR_NULL;
+    std::vector<ndq::DevTensor> table;
+    table.reserve(static_cast<size_t>(n));
+    uint64_t tiles = 0;
+    int any_nvfp4 = 0;
+    for (int i = 0; i < n; ++i) {
+        const ndq_tensor_desc& d = descs[i];
+        ndq::DevTensor t;
+        Geometry g;
+        const int rc = prepare(d.format_id, d.shape, d.ndim, d.out_dtype, d.x, d.x_len, d.y, &t, &g);
+        if (rc != NDQ_OK) return rc;
+        if (g.nblocks == 0) continue;
+        t.tile_begin = tiles;
+        tiles += tiles_of(t);
+        any_nvfp4 |= t.fmt == ndq::KF_NVFP4;
+        table.push_back(t);
+    }
+    if (table.empty()) return NDQ_OK;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign) != 0 ||
+        ws_bytes < table.size() * sizeof(ndq::DevTensor))
+        return NDQ_ERR_WORKSPACE;
+    ndq::DevTensor* dev_table = static_cast<ndq::DevTensor*>(workspace);
+    if (ndq::upload_table(dev_table, table.data(), static_cast<int>(table.size()), stream) != 0) return NDQ_ERR_CUDA;
+    ndq::KParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.table = dev_table;
+    p.n = static_cast<int32_t>(table.size());
+    p.any_nvfp4 = any_nvfp4;
+    p.total_tiles = tiles;
+    return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+}
+
+int ndq_get_device_fault(uint32_t* flags) {
+    if (!flags) return NDQ_ERR_NULL;
+    return ndq::read_fault(flags) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+}
+
+}  // extern "C"

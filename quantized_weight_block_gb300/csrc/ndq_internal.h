@@ -1,0 +1,75 @@
+// ndq_internal.h -- launch descriptors shared by the host ABI (ndq_api.cpp)
+// and the decode kernels (ndq_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace ndq {
+
+// Kernel decode families.  gguf:q8_0 and q8_g32_fp16 share one (their blocks
+// are byte- and value-identical).
+enum KFmt : int32_t {
+    KF_Q8_0 = 0,
+    KF_Q4_0 = 1,
+    KF_IQ4_NL = 2,
+    KF_Q4_K = 3,
+    KF_Q6_K = 4,
+    KF_MXFP4 = 5,
+    KF_GGUF_NVFP4 = 6,
+    KF_NVFP4 = 7,
+    KF_Q4_G64 = 8,
+    KF_COUNT = 9,
+};
+
+// Output element type of a tensor.
+enum KOut : int32_t { KO_F32 = 0, KO_F16 = 1, KO_BF16 = 2, KO_F64 = 3 };
+
+// Work unit: a tile of kTileElems consecutive output elements (a whole number
+// of blocks for every format, since every B divides 8192).  A tile's payload
+// span is (8192 / B) * S bytes: a multiple of 16 for every supported format,
+// so full tiles of a 16-byte-aligned payload are bulk-copyable.
+constexpr int kTileElems = 8192;
+constexpr int kThreads = 256;
+constexpr int kMaxTileBytes = 8704;  // gguf:q8_0: 256 blocks * 34 bytes
+
+// One tensor as the kernel sees it (64 bytes; kept trivially copyable).
+struct DevTensor {
+    const uint8_t* x;         // payload blocks
+    void* y;                  // output
+    uint64_t nblocks;         // blocks in the payload
+    uint64_t tile_begin;      // first global tile index of this tensor
+    const uint8_t* divs;      // nvfp4: FP32 divisor words (may be unaligned)
+    uint64_t blocks_per_div;  // nvfp4: blocks sharing one divisor
+    int32_t fmt;              // KFmt
+    int32_t out;              // KOut
+    uint16_t S;               // bytes per block
+    uint16_t B;               // elements per block
+    uint16_t bpt;             // blocks per tile (kTileElems / B)
+    uint16_t yvec;            // 1 if y is 16-byte aligned
+};
+static_assert(sizeof(DevTensor) == 64, "DevTensor layout");
+
+// Kernel parameters.  A single-tensor launch carries its descriptor inline
+// (table == nullptr, n == 1); a batched launch points at a device table of n
+// descriptors sorted by tile_begin.
+struct KParams {
+    DevTensor single;
+    const DevTensor* table;
+    int32_t n;
+    int32_t any_nvfp4;
+    uint64_t total_tiles;
+};
+
+// Launch one decode over p.total_tiles tiles on `stream` (a cudaStream_t).
+// Returns 0 or a CUDA error code.
+int launch_decode(const KParams& p, void* stream);
+
+// Copy n host descriptors into a device table with kernel launches on
+// `stream` (no host-blocking copy).  Returns 0 or a CUDA error code.
+int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream);
+
+// Read and clear the device fault word of the current device.
+int read_fault(uint32_t* flags);
+
+}  // namespace ndq

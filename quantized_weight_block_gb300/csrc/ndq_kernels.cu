@@ -1,0 +1,764 @@
+// ndq_kernels.cu -- sm_103a decode kernels for packed quantized weights.
+//
+// Decode is a streaming, HBM-bound transform (about 2.5 bytes moved per
+// element for 4-bit formats to 16-bit outputs, 1-2 FP32 operations per
+// element), so the design is about moving bytes, not about tensor cores:
+//
+//  * persistent CTAs (a grid of SMs x resident CTAs) walk a global list of
+//    8192-element tiles that spans one tensor or a whole batch of tensors;
+//  * each tile's payload bytes (a contiguous span, a multiple of 16 bytes)
+//    are staged into shared memory by the Tensor Memory Accelerator with
+//    cp.async.bulk, completing on an mbarrier, through a ring of kStages
+//    buffers issued by one thread, so that loads for the next tiles are in
+//    flight while the current tile decodes;
+//  * every thread decodes 8-element chunks straight from shared memory (the
+//    odd block strides of 17, 18, 34, 36 and 210 bytes are resolved with
+//    aligned 32-bit shared loads and funnel shifts) and writes each chunk
+//    with 16-byte vector stores, so a warp writes 512 contiguous bytes per
+//    instruction;
+//  * all arithmetic follows the ONNX "DequantizePacked decoding
+//    specification" ("Decoding algorithms": every M/A/D rounded separately
+//    to binary32, round-to-nearest-even), with explicit __fmul_rn /
+//    __fsub_rn / __fdiv_rn and -fmad=false, and a single round-to-nearest-
+//    even conversion to the output type.  Integer codes reach FP32 through
+//    the exact 2^23 magic-number construction (a byte placed in the low
+//    mantissa of 2^23, minus 2^23 plus the code offset), never through a
+//    rounding conversion.
+//
+// Every wait on an mbarrier is bounded by the global timer; on expiry the CTA
+// records a fault bit, waits (bounded) for its own copies in flight and
+// returns, so that a lost copy cannot hang the GPU.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ndq_internal.h"
+
+namespace ndq {
+
+__device__ unsigned int g_fault_word;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kInStride = 8832;  // kMaxTileBytes + over-read pad, multiple of 128
+constexpr int kChunksPerThread = kTileElems / 8 / kThreads;  // 4
+constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
+constexpr int kTabEntries = 256 * 8;                         // nvfp4 quotient table
+
+static_assert(kInStride >= kMaxTileBytes + 16, "over-read pad");
+static_assert(kInStride % 128 == 0, "stage alignment");
+
+struct StageInfo {
+    uint64_t block0;  // first block of the tile within its tensor
+    uint32_t nb;      // blocks in the tile
+    int32_t desc;     // tensor index
+    int32_t coop;     // 1: bytes are loaded by the CTA's threads, not TMA
+    int32_t pad;
+};
+
+struct SmemHdr {
+    uint64_t mbar[kStages];
+    StageInfo info[kStages];
+    float lut_iq4[16];  // IQ4_NL table ("Packed layouts and decoding")
+    float lut_v[16];    // doubled E2M1 table V ("Ternary and block-floating formats")
+    uint32_t tab_bits;  // divisor bits the nvfp4 table was built for
+    int32_t tab_valid;
+};
+
+constexpr int kHdrBytes = (sizeof(SmemHdr) + 127) / 128 * 128;
+
+__constant__ int8_t c_iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
+__constant__ int8_t c_v[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, bulk copy, proxy fence, global timer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: true once the phase with `parity` has completed, false after
+// kWaitLimitNs of global time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// TMA bulk copy global -> shared, completing `bytes` of transaction count on
+// `bar`.  dst, src and bytes are multiples of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory byte access and exact scalar constructions.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t lds_u16(const uint8_t* p) {  // p even
+    return *reinterpret_cast<const uint16_t*>(p);
+}
+
+// 8 bytes at byte offset `off` of a 16-byte-aligned shared buffer.
+__device__ __forceinline__ uint2 lds_8(const uint8_t* base, uint32_t off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    const uint32_t sh = (off & 3u) * 8u;
+    const uint32_t a = w[0], b = w[1], c = w[2];
+    return make_uint2(__funnelshift_r(a, b, sh), __funnelshift_r(b, c, sh));
+}
+
+// 4 bytes at byte offset `off`.
+__device__ __forceinline__ uint32_t lds_4(const uint8_t* base, uint32_t off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    return __funnelshift_r(w[0], w[1], (off & 3u) * 8u);
+}
+
+// Exact binary16 -> binary32 (the specification's H).
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// Byte I of w (0..255) as the float 2^23 + byte, minus `bias`: exact for the
+// small integers involved (bias = 2^23 + code offset).
+template <int I>
+__device__ __forceinline__ float byte_minus(uint32_t w, float bias) {
+    return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)), bias);
+}
+
+// MXFP4 half scale: the FLOAT with bit pattern 0x00200000 * 2^e for e < 2,
+// (e-1) * 2^23 otherwise ("Ternary and block-floating formats").
+__device__ __forceinline__ float e8m0_half(uint32_t e) {
+    return __uint_as_float(e < 2u ? (0x00200000u << e) : ((e - 1u) << 23));
+}
+
+// gguf:nvfp4 unsigned-E4M3 half scale: 0 for bytes 0 and 127; otherwise,
+// with E = bits 6:3 and m = bits 2:0 (bit 7 ignored), m * 2^-10 when E == 0
+// and (1 + m/8) * 2^(E-8) else (exponent field E + 119, mantissa m << 20).
+__device__ __forceinline__ float ue4m3_half(uint32_t e) {
+    const uint32_t E = (e >> 3) & 15u, m = e & 7u;
+    const float r = (E == 0u) ? __fmul_rn(static_cast<float>(m), 0.0009765625f)
+                              : __uint_as_float(((E + 119u) << 23) | (m << 20));
+    return (e == 0u || e == 127u) ? 0.0f : r;
+}
+
+// E4M3FN word (NInfer tensor-formats section 3.3): bias 7, subnormal
+// m * 2^-9, e == 15 && m == 7 NaN, sign applies to every word.
+__device__ __forceinline__ float e4m3fn(uint32_t w) {
+    const uint32_t e = (w >> 3) & 15u, m = w & 7u;
+    float mag;
+    if (e == 15u && m == 7u)
+        mag = __uint_as_float(0x7fc00000u);
+    else if (e == 0u)
+        mag = __fmul_rn(static_cast<float>(m), 0.001953125f);
+    else
+        mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (w & 0x80u) ? -mag : mag;
+}
+
+// E2M1 word (section 3.3): positive words 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6;
+// bit 3 negates (0x8 is -0).
+__device__ __forceinline__ float e2m1(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = (e == 0u) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+    return (c & 8u) ? -mag : mag;
+}
+
+// Little-endian FP32 word at any byte address (global memory).
+__device__ __forceinline__ float load_f32_bytes(const uint8_t* p) {
+    const uint32_t u = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
+                       (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24);
+    return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------
+// Per-format chunk decoders: chunk c of a tile = output elements 8c..8c+7 of
+// the tile, produced from the tile's payload bytes `in` (shared memory).
+// ---------------------------------------------------------------------------
+struct NvCtx {
+    const float* tab;        // quotient table, or nullptr for per-element division
+    const uint8_t* divs;     // divisor words (per-element path)
+    uint64_t block0;         // first block of the tile
+    uint64_t blocks_per_div;
+};
+
+template <int F>
+struct Fmt;
+
+// gguf:q8_0 / q8_g32_fp16: y[j] = M(d, q[j]), q signed bytes.
+template <>
+struct Fmt<KF_Q8_0> {
+    static constexpr int B = 32, S = 34, CPB = 4;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 2) * S;
+        const float d = h2f(lds_u16(in + off));
+        const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
+        const uint32_t a = q.x ^ 0x80808080u, b = q.y ^ 0x80808080u;  // signed -> offset-128
+        const float bias = 8388736.0f;                                 // 2^23 + 128
+        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+    }
+};
+
+// Nibble plane p (0 = low, 1 = high) of 8 consecutive code bytes, as bytes.
+__device__ __forceinline__ void nib_plane(uint2 q, uint32_t p, uint32_t& a, uint32_t& b) {
+    a = (q.x >> (4u * p)) & 0x0F0F0F0Fu;
+    b = (q.y >> (4u * p)) & 0x0F0F0F0Fu;
+}
+
+// gguf:q4_0: v = P(q,4,16); y[j] = M(d, v[j] - 8).  Chunk c&3: bytes 8*(c&1)
+// of q, plane c>>1 (16 low nibbles, then 16 high nibbles).
+template <>
+struct Fmt<KF_Q4_0> {
+    static constexpr int B = 32, S = 18, CPB = 4;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_u16(in + off));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
+        const float bias = 8388616.0f;  // 2^23 + 8
+        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+    }
+};
+
+// Table lookup of 8 nibbles (bytes of a, then b) scaled by d: y = M(d, T[v]).
+__device__ __forceinline__ void lut8(const float* T, float d, uint32_t a, uint32_t b, float* v) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = __fmul_rn(d, T[(a >> (8 * i)) & 15u]);
+        v[4 + i] = __fmul_rn(d, T[(b >> (8 * i)) & 15u]);
+    }
+}
+
+// gguf:iq4_nl: v = P(q,4,16); y[j] = M(d, IQ4[v[j]]).
+template <>
+struct Fmt<KF_IQ4_NL> {
+    static constexpr int B = 32, S = 18, CPB = 4;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_u16(in + off));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
+        lut8(H.lut_iq4, d, a, b, v);
+    }
+};
+
+// gguf:mxfp4: d = E8M0 half scale; v = P(q,4,16); y[j] = M(d, V[v[j]]).
+template <>
+struct Fmt<KF_MXFP4> {
+    static constexpr int B = 32, S = 17, CPB = 4;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 2) * S, cc = c & 3u;
+        const float d = e8m0_half(in[off]);
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 1u + 8u * (cc & 1u)), cc >> 1, a, b);
+        lut8(H.lut_v, d, a, b, v);
+    }
+};
+
+// gguf:nvfp4: group g = (c&7)>>1 of 16 values: d = unsigned-E4M3 half scale of
+// scales[g]; v = P(q[8g:8g+8],4,8); y[16g+j] = M(d, V[v[j]]).
+template <>
+struct Fmt<KF_GGUF_NVFP4> {
+    static constexpr int B = 64, S = 36, CPB = 8;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+        const float d = ue4m3_half(in[off + g]);
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
+        lut8(H.lut_v, d, a, b, v);
+    }
+};
+
+// nvfp4 (NInfer section 3.3): W = e2m1(c) * e4m3fn(s) / d_w, the product exact
+// and the quotient rounded once.  With a quotient table (one divisor for the
+// whole tile) the element is tab[s*8 + (c&7)] with the sign of bit 3 applied
+// (RNE division is odd-symmetric, and (-0)*s/d_w is the negated (+0)*s/d_w).
+template <>
+struct Fmt<KF_NVFP4> {
+    static constexpr int B = 64, S = 36, CPB = 8;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx& nv) {
+        const uint32_t off = (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+        const uint32_t s = in[off + g];
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
+        if (nv.tab) {
+            const uint32_t* T = reinterpret_cast<const uint32_t*>(nv.tab) + s * 8u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t ca = (a >> (8 * i)) & 15u, cb = (b >> (8 * i)) & 15u;
+                v[i] = __uint_as_float(T[ca & 7u] ^ ((ca & 8u) << 28));
+                v[4 + i] = __uint_as_float(T[cb & 7u] ^ ((cb & 8u) << 28));
+            }
+        } else {  // the tile spans two divisors: divisor of this block, then divide
+            const float dw = load_f32_bytes(nv.divs + 4u * ((nv.block0 + (c >> 3)) / nv.blocks_per_div));
+            const float sc = e4m3fn(s);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[i] = __fdiv_rn(__fmul_rn(e2m1((a >> (8 * i)) & 15u), sc), dw);
+                v[4 + i] = __fdiv_rn(__fmul_rn(e2m1((b >> (8 * i)) & 15u), sc), dw);
+            }
+        }
+    }
+};
+
+// gguf:q4_k: v = P(q,4,32); 6-bit a[k], m[k] from the 12 scale bytes;
+// y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])), k = floor(j/32).
+// Chunk c&31: sub-block k = cc>>2, byte group cc>>3 (32 bytes), plane
+// (cc>>2)&1, bytes 8*(cc&3) of the group.
+template <>
+struct Fmt<KF_Q4_K> {
+    static constexpr int B = 256, S = 144, CPB = 32;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 5) * S, cc = c & 31u, k = cc >> 2;
+        const float d = h2f(lds_u16(in + off)), dmin = h2f(lds_u16(in + off + 2u));
+        const uint8_t* s = in + off + 4u;
+        uint32_t sa, sm;
+        if (k < 4u) {
+            sa = s[k] & 63u;
+            sm = s[k + 4u] & 63u;
+        } else {
+            sa = (s[k + 4u] & 15u) | ((s[k - 4u] >> 6) << 4);
+            sm = (s[k + 4u] >> 4) | ((s[k] >> 6) << 4);
+        }
+        const float da = __fmul_rn(d, static_cast<float>(sa));
+        const float dm = __fmul_rn(dmin, static_cast<float>(sm));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 16u + 32u * (cc >> 3) + 8u * (cc & 3u)), k & 1u, a, b);
+        const float bias = 8388608.0f;  // 2^23
+        v[0] = __fsub_rn(__fmul_rn(da, byte_minus<0>(a, bias)), dm);
+        v[1] = __fsub_rn(__fmul_rn(da, byte_minus<1>(a, bias)), dm);
+        v[2] = __fsub_rn(__fmul_rn(da, byte_minus<2>(a, bias)), dm);
+        v[3] = __fsub_rn(__fmul_rn(da, byte_minus<3>(a, bias)), dm);
+        v[4] = __fsub_rn(__fmul_rn(da, byte_minus<0>(b, bias)), dm);
+        v[5] = __fsub_rn(__fmul_rn(da, byte_minus<1>(b, bias)), dm);
+        v[6] = __fsub_rn(__fmul_rn(da, byte_minus<2>(b, bias)), dm);
+        v[7] = __fsub_rn(__fmul_rn(da, byte_minus<3>(b, bias)), dm);
+    }
+};
+
+// gguf:q6_k: l = P(low,4,64), h = P(high,2,32), s = scales[floor(j/16)] signed;
+// y[j] = M(M(d, s), l[j] + 16 h[j] - 32).  Chunk c&31 = elements 8cc..8cc+7:
+// low bytes 64*(cc>>4) + 8*(cc&7), plane (cc>>3)&1; high bytes
+// 32*(cc>>4) + 8*(cc&3), 2-bit plane (cc>>2)&3; scale index cc>>1.
+template <>
+struct Fmt<KF_Q6_K> {
+    static constexpr int B = 256, S = 210, CPB = 32;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
+        const float d = h2f(lds_u16(in + off + 208u));
+        const int32_t sc = static_cast<int8_t>(in[off + 192u + (cc >> 1)]);
+        const float ds = __fmul_rn(d, static_cast<float>(sc));
+        const uint2 lo = lds_8(in, off + 64u * gi + 8u * (cc & 7u));
+        const uint2 hi = lds_8(in, off + 128u + 32u * gi + 8u * (cc & 3u));
+        const uint32_t pl = 4u * ((cc >> 3) & 1u), ph = 2u * ((cc >> 2) & 3u);
+        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> ph) & 0x03030303u) << 4);
+        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> ph) & 0x03030303u) << 4);
+        const float bias = 8388640.0f;  // 2^23 + 32
+        v[0] = __fmul_rn(ds, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(ds, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(ds, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(ds, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(ds, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(ds, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(ds, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(ds, byte_minus<3>(b, bias));
+    }
+};
+
+// q4_g64_fp16 (NInfer sections 5-6.2): w = binary32(s32 * q), q the 4-bit
+// two's-complement code; element k sits in bits 4*(k mod 2) of code byte
+// floor(k/2) (layout reading).  XOR 8 maps two's complement to offset-8.
+template <>
+struct Fmt<KF_Q4_G64> {
+    static constexpr int B = 64, S = 34, CPB = 8;
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
+                                                 const NvCtx&) {
+        const uint32_t off = (c >> 3) * S;
+        const float s = h2f(lds_u16(in + off));
+        const uint32_t w = lds_4(in, off + 2u + 4u * (c & 7u));
+        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+        const float bias = 8388616.0f;  // 2^23 + 8
+        v[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
+        v[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
+        v[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
+        v[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
+        v[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
+        v[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
+        v[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
+        v[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Output stage: one RNE conversion per element, 16-byte stores when y is
+// 16-byte aligned (element offsets are multiples of 8, so every chunk then
+// starts on a 16-byte boundary).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int O>
+__device__ __forceinline__ void store8(void* y, uint64_t e0, const float* v, bool vec) {
+    if (O == KO_F32) {
+        float* p = static_cast<float*>(y) + e0;
+        if (vec) {
+            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p[i] = v[i];
+        }
+    } else if (O == KO_F64) {
+        double* p = static_cast<double*>(y) + e0;
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                reinterpret_cast<double2*>(p)[i] =
+                    make_double2(static_cast<double>(v[2 * i]), static_cast<double>(v[2 * i + 1]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p[i] = static_cast<double>(v[i]);
+        }
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+        uint16_t* p = static_cast<uint16_t*>(y) + e0;
+        if (vec) {
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[2 * i] = static_cast<uint16_t>(w[i] & 0xffffu);
+                p[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        }
+    }
+}
+
+template <int F, int O>
+__device__ __forceinline__ void decode_tile_fo(const DevTensor& t, const StageInfo& si, const uint8_t* in,
+                                               const SmemHdr& H, const NvCtx& nv) {
+    using Fm = Fmt<F>;
+    const uint32_t nch = si.nb * static_cast<uint32_t>(Fm::CPB);
+    const uint64_t e_base = si.block0 * static_cast<uint64_t>(Fm::B);
+    const bool vec = t.yvec != 0;
+#pragma unroll
+    for (int k = 0; k < kChunksPerThread; ++k) {
+        const uint32_t c = threadIdx.x + static_cast<uint32_t>(k * kThreads);
+        if (c < nch) {
+            float v[8];
+            Fm::chunk(in, c, v, H, nv);
+            store8<O>(t.y, e_base + 8ull * c, v, vec);
+        }
+    }
+}
+
+template <int F>
+__device__ __forceinline__ void decode_tile_f(const DevTensor& t, const StageInfo& si, const uint8_t* in,
+                                              const SmemHdr& H, const NvCtx& nv) {
+    switch (t.out) {
+        case KO_F32: decode_tile_fo<F, KO_F32>(t, si, in, H, nv); break;
+        case KO_F16: decode_tile_fo<F, KO_F16>(t, si, in, H, nv); break;
+        case KO_BF16: decode_tile_fo<F, KO_BF16>(t, si, in, H, nv); break;
+        default: decode_tile_fo<F, KO_F64>(t, si, in, H, nv); break;
+    }
+}
+
+// nvfp4 divisor for the tile: builds (or reuses) the shared quotient table
+// when the whole tile shares one divisor.  Called by every thread of the CTA
+// (contains barriers; the decision is uniform because it depends only on the
+// tile and on global data).
+__device__ NvCtx nvfp4_prepare(const DevTensor& t, const StageInfo& si, SmemHdr& H, float* tab) {
+    NvCtx nv{nullptr, t.divs, si.block0, t.blocks_per_div};
+    const uint64_t d0 = si.block0 / t.blocks_per_div;
+    const uint64_t d1 = (si.block0 + si.nb - 1u) / t.blocks_per_div;
+    if (d0 != d1) return nv;  // tile spans two divisors: divide per element
+    const float dw = load_f32_bytes(t.divs + 4u * d0);
+    const uint32_t bits = __float_as_uint(dw);
+    const bool have = H.tab_valid && H.tab_bits == bits;
+    __syncthreads();  // everyone has read tab_valid/tab_bits and finished with the old table
+    if (!have) {
+        for (int i = threadIdx.x; i < kTabEntries; i += kThreads)
+            tab[i] = __fdiv_rn(__fmul_rn(e2m1(static_cast<uint32_t>(i) & 7u), e4m3fn(static_cast<uint32_t>(i) >> 3)),
+                               dw);
+        if (threadIdx.x == 0) {
+            H.tab_bits = bits;
+            H.tab_valid = 1;
+        }
+        __syncthreads();
+    }
+    nv.tab = tab;
+    return nv;
+}
+
+__device__ __forceinline__ const DevTensor& tensor_of(const KParams& p, int32_t i) {
+    return p.table ? p.table[i] : p.single;
+}
+
+// Tensor holding global tile `tile`: the last descriptor with tile_begin <= tile.
+__device__ __forceinline__ int32_t find_tensor(const KParams& p, uint64_t tile) {
+    if (!p.table) return 0;
+    int32_t lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (p.table[mid].tile_begin <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Producer (one thread): stage `tile`'s payload bytes into buffer s.
+__device__ void produce(const KParams& p, SmemHdr& H, uint8_t* inbuf, uint64_t tile, int s) {
+    if (tile >= p.total_tiles) return;
+    const int32_t di = find_tensor(p, tile);
+    const DevTensor& t = tensor_of(p, di);
+    const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
+    const uint64_t left = t.nblocks - b0;
+    const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
+    const uint32_t bytes = nb * t.S;
+    const uint8_t* src = t.x + b0 * t.S;
+    const int coop = ((reinterpret_cast<uintptr_t>(src) | bytes) & 15u) != 0;
+    StageInfo& si = H.info[s];
+    si.block0 = b0;
+    si.nb = nb;
+    si.desc = di;
+    si.coop = coop;
+    if (coop) {
+        mbar_arrive(&H.mbar[s]);
+    } else {
+        mbar_arrive_expect_tx(&H.mbar[s], bytes);
+        bulk_load(inbuf + s * kInStride, src, bytes, &H.mbar[s]);
+    }
+}
+
+// Fault exit: record the fault and let thread 0 wait (bounded) for every copy
+// this CTA still has in flight, iterations it .. last_issued.
+__device__ void fault_exit(const KParams& p, SmemHdr& H, int it, uint64_t tile, uint64_t grid) {
+    if (threadIdx.x != 0) return;
+    atomicOr(&g_fault_word, 1u);
+    const int last = (it == 0) ? kStages - 1 : it + kStages - 2;
+    for (int j = it; j <= last; ++j) {
+        const uint64_t tj = tile + static_cast<uint64_t>(j - it) * grid;
+        if (tj >= p.total_tiles) break;
+        mbar_wait_bounded(&H.mbar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_decode(const KParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* inbuf = smem;
+    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
+    float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
+    const uint64_t grid = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&H.mbar[s], 1);
+        H.tab_valid = 0;
+        H.tab_bits = 0;
+        fence_proxy_async();
+    }
+    if (threadIdx.x < 16) {
+        H.lut_iq4[threadIdx.x] = static_cast<float>(c_iq4[threadIdx.x]);
+        H.lut_v[threadIdx.x] = static_cast<float>(c_v[threadIdx.x]);
+    }
+    __syncthreads();
+
+    uint64_t tile = blockIdx.x;
+    if (threadIdx.x == 0)
+        for (int s = 0; s < kStages; ++s) produce(p, H, inbuf, tile + static_cast<uint64_t>(s) * grid, s);
+
+    for (int it = 0; tile < p.total_tiles; tile += grid, ++it) {
+        const int s = it % kStages;
+        const bool ok = mbar_wait_bounded(&H.mbar[s], static_cast<uint32_t>((it / kStages) & 1));
+        // One barrier per tile: it publishes the stage to every thread, makes
+        // the decision to bail out uniform, and proves the previous tile's
+        // buffer is no longer read, so it can be refilled.
+        if (__syncthreads_or(!ok)) {
+            fault_exit(p, H, it, tile, grid);
+            return;
+        }
+        if (threadIdx.x == 0 && it > 0)
+            produce(p, H, inbuf, tile + static_cast<uint64_t>(kStages - 1) * grid, (it - 1) % kStages);
+
+        const StageInfo si = H.info[s];
+        const DevTensor& t = tensor_of(p, si.desc);
+        uint8_t* in = inbuf + s * kInStride;
+        if (si.coop) {  // unaligned payload or ragged tail: plain loads
+            const uint8_t* src = t.x + si.block0 * t.S;
+            const uint32_t bytes = si.nb * t.S;
+            for (uint32_t i = threadIdx.x; i < bytes; i += kThreads) in[i] = src[i];
+            fence_proxy_async();
+            __syncthreads();
+        }
+        NvCtx nv{nullptr, nullptr, 0, 1};
+        if (t.fmt == KF_NVFP4) nv = nvfp4_prepare(t, si, H, tab);
+        switch (t.fmt) {
+            case KF_Q8_0: decode_tile_f<KF_Q8_0>(t, si, in, H, nv); break;
+            case KF_Q4_0: decode_tile_f<KF_Q4_0>(t, si, in, H, nv); break;
+            case KF_IQ4_NL: decode_tile_f<KF_IQ4_NL>(t, si, in, H, nv); break;
+            case KF_Q4_K: decode_tile_f<KF_Q4_K>(t, si, in, H, nv); break;
+            case KF_Q6_K: decode_tile_f<KF_Q6_K>(t, si, in, H, nv); break;
+            case KF_MXFP4: decode_tile_f<KF_MXFP4>(t, si, in, H, nv); break;
+            case KF_GGUF_NVFP4: decode_tile_f<KF_GGUF_NVFP4>(t, si, in, H, nv); break;
+            case KF_NVFP4: decode_tile_f<KF_NVFP4>(t, si, in, H, nv); break;
+            default: decode_tile_f<KF_Q4_G64>(t, si, in, H, nv); break;
+        }
+    }
+}
+
+// Writes n descriptors (kernel parameters) into a device table.
+constexpr int kUploadChunk = 128;
+struct UploadParams {
+    DevTensor* dst;
+    int32_t n;
+    DevTensor d[kUploadChunk];
+};
+
+__global__ void k_upload_table(const UploadParams p) {
+    for (int i = threadIdx.x; i < p.n; i += blockDim.x) p.dst[i] = p.d[i];
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int ctas_per_sm[2] = {0, 0};
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+size_t smem_bytes(bool tab) {
+    return static_cast<size_t>(kStages * kInStride + kHdrBytes) + (tab ? kTabEntries * sizeof(float) : 0);
+}
+
+}  // namespace
+
+int launch_decode(const KParams& p, void* stream) {
+    if (p.total_tiles == 0) return 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+    const bool tab = p.any_nvfp4 != 0;
+    const size_t smem = smem_bytes(tab);
+    DeviceInfo& di = g_dev[dev];
+    // Benign race: concurrent first calls compute the same values.
+    if (di.sms == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_bytes(true)));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        for (int i = 0; i < 2; ++i) {
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode, kThreads, smem_bytes(i == 1));
+            if (e != cudaSuccess) return static_cast<int>(e);
+            di.ctas_per_sm[i] = n > 0 ? n : 1;
+        }
+        di.sms = sms;
+    }
+    const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(di.ctas_per_sm[tab ? 1 : 0]);
+    const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
+    k_decode<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream) {
+    for (int i0 = 0; i0 < n; i0 += kUploadChunk) {
+        UploadParams up;
+        up.dst = dst + i0;
+        up.n = (n - i0) < kUploadChunk ? (n - i0) : kUploadChunk;
+        for (int i = 0; i < up.n; ++i) up.d[i] = src[i0 + i];
+        k_upload_table<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(up);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return static_cast<int>(e);
+    }
+    return 0;
+}
+
+int read_fault(uint32_t* flags) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    *flags = v;
+    return 0;
+}
+
+}  // namespace ndq

@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA decode (through the C ABI) against the CPU oracle,
+bit for bit (0 ULP in FP32 and after the single RNE cast; NaN only needs to
+be NaN), on seeded synthetic payloads.  Sizes span several 8192-element
+tiles with a ragged last tile; edge cases cover unaligned payload/output
+pointers, empty tensors, rank 1 and rank 3, several nvfp4 divisors, every
+special scale byte, and batched launches mixing formats and output types."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_bit_exact
+
+pytestmark = pytest.mark.gpu
+
+import quantized_weight_block_gb300 as ndq  # noqa: E402
+
+FORMATS = ["gguf:q8_0", "q8_g32_fp16", "gguf:q4_0", "gguf:iq4_nl", "gguf:q4_k", "gguf:q6_k",
+           "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16"]
+OUTS = ["float32", "float16", "bfloat16", "float64"]
+TORCH_OUT = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16,
+             "float64": torch.float64}
+DEV = "cuda"
+
+
+def ragged_shape(fmt, rows=3):
+    B, _ = synth.GEOMETRY[fmt]
+    # about 11.7 tiles of 8192 elements in total over `rows` rows, not a multiple of a tile
+    per_row = (8192 * 11 + 5 * 8192 // 7) // rows // B * B
+    return (rows, per_row)
+
+
+def gpu_decode(fmt, shape, x_np, out, x_offset=0, y_offset=0):
+    """Decode through the C ABI; offsets (bytes / elements) misalign x / y."""
+    xs = torch.zeros(x_np.size + x_offset + 16, dtype=torch.uint8, device=DEV)
+    xs[x_offset:x_offset + x_np.size] = torch.from_numpy(x_np).to(DEV)
+    x = xs[x_offset:x_offset + x_np.size]
+    n = int(np.prod(shape, dtype=np.int64))
+    ybuf = torch.full((n + y_offset + 8,), float("nan"), dtype=TORCH_OUT[out], device=DEV)
+    y = ybuf[y_offset:y_offset + n]
+    rc = ndq.ndq_dequantize_packed(ndq.format_id(fmt), shape, ndq.out_dtype_code(TORCH_OUT[out]),
+                                   x.data_ptr(), x_np.size, y.data_ptr(),
+                                   torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, ndq.ndq_status_string(rc)
+    torch.cuda.synchronize()
+    # guard elements around y are untouched
+    if y_offset:
+        assert torch.isnan(ybuf[:y_offset].float()).all()
+    assert torch.isnan(ybuf[y_offset + n:].float()).all()
+    return y.cpu().view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_fault():
+    yield
+    assert ndq.get_device_fault() == 0
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("out", OUTS)
+@pytest.mark.parametrize("dist", ["workload", "bytes"])
+def test_parity_ragged(orc, fmt, out, dist):
+    shape = ragged_shape(fmt)
+    x = synth.payload(fmt, shape, seed=zlib.crc32(f"{fmt}/{dist}".encode()) % 1000, dist=dist)
+    want = orc.decode(fmt, shape, x, out)
+    got = gpu_decode(fmt, shape, x, out)
+    assert_bit_exact(got, want, out, f"{fmt} {out} {dist}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("x_off,y_off", [(1, 0), (3, 1), (8, 3), (0, 1), (5, 4)])
+def test_parity_unaligned_pointers(orc, fmt, x_off, y_off):
+    shape = ragged_shape(fmt, rows=2)
+    x = synth.payload(fmt, shape, seed=17, dist="bytes")
+    for out in ("bfloat16", "float32"):
+        want = orc.decode(fmt, shape, x, out)
+        got = gpu_decode(fmt, shape, x, out, x_offset=x_off, y_offset=y_off)
+        assert_bit_exact(got, want, out, f"{fmt} {out} x+{x_off} y+{y_off}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_parity_small_and_odd_shapes(orc, fmt):
+    B, _ = synth.GEOMETRY[fmt]
+    for shape in [(B,), (1, B), (2, 3, 2 * B), (1, 8192 // B * B), (1, 8192 + B), (5, 3 * B), (8192 // B + 1, B)]:
+        if fmt == "nvfp4" and len(shape) == 1:
+            shape = (1, B)
+        x = synth.payload(fmt, shape, seed=3, dist="bytes")
+        for out in ("float32", "bfloat16"):
+            assert_bit_exact(gpu_decode(fmt, shape, x, out), orc.decode(fmt, shape, x, out), out, f"{fmt} {shape}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_empty_tensors(fmt):
+    B, _ = synth.GEOMETRY[fmt]
+    for shape in [(0, B), (4, 0), (0,)]:
+        y = torch.empty(0, dtype=torch.bfloat16, device=DEV)
+        rc = ndq.ndq_dequantize_packed(ndq.format_id(fmt), shape, ndq.NDQ_BFLOAT16, 0, 0, y.data_ptr() or 0, 0)
+        assert rc == 0
+
+
+@pytest.mark.parametrize("ndiv,rows", [(1, 6), (2, 6), (3, 6), (6, 6), (7, 21), (5, 640)])
+def test_nvfp4_divisors(orc, ndiv, rows):
+    shape = (rows, 64 * 45)  # 45 blocks per row: tiles straddle rows and divisors
+    x = synth.payload("nvfp4", shape, seed=ndiv, dist="workload", ndiv=ndiv)
+    for out in ("float32", "bfloat16"):
+        assert_bit_exact(gpu_decode("nvfp4", shape, x, out), orc.decode("nvfp4", shape, x, out), out,
+                         f"nvfp4 D={ndiv}")
+
+
+def test_nvfp4_every_scale_code_pair(orc):
+    # 256 scale bytes x 16 codes, divisors that exercise rounding
+    codes = np.array([(c | ((15 - c) << 4)) for c in range(8)] * 4, np.uint8)  # all 16 codes per group
+    blocks = []
+    for s in range(256):
+        blocks.append(np.concatenate([np.full(4, s, np.uint8), codes]))
+    blk = np.concatenate(blocks)
+    for dw in (1.0, 26880.0, 3.0, 1e-30, 3e38):
+        x = np.concatenate([blk, np.array([dw], "<f4").view(np.uint8)])
+        assert_bit_exact(gpu_decode("nvfp4", (256, 64), x, "float32"), orc.decode("nvfp4", (256, 64), x, "float32"),
+                         "float32", f"dw={dw}")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:mxfp4", "gguf:nvfp4"])
+def test_every_scale_byte(orc, fmt):
+    B, S = synth.GEOMETRY[fmt]
+    nsc = 1 if fmt == "gguf:mxfp4" else 4
+    codes = np.array([(c | ((15 - c) << 4)) for c in range(8)] * ((S - nsc) // 8), np.uint8)
+    x = np.concatenate([np.concatenate([np.full(nsc, s, np.uint8), codes]) for s in range(256)])
+    for out in OUTS:
+        assert_bit_exact(gpu_decode(fmt, (256, B), x, out), orc.decode(fmt, (256, B), x, out), out, fmt)
+
+
+def test_special_binary16_scales(orc):
+    # every binary16 scale pattern class: zeros, subnormals, max, inf, NaN
+    specials = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x7C01,
+                         0x3C00, 0xBC00], np.uint16)
+    for fmt in ("gguf:q8_0", "gguf:q4_0", "gguf:iq4_nl", "q4_g64_fp16", "gguf:q4_k", "gguf:q6_k"):
+        B, S = synth.GEOMETRY[fmt]
+        nb = len(specials) ** 2
+        x = synth.payload(fmt, (nb, B), seed=5, dist="bytes").reshape(nb, S).copy()
+        a, b = np.meshgrid(specials, specials)
+        offs = {"gguf:q4_k": (0, 2), "gguf:q6_k": (208, 208)}.get(fmt, (0, 0))
+        x[:, offs[0]:offs[0] + 2] = a.reshape(-1, 1).view(np.uint8).reshape(nb, 2)
+        if fmt == "gguf:q4_k":
+            x[:, 2:4] = b.reshape(-1, 1).view(np.uint8).reshape(nb, 2)
+        x = x.reshape(-1)
+        for out in OUTS:
+            assert_bit_exact(gpu_decode(fmt, (nb, B), x, out), orc.decode(fmt, (nb, B), x, out), out, fmt)
+
+
+def test_batched_mixed(orc):
+    specs = []
+    rng = np.random.default_rng(0)
+    for i, fmt in enumerate(FORMATS * 2):
+        B, _ = synth.GEOMETRY[fmt]
+        rows = int(rng.integers(1, 9))
+        k = int(rng.integers(1, 40)) * B
+        out = OUTS[i % 4]
+        specs.append((fmt, (rows, k), out, synth.payload(fmt, (rows, k), seed=200 + i, dist="bytes")))
+    specs.insert(3, ("gguf:q4_k", (0, 256), "bfloat16", np.zeros(0, np.uint8)))  # empty entry
+    items, ys = [], []
+    for fmt, shape, out, x in specs:
+        xt = torch.from_numpy(x).to(DEV) if x.size else torch.empty(0, dtype=torch.uint8, device=DEV)
+        y = torch.empty(shape, dtype=TORCH_OUT[out], device=DEV)
+        items.append((fmt, shape, xt, y))
+        ys.append(y)
+    ws = ndq.dequantize_packed_batched(items)
+    torch.cuda.synchronize()
+    del ws
+    for (fmt, shape, out, x), y in zip(specs, ys):
+        if not x.size:
+            continue
+        got = y.cpu().view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
+        assert_bit_exact(got, orc.decode(fmt, shape, x, out), out, f"batched {fmt} {out}")
+
+
+def test_repeat_is_deterministic():
+    fmt, shape = "gguf:q6_k", (64, 4096)
+    x = torch.from_numpy(synth.payload(fmt, shape, seed=1)).to(DEV)
+    a = ndq.dequantize_packed(fmt, shape, x, torch.bfloat16)
+    b = ndq.dequantize_packed(fmt, shape, x, torch.bfloat16)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---- full-size workloads: sampled blocks against the oracle --------------
+def _sample_blocks(nb, rng, k=1500):
+    idx = np.unique(np.concatenate([rng.integers(0, nb, size=k), [0, 1, nb - 1, nb - 2],
+                                    np.arange(0, nb, max(1, nb // 50))]))
+    return idx[idx < nb]
+
+
+def check_sampled(orc, fmt, shape, x_np, y_t, out, seed=0):
+    B, _ = synth.GEOMETRY[fmt]
+    nb = int(np.prod(shape[:-1], dtype=np.int64)) * (shape[-1] // B)
+    rng = np.random.default_rng(seed)
+    idx = _sample_blocks(nb, rng)
+    yflat = y_t.reshape(-1)
+    got_rows = yflat.view(-1, B)[torch.from_numpy(idx).to(yflat.device)].cpu()
+    got = got_rows.view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
+    want = np.stack([orc.decode_range(fmt, shape, x_np, int(b), int(b) + 1, out) for b in idx])
+    assert_bit_exact(got, want, out, f"{fmt} {shape} sampled")
+
+
+@pytest.mark.parametrize("label,fmt,shape,seed,out", synth.WORKLOADS)
+def test_full_size_workloads_sampled(orc, label, fmt, shape, seed, out):
+    x = synth.payload(fmt, shape, seed)
+    y = ndq.dequantize_packed(fmt, shape, torch.from_numpy(x).to(DEV), TORCH_OUT[out])
+    torch.cuda.synchronize()
+    check_sampled(orc, fmt, shape, x, y, out, seed)
+    if int(np.prod(shape)) <= 1 << 24:  # small enough for the whole-output check
+        got = y.cpu().view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
+        assert_bit_exact(got, orc.decode(fmt, shape, x, out), out, label)
+
+
+def test_whole_model_batched_sampled(orc):
+    """The whole-model workload in the launch configuration the benchmark
+    times (one batched launch over 225 tensors), sampled per tensor."""
+    specs = synth.llama3_8b_tensors()
+    xs_np, items = [], []
+    for s in specs:
+        x = synth.payload(s.fmt, s.shape, s.seed)
+        xs_np.append(x)
+        items.append((s.fmt, s.shape, torch.from_numpy(x).to(DEV),
+                      torch.empty(s.shape, dtype=torch.bfloat16, device=DEV)))
+    ws = ndq.dequantize_packed_batched(items)
+    torch.cuda.synchronize()
+    del ws
+    for i in list(range(0, len(specs), 7)) + [len(specs) - 1]:
+        s = specs[i]
+        check_sampled(orc, s.fmt, s.shape, xs_np[i], items[i][3], "bfloat16", seed=i)
