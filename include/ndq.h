@@ -48,6 +48,7 @@ extern "C" {
 #define NDQ_ERR_CUDA 11              /* a CUDA runtime call or launch failed */
 #define NDQ_ERR_DEVICE_FAULT 12      /* a kernel gave up on a bounded wait */
 #define NDQ_ERR_BAD_COUNT 13         /* batched tensor count < 0 */
+#define NDQ_ERR_TOO_MANY_TENSORS 14  /* no-allocation batch larger than its table */
 
 /* Output element types: the ONNX TensorProto data-type numbers of the four
  * output types DequantizePacked supports ("Signature and storage"). */
@@ -192,6 +193,37 @@ size_t ndq_batched_workspace_bytes(int n);
  * whose tensors are all empty, returns NDQ_OK without a launch. */
 int ndq_dequantize_packed_batched(const ndq_tensor_desc *descs, int n, void *workspace,
                                   size_t ws_bytes, void *stream);
+
+/* Largest batch the no-allocation variant below accepts. */
+#define NDQ_NOALLOC_MAX_TENSORS 1024
+
+/* Batched decode for callers that cannot allocate device memory.  (There is
+ * no counterpart on the pages: this is a convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc or any other allocator: a plain C or
+ * plugin host embedded in a process whose device memory is reserved up front
+ * by another framework's pool, or a runtime with a fixed memory budget, where
+ * an extra allocation would fail, fragment the pool or synchronize the
+ * device.  For them this entry point does the same work as
+ * ndq_dequantize_packed_batched without a workspace argument: the launch
+ * table is kept in a fixed device array inside the library (room for
+ * NDQ_NOALLOC_MAX_TENSORS non-empty tensors, 64 bytes each, i.e. 64 KiB that
+ * every GPU which loads the library holds until the process exits).  The
+ * caller still passes every input and output (descs[i].x and descs[i].y).
+ *   descs   host array of n descriptors (same meaning as for the batched
+ *           call), read during the call only
+ *   stream  cudaStream_t to enqueue on (NULL = legacy default stream)
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  The first call on a device looks up the array's device address
+ * with cudaGetSymbolAddress while that device is current; make that first
+ * call before any stream capture.  Every call rewrites the part of the table
+ * it uses, and the array keeps the last call's contents; calls whose work may
+ * overlap on the GPU (different streams or host threads without ordering)
+ * share the array and race, so order them on one stream.
+ * Errors: n > NDQ_NOALLOC_MAX_TENSORS returns NDQ_ERR_TOO_MANY_TENSORS before
+ * anything is enqueued; n < 0 returns NDQ_ERR_BAD_COUNT; otherwise the same
+ * validation and errors as ndq_dequantize_packed_batched (minus workspace). */
+int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc *descs, int n, void *stream);
 
 /* Read and clear the library's device fault word on the current device.
  * A kernel sets a nonzero bit when one of its bounded waits for staged

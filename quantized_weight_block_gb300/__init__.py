@@ -29,11 +29,12 @@ STATUS = {
     0: "NDQ_OK", 1: "NDQ_ERR_NULL", 2: "NDQ_ERR_UNKNOWN_FORMAT", 3: "NDQ_ERR_UNSUPPORTED_FORMAT",
     4: "NDQ_ERR_BAD_RANK", 5: "NDQ_ERR_NEGATIVE_DIM", 6: "NDQ_ERR_NOT_BLOCK_ALIGNED",
     7: "NDQ_ERR_LENGTH_MISMATCH", 8: "NDQ_ERR_OVERFLOW", 9: "NDQ_ERR_BAD_DTYPE", 10: "NDQ_ERR_WORKSPACE",
-    11: "NDQ_ERR_CUDA", 12: "NDQ_ERR_DEVICE_FAULT", 13: "NDQ_ERR_BAD_COUNT",
+    11: "NDQ_ERR_CUDA", 12: "NDQ_ERR_DEVICE_FAULT", 13: "NDQ_ERR_BAD_COUNT", 14: "NDQ_ERR_TOO_MANY_TENSORS",
 }
 NDQ_FLOAT, NDQ_FLOAT16, NDQ_DOUBLE, NDQ_BFLOAT16 = 1, 10, 11, 16
 NDQ_MAX_RANK = 8
 NDQ_NUM_FORMATS = 30
+NDQ_NOALLOC_MAX_TENSORS = 1024
 
 
 class NdqError(RuntimeError):
@@ -70,12 +71,13 @@ _lib.ndq_batched_workspace_bytes.restype = _c.c_size_t
 _lib.ndq_dequantize_packed_batched.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p, _c.c_size_t,
                                                _c.c_void_p]
 _lib.ndq_get_device_fault.argtypes = [_c.POINTER(_c.c_uint32)]
+_lib.ndq_dequantize_packed_batched_noalloc.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p]
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = (
     "ndq_format_from_name", "ndq_format_name", "ndq_format_geometry", "ndq_format_supported",
     "ndq_status_string", "ndq_payload_geometry", "ndq_dequantize_packed", "ndq_batched_workspace_bytes",
-    "ndq_dequantize_packed_batched", "ndq_get_device_fault",
+    "ndq_dequantize_packed_batched", "ndq_get_device_fault", "ndq_dequantize_packed_batched_noalloc",
 )
 
 
@@ -134,6 +136,13 @@ def ndq_dequantize_packed_batched(descs, workspace_ptr: int, ws_bytes: int, stre
     """Raw call over a sequence of ndq_tensor_desc; returns the status code."""
     arr = (ndq_tensor_desc * max(1, len(descs)))(*descs)
     return _lib.ndq_dequantize_packed_batched(arr, len(descs), workspace_ptr, ws_bytes, stream)
+
+
+def ndq_dequantize_packed_batched_noalloc(descs, stream: int = 0) -> int:
+    """Raw call of the no-allocation batched decode (launch table held in the
+    library's own device array); returns the status code."""
+    arr = (ndq_tensor_desc * max(1, len(descs)))(*descs)
+    return _lib.ndq_dequantize_packed_batched_noalloc(arr, len(descs), stream)
 
 
 def ndq_get_device_fault() -> int:

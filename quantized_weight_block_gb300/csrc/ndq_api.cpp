@@ -17,6 +17,8 @@
 #include "ndq.h"
 #include "ndq_internal.h"
 
+static_assert(NDQ_NOALLOC_MAX_TENSORS == ndq::kNoAllocMaxTensors, "no-allocation table size");
+
 namespace {
 
 struct FormatRow {
@@ -189,6 +191,7 @@ const char* ndq_status_string(int status) {
         case NDQ_ERR_CUDA: return "CUDA error";
         case NDQ_ERR_DEVICE_FAULT: return "device fault (bounded wait expired)";
         case NDQ_ERR_BAD_COUNT: return "bad tensor count";
+        case NDQ_ERR_TOO_MANY_TENSORS: return "more tensors than the no-allocation launch table holds";
         default: return "unknown status";
     }
 }
@@ -260,6 +263,31 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* wor
     p.any_nvfp4 = any_nvfp4;
     p.total_tiles = tiles;
     return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+}
+
+int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc* descs, int n, void* stream) {
+    if (n < 0) return NDQ_ERR_BAD_COUNT;
+    if (n > NDQ_NOALLOC_MAX_TENSORS) return NDQ_ERR_TOO_MANY_TENSORS;
+    if (n == 0) return NDQ_OK;
+    if (!descs) return NDQ_ERR_NULL;
+    ndq::DevTensor table[NDQ_NOALLOC_MAX_TENSORS];  // host stack, 64 KiB
+    int count = 0;
+    uint64_t tiles = 0;
+    int any_nvfp4 = 0;
+    for (int i = 0; i < n; ++i) {
+        const ndq_tensor_desc& d = descs[i];
+        ndq::DevTensor t;
+        Geometry g;
+        const int rc = prepare(d.format_id, d.shape, d.ndim, d.out_dtype, d.x, d.x_len, d.y, &t, &g);
+        if (rc != NDQ_OK) return rc;
+        if (g.nblocks == 0) continue;
+        t.tile_begin = tiles;
+        tiles += tiles_of(t);
+        any_nvfp4 |= t.fmt == ndq::KF_NVFP4;
+        table[count++] = t;
+    }
+    if (count == 0) return NDQ_OK;
+    return ndq::launch_batched_noalloc(table, count, tiles, any_nvfp4, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
 
 int ndq_get_device_fault(uint32_t* flags) {

@@ -69,6 +69,15 @@ int launch_decode(const KParams& p, void* stream);
 // `stream` (no host-blocking copy).  Returns 0 or a CUDA error code.
 int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream);
 
+// Capacity of the library-owned launch table of the no-allocation batched
+// call (64 bytes per entry: 64 KiB per device).
+constexpr int kNoAllocMaxTensors = 1024;
+
+// Batched decode whose launch table lives in the library's own static device
+// array instead of a caller workspace.  `table` is host memory (n entries,
+// tile_begin set).  Returns 0 or a CUDA error code.
+int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int any_nvfp4, void* stream);
+
 // Read and clear the device fault word of the current device.
 int read_fault(uint32_t* flags);
 

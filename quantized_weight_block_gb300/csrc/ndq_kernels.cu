@@ -751,6 +751,47 @@ int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream) {
     return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Batched decode without any device allocation by the caller: the launch
+// table lives in a fixed file-scope device array (kNoAllocMaxTensors entries,
+// 64 KiB) that every GPU which loads this library holds until process exit.
+// The host cannot use the array's name as a device address, so its address
+// is looked up once per device with cudaGetSymbolAddress while that device is
+// current.  Every call overwrites entries [0, n) before the decode launch on
+// the same stream; nothing has to start at zero because the decode reads only
+// the n entries this call wrote.  Calls whose work overlaps on the GPU (other
+// streams, other host threads) share the array and race.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) DevTensor g_noalloc_table[kNoAllocMaxTensors];
+
+namespace {
+DevTensor* g_noalloc_addr[kMaxDevices];  // per-device address, set once
+}
+
+int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int any_nvfp4, void* stream) {
+    if (n < 1 || n > kNoAllocMaxTensors) return static_cast<int>(cudaErrorInvalidValue);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+    if (!g_noalloc_addr[dev]) {  // first call on this device: resolve the symbol
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_noalloc_table);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        g_noalloc_addr[dev] = static_cast<DevTensor*>(addr);
+    }
+    DevTensor* dev_table = g_noalloc_addr[dev];
+    const int rc = upload_table(dev_table, table, n, stream);
+    if (rc != 0) return rc;
+    KParams p;
+    p.single = table[0];
+    p.table = dev_table;
+    p.n = n;
+    p.any_nvfp4 = any_nvfp4;
+    p.total_tiles = total_tiles;
+    return launch_decode(p, stream);
+}
+
 int read_fault(uint32_t* flags) {
     unsigned int v = 0, zero = 0;
     cudaError_t e = cudaDeviceSynchronize();
