@@ -62,6 +62,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-fraction", type=int, default=1,
                     help="CPU baseline decodes 1/N of every tensor's blocks")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="decoder layers of the model workload (profiling runs use fewer)")
+    ap.add_argument("--no-embedding", action="store_true", help="leave the embedding out of the model workload")
+    ap.add_argument("--only", default=None,
+                    help="time one single-format workload (a label of synth.WORKLOADS) for --steps steps and exit")
     return ap.parse_args()
 
 
@@ -231,7 +236,8 @@ def profiled_traffic(profile_name: str):
 
 def time_single_workloads(torch, ndq, stream, peak):
     """Single-format workloads, L2 flushed before every repetition."""
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    flush_sink = torch.empty((), dtype=torch.uint8, device="cuda")
     out = {}
     tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}
     for label, fmt, shape, seed, od in synth.WORKLOADS:
@@ -242,7 +248,10 @@ def time_single_workloads(torch, ndq, stream, peak):
             ndq.dequantize_packed(fmt, shape, x, tdt[od], y=y)
         times = []
         for _ in range(20):
-            flush.fill_(1)
+            # Evict the previous repetition's lines by reading 512 MB: L2 is left
+            # full of clean lines, so no write-back of a flush lands on the
+            # timed kernel.
+            flush_sink.copy_(flush.max())
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -256,10 +265,37 @@ def time_single_workloads(torch, ndq, stream, peak):
         out[label] = {"ms": round(ms, 5), "ms_best": round(min(times), 5), "GB/s": round(gbs, 1),
                       "elements/s": float(f"{y.numel() / (ms * 1e-3):.4g}"),
                       "frac_of_8TBs": round(gbs / 8000.0, 4), "frac_of_measured": round(gbs / peak, 4),
-                      "bytes": nbytes, "l2": "flushed (512 MB write) before each repetition"}
+                      "bytes": nbytes, "l2": "evicted before each repetition (512 MB read)"}
         del x, y
-    del flush
+    del flush, flush_sink
     return out
+
+
+def run_only(args, torch, ndq):
+    """One single-format workload, --warmup untimed then --steps timed
+    launches (used for focused profiling of one format)."""
+    match = [w for w in synth.WORKLOADS if w[0] == args.only]
+    if not match:
+        raise SystemExit(f"unknown workload {args.only!r}; choose from {[w[0] for w in synth.WORKLOADS]}")
+    label, fmt, shape, seed, od = match[0]
+    tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}[od]
+    x_np = synth.payload(fmt, shape, seed)
+    x = torch.from_numpy(x_np).cuda()
+    y = torch.empty(shape, dtype=tdt, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ndq.dequantize_packed(fmt, shape, x, tdt, y=y)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        ndq.dequantize_packed(fmt, shape, x, tdt, y=y)
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    nbytes = x_np.size + y.numel() * y.element_size()
+    print(json.dumps({"workload": label, "ms_per_step": round(ms, 5), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "steps": args.steps, "l2": "back-to-back launches (no flush)"}), flush=True)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -273,7 +309,13 @@ def run_ours(args, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     peak, peak_src = measured_peaks()
-    work = ModelWorkload(synth.llama3_8b_tensors())
+    if args.only:
+        return run_only(args, torch, ndq)
+    specs = synth.llama3_8b_tensors()
+    if args.layers != 32 or args.no_embedding:
+        specs = [t for t in specs if (t.name.startswith("layers.") and int(t.name.split(".")[1]) < args.layers)
+                 or (t.name == "embed" and not args.no_embedding)]
+    work = ModelWorkload(specs)
 
     # host payloads (pinned, for the end-to-end leg and the CPU baseline)
     x_host = torch.empty(work.x_total, dtype=torch.uint8, pin_memory=True)

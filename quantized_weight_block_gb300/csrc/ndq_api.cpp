@@ -218,7 +218,7 @@ int ndq_dequantize_packed(int format_id, const int64_t* shape, int ndim, int out
     p.single.tile_begin = 0;
     p.table = nullptr;
     p.n = 1;
-    p.any_nvfp4 = p.single.fmt == ndq::KF_NVFP4;
+    p.nv_index = p.single.fmt == ndq::KF_NVFP4 ? 0 : -1;
     p.total_tiles = tiles_of(p.single);
     return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
@@ -237,7 +237,7 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* wor
     std::vector<ndq::DevTensor> table;
     table.reserve(static_cast<size_t>(n));
     uint64_t tiles = 0;
-    int any_nvfp4 = 0;
+    int nv_index = -1;
     for (int i = 0; i < n; ++i) {
         const ndq_tensor_desc& d = descs[i];
         ndq::DevTensor t;
@@ -247,7 +247,7 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* wor
         if (g.nblocks == 0) continue;
         t.tile_begin = tiles;
         tiles += tiles_of(t);
-        any_nvfp4 |= t.fmt == ndq::KF_NVFP4;
+        if (nv_index < 0 && t.fmt == ndq::KF_NVFP4) nv_index = static_cast<int>(table.size());
         table.push_back(t);
     }
     if (table.empty()) return NDQ_OK;
@@ -260,7 +260,7 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* wor
     std::memset(&p, 0, sizeof(p));
     p.table = dev_table;
     p.n = static_cast<int32_t>(table.size());
-    p.any_nvfp4 = any_nvfp4;
+    p.nv_index = nv_index;
     p.total_tiles = tiles;
     return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
@@ -273,7 +273,7 @@ int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc* descs, int n, v
     ndq::DevTensor table[NDQ_NOALLOC_MAX_TENSORS];  // host stack, 64 KiB
     int count = 0;
     uint64_t tiles = 0;
-    int any_nvfp4 = 0;
+    int nv_index = -1;
     for (int i = 0; i < n; ++i) {
         const ndq_tensor_desc& d = descs[i];
         ndq::DevTensor t;
@@ -283,11 +283,11 @@ int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc* descs, int n, v
         if (g.nblocks == 0) continue;
         t.tile_begin = tiles;
         tiles += tiles_of(t);
-        any_nvfp4 |= t.fmt == ndq::KF_NVFP4;
+        if (nv_index < 0 && t.fmt == ndq::KF_NVFP4) nv_index = count;
         table[count++] = t;
     }
     if (count == 0) return NDQ_OK;
-    return ndq::launch_batched_noalloc(table, count, tiles, any_nvfp4, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    return ndq::launch_batched_noalloc(table, count, tiles, nv_index, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
 
 int ndq_get_device_fault(uint32_t* flags) {

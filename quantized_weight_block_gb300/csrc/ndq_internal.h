@@ -57,7 +57,7 @@ struct KParams {
     DevTensor single;
     const DevTensor* table;
     int32_t n;
-    int32_t any_nvfp4;
+    int32_t nv_index;  // first nvfp4 tensor of the launch (its divisor seeds the quotient table), or -1
     uint64_t total_tiles;
 };
 
@@ -76,7 +76,7 @@ constexpr int kNoAllocMaxTensors = 1024;
 // Batched decode whose launch table lives in the library's own static device
 // array instead of a caller workspace.  `table` is host memory (n entries,
 // tile_begin set).  Returns 0 or a CUDA error code.
-int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int any_nvfp4, void* stream);
+int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int nv_index, void* stream);
 
 // Read and clear the device fault word of the current device.
 int read_fault(uint32_t* flags);

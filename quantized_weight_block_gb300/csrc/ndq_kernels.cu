@@ -6,16 +6,21 @@
 //
 //  * persistent CTAs (a grid of SMs x resident CTAs) walk a global list of
 //    8192-element tiles that spans one tensor or a whole batch of tensors;
-//  * each tile's payload bytes (a contiguous span, a multiple of 16 bytes)
-//    are staged into shared memory by the Tensor Memory Accelerator with
-//    cp.async.bulk, completing on an mbarrier, through a ring of kStages
-//    buffers issued by one thread, so that loads for the next tiles are in
-//    flight while the current tile decodes;
-//  * every thread decodes 8-element chunks straight from shared memory (the
-//    odd block strides of 17, 18, 34, 36 and 210 bytes are resolved with
-//    aligned 32-bit shared loads and funnel shifts) and writes each chunk
-//    with 16-byte vector stores, so a warp writes 512 contiguous bytes per
-//    instruction;
+//  * one producer warp per CTA stages each tile's payload bytes (one
+//    contiguous span) into shared memory with the Tensor Memory Accelerator
+//    (cp.async.bulk, completing on a "full" mbarrier), running up to kStages
+//    tiles ahead; it copies the tile's tensor descriptor next to the bytes;
+//  * eight consumer warps decode 8-element chunks straight from shared
+//    memory (the odd block strides of 17, 18, 34, 36 and 210 bytes are
+//    resolved with aligned 32-bit shared loads and funnel shifts), write
+//    each chunk with 16-byte vector stores (a warp covers 512 contiguous
+//    bytes per instruction), and release the stage on an "empty" mbarrier.
+//    Consumers never meet at a CTA-wide barrier inside the loop;
+//  * a span that does not start on a 16-byte boundary (an unaligned payload,
+//    a ragged last tile) is staged from the 16-byte boundary below it to the
+//    one above its end, and decoded at its byte phase within the stage; the
+//    extra bytes lie in the same 16-byte lines as payload bytes, hence in
+//    mapped memory;
 //  * all arithmetic follows the ONNX "DequantizePacked decoding
 //    specification" ("Decoding algorithms": every M/A/D rounded separately
 //    to binary32, round-to-nearest-even), with explicit __fmul_rn /
@@ -25,9 +30,10 @@
 //    mantissa of 2^23, minus 2^23 plus the code offset), never through a
 //    rounding conversion.
 //
-// Every wait on an mbarrier is bounded by the global timer; on expiry the CTA
-// records a fault bit, waits (bounded) for its own copies in flight and
-// returns, so that a lost copy cannot hang the GPU.
+// Every mbarrier wait is bounded by the global timer; on expiry the warp
+// records a fault bit and stops, and the producer waits (bounded) for the
+// copies it still has in flight before it exits, so a lost copy cannot hang
+// the GPU.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,29 +50,36 @@ __device__ unsigned int g_fault_word;
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kInStride = 8832;  // kMaxTileBytes + over-read pad, multiple of 128
+constexpr int kConsumerWarps = kThreads / 32;     // 8
+constexpr int kBlockThreads = kThreads + 32;      // consumers + one producer warp
+constexpr int kInStride = 8832;                   // tile bytes + phase + rounding + over-read
 constexpr int kChunksPerThread = kTileElems / 8 / kThreads;  // 4
 constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
 constexpr int kTabEntries = 256 * 8;                         // nvfp4 quotient table
 
-static_assert(kInStride >= kMaxTileBytes + 16, "over-read pad");
+static_assert(kInStride >= kMaxTileBytes + 15 + 15 + 12, "stage size");
 static_assert(kInStride % 128 == 0, "stage alignment");
 
+// Written by the producer before it arms the stage's full barrier.
 struct StageInfo {
-    uint64_t block0;  // first block of the tile within its tensor
+    DevTensor t;      // the tile's tensor
+    uint64_t block0;  // first block of the tile within the tensor
     uint32_t nb;      // blocks in the tile
-    int32_t desc;     // tensor index
-    int32_t coop;     // 1: bytes are loaded by the CTA's threads, not TMA
-    int32_t pad;
+    uint32_t phase;   // byte offset of the first block within the stage (0..15)
+    uint32_t nv_tab;  // nvfp4: the whole tile uses the divisor the shared table was built for
+    uint32_t pad[11];
 };
+static_assert(sizeof(StageInfo) == 128, "StageInfo layout");
 
 struct SmemHdr {
-    uint64_t mbar[kStages];
-    StageInfo info[kStages];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
     float lut_iq4[16];  // IQ4_NL table ("Packed layouts and decoding")
     float lut_v[16];    // doubled E2M1 table V ("Ternary and block-floating formats")
     uint32_t tab_bits;  // divisor bits the nvfp4 table was built for
     int32_t tab_valid;
+    int32_t pad[30];
+    StageInfo info[kStages];
 };
 
 constexpr int kHdrBytes = (sizeof(SmemHdr) + 127) / 128 * 128;
@@ -75,7 +88,7 @@ __constant__ int8_t c_iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13
 __constant__ int8_t c_v[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
 
 // ---------------------------------------------------------------------------
-// PTX wrappers: mbarrier, bulk copy, proxy fence, global timer.
+// PTX wrappers: mbarrier, bulk copy, global timer.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -134,20 +147,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory accesses before later
-// async-proxy (TMA) accesses.
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Shared-memory byte access and exact scalar constructions.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint16_t lds_u16(const uint8_t* p) {  // p even
-    return *reinterpret_cast<const uint16_t*>(p);
+// 16-bit little-endian field at byte offset `off` of a 16-byte-aligned stage.
+// With PH (a stage decoded at a nonzero byte phase) the field may be
+// unaligned.
+template <bool PH>
+__device__ __forceinline__ uint32_t lds_2(const uint8_t* base, uint32_t off) {
+    if (PH) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+        return __funnelshift_r(w[0], w[1], (off & 3u) * 8u) & 0xffffu;
+    }
+    return *reinterpret_cast<const uint16_t*>(base + off);
 }
 
-// 8 bytes at byte offset `off` of a 16-byte-aligned shared buffer.
+// 8 bytes at byte offset `off` of a 16-byte-aligned stage.
 __device__ __forceinline__ uint2 lds_8(const uint8_t* base, uint32_t off) {
     const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
     const uint32_t sh = (off & 3u) * 8u;
@@ -162,7 +177,9 @@ __device__ __forceinline__ uint32_t lds_4(const uint8_t* base, uint32_t off) {
 }
 
 // Exact binary16 -> binary32 (the specification's H).
-__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ float h2f(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
 
 // Byte I of w (0..255) as the float 2^23 + byte, minus `bias`: exact for the
 // small integers involved (bias = 2^23 + code offset).
@@ -218,12 +235,14 @@ __device__ __forceinline__ float load_f32_bytes(const uint8_t* p) {
 
 // ---------------------------------------------------------------------------
 // Per-format chunk decoders: chunk c of a tile = output elements 8c..8c+7 of
-// the tile, produced from the tile's payload bytes `in` (shared memory).
+// the tile, produced from the tile's payload bytes staged at `in` (byte
+// phase `ph`: the tile's first block starts at in + ph).
 // ---------------------------------------------------------------------------
-struct NvCtx {
-    const float* tab;        // quotient table, or nullptr for per-element division
-    const uint8_t* divs;     // divisor words (per-element path)
-    uint64_t block0;         // first block of the tile
+struct Ctx {
+    const SmemHdr* H;
+    const float* tab;  // nvfp4 quotient table, or nullptr for per-element division
+    const uint8_t* divs;
+    uint64_t block0;
     uint64_t blocks_per_div;
 };
 
@@ -234,10 +253,10 @@ struct Fmt;
 template <>
 struct Fmt<KF_Q8_0> {
     static constexpr int B = 32, S = 34, CPB = 4;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 2) * S;
-        const float d = h2f(lds_u16(in + off));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 2) * S;
+        const float d = h2f(lds_2<PH>(in, off));
         const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
         const uint32_t a = q.x ^ 0x80808080u, b = q.y ^ 0x80808080u;  // signed -> offset-128
         const float bias = 8388736.0f;                                 // 2^23 + 128
@@ -263,10 +282,10 @@ __device__ __forceinline__ void nib_plane(uint2 q, uint32_t p, uint32_t& a, uint
 template <>
 struct Fmt<KF_Q4_0> {
     static constexpr int B = 32, S = 18, CPB = 4;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 2) * S, cc = c & 3u;
-        const float d = h2f(lds_u16(in + off));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_2<PH>(in, off));
         uint32_t a, b;
         nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
         const float bias = 8388616.0f;  // 2^23 + 8
@@ -294,13 +313,14 @@ __device__ __forceinline__ void lut8(const float* T, float d, uint32_t a, uint32
 template <>
 struct Fmt<KF_IQ4_NL> {
     static constexpr int B = 32, S = 18, CPB = 4;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 2) * S, cc = c & 3u;
-        const float d = h2f(lds_u16(in + off));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_2<PH>(in, off));
         uint32_t a, b;
         nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(H.lut_iq4, d, a, b, v);
+        lut8(x.H->lut_iq4, d, a, b, v);
     }
 };
 
@@ -308,13 +328,14 @@ struct Fmt<KF_IQ4_NL> {
 template <>
 struct Fmt<KF_MXFP4> {
     static constexpr int B = 32, S = 17, CPB = 4;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 2) * S, cc = c & 3u;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
         const float d = e8m0_half(in[off]);
         uint32_t a, b;
         nib_plane(lds_8(in, off + 1u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(H.lut_v, d, a, b, v);
+        lut8(x.H->lut_v, d, a, b, v);
     }
 };
 
@@ -323,13 +344,14 @@ struct Fmt<KF_MXFP4> {
 template <>
 struct Fmt<KF_GGUF_NVFP4> {
     static constexpr int B = 64, S = 36, CPB = 8;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr& H,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
         const float d = ue4m3_half(in[off + g]);
         uint32_t a, b;
         nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        lut8(H.lut_v, d, a, b, v);
+        lut8(x.H->lut_v, d, a, b, v);
     }
 };
 
@@ -340,22 +362,23 @@ struct Fmt<KF_GGUF_NVFP4> {
 template <>
 struct Fmt<KF_NVFP4> {
     static constexpr int B = 64, S = 36, CPB = 8;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx& nv) {
-        const uint32_t off = (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
         const uint32_t s = in[off + g];
         uint32_t a, b;
         nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        if (nv.tab) {
-            const uint32_t* T = reinterpret_cast<const uint32_t*>(nv.tab) + s * 8u;
+        if (x.tab) {
+            const uint32_t* T = reinterpret_cast<const uint32_t*>(x.tab) + s * 8u;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t ca = (a >> (8 * i)) & 15u, cb = (b >> (8 * i)) & 15u;
                 v[i] = __uint_as_float(T[ca & 7u] ^ ((ca & 8u) << 28));
                 v[4 + i] = __uint_as_float(T[cb & 7u] ^ ((cb & 8u) << 28));
             }
-        } else {  // the tile spans two divisors: divisor of this block, then divide
-            const float dw = load_f32_bytes(nv.divs + 4u * ((nv.block0 + (c >> 3)) / nv.blocks_per_div));
+        } else {  // divisor of this block, then divide
+            const float dw = load_f32_bytes(x.divs + 4u * ((x.block0 + (c >> 3)) / x.blocks_per_div));
             const float sc = e4m3fn(s);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -373,10 +396,10 @@ struct Fmt<KF_NVFP4> {
 template <>
 struct Fmt<KF_Q4_K> {
     static constexpr int B = 256, S = 144, CPB = 32;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 5) * S, cc = c & 31u, k = cc >> 2;
-        const float d = h2f(lds_u16(in + off)), dmin = h2f(lds_u16(in + off + 2u));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, k = cc >> 2;
+        const float d = h2f(lds_2<PH>(in, off)), dmin = h2f(lds_2<PH>(in, off + 2u));
         const uint8_t* s = in + off + 4u;
         uint32_t sa, sm;
         if (k < 4u) {
@@ -409,17 +432,17 @@ struct Fmt<KF_Q4_K> {
 template <>
 struct Fmt<KF_Q6_K> {
     static constexpr int B = 256, S = 210, CPB = 32;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
-        const float d = h2f(lds_u16(in + off + 208u));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
+        const float d = h2f(lds_2<PH>(in, off + 208u));
         const int32_t sc = static_cast<int8_t>(in[off + 192u + (cc >> 1)]);
         const float ds = __fmul_rn(d, static_cast<float>(sc));
         const uint2 lo = lds_8(in, off + 64u * gi + 8u * (cc & 7u));
         const uint2 hi = lds_8(in, off + 128u + 32u * gi + 8u * (cc & 3u));
-        const uint32_t pl = 4u * ((cc >> 3) & 1u), ph = 2u * ((cc >> 2) & 3u);
-        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> ph) & 0x03030303u) << 4);
-        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> ph) & 0x03030303u) << 4);
+        const uint32_t pl = 4u * ((cc >> 3) & 1u), phh = 2u * ((cc >> 2) & 3u);
+        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> phh) & 0x03030303u) << 4);
+        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> phh) & 0x03030303u) << 4);
         const float bias = 8388640.0f;  // 2^23 + 32
         v[0] = __fmul_rn(ds, byte_minus<0>(a, bias));
         v[1] = __fmul_rn(ds, byte_minus<1>(a, bias));
@@ -438,10 +461,10 @@ struct Fmt<KF_Q6_K> {
 template <>
 struct Fmt<KF_Q4_G64> {
     static constexpr int B = 64, S = 34, CPB = 8;
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t c, float* v, const SmemHdr&,
-                                                 const NvCtx&) {
-        const uint32_t off = (c >> 3) * S;
-        const float s = h2f(lds_u16(in + off));
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 3) * S;
+        const float s = h2f(lds_2<PH>(in, off));
         const uint32_t w = lds_4(in, off + 2u + 4u * (c & 7u));
         const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
         const float bias = 8388616.0f;  // 2^23 + 8
@@ -510,174 +533,163 @@ __device__ __forceinline__ void store8(void* y, uint64_t e0, const float* v, boo
     }
 }
 
-template <int F, int O>
-__device__ __forceinline__ void decode_tile_fo(const DevTensor& t, const StageInfo& si, const uint8_t* in,
-                                               const SmemHdr& H, const NvCtx& nv) {
+template <int F, int O, bool PH>
+__device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
     using Fm = Fmt<F>;
     const uint32_t nch = si.nb * static_cast<uint32_t>(Fm::CPB);
     const uint64_t e_base = si.block0 * static_cast<uint64_t>(Fm::B);
-    const bool vec = t.yvec != 0;
+    const bool vec = si.t.yvec != 0;
+    void* y = si.t.y;
+    const uint32_t ph = PH ? si.phase : 0u;
 #pragma unroll
     for (int k = 0; k < kChunksPerThread; ++k) {
-        const uint32_t c = threadIdx.x + static_cast<uint32_t>(k * kThreads);
+        const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
         if (c < nch) {
             float v[8];
-            Fm::chunk(in, c, v, H, nv);
-            store8<O>(t.y, e_base + 8ull * c, v, vec);
+            Fm::template chunk<PH>(in, ph, c, v, x);
+            store8<O>(y, e_base + 8ull * c, v, vec);
         }
     }
+}
+
+template <int F, int O>
+__device__ __forceinline__ void decode_tile_fo(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
+    if (si.phase == 0u)
+        decode_tile_fop<F, O, false>(si, in, x, tid);
+    else
+        decode_tile_fop<F, O, true>(si, in, x, tid);
 }
 
 template <int F>
-__device__ __forceinline__ void decode_tile_f(const DevTensor& t, const StageInfo& si, const uint8_t* in,
-                                              const SmemHdr& H, const NvCtx& nv) {
-    switch (t.out) {
-        case KO_F32: decode_tile_fo<F, KO_F32>(t, si, in, H, nv); break;
-        case KO_F16: decode_tile_fo<F, KO_F16>(t, si, in, H, nv); break;
-        case KO_BF16: decode_tile_fo<F, KO_BF16>(t, si, in, H, nv); break;
-        default: decode_tile_fo<F, KO_F64>(t, si, in, H, nv); break;
+__device__ __forceinline__ void decode_tile_f(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
+    switch (si.t.out) {
+        case KO_F32: decode_tile_fo<F, KO_F32>(si, in, x, tid); break;
+        case KO_F16: decode_tile_fo<F, KO_F16>(si, in, x, tid); break;
+        case KO_BF16: decode_tile_fo<F, KO_BF16>(si, in, x, tid); break;
+        default: decode_tile_fo<F, KO_F64>(si, in, x, tid); break;
     }
 }
 
-// nvfp4 divisor for the tile: builds (or reuses) the shared quotient table
-// when the whole tile shares one divisor.  Called by every thread of the CTA
-// (contains barriers; the decision is uniform because it depends only on the
-// tile and on global data).
-__device__ NvCtx nvfp4_prepare(const DevTensor& t, const StageInfo& si, SmemHdr& H, float* tab) {
-    NvCtx nv{nullptr, t.divs, si.block0, t.blocks_per_div};
-    const uint64_t d0 = si.block0 / t.blocks_per_div;
-    const uint64_t d1 = (si.block0 + si.nb - 1u) / t.blocks_per_div;
-    if (d0 != d1) return nv;  // tile spans two divisors: divide per element
-    const float dw = load_f32_bytes(t.divs + 4u * d0);
-    const uint32_t bits = __float_as_uint(dw);
-    const bool have = H.tab_valid && H.tab_bits == bits;
-    __syncthreads();  // everyone has read tab_valid/tab_bits and finished with the old table
-    if (!have) {
-        for (int i = threadIdx.x; i < kTabEntries; i += kThreads)
-            tab[i] = __fdiv_rn(__fmul_rn(e2m1(static_cast<uint32_t>(i) & 7u), e4m3fn(static_cast<uint32_t>(i) >> 3)),
-                               dw);
-        if (threadIdx.x == 0) {
-            H.tab_bits = bits;
-            H.tab_valid = 1;
+__device__ __forceinline__ void decode_tile(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
+    switch (si.t.fmt) {
+        case KF_Q8_0: decode_tile_f<KF_Q8_0>(si, in, x, tid); break;
+        case KF_Q4_0: decode_tile_f<KF_Q4_0>(si, in, x, tid); break;
+        case KF_IQ4_NL: decode_tile_f<KF_IQ4_NL>(si, in, x, tid); break;
+        case KF_Q4_K: decode_tile_f<KF_Q4_K>(si, in, x, tid); break;
+        case KF_Q6_K: decode_tile_f<KF_Q6_K>(si, in, x, tid); break;
+        case KF_MXFP4: decode_tile_f<KF_MXFP4>(si, in, x, tid); break;
+        case KF_GGUF_NVFP4: decode_tile_f<KF_GGUF_NVFP4>(si, in, x, tid); break;
+        case KF_NVFP4: decode_tile_f<KF_NVFP4>(si, in, x, tid); break;
+        default: decode_tile_f<KF_Q4_G64>(si, in, x, tid); break;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Producer warp (lane 0): stages tiles it = 0, 1, ... of this CTA.
+// ---------------------------------------------------------------------------
+__device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
+    const uint64_t grid = gridDim.x;
+    int32_t di = 0;   // current tensor (tiles of a CTA increase, so it only moves forward)
+    int issued = 0;   // tiles staged so far
+    bool fault = false;
+    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
+        const int s = issued % kStages;
+        if (issued >= kStages &&
+            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1))) {
+            fault = true;
+            break;
         }
-        __syncthreads();
+        if (p.table)
+            while (di + 1 < p.n && p.table[di + 1].tile_begin <= tile) ++di;
+        const DevTensor& t = p.table ? p.table[di] : p.single;
+        StageInfo& si = H.info[s];
+        si.t = t;
+        const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
+        const uint64_t left = t.nblocks - b0;
+        const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
+        const uint8_t* src = t.x + b0 * t.S;
+        const uint32_t phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+        const uint32_t bytes = (phase + nb * t.S + 15u) & ~15u;
+        si.block0 = b0;
+        si.nb = nb;
+        si.phase = phase;
+        uint32_t nv_tab = 0;
+        if (t.fmt == KF_NVFP4 && H.tab_valid) {
+            const uint64_t d0 = b0 / t.blocks_per_div, d1 = (b0 + nb - 1u) / t.blocks_per_div;
+            nv_tab = d0 == d1 && __float_as_uint(load_f32_bytes(t.divs + 4u * d0)) == H.tab_bits;
+        }
+        si.nv_tab = nv_tab;
+        mbar_arrive_expect_tx(&H.full[s], bytes);
+        bulk_load(inbuf + s * kInStride, src - phase, bytes, &H.full[s]);
     }
-    nv.tab = tab;
-    return nv;
-}
-
-__device__ __forceinline__ const DevTensor& tensor_of(const KParams& p, int32_t i) {
-    return p.table ? p.table[i] : p.single;
-}
-
-// Tensor holding global tile `tile`: the last descriptor with tile_begin <= tile.
-__device__ __forceinline__ int32_t find_tensor(const KParams& p, uint64_t tile) {
-    if (!p.table) return 0;
-    int32_t lo = 0, hi = p.n - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (p.table[mid].tile_begin <= tile) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Producer (one thread): stage `tile`'s payload bytes into buffer s.
-__device__ void produce(const KParams& p, SmemHdr& H, uint8_t* inbuf, uint64_t tile, int s) {
-    if (tile >= p.total_tiles) return;
-    const int32_t di = find_tensor(p, tile);
-    const DevTensor& t = tensor_of(p, di);
-    const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
-    const uint64_t left = t.nblocks - b0;
-    const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
-    const uint32_t bytes = nb * t.S;
-    const uint8_t* src = t.x + b0 * t.S;
-    const int coop = ((reinterpret_cast<uintptr_t>(src) | bytes) & 15u) != 0;
-    StageInfo& si = H.info[s];
-    si.block0 = b0;
-    si.nb = nb;
-    si.desc = di;
-    si.coop = coop;
-    if (coop) {
-        mbar_arrive(&H.mbar[s]);
-    } else {
-        mbar_arrive_expect_tx(&H.mbar[s], bytes);
-        bulk_load(inbuf + s * kInStride, src, bytes, &H.mbar[s]);
+    if (fault) {
+        atomicOr(&g_fault_word, 1u);
+        // Wait (bounded) for every copy still in flight: the last kStages
+        // stagings, whose full phases are the latest ones of their stages.
+        for (int j = issued - kStages; j < issued; ++j)
+            if (j >= 0) mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
     }
 }
 
-// Fault exit: record the fault and let thread 0 wait (bounded) for every copy
-// this CTA still has in flight, iterations it .. last_issued.
-__device__ void fault_exit(const KParams& p, SmemHdr& H, int it, uint64_t tile, uint64_t grid) {
-    if (threadIdx.x != 0) return;
-    atomicOr(&g_fault_word, 1u);
-    const int last = (it == 0) ? kStages - 1 : it + kStages - 2;
-    for (int j = it; j <= last; ++j) {
-        const uint64_t tj = tile + static_cast<uint64_t>(j - it) * grid;
-        if (tj >= p.total_tiles) break;
-        mbar_wait_bounded(&H.mbar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
-    }
-}
-
-__global__ void __launch_bounds__(kThreads) k_decode(const KParams p) {
+__global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* inbuf = smem;
     SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
     float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
-    const uint64_t grid = gridDim.x;
+    const uint32_t tid = threadIdx.x;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&H.mbar[s], 1);
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&H.full[s], 1);
+            mbar_init(&H.empty[s], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         H.tab_valid = 0;
-        H.tab_bits = 0;
-        fence_proxy_async();
     }
-    if (threadIdx.x < 16) {
-        H.lut_iq4[threadIdx.x] = static_cast<float>(c_iq4[threadIdx.x]);
-        H.lut_v[threadIdx.x] = static_cast<float>(c_v[threadIdx.x]);
+    if (tid < 16) {
+        H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
+        H.lut_v[tid] = static_cast<float>(c_v[tid]);
+    }
+    // nvfp4: build the quotient table for the first divisor of the first
+    // nvfp4 tensor of the launch; tiles with another divisor divide per element.
+    if (p.nv_index >= 0) {
+        const DevTensor& t = p.table ? p.table[p.nv_index] : p.single;
+        const float dw = load_f32_bytes(t.divs);
+        for (uint32_t i = tid; i < kTabEntries; i += kBlockThreads)
+            tab[i] = __fdiv_rn(__fmul_rn(e2m1(i & 7u), e4m3fn(i >> 3)), dw);
+        if (tid == 0) {
+            H.tab_bits = __float_as_uint(dw);
+            H.tab_valid = 1;
+        }
     }
     __syncthreads();
 
-    uint64_t tile = blockIdx.x;
-    if (threadIdx.x == 0)
-        for (int s = 0; s < kStages; ++s) produce(p, H, inbuf, tile + static_cast<uint64_t>(s) * grid, s);
+    if (tid >= kThreads) {  // producer warp
+        if (tid == kThreads) producer(p, H, inbuf);
+        return;
+    }
 
-    for (int it = 0; tile < p.total_tiles; tile += grid, ++it) {
+    // consumer warps
+    const uint64_t grid = gridDim.x;
+    const uint32_t lane = tid & 31u;
+    int it = 0;
+    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
         const int s = it % kStages;
-        const bool ok = mbar_wait_bounded(&H.mbar[s], static_cast<uint32_t>((it / kStages) & 1));
-        // One barrier per tile: it publishes the stage to every thread, makes
-        // the decision to bail out uniform, and proves the previous tile's
-        // buffer is no longer read, so it can be refilled.
-        if (__syncthreads_or(!ok)) {
-            fault_exit(p, H, it, tile, grid);
+        if (!mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1))) {
+            if (lane == 0) atomicOr(&g_fault_word, 2u);
             return;
         }
-        if (threadIdx.x == 0 && it > 0)
-            produce(p, H, inbuf, tile + static_cast<uint64_t>(kStages - 1) * grid, (it - 1) % kStages);
-
-        const StageInfo si = H.info[s];
-        const DevTensor& t = tensor_of(p, si.desc);
-        uint8_t* in = inbuf + s * kInStride;
-        if (si.coop) {  // unaligned payload or ragged tail: plain loads
-            const uint8_t* src = t.x + si.block0 * t.S;
-            const uint32_t bytes = si.nb * t.S;
-            for (uint32_t i = threadIdx.x; i < bytes; i += kThreads) in[i] = src[i];
-            fence_proxy_async();
-            __syncthreads();
+        const StageInfo& si = H.info[s];
+        Ctx x{&H, nullptr, nullptr, 0, 1};
+        if (si.t.fmt == KF_NVFP4) {
+            x.tab = si.nv_tab ? tab : nullptr;
+            x.divs = si.t.divs;
+            x.block0 = si.block0;
+            x.blocks_per_div = si.t.blocks_per_div;
         }
-        NvCtx nv{nullptr, nullptr, 0, 1};
-        if (t.fmt == KF_NVFP4) nv = nvfp4_prepare(t, si, H, tab);
-        switch (t.fmt) {
-            case KF_Q8_0: decode_tile_f<KF_Q8_0>(t, si, in, H, nv); break;
-            case KF_Q4_0: decode_tile_f<KF_Q4_0>(t, si, in, H, nv); break;
-            case KF_IQ4_NL: decode_tile_f<KF_IQ4_NL>(t, si, in, H, nv); break;
-            case KF_Q4_K: decode_tile_f<KF_Q4_K>(t, si, in, H, nv); break;
-            case KF_Q6_K: decode_tile_f<KF_Q6_K>(t, si, in, H, nv); break;
-            case KF_MXFP4: decode_tile_f<KF_MXFP4>(t, si, in, H, nv); break;
-            case KF_GGUF_NVFP4: decode_tile_f<KF_GGUF_NVFP4>(t, si, in, H, nv); break;
-            case KF_NVFP4: decode_tile_f<KF_NVFP4>(t, si, in, H, nv); break;
-            default: decode_tile_f<KF_Q4_G64>(t, si, in, H, nv); break;
-        }
+        decode_tile(si, inbuf + s * kInStride, x, tid);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&H.empty[s]);
     }
 }
 
@@ -713,7 +725,7 @@ int launch_decode(const KParams& p, void* stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return static_cast<int>(e);
     if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
-    const bool tab = p.any_nvfp4 != 0;
+    const bool tab = p.nv_index >= 0;
     const size_t smem = smem_bytes(tab);
     DeviceInfo& di = g_dev[dev];
     // Benign race: concurrent first calls compute the same values.
@@ -726,7 +738,7 @@ int launch_decode(const KParams& p, void* stream) {
         if (e != cudaSuccess) return static_cast<int>(e);
         for (int i = 0; i < 2; ++i) {
             int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode, kThreads, smem_bytes(i == 1));
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode, kBlockThreads, smem_bytes(i == 1));
             if (e != cudaSuccess) return static_cast<int>(e);
             di.ctas_per_sm[i] = n > 0 ? n : 1;
         }
@@ -734,7 +746,7 @@ int launch_decode(const KParams& p, void* stream) {
     }
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(di.ctas_per_sm[tab ? 1 : 0]);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
-    k_decode<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    k_decode<<<grid, kBlockThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -768,7 +780,7 @@ namespace {
 DevTensor* g_noalloc_addr[kMaxDevices];  // per-device address, set once
 }
 
-int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int any_nvfp4, void* stream) {
+int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int nv_index, void* stream) {
     if (n < 1 || n > kNoAllocMaxTensors) return static_cast<int>(cudaErrorInvalidValue);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -787,7 +799,7 @@ int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, 
     p.single = table[0];
     p.table = dev_table;
     p.n = n;
-    p.any_nvfp4 = any_nvfp4;
+    p.nv_index = nv_index;
     p.total_tiles = total_tiles;
     return launch_decode(p, stream);
 }
