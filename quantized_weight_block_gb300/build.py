@@ -1,9 +1,9 @@
 """Build the in-tree CUDA library ``_build/libndq.so`` for sm_103a.
 
-Two translation units compile in parallel: the decode kernels (nvcc, one
-``-gencode`` for sm_103a, ``-fmad=false`` so that no multiply-add is
-contracted) and the host C ABI (g++).  No CMake; a clean build takes well
-under a minute on one core.
+Every translation unit compiles in parallel: one instantiation file per
+format plus a generic one (nvcc, one ``-gencode`` for sm_103a,
+``-fmad=false`` so that no multiply-add is contracted), the launcher, and the
+host C ABI (g++).  No CMake.
 """
 from __future__ import annotations
 
@@ -33,7 +33,7 @@ def _cuda_home() -> str:
 
 
 def _sources() -> list[str]:
-    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cpp", ".cuh", ".h"))]
 
 
 def up_to_date() -> bool:
@@ -51,23 +51,34 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
     inc = ["-I", INCLUDE, "-I", CSRC]
-    k_obj = os.path.join(OUT_DIR, "ndq_kernels.o")
-    a_obj = os.path.join(OUT_DIR, "ndq_api.o")
-    k_cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
-             "-c", os.path.join(CSRC, "ndq_kernels.cu"), "-o", k_obj, *inc]
-    if ptxas_info:
-        k_cmd += ["-Xptxas", "-v"]
-    a_cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-c", os.path.join(CSRC, "ndq_api.cpp"),
-             "-o", a_obj, *inc, "-I", os.path.join(cuda, "include")]
-    procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for c in (k_cmd, a_cmd)]
-    for c, p in zip((k_cmd, a_cmd), procs):
+    cmds, objs = [], []
+    for src in _sources():
+        obj = os.path.join(OUT_DIR, os.path.basename(src).rsplit(".", 1)[0] + ".o")
+        if src.endswith(".cu"):
+            cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
+                   "-c", src, "-o", obj, *inc]
+            if ptxas_info:
+                cmd += ["-Xptxas", "-v"]
+        elif src.endswith(".cpp"):
+            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-c", src, "-o", obj, *inc,
+                   "-I", os.path.join(cuda, "include")]
+        else:
+            continue
+        cmds.append(cmd)
+        objs.append(obj)
+    # every translation unit compiles in parallel
+    procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for c in cmds]
+    failed = None
+    for c, p in zip(cmds, procs):
         out, _ = p.communicate()
         if verbose or ptxas_info or p.returncode:
             sys.stderr.write(out)
-        if p.returncode:
-            raise RuntimeError(f"compile failed ({p.returncode}): {' '.join(c)}")
+        if p.returncode and failed is None:
+            failed = c
+    if failed:
+        raise RuntimeError("compile failed: " + " ".join(failed))
     tmp = LIB + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-o", tmp, k_obj, a_obj, "-cudart", "static", "-Xcompiler", "-fPIC"]
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-Xcompiler", "-fPIC"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout)

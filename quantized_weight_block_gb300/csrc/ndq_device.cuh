@@ -1,0 +1,751 @@
+// ndq_device.cuh -- sm_103a decode kernels for packed quantized weights.
+//
+// Included by one instantiation file per format (ndq_inst_*.cu) so that the
+// specialised kernels compile in parallel; everything here has internal
+// linkage.
+//
+// Decode is a streaming, HBM-bound transform (about 2.5 bytes moved per
+// element for 4-bit formats to 16-bit outputs, 1-2 FP32 operations per
+// element), so the design is about moving bytes, not about tensor cores:
+//
+//  * persistent CTAs (a grid of SMs x resident CTAs) walk a global list of
+//    8192-element tiles that spans one tensor or a whole batch of tensors;
+//  * one producer warp per CTA stages each tile's payload bytes (one
+//    contiguous span) into shared memory with the Tensor Memory Accelerator
+//    (cp.async.bulk, completing on a "full" mbarrier), running up to kStages
+//    tiles ahead; it copies the tile's tensor descriptor next to the bytes;
+//  * eight consumer warps decode 8-element chunks straight from shared
+//    memory (the odd block strides of 17, 18, 34, 36 and 210 bytes are
+//    resolved with aligned 32-bit shared loads and funnel shifts), write
+//    each chunk with 16-byte vector stores (a warp covers 512 contiguous
+//    bytes per instruction), and release the stage on an "empty" mbarrier.
+//    Consumers never meet at a CTA-wide barrier inside the loop;
+//  * a span that does not start on a 16-byte boundary (an unaligned payload,
+//    a ragged last tile) is staged from the 16-byte boundary below it to the
+//    one above its end, and decoded at its byte phase within the stage; the
+//    extra bytes lie in the same 16-byte lines as payload bytes, hence in
+//    mapped memory;
+//  * all arithmetic follows the ONNX "DequantizePacked decoding
+//    specification" ("Decoding algorithms": every M/A/D rounded separately
+//    to binary32, round-to-nearest-even), with explicit __fmul_rn /
+//    __fsub_rn / __fdiv_rn and -fmad=false, and a single round-to-nearest-
+//    even conversion to the output type.  Integer codes reach FP32 through
+//    the exact 2^23 magic-number construction (a byte placed in the low
+//    mantissa of 2^23, minus 2^23 plus the code offset), never through a
+//    rounding conversion.
+//
+// Every mbarrier wait is bounded by the global timer; on expiry the warp
+// records a fault bit and stops, and the producer waits (bounded) for the
+// copies it still has in flight before it exits, so a lost copy cannot hang
+// the GPU.
+
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ndq_internal.h"
+
+namespace ndq {
+namespace {
+
+constexpr int kConsumerWarps = kThreads / 32;     // 8
+constexpr int kChunksPerThread = kTileElems / 8 / kThreads;  // 4
+constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
+
+static_assert(kInStride >= kMaxTileBytes + 15 + 15 + 12, "stage size");
+static_assert(kInStride % 128 == 0, "stage alignment");
+
+// Written by the producer before it arms the stage's full barrier.
+struct StageInfo {
+    DevTensor t;      // the tile's tensor
+    uint64_t block0;  // first block of the tile within the tensor
+    uint32_t nb;      // blocks in the tile
+    uint32_t phase;   // byte offset of the first block within the stage (0..15)
+    uint32_t nv_tab;  // nvfp4: the whole tile uses the divisor the shared table was built for
+    uint32_t pad[11];
+};
+static_assert(sizeof(StageInfo) == 128, "StageInfo layout");
+
+struct SmemHdr {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    float lut_iq4[16];  // IQ4_NL table ("Packed layouts and decoding")
+    float lut_v[16];    // doubled E2M1 table V ("Ternary and block-floating formats")
+    uint32_t tab_bits;  // divisor bits the nvfp4 table was built for
+    int32_t tab_valid;
+    int32_t pad[30];
+    StageInfo info[kStages];
+};
+
+constexpr int kHdrBytes = (sizeof(SmemHdr) + 127) / 128 * 128;
+
+__constant__ int8_t c_iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
+__constant__ int8_t c_v[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, bulk copy, global timer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: true once the phase with `parity` has completed, false after
+// kWaitLimitNs of global time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// TMA bulk copy global -> shared, completing `bytes` of transaction count on
+// `bar`.  dst, src and bytes are multiples of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory byte access and exact scalar constructions.
+// ---------------------------------------------------------------------------
+// 16-bit little-endian field at byte offset `off` of a 16-byte-aligned stage.
+// With PH (a stage decoded at a nonzero byte phase) the field may be
+// unaligned.
+template <bool PH>
+__device__ __forceinline__ uint32_t lds_2(const uint8_t* base, uint32_t off) {
+    if (PH) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+        return __funnelshift_r(w[0], w[1], (off & 3u) * 8u) & 0xffffu;
+    }
+    return *reinterpret_cast<const uint16_t*>(base + off);
+}
+
+// 8 bytes at byte offset `off` of a 16-byte-aligned stage.
+__device__ __forceinline__ uint2 lds_8(const uint8_t* base, uint32_t off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    const uint32_t sh = (off & 3u) * 8u;
+    const uint32_t a = w[0], b = w[1], c = w[2];
+    return make_uint2(__funnelshift_r(a, b, sh), __funnelshift_r(b, c, sh));
+}
+
+// 4 bytes at byte offset `off`.
+__device__ __forceinline__ uint32_t lds_4(const uint8_t* base, uint32_t off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    return __funnelshift_r(w[0], w[1], (off & 3u) * 8u);
+}
+
+// Exact binary16 -> binary32 (the specification's H).
+__device__ __forceinline__ float h2f(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// Byte I of w (0..255) as the float 2^23 + byte, minus `bias`: exact for the
+// small integers involved (bias = 2^23 + code offset).
+template <int I>
+__device__ __forceinline__ float byte_minus(uint32_t w, float bias) {
+    return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)), bias);
+}
+
+// MXFP4 half scale: the FLOAT with bit pattern 0x00200000 * 2^e for e < 2,
+// (e-1) * 2^23 otherwise ("Ternary and block-floating formats").
+__device__ __forceinline__ float e8m0_half(uint32_t e) {
+    return __uint_as_float(e < 2u ? (0x00200000u << e) : ((e - 1u) << 23));
+}
+
+// gguf:nvfp4 unsigned-E4M3 half scale: 0 for bytes 0 and 127; otherwise,
+// with E = bits 6:3 and m = bits 2:0 (bit 7 ignored), m * 2^-10 when E == 0
+// and (1 + m/8) * 2^(E-8) else (exponent field E + 119, mantissa m << 20).
+__device__ __forceinline__ float ue4m3_half(uint32_t e) {
+    const uint32_t E = (e >> 3) & 15u, m = e & 7u;
+    const float r = (E == 0u) ? __fmul_rn(static_cast<float>(m), 0.0009765625f)
+                              : __uint_as_float(((E + 119u) << 23) | (m << 20));
+    return (e == 0u || e == 127u) ? 0.0f : r;
+}
+
+// E4M3FN word (NInfer tensor-formats section 3.3): bias 7, subnormal
+// m * 2^-9, e == 15 && m == 7 NaN, sign applies to every word.
+__device__ __forceinline__ float e4m3fn(uint32_t w) {
+    const uint32_t e = (w >> 3) & 15u, m = w & 7u;
+    float mag;
+    if (e == 15u && m == 7u)
+        mag = __uint_as_float(0x7fc00000u);
+    else if (e == 0u)
+        mag = __fmul_rn(static_cast<float>(m), 0.001953125f);
+    else
+        mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (w & 0x80u) ? -mag : mag;
+}
+
+// E2M1 word (section 3.3): positive words 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6;
+// bit 3 negates (0x8 is -0).
+__device__ __forceinline__ float e2m1(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = (e == 0u) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+    return (c & 8u) ? -mag : mag;
+}
+
+// Little-endian FP32 word at any byte address (global memory).
+__device__ __forceinline__ float load_f32_bytes(const uint8_t* p) {
+    const uint32_t u = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
+                       (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24);
+    return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------
+// Per-format chunk decoders: chunk c of a tile = output elements 8c..8c+7 of
+// the tile, produced from the tile's payload bytes staged at `in` (byte
+// phase `ph`: the tile's first block starts at in + ph).
+// ---------------------------------------------------------------------------
+struct Ctx {
+    const SmemHdr* H;
+    const float* tab;  // nvfp4 quotient table, or nullptr for per-element division
+    const uint8_t* divs;
+    uint64_t block0;
+    uint64_t blocks_per_div;
+};
+
+template <int F>
+struct Fmt;
+
+// gguf:q8_0 / q8_g32_fp16: y[j] = M(d, q[j]), q signed bytes.
+template <>
+struct Fmt<KF_Q8_0> {
+    static constexpr int B = 32, S = 34, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 2) * S;
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
+        const uint32_t a = q.x ^ 0x80808080u, b = q.y ^ 0x80808080u;  // signed -> offset-128
+        const float bias = 8388736.0f;                                 // 2^23 + 128
+        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+    }
+};
+
+// Nibble plane p (0 = low, 1 = high) of 8 consecutive code bytes, as bytes.
+__device__ __forceinline__ void nib_plane(uint2 q, uint32_t p, uint32_t& a, uint32_t& b) {
+    a = (q.x >> (4u * p)) & 0x0F0F0F0Fu;
+    b = (q.y >> (4u * p)) & 0x0F0F0F0Fu;
+}
+
+// gguf:q4_0: v = P(q,4,16); y[j] = M(d, v[j] - 8).  Chunk c&3: bytes 8*(c&1)
+// of q, plane c>>1 (16 low nibbles, then 16 high nibbles).
+template <>
+struct Fmt<KF_Q4_0> {
+    static constexpr int B = 32, S = 18, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_2<PH>(in, off));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
+        const float bias = 8388616.0f;  // 2^23 + 8
+        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+    }
+};
+
+// Table lookup of 8 nibbles (bytes of a, then b) scaled by d: y = M(d, T[v]).
+__device__ __forceinline__ void lut8(const float* T, float d, uint32_t a, uint32_t b, float* v) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = __fmul_rn(d, T[(a >> (8 * i)) & 15u]);
+        v[4 + i] = __fmul_rn(d, T[(b >> (8 * i)) & 15u]);
+    }
+}
+
+// gguf:iq4_nl: v = P(q,4,16); y[j] = M(d, IQ4[v[j]]).
+template <>
+struct Fmt<KF_IQ4_NL> {
+    static constexpr int B = 32, S = 18, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const float d = h2f(lds_2<PH>(in, off));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
+        lut8(x.H->lut_iq4, d, a, b, v);
+    }
+};
+
+// gguf:mxfp4: d = E8M0 half scale; v = P(q,4,16); y[j] = M(d, V[v[j]]).
+template <>
+struct Fmt<KF_MXFP4> {
+    static constexpr int B = 32, S = 17, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const float d = e8m0_half(in[off]);
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 1u + 8u * (cc & 1u)), cc >> 1, a, b);
+        lut8(x.H->lut_v, d, a, b, v);
+    }
+};
+
+// gguf:nvfp4: group g = (c&7)>>1 of 16 values: d = unsigned-E4M3 half scale of
+// scales[g]; v = P(q[8g:8g+8],4,8); y[16g+j] = M(d, V[v[j]]).
+template <>
+struct Fmt<KF_GGUF_NVFP4> {
+    static constexpr int B = 64, S = 36, CPB = 8;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+        const float d = ue4m3_half(in[off + g]);
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
+        lut8(x.H->lut_v, d, a, b, v);
+    }
+};
+
+// nvfp4 (NInfer section 3.3): W = e2m1(c) * e4m3fn(s) / d_w, the product exact
+// and the quotient rounded once.  With a quotient table (one divisor for the
+// whole tile) the element is tab[16*s + c].
+template <>
+struct Fmt<KF_NVFP4> {
+    static constexpr int B = 64, S = 36, CPB = 8;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+        const uint32_t s = in[off + g];
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
+        if (x.tab) {
+            const float* T = x.tab + s * 16u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[i] = T[(a >> (8 * i)) & 15u];
+                v[4 + i] = T[(b >> (8 * i)) & 15u];
+            }
+        } else {  // divisor of this block, then divide
+            const float dw = load_f32_bytes(x.divs + 4u * ((x.block0 + (c >> 3)) / x.blocks_per_div));
+            const float sc = e4m3fn(s);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[i] = __fdiv_rn(__fmul_rn(e2m1((a >> (8 * i)) & 15u), sc), dw);
+                v[4 + i] = __fdiv_rn(__fmul_rn(e2m1((b >> (8 * i)) & 15u), sc), dw);
+            }
+        }
+    }
+};
+
+// gguf:q4_k: v = P(q,4,32); 6-bit a[k], m[k] from the 12 scale bytes;
+// y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])), k = floor(j/32).
+// Chunk c&31: sub-block k = cc>>2, byte group cc>>3 (32 bytes), plane
+// (cc>>2)&1, bytes 8*(cc&3) of the group.
+template <>
+struct Fmt<KF_Q4_K> {
+    static constexpr int B = 256, S = 144, CPB = 32;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, k = cc >> 2;
+        const float d = h2f(lds_2<PH>(in, off)), dmin = h2f(lds_2<PH>(in, off + 2u));
+        // Scale bytes s[0..11] as three words; with j = k mod 4, byte j of each
+        // word is s[j], s[j+4], s[j+8].  Both unpack rules are formed and one
+        // is selected, so the lanes of a warp (k = lane/4) do not diverge.
+        const uint32_t j8 = 8u * (k & 3u);
+        const uint32_t b0 = (lds_4(in, off + 4u) >> j8) & 0xffu;
+        const uint32_t b1 = (lds_4(in, off + 8u) >> j8) & 0xffu;
+        const uint32_t b2 = (lds_4(in, off + 12u) >> j8) & 0xffu;
+        const bool lo = k < 4u;
+        const uint32_t sa = lo ? (b0 & 63u) : ((b2 & 15u) | ((b0 >> 6) << 4));
+        const uint32_t sm = lo ? (b1 & 63u) : ((b2 >> 4) | ((b1 >> 6) << 4));
+        const float da = __fmul_rn(d, static_cast<float>(sa));
+        const float dm = __fmul_rn(dmin, static_cast<float>(sm));
+        uint32_t a, b;
+        nib_plane(lds_8(in, off + 16u + 32u * (cc >> 3) + 8u * (cc & 3u)), k & 1u, a, b);
+        const float bias = 8388608.0f;  // 2^23
+        v[0] = __fsub_rn(__fmul_rn(da, byte_minus<0>(a, bias)), dm);
+        v[1] = __fsub_rn(__fmul_rn(da, byte_minus<1>(a, bias)), dm);
+        v[2] = __fsub_rn(__fmul_rn(da, byte_minus<2>(a, bias)), dm);
+        v[3] = __fsub_rn(__fmul_rn(da, byte_minus<3>(a, bias)), dm);
+        v[4] = __fsub_rn(__fmul_rn(da, byte_minus<0>(b, bias)), dm);
+        v[5] = __fsub_rn(__fmul_rn(da, byte_minus<1>(b, bias)), dm);
+        v[6] = __fsub_rn(__fmul_rn(da, byte_minus<2>(b, bias)), dm);
+        v[7] = __fsub_rn(__fmul_rn(da, byte_minus<3>(b, bias)), dm);
+    }
+};
+
+// gguf:q6_k: l = P(low,4,64), h = P(high,2,32), s = scales[floor(j/16)] signed;
+// y[j] = M(M(d, s), l[j] + 16 h[j] - 32).  Chunk c&31 = elements 8cc..8cc+7:
+// low bytes 64*(cc>>4) + 8*(cc&7), plane (cc>>3)&1; high bytes
+// 32*(cc>>4) + 8*(cc&3), 2-bit plane (cc>>2)&3; scale index cc>>1.
+template <>
+struct Fmt<KF_Q6_K> {
+    static constexpr int B = 256, S = 210, CPB = 32;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
+        const float d = h2f(lds_2<PH>(in, off + 208u));
+        const int32_t sc = static_cast<int8_t>(in[off + 192u + (cc >> 1)]);
+        const float ds = __fmul_rn(d, static_cast<float>(sc));
+        const uint2 lo = lds_8(in, off + 64u * gi + 8u * (cc & 7u));
+        const uint2 hi = lds_8(in, off + 128u + 32u * gi + 8u * (cc & 3u));
+        const uint32_t pl = 4u * ((cc >> 3) & 1u), phh = 2u * ((cc >> 2) & 3u);
+        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> phh) & 0x03030303u) << 4);
+        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> phh) & 0x03030303u) << 4);
+        const float bias = 8388640.0f;  // 2^23 + 32
+        v[0] = __fmul_rn(ds, byte_minus<0>(a, bias));
+        v[1] = __fmul_rn(ds, byte_minus<1>(a, bias));
+        v[2] = __fmul_rn(ds, byte_minus<2>(a, bias));
+        v[3] = __fmul_rn(ds, byte_minus<3>(a, bias));
+        v[4] = __fmul_rn(ds, byte_minus<0>(b, bias));
+        v[5] = __fmul_rn(ds, byte_minus<1>(b, bias));
+        v[6] = __fmul_rn(ds, byte_minus<2>(b, bias));
+        v[7] = __fmul_rn(ds, byte_minus<3>(b, bias));
+    }
+};
+
+// q4_g64_fp16 (NInfer sections 5-6.2): w = binary32(s32 * q), q the 4-bit
+// two's-complement code; element k sits in bits 4*(k mod 2) of code byte
+// floor(k/2) (layout reading).  XOR 8 maps two's complement to offset-8.
+template <>
+struct Fmt<KF_Q4_G64> {
+    static constexpr int B = 64, S = 34, CPB = 8;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 3) * S;
+        const float s = h2f(lds_2<PH>(in, off));
+        const uint32_t w = lds_4(in, off + 2u + 4u * (c & 7u));
+        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+        const float bias = 8388616.0f;  // 2^23 + 8
+        v[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
+        v[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
+        v[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
+        v[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
+        v[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
+        v[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
+        v[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
+        v[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Output stage: one RNE conversion per element, 16-byte stores when y is
+// 16-byte aligned (element offsets are multiples of 8, so every chunk then
+// starts on a 16-byte boundary).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int O>
+__device__ __forceinline__ void store8(void* y, uint64_t e0, const float* v, bool vec) {
+    if (O == KO_F32) {
+        float* p = static_cast<float*>(y) + e0;
+        if (vec) {
+            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p[i] = v[i];
+        }
+    } else if (O == KO_F64) {
+        double* p = static_cast<double*>(y) + e0;
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                reinterpret_cast<double2*>(p)[i] =
+                    make_double2(static_cast<double>(v[2 * i]), static_cast<double>(v[2 * i + 1]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p[i] = static_cast<double>(v[i]);
+        }
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+        uint16_t* p = static_cast<uint16_t*>(y) + e0;
+        if (vec) {
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[2 * i] = static_cast<uint16_t>(w[i] & 0xffffu);
+                p[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        }
+    }
+}
+
+template <int F, int O, bool PH>
+__device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
+    using Fm = Fmt<F>;
+    const uint32_t nch = si.nb * static_cast<uint32_t>(Fm::CPB);
+    const uint64_t e_base = si.block0 * static_cast<uint64_t>(Fm::B);
+    const bool vec = si.t.yvec != 0;
+    void* y = si.t.y;
+    const uint32_t ph = PH ? si.phase : 0u;
+#pragma unroll
+    for (int k = 0; k < kChunksPerThread; ++k) {
+        const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
+        if (c < nch) {
+            float v[8];
+            Fm::template chunk<PH>(in, ph, c, v, x);
+            store8<O>(y, e_base + 8ull * c, v, vec);
+        }
+    }
+}
+
+// Slow path, shared by every kernel and never inlined: a stage at a nonzero
+// byte phase (an unaligned payload pointer) or an nvfp4 tile whose divisor is
+// not the one the shared quotient table holds (per-element division).
+template <int F>
+__device__ __forceinline__ void decode_tile_slow_f(const StageInfo& si, const uint8_t* in, const Ctx& x,
+                                                   uint32_t tid) {
+    switch (si.t.out) {
+        case KO_F32: decode_tile_fop<F, KO_F32, true>(si, in, x, tid); break;
+        case KO_F16: decode_tile_fop<F, KO_F16, true>(si, in, x, tid); break;
+        case KO_BF16: decode_tile_fop<F, KO_BF16, true>(si, in, x, tid); break;
+        default: decode_tile_fop<F, KO_F64, true>(si, in, x, tid); break;
+    }
+}
+
+__device__ __noinline__ void decode_tile_slow(const StageInfo& si, const uint8_t* in, const Ctx x, uint32_t tid) {
+    switch (si.t.fmt) {
+        case KF_Q8_0: decode_tile_slow_f<KF_Q8_0>(si, in, x, tid); break;
+        case KF_Q4_0: decode_tile_slow_f<KF_Q4_0>(si, in, x, tid); break;
+        case KF_IQ4_NL: decode_tile_slow_f<KF_IQ4_NL>(si, in, x, tid); break;
+        case KF_Q4_K: decode_tile_slow_f<KF_Q4_K>(si, in, x, tid); break;
+        case KF_Q6_K: decode_tile_slow_f<KF_Q6_K>(si, in, x, tid); break;
+        case KF_MXFP4: decode_tile_slow_f<KF_MXFP4>(si, in, x, tid); break;
+        case KF_GGUF_NVFP4: decode_tile_slow_f<KF_GGUF_NVFP4>(si, in, x, tid); break;
+        case KF_NVFP4: decode_tile_slow_f<KF_NVFP4>(si, in, x, tid); break;
+        default: decode_tile_slow_f<KF_Q4_G64>(si, in, x, tid); break;
+    }
+}
+
+// Fast path: 16-byte-aligned stage (and, for nvfp4, the shared table).
+// OSEL / FSEL fix the output type / format at compile time, or are -1 for a
+// runtime switch (batched launches that mix them).
+template <int F, int OSEL>
+__device__ __forceinline__ void decode_tile_fast_f(const StageInfo& si, const uint8_t* in, const Ctx& x,
+                                                   uint32_t tid) {
+    if (OSEL >= 0) {
+        decode_tile_fop<F, (OSEL >= 0 ? OSEL : 0), false>(si, in, x, tid);
+        return;
+    }
+    switch (si.t.out) {
+        case KO_F32: decode_tile_fop<F, KO_F32, false>(si, in, x, tid); break;
+        case KO_F16: decode_tile_fop<F, KO_F16, false>(si, in, x, tid); break;
+        case KO_BF16: decode_tile_fop<F, KO_BF16, false>(si, in, x, tid); break;
+        default: decode_tile_fop<F, KO_F64, false>(si, in, x, tid); break;
+    }
+}
+
+template <int FSEL, int OSEL>
+__device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint8_t* in, const Ctx& x,
+                                                 uint32_t tid) {
+    if (FSEL >= 0) {
+        decode_tile_fast_f<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, x, tid);
+        return;
+    }
+    switch (si.t.fmt) {
+        case KF_Q8_0: decode_tile_fast_f<KF_Q8_0, OSEL>(si, in, x, tid); break;
+        case KF_Q4_0: decode_tile_fast_f<KF_Q4_0, OSEL>(si, in, x, tid); break;
+        case KF_IQ4_NL: decode_tile_fast_f<KF_IQ4_NL, OSEL>(si, in, x, tid); break;
+        case KF_Q4_K: decode_tile_fast_f<KF_Q4_K, OSEL>(si, in, x, tid); break;
+        case KF_Q6_K: decode_tile_fast_f<KF_Q6_K, OSEL>(si, in, x, tid); break;
+        case KF_MXFP4: decode_tile_fast_f<KF_MXFP4, OSEL>(si, in, x, tid); break;
+        case KF_GGUF_NVFP4: decode_tile_fast_f<KF_GGUF_NVFP4, OSEL>(si, in, x, tid); break;
+        case KF_NVFP4: decode_tile_fast_f<KF_NVFP4, OSEL>(si, in, x, tid); break;
+        default: decode_tile_fast_f<KF_Q4_G64, OSEL>(si, in, x, tid); break;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Producer warp (lane 0): stages tiles it = 0, 1, ... of this CTA.
+// ---------------------------------------------------------------------------
+__device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
+    const uint64_t grid = gridDim.x;
+    int32_t di = 0;   // current tensor (tiles of a CTA increase, so it only moves forward)
+    int issued = 0;   // tiles staged so far
+    bool fault = false;
+    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
+        const int s = issued % kStages;
+        if (issued >= kStages &&
+            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1))) {
+            fault = true;
+            break;
+        }
+        if (p.table)
+            while (di + 1 < p.n && p.table[di + 1].tile_begin <= tile) ++di;
+        const DevTensor& t = p.table ? p.table[di] : p.single;
+        StageInfo& si = H.info[s];
+        si.t = t;
+        const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
+        const uint64_t left = t.nblocks - b0;
+        const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
+        const uint8_t* src = t.x + b0 * t.S;
+        const uint32_t phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+        const uint32_t bytes = (phase + nb * t.S + 15u) & ~15u;
+        si.block0 = b0;
+        si.nb = nb;
+        si.phase = phase;
+        uint32_t nv_tab = 0;
+        if (t.fmt == KF_NVFP4 && H.tab_valid) {
+            const uint64_t d0 = b0 / t.blocks_per_div, d1 = (b0 + nb - 1u) / t.blocks_per_div;
+            nv_tab = d0 == d1 && __float_as_uint(load_f32_bytes(t.divs + 4u * d0)) == H.tab_bits;
+        }
+        si.nv_tab = nv_tab;
+        mbar_arrive_expect_tx(&H.full[s], bytes);
+        bulk_load(inbuf + s * kInStride, src - phase, bytes, &H.full[s]);
+    }
+    if (fault) {
+        atomicOr(p.fault, 1u);
+        // Wait (bounded) for every copy still in flight: the last kStages
+        // stagings, whose full phases are the latest ones of their stages.
+        for (int j = issued - kStages; j < issued; ++j)
+            if (j >= 0) mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+    }
+}
+
+// FSEL / OSEL: the launch's format and output type when every tensor shares
+// them (the host picks the instantiation), else -1.
+template <int FSEL, int OSEL>
+__global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* inbuf = smem;
+    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
+    float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
+    const uint32_t tid = threadIdx.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&H.full[s], 1);
+            mbar_init(&H.empty[s], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        H.tab_valid = 0;
+    }
+    if (tid < 16) {
+        H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
+        H.lut_v[tid] = static_cast<float>(c_v[tid]);
+    }
+    // nvfp4: build the quotient table for the first divisor of the first
+    // nvfp4 tensor of the launch; tiles with another divisor divide per element.
+    // Entry 16*s + c is e2m1(c) * e4m3fn(s) / d_w; only codes 0..7 divide: the
+    // entry of c | 8 is the same quotient with the sign bit flipped (RNE
+    // division is odd-symmetric, and (-0)*s/d_w is the negated (+0)*s/d_w).
+    if (p.nv_index >= 0) {
+        const DevTensor& t = p.table ? p.table[p.nv_index] : p.single;
+        const float dw = load_f32_bytes(t.divs);
+        for (uint32_t i = tid; i < kTabEntries / 2; i += kBlockThreads) {
+            const uint32_t sb = i >> 3, c = i & 7u;
+            const float q = __fdiv_rn(__fmul_rn(e2m1(c), e4m3fn(sb)), dw);
+            tab[16u * sb + c] = q;
+            tab[16u * sb + c + 8u] = __uint_as_float(__float_as_uint(q) ^ 0x80000000u);
+        }
+        if (tid == 0) {
+            H.tab_bits = __float_as_uint(dw);
+            H.tab_valid = 1;
+        }
+    }
+    __syncthreads();
+
+    if (tid >= kThreads) {  // producer warp
+        if (tid == kThreads) producer(p, H, inbuf);
+        return;
+    }
+
+    // consumer warps
+    const uint64_t grid = gridDim.x;
+    const uint32_t lane = tid & 31u;
+    int it = 0;
+    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1))) {
+            if (lane == 0) atomicOr(p.fault, 2u);
+            return;
+        }
+        const StageInfo& si = H.info[s];
+        const uint8_t* in = inbuf + s * kInStride;
+        const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
+        if (si.phase != 0u || (nv && !si.nv_tab)) {
+            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div},
+                             tid);
+        } else {
+            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, nullptr, 0, 1}, tid);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&H.empty[s]);
+    }
+}
+
+// Kernel of format F for output type `osel`.
+template <int F>
+KernelFn kernel_row(int osel) {
+    switch (osel) {
+        case KO_F32: return k_decode<F, KO_F32>;
+        case KO_F16: return k_decode<F, KO_F16>;
+        case KO_BF16: return k_decode<F, KO_BF16>;
+        case KO_F64: return k_decode<F, KO_F64>;
+        default: return k_decode<F, -1>;
+    }
+}
+
+}  // namespace
+}  // namespace ndq

@@ -1,0 +1,6 @@
+// Decode kernels specialised for KF_GGUF_NVFP4 (one per output type).
+#include "ndq_device.cuh"
+
+namespace ndq {
+KernelFn kernel_gguf_nvfp4(int osel) { return kernel_row<KF_GGUF_NVFP4>(osel); }
+}  // namespace ndq

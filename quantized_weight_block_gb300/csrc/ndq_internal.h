@@ -32,6 +32,10 @@ enum KOut : int32_t { KO_F32 = 0, KO_F16 = 1, KO_BF16 = 2, KO_F64 = 3 };
 constexpr int kTileElems = 8192;
 constexpr int kThreads = 256;
 constexpr int kMaxTileBytes = 8704;  // gguf:q8_0: 256 blocks * 34 bytes
+constexpr int kBlockThreads = kThreads + 32;  // consumer warps + one producer warp
+constexpr int kStages = 4;                    // staged tiles in flight per CTA
+constexpr int kInStride = 8832;               // tile bytes + phase + rounding + over-read
+constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
 
 // One tensor as the kernel sees it (64 bytes; kept trivially copyable).
 struct DevTensor {
@@ -59,7 +63,27 @@ struct KParams {
     int32_t n;
     int32_t nv_index;  // first nvfp4 tensor of the launch (its divisor seeds the quotient table), or -1
     uint64_t total_tiles;
+    int32_t fsel;      // KFmt shared by every tensor of the launch, or -1
+    int32_t osel;      // KOut shared by every tensor of the launch, or -1
+    unsigned int* fault;  // device fault word (set by the launcher)
 };
+
+using KernelFn = void (*)(KParams);
+
+// Kernel getters, one per instantiation file (osel: KOut, or -1 for any).
+KernelFn kernel_q8_0(int osel);
+KernelFn kernel_q4_0(int osel);
+KernelFn kernel_iq4_nl(int osel);
+KernelFn kernel_q4_k(int osel);
+KernelFn kernel_q6_k(int osel);
+KernelFn kernel_mxfp4(int osel);
+KernelFn kernel_gguf_nvfp4(int osel);
+KernelFn kernel_nvfp4(int osel);
+KernelFn kernel_q4_g64(int osel);
+KernelFn kernel_generic(int osel);
+
+// Dynamic shared memory of a decode CTA (with or without the nvfp4 table).
+size_t decode_smem_bytes(bool tab);
 
 // Launch one decode over p.total_tiles tiles on `stream` (a cudaStream_t).
 // Returns 0 or a CUDA error code.

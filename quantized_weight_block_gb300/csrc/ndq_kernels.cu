@@ -1,42 +1,9 @@
-// ndq_kernels.cu -- sm_103a decode kernels for packed quantized weights.
-//
-// Decode is a streaming, HBM-bound transform (about 2.5 bytes moved per
-// element for 4-bit formats to 16-bit outputs, 1-2 FP32 operations per
-// element), so the design is about moving bytes, not about tensor cores:
-//
-//  * persistent CTAs (a grid of SMs x resident CTAs) walk a global list of
-//    8192-element tiles that spans one tensor or a whole batch of tensors;
-//  * one producer warp per CTA stages each tile's payload bytes (one
-//    contiguous span) into shared memory with the Tensor Memory Accelerator
-//    (cp.async.bulk, completing on a "full" mbarrier), running up to kStages
-//    tiles ahead; it copies the tile's tensor descriptor next to the bytes;
-//  * eight consumer warps decode 8-element chunks straight from shared
-//    memory (the odd block strides of 17, 18, 34, 36 and 210 bytes are
-//    resolved with aligned 32-bit shared loads and funnel shifts), write
-//    each chunk with 16-byte vector stores (a warp covers 512 contiguous
-//    bytes per instruction), and release the stage on an "empty" mbarrier.
-//    Consumers never meet at a CTA-wide barrier inside the loop;
-//  * a span that does not start on a 16-byte boundary (an unaligned payload,
-//    a ragged last tile) is staged from the 16-byte boundary below it to the
-//    one above its end, and decoded at its byte phase within the stage; the
-//    extra bytes lie in the same 16-byte lines as payload bytes, hence in
-//    mapped memory;
-//  * all arithmetic follows the ONNX "DequantizePacked decoding
-//    specification" ("Decoding algorithms": every M/A/D rounded separately
-//    to binary32, round-to-nearest-even), with explicit __fmul_rn /
-//    __fsub_rn / __fdiv_rn and -fmad=false, and a single round-to-nearest-
-//    even conversion to the output type.  Integer codes reach FP32 through
-//    the exact 2^23 magic-number construction (a byte placed in the low
-//    mantissa of 2^23, minus 2^23 plus the code offset), never through a
-//    rounding conversion.
-//
-// Every mbarrier wait is bounded by the global timer; on expiry the warp
-// records a fault bit and stops, and the producer waits (bounded) for the
-// copies it still has in flight before it exits, so a lost copy cannot hang
-// the GPU.
+// ndq_kernels.cu -- launcher of the decode kernels: kernel selection,
+// occupancy-sized persistent grids, the launch-table upload, the library-owned
+// table of the no-allocation batched call and the device fault word.  The
+// decode kernels themselves are in ndq_device.cuh, instantiated by
+// ndq_inst_*.cu.
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -45,653 +12,10 @@
 
 namespace ndq {
 
+// Set by a kernel whose bounded wait gave up (see ndq_get_device_fault).
 __device__ unsigned int g_fault_word;
 
 namespace {
-
-constexpr int kStages = 4;
-constexpr int kConsumerWarps = kThreads / 32;     // 8
-constexpr int kBlockThreads = kThreads + 32;      // consumers + one producer warp
-constexpr int kInStride = 8832;                   // tile bytes + phase + rounding + over-read
-constexpr int kChunksPerThread = kTileElems / 8 / kThreads;  // 4
-constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
-constexpr int kTabEntries = 256 * 8;                         // nvfp4 quotient table
-
-static_assert(kInStride >= kMaxTileBytes + 15 + 15 + 12, "stage size");
-static_assert(kInStride % 128 == 0, "stage alignment");
-
-// Written by the producer before it arms the stage's full barrier.
-struct StageInfo {
-    DevTensor t;      // the tile's tensor
-    uint64_t block0;  // first block of the tile within the tensor
-    uint32_t nb;      // blocks in the tile
-    uint32_t phase;   // byte offset of the first block within the stage (0..15)
-    uint32_t nv_tab;  // nvfp4: the whole tile uses the divisor the shared table was built for
-    uint32_t pad[11];
-};
-static_assert(sizeof(StageInfo) == 128, "StageInfo layout");
-
-struct SmemHdr {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    float lut_iq4[16];  // IQ4_NL table ("Packed layouts and decoding")
-    float lut_v[16];    // doubled E2M1 table V ("Ternary and block-floating formats")
-    uint32_t tab_bits;  // divisor bits the nvfp4 table was built for
-    int32_t tab_valid;
-    int32_t pad[30];
-    StageInfo info[kStages];
-};
-
-constexpr int kHdrBytes = (sizeof(SmemHdr) + 127) / 128 * 128;
-
-__constant__ int8_t c_iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
-__constant__ int8_t c_v[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
-
-// ---------------------------------------------------------------------------
-// PTX wrappers: mbarrier, bulk copy, global timer.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: true once the phase with `parity` has completed, false after
-// kWaitLimitNs of global time.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
-}
-
-// TMA bulk copy global -> shared, completing `bytes` of transaction count on
-// `bar`.  dst, src and bytes are multiples of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// Shared-memory byte access and exact scalar constructions.
-// ---------------------------------------------------------------------------
-// 16-bit little-endian field at byte offset `off` of a 16-byte-aligned stage.
-// With PH (a stage decoded at a nonzero byte phase) the field may be
-// unaligned.
-template <bool PH>
-__device__ __forceinline__ uint32_t lds_2(const uint8_t* base, uint32_t off) {
-    if (PH) {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
-        return __funnelshift_r(w[0], w[1], (off & 3u) * 8u) & 0xffffu;
-    }
-    return *reinterpret_cast<const uint16_t*>(base + off);
-}
-
-// 8 bytes at byte offset `off` of a 16-byte-aligned stage.
-__device__ __forceinline__ uint2 lds_8(const uint8_t* base, uint32_t off) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
-    const uint32_t sh = (off & 3u) * 8u;
-    const uint32_t a = w[0], b = w[1], c = w[2];
-    return make_uint2(__funnelshift_r(a, b, sh), __funnelshift_r(b, c, sh));
-}
-
-// 4 bytes at byte offset `off`.
-__device__ __forceinline__ uint32_t lds_4(const uint8_t* base, uint32_t off) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
-    return __funnelshift_r(w[0], w[1], (off & 3u) * 8u);
-}
-
-// Exact binary16 -> binary32 (the specification's H).
-__device__ __forceinline__ float h2f(uint32_t h) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-}
-
-// Byte I of w (0..255) as the float 2^23 + byte, minus `bias`: exact for the
-// small integers involved (bias = 2^23 + code offset).
-template <int I>
-__device__ __forceinline__ float byte_minus(uint32_t w, float bias) {
-    return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)), bias);
-}
-
-// MXFP4 half scale: the FLOAT with bit pattern 0x00200000 * 2^e for e < 2,
-// (e-1) * 2^23 otherwise ("Ternary and block-floating formats").
-__device__ __forceinline__ float e8m0_half(uint32_t e) {
-    return __uint_as_float(e < 2u ? (0x00200000u << e) : ((e - 1u) << 23));
-}
-
-// gguf:nvfp4 unsigned-E4M3 half scale: 0 for bytes 0 and 127; otherwise,
-// with E = bits 6:3 and m = bits 2:0 (bit 7 ignored), m * 2^-10 when E == 0
-// and (1 + m/8) * 2^(E-8) else (exponent field E + 119, mantissa m << 20).
-__device__ __forceinline__ float ue4m3_half(uint32_t e) {
-    const uint32_t E = (e >> 3) & 15u, m = e & 7u;
-    const float r = (E == 0u) ? __fmul_rn(static_cast<float>(m), 0.0009765625f)
-                              : __uint_as_float(((E + 119u) << 23) | (m << 20));
-    return (e == 0u || e == 127u) ? 0.0f : r;
-}
-
-// E4M3FN word (NInfer tensor-formats section 3.3): bias 7, subnormal
-// m * 2^-9, e == 15 && m == 7 NaN, sign applies to every word.
-__device__ __forceinline__ float e4m3fn(uint32_t w) {
-    const uint32_t e = (w >> 3) & 15u, m = w & 7u;
-    float mag;
-    if (e == 15u && m == 7u)
-        mag = __uint_as_float(0x7fc00000u);
-    else if (e == 0u)
-        mag = __fmul_rn(static_cast<float>(m), 0.001953125f);
-    else
-        mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
-    return (w & 0x80u) ? -mag : mag;
-}
-
-// E2M1 word (section 3.3): positive words 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6;
-// bit 3 negates (0x8 is -0).
-__device__ __forceinline__ float e2m1(uint32_t c) {
-    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-    const float mag = (e == 0u) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
-    return (c & 8u) ? -mag : mag;
-}
-
-// Little-endian FP32 word at any byte address (global memory).
-__device__ __forceinline__ float load_f32_bytes(const uint8_t* p) {
-    const uint32_t u = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
-                       (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24);
-    return __uint_as_float(u);
-}
-
-// ---------------------------------------------------------------------------
-// Per-format chunk decoders: chunk c of a tile = output elements 8c..8c+7 of
-// the tile, produced from the tile's payload bytes staged at `in` (byte
-// phase `ph`: the tile's first block starts at in + ph).
-// ---------------------------------------------------------------------------
-struct Ctx {
-    const SmemHdr* H;
-    const float* tab;  // nvfp4 quotient table, or nullptr for per-element division
-    const uint8_t* divs;
-    uint64_t block0;
-    uint64_t blocks_per_div;
-};
-
-template <int F>
-struct Fmt;
-
-// gguf:q8_0 / q8_g32_fp16: y[j] = M(d, q[j]), q signed bytes.
-template <>
-struct Fmt<KF_Q8_0> {
-    static constexpr int B = 32, S = 34, CPB = 4;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 2) * S;
-        const float d = h2f(lds_2<PH>(in, off));
-        const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
-        const uint32_t a = q.x ^ 0x80808080u, b = q.y ^ 0x80808080u;  // signed -> offset-128
-        const float bias = 8388736.0f;                                 // 2^23 + 128
-        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
-    }
-};
-
-// Nibble plane p (0 = low, 1 = high) of 8 consecutive code bytes, as bytes.
-__device__ __forceinline__ void nib_plane(uint2 q, uint32_t p, uint32_t& a, uint32_t& b) {
-    a = (q.x >> (4u * p)) & 0x0F0F0F0Fu;
-    b = (q.y >> (4u * p)) & 0x0F0F0F0Fu;
-}
-
-// gguf:q4_0: v = P(q,4,16); y[j] = M(d, v[j] - 8).  Chunk c&3: bytes 8*(c&1)
-// of q, plane c>>1 (16 low nibbles, then 16 high nibbles).
-template <>
-struct Fmt<KF_Q4_0> {
-    static constexpr int B = 32, S = 18, CPB = 4;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
-        const float d = h2f(lds_2<PH>(in, off));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
-        const float bias = 8388616.0f;  // 2^23 + 8
-        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
-    }
-};
-
-// Table lookup of 8 nibbles (bytes of a, then b) scaled by d: y = M(d, T[v]).
-__device__ __forceinline__ void lut8(const float* T, float d, uint32_t a, uint32_t b, float* v) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[i] = __fmul_rn(d, T[(a >> (8 * i)) & 15u]);
-        v[4 + i] = __fmul_rn(d, T[(b >> (8 * i)) & 15u]);
-    }
-}
-
-// gguf:iq4_nl: v = P(q,4,16); y[j] = M(d, IQ4[v[j]]).
-template <>
-struct Fmt<KF_IQ4_NL> {
-    static constexpr int B = 32, S = 18, CPB = 4;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
-                                                 const Ctx& x) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
-        const float d = h2f(lds_2<PH>(in, off));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(x.H->lut_iq4, d, a, b, v);
-    }
-};
-
-// gguf:mxfp4: d = E8M0 half scale; v = P(q,4,16); y[j] = M(d, V[v[j]]).
-template <>
-struct Fmt<KF_MXFP4> {
-    static constexpr int B = 32, S = 17, CPB = 4;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
-                                                 const Ctx& x) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
-        const float d = e8m0_half(in[off]);
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 1u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(x.H->lut_v, d, a, b, v);
-    }
-};
-
-// gguf:nvfp4: group g = (c&7)>>1 of 16 values: d = unsigned-E4M3 half scale of
-// scales[g]; v = P(q[8g:8g+8],4,8); y[16g+j] = M(d, V[v[j]]).
-template <>
-struct Fmt<KF_GGUF_NVFP4> {
-    static constexpr int B = 64, S = 36, CPB = 8;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
-                                                 const Ctx& x) {
-        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
-        const float d = ue4m3_half(in[off + g]);
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        lut8(x.H->lut_v, d, a, b, v);
-    }
-};
-
-// nvfp4 (NInfer section 3.3): W = e2m1(c) * e4m3fn(s) / d_w, the product exact
-// and the quotient rounded once.  With a quotient table (one divisor for the
-// whole tile) the element is tab[s*8 + (c&7)] with the sign of bit 3 applied
-// (RNE division is odd-symmetric, and (-0)*s/d_w is the negated (+0)*s/d_w).
-template <>
-struct Fmt<KF_NVFP4> {
-    static constexpr int B = 64, S = 36, CPB = 8;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
-                                                 const Ctx& x) {
-        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
-        const uint32_t s = in[off + g];
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        if (x.tab) {
-            const uint32_t* T = reinterpret_cast<const uint32_t*>(x.tab) + s * 8u;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t ca = (a >> (8 * i)) & 15u, cb = (b >> (8 * i)) & 15u;
-                v[i] = __uint_as_float(T[ca & 7u] ^ ((ca & 8u) << 28));
-                v[4 + i] = __uint_as_float(T[cb & 7u] ^ ((cb & 8u) << 28));
-            }
-        } else {  // divisor of this block, then divide
-            const float dw = load_f32_bytes(x.divs + 4u * ((x.block0 + (c >> 3)) / x.blocks_per_div));
-            const float sc = e4m3fn(s);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[i] = __fdiv_rn(__fmul_rn(e2m1((a >> (8 * i)) & 15u), sc), dw);
-                v[4 + i] = __fdiv_rn(__fmul_rn(e2m1((b >> (8 * i)) & 15u), sc), dw);
-            }
-        }
-    }
-};
-
-// gguf:q4_k: v = P(q,4,32); 6-bit a[k], m[k] from the 12 scale bytes;
-// y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])), k = floor(j/32).
-// Chunk c&31: sub-block k = cc>>2, byte group cc>>3 (32 bytes), plane
-// (cc>>2)&1, bytes 8*(cc&3) of the group.
-template <>
-struct Fmt<KF_Q4_K> {
-    static constexpr int B = 256, S = 144, CPB = 32;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, k = cc >> 2;
-        const float d = h2f(lds_2<PH>(in, off)), dmin = h2f(lds_2<PH>(in, off + 2u));
-        const uint8_t* s = in + off + 4u;
-        uint32_t sa, sm;
-        if (k < 4u) {
-            sa = s[k] & 63u;
-            sm = s[k + 4u] & 63u;
-        } else {
-            sa = (s[k + 4u] & 15u) | ((s[k - 4u] >> 6) << 4);
-            sm = (s[k + 4u] >> 4) | ((s[k] >> 6) << 4);
-        }
-        const float da = __fmul_rn(d, static_cast<float>(sa));
-        const float dm = __fmul_rn(dmin, static_cast<float>(sm));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 16u + 32u * (cc >> 3) + 8u * (cc & 3u)), k & 1u, a, b);
-        const float bias = 8388608.0f;  // 2^23
-        v[0] = __fsub_rn(__fmul_rn(da, byte_minus<0>(a, bias)), dm);
-        v[1] = __fsub_rn(__fmul_rn(da, byte_minus<1>(a, bias)), dm);
-        v[2] = __fsub_rn(__fmul_rn(da, byte_minus<2>(a, bias)), dm);
-        v[3] = __fsub_rn(__fmul_rn(da, byte_minus<3>(a, bias)), dm);
-        v[4] = __fsub_rn(__fmul_rn(da, byte_minus<0>(b, bias)), dm);
-        v[5] = __fsub_rn(__fmul_rn(da, byte_minus<1>(b, bias)), dm);
-        v[6] = __fsub_rn(__fmul_rn(da, byte_minus<2>(b, bias)), dm);
-        v[7] = __fsub_rn(__fmul_rn(da, byte_minus<3>(b, bias)), dm);
-    }
-};
-
-// gguf:q6_k: l = P(low,4,64), h = P(high,2,32), s = scales[floor(j/16)] signed;
-// y[j] = M(M(d, s), l[j] + 16 h[j] - 32).  Chunk c&31 = elements 8cc..8cc+7:
-// low bytes 64*(cc>>4) + 8*(cc&7), plane (cc>>3)&1; high bytes
-// 32*(cc>>4) + 8*(cc&3), 2-bit plane (cc>>2)&3; scale index cc>>1.
-template <>
-struct Fmt<KF_Q6_K> {
-    static constexpr int B = 256, S = 210, CPB = 32;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
-        const float d = h2f(lds_2<PH>(in, off + 208u));
-        const int32_t sc = static_cast<int8_t>(in[off + 192u + (cc >> 1)]);
-        const float ds = __fmul_rn(d, static_cast<float>(sc));
-        const uint2 lo = lds_8(in, off + 64u * gi + 8u * (cc & 7u));
-        const uint2 hi = lds_8(in, off + 128u + 32u * gi + 8u * (cc & 3u));
-        const uint32_t pl = 4u * ((cc >> 3) & 1u), phh = 2u * ((cc >> 2) & 3u);
-        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> phh) & 0x03030303u) << 4);
-        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> phh) & 0x03030303u) << 4);
-        const float bias = 8388640.0f;  // 2^23 + 32
-        v[0] = __fmul_rn(ds, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(ds, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(ds, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(ds, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(ds, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(ds, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(ds, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(ds, byte_minus<3>(b, bias));
-    }
-};
-
-// q4_g64_fp16 (NInfer sections 5-6.2): w = binary32(s32 * q), q the 4-bit
-// two's-complement code; element k sits in bits 4*(k mod 2) of code byte
-// floor(k/2) (layout reading).  XOR 8 maps two's complement to offset-8.
-template <>
-struct Fmt<KF_Q4_G64> {
-    static constexpr int B = 64, S = 34, CPB = 8;
-    template <bool PH>
-    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 3) * S;
-        const float s = h2f(lds_2<PH>(in, off));
-        const uint32_t w = lds_4(in, off + 2u + 4u * (c & 7u));
-        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-        const float bias = 8388616.0f;  // 2^23 + 8
-        v[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
-        v[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
-        v[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
-        v[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
-        v[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
-        v[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
-        v[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
-        v[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
-    }
-};
-
-// ---------------------------------------------------------------------------
-// Output stage: one RNE conversion per element, 16-byte stores when y is
-// 16-byte aligned (element offsets are multiples of 8, so every chunk then
-// starts on a 16-byte boundary).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-template <int O>
-__device__ __forceinline__ void store8(void* y, uint64_t e0, const float* v, bool vec) {
-    if (O == KO_F32) {
-        float* p = static_cast<float*>(y) + e0;
-        if (vec) {
-            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = v[i];
-        }
-    } else if (O == KO_F64) {
-        double* p = static_cast<double*>(y) + e0;
-        if (vec) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                reinterpret_cast<double2*>(p)[i] =
-                    make_double2(static_cast<double>(v[2 * i]), static_cast<double>(v[2 * i + 1]));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = static_cast<double>(v[i]);
-        }
-    } else {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
-        uint16_t* p = static_cast<uint16_t*>(y) + e0;
-        if (vec) {
-            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p[2 * i] = static_cast<uint16_t>(w[i] & 0xffffu);
-                p[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
-            }
-        }
-    }
-}
-
-template <int F, int O, bool PH>
-__device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
-    using Fm = Fmt<F>;
-    const uint32_t nch = si.nb * static_cast<uint32_t>(Fm::CPB);
-    const uint64_t e_base = si.block0 * static_cast<uint64_t>(Fm::B);
-    const bool vec = si.t.yvec != 0;
-    void* y = si.t.y;
-    const uint32_t ph = PH ? si.phase : 0u;
-#pragma unroll
-    for (int k = 0; k < kChunksPerThread; ++k) {
-        const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
-        if (c < nch) {
-            float v[8];
-            Fm::template chunk<PH>(in, ph, c, v, x);
-            store8<O>(y, e_base + 8ull * c, v, vec);
-        }
-    }
-}
-
-template <int F, int O>
-__device__ __forceinline__ void decode_tile_fo(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
-    if (si.phase == 0u)
-        decode_tile_fop<F, O, false>(si, in, x, tid);
-    else
-        decode_tile_fop<F, O, true>(si, in, x, tid);
-}
-
-template <int F>
-__device__ __forceinline__ void decode_tile_f(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
-    switch (si.t.out) {
-        case KO_F32: decode_tile_fo<F, KO_F32>(si, in, x, tid); break;
-        case KO_F16: decode_tile_fo<F, KO_F16>(si, in, x, tid); break;
-        case KO_BF16: decode_tile_fo<F, KO_BF16>(si, in, x, tid); break;
-        default: decode_tile_fo<F, KO_F64>(si, in, x, tid); break;
-    }
-}
-
-__device__ __forceinline__ void decode_tile(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
-    switch (si.t.fmt) {
-        case KF_Q8_0: decode_tile_f<KF_Q8_0>(si, in, x, tid); break;
-        case KF_Q4_0: decode_tile_f<KF_Q4_0>(si, in, x, tid); break;
-        case KF_IQ4_NL: decode_tile_f<KF_IQ4_NL>(si, in, x, tid); break;
-        case KF_Q4_K: decode_tile_f<KF_Q4_K>(si, in, x, tid); break;
-        case KF_Q6_K: decode_tile_f<KF_Q6_K>(si, in, x, tid); break;
-        case KF_MXFP4: decode_tile_f<KF_MXFP4>(si, in, x, tid); break;
-        case KF_GGUF_NVFP4: decode_tile_f<KF_GGUF_NVFP4>(si, in, x, tid); break;
-        case KF_NVFP4: decode_tile_f<KF_NVFP4>(si, in, x, tid); break;
-        default: decode_tile_f<KF_Q4_G64>(si, in, x, tid); break;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Producer warp (lane 0): stages tiles it = 0, 1, ... of this CTA.
-// ---------------------------------------------------------------------------
-__device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
-    const uint64_t grid = gridDim.x;
-    int32_t di = 0;   // current tensor (tiles of a CTA increase, so it only moves forward)
-    int issued = 0;   // tiles staged so far
-    bool fault = false;
-    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
-        const int s = issued % kStages;
-        if (issued >= kStages &&
-            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1))) {
-            fault = true;
-            break;
-        }
-        if (p.table)
-            while (di + 1 < p.n && p.table[di + 1].tile_begin <= tile) ++di;
-        const DevTensor& t = p.table ? p.table[di] : p.single;
-        StageInfo& si = H.info[s];
-        si.t = t;
-        const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
-        const uint64_t left = t.nblocks - b0;
-        const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
-        const uint8_t* src = t.x + b0 * t.S;
-        const uint32_t phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-        const uint32_t bytes = (phase + nb * t.S + 15u) & ~15u;
-        si.block0 = b0;
-        si.nb = nb;
-        si.phase = phase;
-        uint32_t nv_tab = 0;
-        if (t.fmt == KF_NVFP4 && H.tab_valid) {
-            const uint64_t d0 = b0 / t.blocks_per_div, d1 = (b0 + nb - 1u) / t.blocks_per_div;
-            nv_tab = d0 == d1 && __float_as_uint(load_f32_bytes(t.divs + 4u * d0)) == H.tab_bits;
-        }
-        si.nv_tab = nv_tab;
-        mbar_arrive_expect_tx(&H.full[s], bytes);
-        bulk_load(inbuf + s * kInStride, src - phase, bytes, &H.full[s]);
-    }
-    if (fault) {
-        atomicOr(&g_fault_word, 1u);
-        // Wait (bounded) for every copy still in flight: the last kStages
-        // stagings, whose full phases are the latest ones of their stages.
-        for (int j = issued - kStages; j < issued; ++j)
-            if (j >= 0) mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
-    }
-}
-
-__global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* inbuf = smem;
-    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
-    float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
-    const uint32_t tid = threadIdx.x;
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&H.full[s], 1);
-            mbar_init(&H.empty[s], kConsumerWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        H.tab_valid = 0;
-    }
-    if (tid < 16) {
-        H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
-        H.lut_v[tid] = static_cast<float>(c_v[tid]);
-    }
-    // nvfp4: build the quotient table for the first divisor of the first
-    // nvfp4 tensor of the launch; tiles with another divisor divide per element.
-    if (p.nv_index >= 0) {
-        const DevTensor& t = p.table ? p.table[p.nv_index] : p.single;
-        const float dw = load_f32_bytes(t.divs);
-        for (uint32_t i = tid; i < kTabEntries; i += kBlockThreads)
-            tab[i] = __fdiv_rn(__fmul_rn(e2m1(i & 7u), e4m3fn(i >> 3)), dw);
-        if (tid == 0) {
-            H.tab_bits = __float_as_uint(dw);
-            H.tab_valid = 1;
-        }
-    }
-    __syncthreads();
-
-    if (tid >= kThreads) {  // producer warp
-        if (tid == kThreads) producer(p, H, inbuf);
-        return;
-    }
-
-    // consumer warps
-    const uint64_t grid = gridDim.x;
-    const uint32_t lane = tid & 31u;
-    int it = 0;
-    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
-        const int s = it % kStages;
-        if (!mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1))) {
-            if (lane == 0) atomicOr(&g_fault_word, 2u);
-            return;
-        }
-        const StageInfo& si = H.info[s];
-        Ctx x{&H, nullptr, nullptr, 0, 1};
-        if (si.t.fmt == KF_NVFP4) {
-            x.tab = si.nv_tab ? tab : nullptr;
-            x.divs = si.t.divs;
-            x.block0 = si.block0;
-            x.blocks_per_div = si.t.blocks_per_div;
-        }
-        decode_tile(si, inbuf + s * kInStride, x, tid);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&H.empty[s]);
-    }
-}
 
 // Writes n descriptors (kernel parameters) into a device table.
 constexpr int kUploadChunk = 128;
@@ -705,17 +29,39 @@ __global__ void k_upload_table(const UploadParams p) {
     for (int i = threadIdx.x; i < p.n; i += blockDim.x) p.dst[i] = p.d[i];
 }
 
+// Specialised kernels live in one instantiation file per format.
+KernelFn pick_kernel(int fsel, int osel) {
+    if (osel < 0) return kernel_generic(-1);
+    switch (fsel) {
+        case KF_Q8_0: return kernel_q8_0(osel);
+        case KF_Q4_0: return kernel_q4_0(osel);
+        case KF_IQ4_NL: return kernel_iq4_nl(osel);
+        case KF_Q4_K: return kernel_q4_k(osel);
+        case KF_Q6_K: return kernel_q6_k(osel);
+        case KF_MXFP4: return kernel_mxfp4(osel);
+        case KF_GGUF_NVFP4: return kernel_gguf_nvfp4(osel);
+        case KF_NVFP4: return kernel_nvfp4(osel);
+        case KF_Q4_G64: return kernel_q4_g64(osel);
+        default: return kernel_generic(osel);
+    }
+}
+
+constexpr int kKernelSlots = (KF_COUNT + 1) * 5;
+
+int slot_of(int fsel, int osel) { return (osel < 0) ? 0 : (fsel + 1) * 5 + osel + 1; }
+
 struct DeviceInfo {
     int sms = 0;
-    int ctas_per_sm[2] = {0, 0};
+    int ctas_per_sm[kKernelSlots][2] = {};  // 0 = not yet queried
 };
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 
-size_t smem_bytes(bool tab) {
-    return static_cast<size_t>(kStages * kInStride + kHdrBytes) + (tab ? kTabEntries * sizeof(float) : 0);
-}
+size_t smem_bytes(bool tab) { return decode_smem_bytes(tab); }
+
+// Device address of the fault word, resolved once per device.
+unsigned int* g_fault_addr[kMaxDevices];
 
 }  // namespace
 
@@ -727,27 +73,40 @@ int launch_decode(const KParams& p, void* stream) {
     if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
     const bool tab = p.nv_index >= 0;
     const size_t smem = smem_bytes(tab);
+    const int fsel = (p.fsel >= 0 && p.fsel < KF_COUNT) ? p.fsel : -1;
+    const int osel = (p.osel >= 0 && p.osel <= KO_F64) ? p.osel : -1;
+    const KernelFn fn = pick_kernel(fsel, osel);
     DeviceInfo& di = g_dev[dev];
-    // Benign race: concurrent first calls compute the same values.
+    // Benign race: concurrent first calls compute and store the same values.
     if (di.sms == 0) {
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return static_cast<int>(e);
-        e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes(true)));
-        if (e != cudaSuccess) return static_cast<int>(e);
-        for (int i = 0; i < 2; ++i) {
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode, kBlockThreads, smem_bytes(i == 1));
-            if (e != cudaSuccess) return static_cast<int>(e);
-            di.ctas_per_sm[i] = n > 0 ? n : 1;
-        }
         di.sms = sms;
     }
-    const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(di.ctas_per_sm[tab ? 1 : 0]);
+    int& cps = di.ctas_per_sm[slot_of(fsel, osel)][tab ? 1 : 0];
+    if (cps == 0) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes(true)));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        cps = n > 0 ? n : 1;
+    }
+    if (!g_fault_addr[dev]) {
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_fault_word);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        g_fault_addr[dev] = static_cast<unsigned int*>(addr);
+    }
+    KParams q = p;
+    q.fault = g_fault_addr[dev];
+    const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
-    k_decode<<<grid, kBlockThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    void* args[] = {&q};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
+                         static_cast<cudaStream_t>(stream));
+    return static_cast<int>(e);
 }
 
 int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream) {
@@ -801,6 +160,12 @@ int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, 
     p.n = n;
     p.nv_index = nv_index;
     p.total_tiles = total_tiles;
+    p.fsel = table[0].fmt;
+    p.osel = table[0].out;
+    for (int i = 1; i < n; ++i) {
+        if (table[i].fmt != p.fsel) p.fsel = -1;
+        if (table[i].out != p.osel) p.osel = -1;
+    }
     return launch_decode(p, stream);
 }
 
