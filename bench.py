@@ -80,6 +80,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over all ranks (the slowest rank sets the job time)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -409,13 +426,9 @@ def end_to_end(args, torch, ndq, work, x_host, x_dev, y_dev, stream, world, step
         one_step()
     b.record(stream)
     b.synchronize()
-    e_ms = a.elapsed_time(b) / e_steps
-    if world > 1:
-        t = torch.tensor([e_ms], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, "cuda")
     del y_host
-    return {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(job_gbs(step_bytes, world, e_ms), 2), "unit": "GB/s",
             "ms_per_step": round(e_ms, 3), "steps": e_steps,
             "h2d_bytes_per_step": work.x_total, "d2h_bytes_per_step": work.y_total,
             "link_alone_GB/s": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1)},
@@ -489,13 +502,9 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, "cuda")
     step_bytes = work.bytes_in + work.bytes_out
-    value = world * step_bytes / (ms * 1e-3) / 1e9
+    value = job_gbs(step_bytes, world, ms)
     if ndq.get_device_fault():
         raise RuntimeError("device fault word set during the timed region")
 

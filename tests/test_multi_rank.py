@@ -1,0 +1,50 @@
+"""Multi-rank host logic of the benchmark, on CPU with the gloo backend
+(world size 2): the job time is the slowest rank's, the job throughput counts
+every rank's bytes, and the reference arm does work on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(1.0 + 2.5 * rank, "cpu")  # rank 1 is slower
+        out[rank] = (ms, bench.job_gbs(1_000_000_000, world, ms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput():
+    world, port = 2, _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+    for rank in range(world):
+        ms, gbs = out[rank]
+        assert ms == pytest.approx(3.5)
+        assert gbs == pytest.approx(2 * 1e9 / 3.5e-3 / 1e9)
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(4.25, "cpu") == 4.25
+    assert bench.job_gbs(2_000_000_000, 1, 1000.0) == pytest.approx(2.0)
+
+
+def test_reference_arm_does_nothing_on_other_ranks(capsys):
+    class A:
+        steps, warmup = 1, 0
+    bench.run_reference(A(), rank=1, world=2)
+    assert capsys.readouterr().out == ""
