@@ -77,7 +77,13 @@ struct SmemHdr {
     float lut_v[16];    // doubled E2M1 table V ("Ternary and block-floating formats")
     uint32_t tab_bits;  // divisor bits the nvfp4 table was built for
     int32_t tab_valid;
-    int32_t pad[30];
+    // nvfp4 per-scale quotients: nv_q[s] = (RN(s/d_w), RN(1.5*s/d_w)); bit s
+    // of nv_ok is set when every code of scale byte s is reproduced exactly
+    // by nv_q and nv_code (checked against the full table at build time).
+    uint32_t nv_ok[8];
+    uint2 nv_code[16];  // per E2M1 code: prmt selector of Q1/Q15, bits of +-2^k or +-0
+    float2 nv_q[256];
+    int32_t pad[6];
     StageInfo info[kStages];
 };
 
@@ -367,7 +373,20 @@ struct Fmt<KF_NVFP4> {
         const uint32_t s = in[off + g];
         uint32_t a, b;
         nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        if (x.tab) {
+        if (x.tab && ((x.H->nv_ok[s >> 5] >> (s & 31u)) & 1u)) {
+            // Every E2M1 magnitude is 2^k * {1, 1.5}: the element is the exact
+            // quotient for m = 1 or 1.5 times +-2^k (or +-0).  Both lookups hit
+            // 16-entry tables, so a warp's accesses never conflict in banks.
+            const float2 q = x.H->nv_q[s];
+            const uint32_t q1 = __float_as_uint(q.x), q15 = __float_as_uint(q.y);
+            const uint2* K = x.H->nv_code;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint2 ka = K[(a >> (8 * i)) & 15u], kb = K[(b >> (8 * i)) & 15u];
+                v[i] = __fmul_rn(__uint_as_float(__byte_perm(q1, q15, ka.x)), __uint_as_float(ka.y));
+                v[4 + i] = __fmul_rn(__uint_as_float(__byte_perm(q1, q15, kb.x)), __uint_as_float(kb.y));
+            }
+        } else if (x.tab) {
             const float* T = x.tab + s * 16u;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -699,9 +718,36 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
             tab[16u * sb + c] = q;
             tab[16u * sb + c + 8u] = __uint_as_float(__float_as_uint(q) ^ 0x80000000u);
         }
+        if (tid < 256) {  // per-scale quotients for m = 1 and m = 1.5 (1.5*s is exact)
+            const float sc = e4m3fn(tid);
+            H.nv_q[tid] = make_float2(__fdiv_rn(sc, dw), __fdiv_rn(__fmul_rn(1.5f, sc), dw));
+        }
+        if (tid < 16) {  // E2M1 code c = 2^k * m: selector of Q_m and +-2^k (+-0 for zero codes)
+            const uint32_t e = (tid >> 1) & 3u, m = tid & 1u;
+            const bool half = (e >= 1u) && m;  // magnitudes 1.5, 3, 6
+            const float scale = (e == 0u) ? (m ? 0.5f : 0.0f) : __uint_as_float((e + 126u) << 23);
+            H.nv_code[tid] = make_uint2(half ? 0x7654u : 0x3210u,
+                                        __float_as_uint(scale) | ((tid & 8u) ? 0x80000000u : 0u));
+        }
+        if (tid < 8) H.nv_ok[tid] = 0u;
         if (tid == 0) {
             H.tab_bits = __float_as_uint(dw);
             H.tab_valid = 1;
+        }
+    }
+    __syncthreads();
+    if (p.nv_index >= 0) {  // verify the per-scale form against the table, scale byte by scale byte
+        for (uint32_t sb = tid; sb < 256u; sb += kBlockThreads) {
+            const float2 q = H.nv_q[sb];
+            bool ok = true;
+            for (uint32_t c = 0; c < 16u; ++c) {
+                const uint2 k = H.nv_code[c];
+                const float v = __fmul_rn(__uint_as_float(__byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), k.x)),
+                                          __uint_as_float(k.y));
+                const float w = tab[16u * sb + c];
+                ok = ok && ((w != w) ? (v != v) : (__float_as_uint(v) == __float_as_uint(w)));
+            }
+            if (ok) atomicOr(&H.nv_ok[sb >> 5], 1u << (sb & 31u));
         }
     }
     __syncthreads();
