@@ -234,8 +234,12 @@ def cpu_oracle_sample(work: ModelWorkload, x_host_np, fraction: int, cores: int)
 # our arm
 # --------------------------------------------------------------------------
 def kernel_source_sha() -> str:
-    p = os.path.join(ROOT, "quantized_weight_block_gb300", "csrc", "ndq_kernels.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+    """Hash of the decode kernel's sources (device code, launcher, shared header)."""
+    h = hashlib.sha256()
+    for f in ("ndq_device.cuh", "ndq_kernels.cu", "ndq_internal.h"):
+        with open(os.path.join(ROOT, "quantized_weight_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def profiled_traffic(profile_name: str):

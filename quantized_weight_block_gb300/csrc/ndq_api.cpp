@@ -149,17 +149,6 @@ uint64_t tiles_of(const ndq::DevTensor& t) { return (t.nblocks + t.bpt - 1) / t.
 
 constexpr size_t kWorkspaceAlign = 16;
 
-// Format and output type shared by every tensor of a launch (-1 if mixed):
-// they select the specialised kernel.
-void shared_selectors(const ndq::DevTensor* t, int n, int32_t* fsel, int32_t* osel) {
-    *fsel = t[0].fmt;
-    *osel = t[0].out;
-    for (int i = 1; i < n; ++i) {
-        if (t[i].fmt != *fsel) *fsel = -1;
-        if (t[i].out != *osel) *osel = -1;
-    }
-}
-
 }  // namespace
 
 extern "C" {
@@ -275,7 +264,7 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc* descs, int n, void* wor
     p.n = static_cast<int32_t>(table.size());
     p.nv_index = nv_index;
     p.total_tiles = tiles;
-    shared_selectors(table.data(), static_cast<int>(table.size()), &p.fsel, &p.osel);
+    ndq::select_kernel(table.data(), static_cast<int>(table.size()), &p.fsel, &p.osel);
     return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
 

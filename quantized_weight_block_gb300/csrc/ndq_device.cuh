@@ -53,7 +53,6 @@ namespace ndq {
 namespace {
 
 constexpr int kConsumerWarps = kThreads / 32;     // 8
-constexpr int kChunksPerThread = kTileElems / 8 / kThreads;  // 4
 constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
 
 static_assert(kInStride >= kMaxTileBytes + 15 + 15 + 12, "stage size");
@@ -239,9 +238,12 @@ __device__ __forceinline__ float load_f32_bytes(const uint8_t* p) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-format chunk decoders: chunk c of a tile = output elements 8c..8c+7 of
-// the tile, produced from the tile's payload bytes staged at `in` (byte
-// phase `ph`: the tile's first block starts at in + ph).
+// Per-format chunk decoders: chunk c of a tile = output elements
+// CE*c..CE*c+CE-1 of the tile (CE = 16, or 8 for nvfp4: consecutive elements
+// of one block), produced from the tile's payload bytes staged at `in` (byte
+// phase `ph`: the tile's first block starts at in + ph).  A warp's 32 chunks
+// cover 32*CE consecutive outputs; per-chunk work (addresses, scale decode,
+// loads) is shared by CE elements.
 // ---------------------------------------------------------------------------
 struct Ctx {
     const SmemHdr* H;
@@ -251,134 +253,162 @@ struct Ctx {
     uint64_t blocks_per_div;
 };
 
+// 16 bytes at byte offset `off` of a 16-byte-aligned stage (ALIGNED: off is a
+// multiple of 16, one 16-byte load).
+template <bool ALIGNED>
+__device__ __forceinline__ uint4 lds_16(const uint8_t* base, uint32_t off) {
+    if (ALIGNED) return *reinterpret_cast<const uint4*>(base + off);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    const uint32_t sh = (off & 3u) * 8u;
+    const uint32_t a = w[0], b = w[1], c = w[2], d = w[3], e = w[4];
+    return make_uint4(__funnelshift_r(a, b, sh), __funnelshift_r(b, c, sh), __funnelshift_r(c, d, sh),
+                      __funnelshift_r(d, e, sh));
+}
+
+// Four bytes of w (values < 256) as exact floats minus the code offset, times
+// d: v[i] = M(d, byte_i - offset) with bias = 2^23 + offset.
+__device__ __forceinline__ void mul4(float d, uint32_t w, float bias, float* v) {
+    v[0] = __fmul_rn(d, byte_minus<0>(w, bias));
+    v[1] = __fmul_rn(d, byte_minus<1>(w, bias));
+    v[2] = __fmul_rn(d, byte_minus<2>(w, bias));
+    v[3] = __fmul_rn(d, byte_minus<3>(w, bias));
+}
+
+// Table lookup of four nibbles (bytes of w) scaled by d: v[i] = M(d, T[n_i]).
+__device__ __forceinline__ void lut4(const float* T, float d, uint32_t w, float* v) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(d, T[(w >> (8 * i)) & 15u]);
+}
+
 template <int F>
 struct Fmt;
 
-// gguf:q8_0 / q8_g32_fp16: y[j] = M(d, q[j]), q signed bytes.
+// gguf:q8_0 / q8_g32_fp16: y[j] = M(d, q[j]), q signed bytes; chunk c&1 holds
+// q[16*(c&1) .. +16].
 template <>
 struct Fmt<KF_Q8_0> {
-    static constexpr int B = 32, S = 34, CPB = 4;
+    static constexpr int B = 32, S = 34, CE = 16, CPB = 2;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 2) * S;
+        const uint32_t off = ph + (c >> 1) * S;
         const float d = h2f(lds_2<PH>(in, off));
-        const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
-        const uint32_t a = q.x ^ 0x80808080u, b = q.y ^ 0x80808080u;  // signed -> offset-128
-        const float bias = 8388736.0f;                                 // 2^23 + 128
-        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+        const uint4 q = lds_16<false>(in, off + 2u + 16u * (c & 1u));
+        const float bias = 8388736.0f;  // 2^23 + 128; XOR 0x80 maps signed to offset-128
+        mul4(d, q.x ^ 0x80808080u, bias, v);
+        mul4(d, q.y ^ 0x80808080u, bias, v + 4);
+        mul4(d, q.z ^ 0x80808080u, bias, v + 8);
+        mul4(d, q.w ^ 0x80808080u, bias, v + 12);
     }
 };
 
-// Nibble plane p (0 = low, 1 = high) of 8 consecutive code bytes, as bytes.
-__device__ __forceinline__ void nib_plane(uint2 q, uint32_t p, uint32_t& a, uint32_t& b) {
-    a = (q.x >> (4u * p)) & 0x0F0F0F0Fu;
-    b = (q.y >> (4u * p)) & 0x0F0F0F0Fu;
+// Nibble plane p (0 = low, 1 = high) of 16 consecutive code bytes, as bytes.
+__device__ __forceinline__ uint4 nib_plane16(uint4 q, uint32_t p) {
+    const uint32_t s = 4u * p;
+    return make_uint4((q.x >> s) & 0x0F0F0F0Fu, (q.y >> s) & 0x0F0F0F0Fu, (q.z >> s) & 0x0F0F0F0Fu,
+                      (q.w >> s) & 0x0F0F0F0Fu);
 }
 
-// gguf:q4_0: v = P(q,4,16); y[j] = M(d, v[j] - 8).  Chunk c&3: bytes 8*(c&1)
-// of q, plane c>>1 (16 low nibbles, then 16 high nibbles).
+// gguf:q4_0: v = P(q,4,16) (16 low nibbles, then 16 high nibbles), so chunk
+// c&1 is plane c&1 of the 16 code bytes; y[j] = M(d, v[j] - 8).
 template <>
 struct Fmt<KF_Q4_0> {
-    static constexpr int B = 32, S = 18, CPB = 4;
+    static constexpr int B = 32, S = 18, CE = 16, CPB = 2;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const uint32_t off = ph + (c >> 1) * S;
         const float d = h2f(lds_2<PH>(in, off));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
+        const uint4 n = nib_plane16(lds_16<false>(in, off + 2u), c & 1u);
         const float bias = 8388616.0f;  // 2^23 + 8
-        v[0] = __fmul_rn(d, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(d, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(d, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(d, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(d, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(d, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(d, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(d, byte_minus<3>(b, bias));
+        mul4(d, n.x, bias, v);
+        mul4(d, n.y, bias, v + 4);
+        mul4(d, n.z, bias, v + 8);
+        mul4(d, n.w, bias, v + 12);
     }
 };
-
-// Table lookup of 8 nibbles (bytes of a, then b) scaled by d: y = M(d, T[v]).
-__device__ __forceinline__ void lut8(const float* T, float d, uint32_t a, uint32_t b, float* v) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[i] = __fmul_rn(d, T[(a >> (8 * i)) & 15u]);
-        v[4 + i] = __fmul_rn(d, T[(b >> (8 * i)) & 15u]);
-    }
-}
 
 // gguf:iq4_nl: v = P(q,4,16); y[j] = M(d, IQ4[v[j]]).
 template <>
 struct Fmt<KF_IQ4_NL> {
-    static constexpr int B = 32, S = 18, CPB = 4;
+    static constexpr int B = 32, S = 18, CE = 16, CPB = 2;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
                                                  const Ctx& x) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const uint32_t off = ph + (c >> 1) * S;
         const float d = h2f(lds_2<PH>(in, off));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 2u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(x.H->lut_iq4, d, a, b, v);
+        const uint4 n = nib_plane16(lds_16<false>(in, off + 2u), c & 1u);
+        const float* T = x.H->lut_iq4;
+        lut4(T, d, n.x, v);
+        lut4(T, d, n.y, v + 4);
+        lut4(T, d, n.z, v + 8);
+        lut4(T, d, n.w, v + 12);
     }
 };
 
 // gguf:mxfp4: d = E8M0 half scale; v = P(q,4,16); y[j] = M(d, V[v[j]]).
 template <>
 struct Fmt<KF_MXFP4> {
-    static constexpr int B = 32, S = 17, CPB = 4;
+    static constexpr int B = 32, S = 17, CE = 16, CPB = 2;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
                                                  const Ctx& x) {
-        const uint32_t off = ph + (c >> 2) * S, cc = c & 3u;
+        const uint32_t off = ph + (c >> 1) * S;
         const float d = e8m0_half(in[off]);
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 1u + 8u * (cc & 1u)), cc >> 1, a, b);
-        lut8(x.H->lut_v, d, a, b, v);
+        const uint4 n = nib_plane16(lds_16<false>(in, off + 1u), c & 1u);
+        const float* T = x.H->lut_v;
+        lut4(T, d, n.x, v);
+        lut4(T, d, n.y, v + 4);
+        lut4(T, d, n.z, v + 8);
+        lut4(T, d, n.w, v + 12);
     }
 };
 
-// gguf:nvfp4: group g = (c&7)>>1 of 16 values: d = unsigned-E4M3 half scale of
-// scales[g]; v = P(q[8g:8g+8],4,8); y[16g+j] = M(d, V[v[j]]).
+// gguf:nvfp4: chunk c&3 is group g of 16 values: d = unsigned-E4M3 half scale
+// of scales[g]; v = P(q[8g:8g+8],4,8) (8 low nibbles, then 8 high);
+// y[16g+j] = M(d, V[v[j]]).
 template <>
 struct Fmt<KF_GGUF_NVFP4> {
-    static constexpr int B = 64, S = 36, CPB = 8;
+    static constexpr int B = 64, S = 36, CE = 16, CPB = 4;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
                                                  const Ctx& x) {
-        const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
+        const uint32_t off = ph + (c >> 2) * S, g = c & 3u;
         const float d = ue4m3_half(in[off + g]);
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
-        lut8(x.H->lut_v, d, a, b, v);
+        const uint2 q = lds_8(in, off + 4u + 8u * g);
+        const float* T = x.H->lut_v;
+        lut4(T, d, q.x & 0x0F0F0F0Fu, v);
+        lut4(T, d, q.y & 0x0F0F0F0Fu, v + 4);
+        lut4(T, d, (q.x >> 4) & 0x0F0F0F0Fu, v + 8);
+        lut4(T, d, (q.y >> 4) & 0x0F0F0F0Fu, v + 12);
     }
 };
 
 // nvfp4 (NInfer section 3.3): W = e2m1(c) * e4m3fn(s) / d_w, the product exact
-// and the quotient rounded once.  With a quotient table (one divisor for the
-// whole tile) the element is tab[16*s + c].
+// and the quotient rounded once.  Chunk c&3 is group g (scale byte g, codes
+// laid out as gguf:nvfp4).  With the per-scale quotients (the tile uses the
+// divisor the shared tables were built for, and scale byte s passed the
+// build-time check), the element is Q_m(s) * (+-2^k or +-0) for the code's
+// E2M1 magnitude 2^k * m; failing that, the full quotient table
+// tab[16*s + c]; for a tile that spans two divisors, a division.
 template <>
 struct Fmt<KF_NVFP4> {
-    static constexpr int B = 64, S = 36, CPB = 8;
+    // 8-element chunks: this decoder needs more registers than the others,
+    // and at 16 elements per chunk it loses a resident CTA per SM.
+    static constexpr int B = 64, S = 36, CE = 8, CPB = 8;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
                                                  const Ctx& x) {
+        // chunk c&7: group g = (c&7)>>1 (scale byte g), plane (c&1) of its 8 code bytes
         const uint32_t off = ph + (c >> 3) * S, cc = c & 7u, g = cc >> 1;
         const uint32_t s = in[off + g];
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 4u + 8u * g), cc & 1u, a, b);
+        const uint2 q = lds_8(in, off + 4u + 8u * g);
+        const uint32_t sh = 4u * (cc & 1u);
+        const uint32_t a = (q.x >> sh) & 0x0F0F0F0Fu, b = (q.y >> sh) & 0x0F0F0F0Fu;
         if (x.tab && ((x.H->nv_ok[s >> 5] >> (s & 31u)) & 1u)) {
-            // Every E2M1 magnitude is 2^k * {1, 1.5}: the element is the exact
-            // quotient for m = 1 or 1.5 times +-2^k (or +-0).  Both lookups hit
+            // Every E2M1 magnitude is 2^k * m, m in {1, 1.5}: the element is the
+            // exact quotient Q_m(s) times +-2^k (or +-0); both lookups are
             // 16-entry tables, so a warp's accesses never conflict in banks.
-            const float2 q = x.H->nv_q[s];
-            const uint32_t q1 = __float_as_uint(q.x), q15 = __float_as_uint(q.y);
+            const float2 qq = x.H->nv_q[s];
+            const uint32_t q1 = __float_as_uint(qq.x), q15 = __float_as_uint(qq.y);
             const uint2* K = x.H->nv_code;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -407,99 +437,103 @@ struct Fmt<KF_NVFP4> {
 
 // gguf:q4_k: v = P(q,4,32); 6-bit a[k], m[k] from the 12 scale bytes;
 // y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])), k = floor(j/32).
-// Chunk c&31: sub-block k = cc>>2, byte group cc>>3 (32 bytes), plane
-// (cc>>2)&1, bytes 8*(cc&3) of the group.
+// Chunk c&15 = elements 16cc..16cc+15: sub-block k = cc>>1, byte group cc>>2
+// (32 bytes), plane (cc>>1)&1, bytes 16*(cc&1) of the group.
 template <>
 struct Fmt<KF_Q4_K> {
-    static constexpr int B = 256, S = 144, CPB = 32;
+    static constexpr int B = 256, S = 144, CE = 16, CPB = 16;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, k = cc >> 2;
-        const float d = h2f(lds_2<PH>(in, off)), dmin = h2f(lds_2<PH>(in, off + 2u));
-        // Scale bytes s[0..11] as three words; with j = k mod 4, byte j of each
-        // word is s[j], s[j+4], s[j+8].  Both unpack rules are formed and one
-        // is selected, so the lanes of a warp (k = lane/4) do not diverge.
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, k = cc >> 1;
+        // Block header: d, dmin and the scale bytes s[0..11] as three words
+        // (byte j of word w is s[4w + j]); one 16-byte load when aligned.
+        const uint4 hdr = lds_16<!PH>(in, off);
+        const float d = h2f(hdr.x & 0xffffu), dmin = h2f(hdr.x >> 16);
+        // With j = k mod 4, byte j of each word is s[j], s[j+4], s[j+8].  Both
+        // unpack rules are formed and one is selected, so the lanes of a warp
+        // (k = (lane mod 16)/2) do not diverge.
         const uint32_t j8 = 8u * (k & 3u);
-        const uint32_t b0 = (lds_4(in, off + 4u) >> j8) & 0xffu;
-        const uint32_t b1 = (lds_4(in, off + 8u) >> j8) & 0xffu;
-        const uint32_t b2 = (lds_4(in, off + 12u) >> j8) & 0xffu;
+        const uint32_t b0 = (hdr.y >> j8) & 0xffu, b1 = (hdr.z >> j8) & 0xffu, b2 = (hdr.w >> j8) & 0xffu;
         const bool lo = k < 4u;
         const uint32_t sa = lo ? (b0 & 63u) : ((b2 & 15u) | ((b0 >> 6) << 4));
         const uint32_t sm = lo ? (b1 & 63u) : ((b2 >> 4) | ((b1 >> 6) << 4));
         const float da = __fmul_rn(d, static_cast<float>(sa));
-        const float dm = __fmul_rn(dmin, static_cast<float>(sm));
-        uint32_t a, b;
-        nib_plane(lds_8(in, off + 16u + 32u * (cc >> 3) + 8u * (cc & 3u)), k & 1u, a, b);
+        const float ndm = -__fmul_rn(dmin, static_cast<float>(sm));
+        const uint4 n = nib_plane16(lds_16<!PH>(in, off + 16u + 32u * (cc >> 2) + 16u * (cc & 1u)), k & 1u);
+        // D(M(da, v), dm) as one fused multiply-add: da = M(d, a) has at most
+        // 17 significant bits and v at most 4, so M(da, v) is exact in
+        // binary32 and the FMA rounds the same exact difference once (the
+        // product cannot overflow, and inf/NaN/zero cases match term by term).
         const float bias = 8388608.0f;  // 2^23
-        v[0] = __fsub_rn(__fmul_rn(da, byte_minus<0>(a, bias)), dm);
-        v[1] = __fsub_rn(__fmul_rn(da, byte_minus<1>(a, bias)), dm);
-        v[2] = __fsub_rn(__fmul_rn(da, byte_minus<2>(a, bias)), dm);
-        v[3] = __fsub_rn(__fmul_rn(da, byte_minus<3>(a, bias)), dm);
-        v[4] = __fsub_rn(__fmul_rn(da, byte_minus<0>(b, bias)), dm);
-        v[5] = __fsub_rn(__fmul_rn(da, byte_minus<1>(b, bias)), dm);
-        v[6] = __fsub_rn(__fmul_rn(da, byte_minus<2>(b, bias)), dm);
-        v[7] = __fsub_rn(__fmul_rn(da, byte_minus<3>(b, bias)), dm);
+        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[4 * q + 0] = __fmaf_rn(da, byte_minus<0>(w[q], bias), ndm);
+            v[4 * q + 1] = __fmaf_rn(da, byte_minus<1>(w[q], bias), ndm);
+            v[4 * q + 2] = __fmaf_rn(da, byte_minus<2>(w[q], bias), ndm);
+            v[4 * q + 3] = __fmaf_rn(da, byte_minus<3>(w[q], bias), ndm);
+        }
     }
 };
 
 // gguf:q6_k: l = P(low,4,64), h = P(high,2,32), s = scales[floor(j/16)] signed;
-// y[j] = M(M(d, s), l[j] + 16 h[j] - 32).  Chunk c&31 = elements 8cc..8cc+7:
-// low bytes 64*(cc>>4) + 8*(cc&7), plane (cc>>3)&1; high bytes
-// 32*(cc>>4) + 8*(cc&3), 2-bit plane (cc>>2)&3; scale index cc>>1.
+// y[j] = M(M(d, s), l[j] + 16 h[j] - 32).  Chunk c&15 = elements
+// 16cc..16cc+15 shares scale cc: low bytes 64*(cc>>3) + 16*(cc&3), plane
+// (cc>>2)&1; high bytes 32*(cc>>3) + 16*(cc&1), 2-bit plane (cc>>1)&3.
 template <>
 struct Fmt<KF_Q6_K> {
-    static constexpr int B = 256, S = 210, CPB = 32;
+    static constexpr int B = 256, S = 210, CE = 16, CPB = 16;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 5) * S, cc = c & 31u, gi = cc >> 4;
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, gi = cc >> 3;
         const float d = h2f(lds_2<PH>(in, off + 208u));
-        const int32_t sc = static_cast<int8_t>(in[off + 192u + (cc >> 1)]);
+        const int32_t sc = static_cast<int8_t>(in[off + 192u + cc]);
         const float ds = __fmul_rn(d, static_cast<float>(sc));
-        const uint2 lo = lds_8(in, off + 64u * gi + 8u * (cc & 7u));
-        const uint2 hi = lds_8(in, off + 128u + 32u * gi + 8u * (cc & 3u));
-        const uint32_t pl = 4u * ((cc >> 3) & 1u), phh = 2u * ((cc >> 2) & 3u);
-        const uint32_t a = ((lo.x >> pl) & 0x0F0F0F0Fu) | (((hi.x >> phh) & 0x03030303u) << 4);
-        const uint32_t b = ((lo.y >> pl) & 0x0F0F0F0Fu) | (((hi.y >> phh) & 0x03030303u) << 4);
+        const uint4 lo = lds_16<false>(in, off + 64u * gi + 16u * (cc & 3u));
+        const uint4 hi = lds_16<false>(in, off + 128u + 32u * gi + 16u * (cc & 1u));
+        const uint32_t pl = 4u * ((cc >> 2) & 1u), phh = 2u * ((cc >> 1) & 3u);
+        const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
         const float bias = 8388640.0f;  // 2^23 + 32
-        v[0] = __fmul_rn(ds, byte_minus<0>(a, bias));
-        v[1] = __fmul_rn(ds, byte_minus<1>(a, bias));
-        v[2] = __fmul_rn(ds, byte_minus<2>(a, bias));
-        v[3] = __fmul_rn(ds, byte_minus<3>(a, bias));
-        v[4] = __fmul_rn(ds, byte_minus<0>(b, bias));
-        v[5] = __fmul_rn(ds, byte_minus<1>(b, bias));
-        v[6] = __fmul_rn(ds, byte_minus<2>(b, bias));
-        v[7] = __fmul_rn(ds, byte_minus<3>(b, bias));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mul4(ds, ((lw[q] >> pl) & 0x0F0F0F0Fu) | (((hw[q] >> phh) & 0x03030303u) << 4), bias, v + 4 * q);
     }
 };
 
 // q4_g64_fp16 (NInfer sections 5-6.2): w = binary32(s32 * q), q the 4-bit
 // two's-complement code; element k sits in bits 4*(k mod 2) of code byte
-// floor(k/2) (layout reading).  XOR 8 maps two's complement to offset-8.
+// floor(k/2) (layout reading), so chunk c&3 is code bytes 8*(c&3)..+8.
+// XOR 8 maps two's complement to offset-8.
 template <>
 struct Fmt<KF_Q4_G64> {
-    static constexpr int B = 64, S = 34, CPB = 8;
+    static constexpr int B = 64, S = 34, CE = 16, CPB = 4;
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
-        const uint32_t off = ph + (c >> 3) * S;
+        const uint32_t off = ph + (c >> 2) * S;
         const float s = h2f(lds_2<PH>(in, off));
-        const uint32_t w = lds_4(in, off + 2u + 4u * (c & 7u));
-        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+        const uint2 q = lds_8(in, off + 2u + 8u * (c & 3u));
         const float bias = 8388616.0f;  // 2^23 + 8
-        v[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
-        v[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
-        v[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
-        v[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
-        v[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
-        v[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
-        v[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
-        v[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
+        const uint32_t wv[2] = {q.x, q.y};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t lo = (wv[h] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((wv[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+            float* o = v + 8 * h;
+            o[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
+            o[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
+            o[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
+            o[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
+            o[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
+            o[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
+            o[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
+            o[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
+        }
     }
 };
 
 // ---------------------------------------------------------------------------
-// Output stage: one RNE conversion per element, 16-byte stores when y is
-// 16-byte aligned (element offsets are multiples of 8, so every chunk then
-// starts on a 16-byte boundary).
+// Output stage: one RNE conversion per element; 16-byte stores when y is
+// 16-byte aligned (chunk offsets are multiples of 8 elements, so every chunk
+// then starts on a 16-byte boundary).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -510,39 +544,42 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int O>
-__device__ __forceinline__ void store8(void* y, uint64_t e0, const float* v, bool vec) {
+template <int O, int N>
+__device__ __forceinline__ void store_chunk(void* y, uint64_t e0, const float* v, bool vec) {
     if (O == KO_F32) {
         float* p = static_cast<float*>(y) + e0;
         if (vec) {
-            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+            for (int i = 0; i < N / 4; ++i)
+                reinterpret_cast<float4*>(p)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = v[i];
+            for (int i = 0; i < N; ++i) p[i] = v[i];
         }
     } else if (O == KO_F64) {
         double* p = static_cast<double*>(y) + e0;
         if (vec) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < N / 2; ++i)
                 reinterpret_cast<double2*>(p)[i] =
                     make_double2(static_cast<double>(v[2 * i]), static_cast<double>(v[2 * i + 1]));
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = static_cast<double>(v[i]);
+            for (int i = 0; i < N; ++i) p[i] = static_cast<double>(v[i]);
         }
     } else {
-        uint32_t w[4];
+        uint32_t w[N / 2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < N / 2; ++i)
             w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
         uint16_t* p = static_cast<uint16_t*>(y) + e0;
         if (vec) {
-            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int i = 0; i < N / 8; ++i)
+                reinterpret_cast<uint4*>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < N / 2; ++i) {
                 p[2 * i] = static_cast<uint16_t>(w[i] & 0xffffu);
                 p[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
             }
@@ -558,13 +595,14 @@ __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8
     const bool vec = si.t.yvec != 0;
     void* y = si.t.y;
     const uint32_t ph = PH ? si.phase : 0u;
+    constexpr int kPerThread = kTileElems / Fm::CE / kThreads;  // chunks per thread per tile
 #pragma unroll
-    for (int k = 0; k < kChunksPerThread; ++k) {
+    for (int k = 0; k < kPerThread; ++k) {
         const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
         if (c < nch) {
-            float v[8];
+            float v[Fm::CE];
             Fm::template chunk<PH>(in, ph, c, v, x);
-            store8<O>(y, e_base + 8ull * c, v, vec);
+            store_chunk<O, Fm::CE>(y, e_base + static_cast<uint64_t>(Fm::CE) * c, v, vec);
         }
     }
 }
@@ -620,6 +658,15 @@ __device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint
                                                  uint32_t tid) {
     if (FSEL >= 0) {
         decode_tile_fast_f<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, x, tid);
+        return;
+    }
+    if (FSEL == kFselKQuantMix) {  // q8_0 / q4_k / q6_k only (other formats: slow path)
+        switch (si.t.fmt) {
+            case KF_Q8_0: decode_tile_fast_f<KF_Q8_0, OSEL>(si, in, x, tid); break;
+            case KF_Q4_K: decode_tile_fast_f<KF_Q4_K, OSEL>(si, in, x, tid); break;
+            case KF_Q6_K: decode_tile_fast_f<KF_Q6_K, OSEL>(si, in, x, tid); break;
+            default: decode_tile_slow(si, in, x, tid); break;
+        }
         return;
     }
     switch (si.t.fmt) {
@@ -683,7 +730,8 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
 }
 
 // FSEL / OSEL: the launch's format and output type when every tensor shares
-// them (the host picks the instantiation), else -1.
+// them (the host picks the instantiation), else -1; FSEL == kFselKQuantMix
+// for a launch whose tensors are all gguf:q8_0, gguf:q4_k or gguf:q6_k.
 template <int FSEL, int OSEL>
 __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     extern __shared__ __align__(128) uint8_t smem[];

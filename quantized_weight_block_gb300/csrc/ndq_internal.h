@@ -22,6 +22,10 @@ enum KFmt : int32_t {
     KF_COUNT = 9,
 };
 
+// Format selector of a launch whose tensors mix only gguf:q8_0, gguf:q4_k and
+// gguf:q6_k (the usual K-quant model mix): a kernel with just those decoders.
+constexpr int32_t kFselKQuantMix = -2;
+
 // Output element type of a tensor.
 enum KOut : int32_t { KO_F32 = 0, KO_F16 = 1, KO_BF16 = 2, KO_F64 = 3 };
 
@@ -36,6 +40,10 @@ constexpr int kBlockThreads = kThreads + 32;  // consumer warps + one producer w
 constexpr int kStages = 4;                    // staged tiles in flight per CTA
 constexpr int kInStride = 8832;               // tile bytes + phase + rounding + over-read
 constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
+// Resident CTAs per SM for launches that mix formats (the whole-model decode):
+// measured fastest at 2 even when registers and shared memory allow 3.
+// Single-format launches use every CTA the occupancy calculator allows.
+constexpr int kMixedCtasPerSm = 2;
 
 // One tensor as the kernel sees it (64 bytes; kept trivially copyable).
 struct DevTensor {
@@ -63,7 +71,7 @@ struct KParams {
     int32_t n;
     int32_t nv_index;  // first nvfp4 tensor of the launch (its divisor seeds the quotient table), or -1
     uint64_t total_tiles;
-    int32_t fsel;      // KFmt shared by every tensor of the launch, or -1
+    int32_t fsel;      // KFmt shared by every tensor of the launch, kFselKQuantMix, or -1
     int32_t osel;      // KOut shared by every tensor of the launch, or -1
     unsigned int* fault;  // device fault word (set by the launcher)
 };
@@ -81,6 +89,7 @@ KernelFn kernel_gguf_nvfp4(int osel);
 KernelFn kernel_nvfp4(int osel);
 KernelFn kernel_q4_g64(int osel);
 KernelFn kernel_generic(int osel);
+KernelFn kernel_kquant_mix(int osel);
 
 // Dynamic shared memory of a decode CTA (with or without the nvfp4 table).
 size_t decode_smem_bytes(bool tab);
@@ -101,6 +110,10 @@ constexpr int kNoAllocMaxTensors = 1024;
 // array instead of a caller workspace.  `table` is host memory (n entries,
 // tile_begin set).  Returns 0 or a CUDA error code.
 int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int nv_index, void* stream);
+
+// Kernel selectors of a launch over tensors t[0..n): the shared format (or
+// kFselKQuantMix, or -1) and the shared output type (or -1).
+void select_kernel(const DevTensor* t, int n, int32_t* fsel, int32_t* osel);
 
 // Read and clear the device fault word of the current device.
 int read_fault(uint32_t* flags);

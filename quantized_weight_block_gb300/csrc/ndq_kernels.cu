@@ -32,6 +32,7 @@ __global__ void k_upload_table(const UploadParams p) {
 // Specialised kernels live in one instantiation file per format.
 KernelFn pick_kernel(int fsel, int osel) {
     if (osel < 0) return kernel_generic(-1);
+    if (fsel == kFselKQuantMix) return kernel_kquant_mix(osel);
     switch (fsel) {
         case KF_Q8_0: return kernel_q8_0(osel);
         case KF_Q4_0: return kernel_q4_0(osel);
@@ -46,9 +47,9 @@ KernelFn pick_kernel(int fsel, int osel) {
     }
 }
 
-constexpr int kKernelSlots = (KF_COUNT + 1) * 5;
+constexpr int kKernelSlots = (KF_COUNT + 2) * 5;
 
-int slot_of(int fsel, int osel) { return (osel < 0) ? 0 : (fsel + 1) * 5 + osel + 1; }
+int slot_of(int fsel, int osel) { return (osel < 0) ? 0 : (fsel + 2) * 5 + osel + 1; }
 
 struct DeviceInfo {
     int sms = 0;
@@ -73,7 +74,7 @@ int launch_decode(const KParams& p, void* stream) {
     if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
     const bool tab = p.nv_index >= 0;
     const size_t smem = smem_bytes(tab);
-    const int fsel = (p.fsel >= 0 && p.fsel < KF_COUNT) ? p.fsel : -1;
+    const int fsel = ((p.fsel >= 0 && p.fsel < KF_COUNT) || p.fsel == kFselKQuantMix) ? p.fsel : -1;
     const int osel = (p.osel >= 0 && p.osel <= KO_F64) ? p.osel : -1;
     const KernelFn fn = pick_kernel(fsel, osel);
     DeviceInfo& di = g_dev[dev];
@@ -91,6 +92,7 @@ int launch_decode(const KParams& p, void* stream) {
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
         if (e != cudaSuccess) return static_cast<int>(e);
+        if (fsel < 0 && n > kMixedCtasPerSm) n = kMixedCtasPerSm;
         cps = n > 0 ? n : 1;
     }
     if (!g_fault_addr[dev]) {
@@ -160,13 +162,20 @@ int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, 
     p.n = n;
     p.nv_index = nv_index;
     p.total_tiles = total_tiles;
-    p.fsel = table[0].fmt;
-    p.osel = table[0].out;
-    for (int i = 1; i < n; ++i) {
-        if (table[i].fmt != p.fsel) p.fsel = -1;
-        if (table[i].out != p.osel) p.osel = -1;
-    }
+    select_kernel(table, n, &p.fsel, &p.osel);
     return launch_decode(p, stream);
+}
+
+void select_kernel(const DevTensor* t, int n, int32_t* fsel, int32_t* osel) {
+    *fsel = t[0].fmt;
+    *osel = t[0].out;
+    bool kmix = true;
+    for (int i = 0; i < n; ++i) {
+        if (t[i].fmt != *fsel) *fsel = -1;
+        if (t[i].out != *osel) *osel = -1;
+        kmix = kmix && (t[i].fmt == KF_Q8_0 || t[i].fmt == KF_Q4_K || t[i].fmt == KF_Q6_K);
+    }
+    if (*fsel < 0 && kmix) *fsel = kFselKQuantMix;
 }
 
 int read_fault(uint32_t* flags) {
