@@ -68,20 +68,20 @@ typedef struct {
 } or_format;
 
 static const or_format OR_FORMATS[] = {
-    {"gguf:q4_0", 32, 18, 1},     {"gguf:q4_1", 32, 20, 0},
-    {"gguf:q5_0", 32, 22, 0},     {"gguf:q5_1", 32, 24, 0},
-    {"gguf:q8_0", 32, 34, 1},     {"gguf:q8_1", 32, 36, 0},
-    {"gguf:q2_k", 256, 84, 0},    {"gguf:q3_k", 256, 110, 0},
-    {"gguf:q4_k", 256, 144, 1},   {"gguf:q5_k", 256, 176, 0},
-    {"gguf:q6_k", 256, 210, 1},   {"gguf:q8_k", 256, 292, 0},
+    {"gguf:q4_0", 32, 18, 1},     {"gguf:q4_1", 32, 20, 1},
+    {"gguf:q5_0", 32, 22, 1},     {"gguf:q5_1", 32, 24, 1},
+    {"gguf:q8_0", 32, 34, 1},     {"gguf:q8_1", 32, 36, 1},
+    {"gguf:q2_k", 256, 84, 1},    {"gguf:q3_k", 256, 110, 1},
+    {"gguf:q4_k", 256, 144, 1},   {"gguf:q5_k", 256, 176, 1},
+    {"gguf:q6_k", 256, 210, 1},   {"gguf:q8_k", 256, 292, 1},
     {"gguf:iq2_xxs", 256, 66, 0}, {"gguf:iq2_xs", 256, 74, 0},
     {"gguf:iq3_xxs", 256, 98, 0}, {"gguf:iq1_s", 256, 50, 0},
     {"gguf:iq4_nl", 32, 18, 1},   {"gguf:iq3_s", 256, 110, 0},
-    {"gguf:iq2_s", 256, 82, 0},   {"gguf:iq4_xs", 256, 136, 0},
-    {"gguf:iq1_m", 256, 56, 0},   {"gguf:tq1_0", 256, 54, 0},
-    {"gguf:tq2_0", 256, 66, 0},   {"gguf:mxfp4", 32, 17, 1},
-    {"gguf:nvfp4", 64, 36, 1},    {"gguf:q1_0", 128, 18, 0},
-    {"gguf:q2_0", 64, 18, 0},
+    {"gguf:iq2_s", 256, 82, 0},   {"gguf:iq4_xs", 256, 136, 1},
+    {"gguf:iq1_m", 256, 56, 0},   {"gguf:tq1_0", 256, 54, 1},
+    {"gguf:tq2_0", 256, 66, 1},   {"gguf:mxfp4", 32, 17, 1},
+    {"gguf:nvfp4", 64, 36, 1},    {"gguf:q1_0", 128, 18, 1},
+    {"gguf:q2_0", 64, 18, 1},
     /* [NINF] formats.  READING: nvfp4 uses the gguf:nvfp4 block geometry
      * (4 scale bytes then 32 code bytes per 64 values) and appends its FP32
      * divisors after the last block; q4_g64_fp16 is one binary16 scale then
@@ -382,6 +382,185 @@ static void dec_q4_g64(const uint8_t *b, float *y) {
     }
 }
 
+/* gguf:q4_1.  Fields h d, m; u8 q[16].  v = P(q,4,16); y[j] = A(M(d,v[j]),m). */
+static void dec_q4_1(const uint8_t *b, float *y) {
+    uint32_t v[32];
+    float d = H(b), m = H(b + 2);
+    P(b + 4, 16, 4, 16, v);
+    for (int j = 0; j < 32; ++j) y[j] = A(M(d, (float)v[j]), m);
+}
+
+/* gguf:q5_0 / q5_1.  Q5_0 fields h d; u8 high[4]; u8 q[16].  Q5_1 fields
+ * h d, m; u8 high[4]; u8 q[16].  v = P(q,4,16) with v[j] + 16*bit(U(high),j);
+ * Q5_0: y[j] = M(d, v[j]-16); Q5_1: y[j] = A(M(d, v[j]), m). */
+static void dec_q5(const uint8_t *b, int affine, float *y) {
+    uint32_t v[32];
+    int o = affine ? 4 : 2;
+    float d = H(b), m = affine ? H(b + 2) : 0.0f;
+    uint32_t high = U(b + o, 4);
+    P(b + o + 4, 16, 4, 16, v);
+    for (int j = 0; j < 32; ++j) {
+        uint32_t vj = v[j] + 16u * ((high >> j) & 1u);
+        y[j] = affine ? A(M(d, (float)vj), m) : M(d, (float)((int32_t)vj - 16));
+    }
+}
+
+/* gguf:q8_1 (fields h d, s; i8 q[32]) and gguf:q8_k (fields f d; i8 q[256];
+ * i16 sums[16]): y[j] = M(d, q[j]); the cached sum fields are ignored,
+ * bits included. */
+static void dec_q8_1(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int j = 0; j < 32; ++j) y[j] = M(d, (float)signed8(b[4 + j]));
+}
+
+static void dec_q8_k(const uint8_t *b, float *y) {
+    float d = or_f32(U(b, 4));
+    for (int j = 0; j < 256; ++j) y[j] = M(d, (float)signed8(b[4 + j]));
+}
+
+/* gguf:q2_k.  Fields u8 scales[16], q[64]; h d, dmin.  v = P(q,2,32),
+ * s = scales[floor(j/16)]; y[j] = D(M(M(d, s mod 16), v[j]), M(dmin, floor(s/16))). */
+static void dec_q2_k(const uint8_t *b, float *y) {
+    uint32_t v[256];
+    float d = H(b + 80), dmin = H(b + 82);
+    P(b + 16, 64, 2, 32, v);
+    for (int j = 0; j < 256; ++j) {
+        uint32_t sc = b[j / 16];
+        y[j] = D(M(M(d, (float)(sc % 16u)), (float)v[j]), M(dmin, (float)(sc / 16u)));
+    }
+}
+
+/* gguf:q3_k.  Fields u8 mask[32], q[64], scales[12]; h d.  v = P(q,2,32),
+ * h = P(mask,1,32), l = P(b[96:104],4,8), a = P(b[104:108],2,4); with
+ * k = floor(j/16) and s = l[k] + 16*a[k] - 32:
+ * y[j] = M(M(d, s), v[j] - 4*(1 - h[j])). */
+static void dec_q3_k(const uint8_t *b, float *y) {
+    uint32_t v[256], h[256], l[16], a[16];
+    float d = H(b + 108);
+    P(b + 32, 64, 2, 32, v);
+    P(b, 32, 1, 32, h);
+    P(b + 96, 8, 4, 8, l);
+    P(b + 104, 4, 2, 4, a);
+    for (int j = 0; j < 256; ++j) {
+        int k = j / 16;
+        int32_t sc = (int32_t)l[k] + 16 * (int32_t)a[k] - 32;
+        int32_t q = (int32_t)v[j] - 4 * (1 - (int32_t)h[j]);
+        y[j] = M(M(d, (float)sc), (float)q);
+    }
+}
+
+/* 6-bit scale a[k] and minimum m[k] of Q4_K / Q5_K from the 12-byte scales
+ * field s (see dec_q4_k). */
+static void kq_scale_min(const uint8_t *s, int k, uint32_t *a, uint32_t *m) {
+    if (k < 4) {
+        *a = s[k] % 64u;
+        *m = s[k + 4] % 64u;
+    } else {
+        *a = (s[k + 4] % 16u) + 16u * (uint32_t)(s[k - 4] / 64u);
+        *m = (uint32_t)(s[k + 4] / 16u) + 16u * (uint32_t)(s[k] / 64u);
+    }
+}
+
+/* gguf:q5_k.  Fields h d, dmin; u8 scales[12], high[32], q[128].
+ * v = P(q,4,32) + 16*P(high,1,32); a, m as Q4_K;
+ * y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])), k = floor(j/32). */
+static void dec_q5_k(const uint8_t *b, float *y) {
+    uint32_t v[256], hb[256];
+    float d = H(b), dmin = H(b + 2);
+    P(b + 48, 128, 4, 32, v);
+    P(b + 16, 32, 1, 32, hb);
+    for (int j = 0; j < 256; ++j) {
+        uint32_t a, m;
+        kq_scale_min(b + 4, j / 32, &a, &m);
+        y[j] = D(M(M(d, (float)a), (float)(v[j] + 16u * hb[j])), M(dmin, (float)m));
+    }
+}
+
+/* gguf:iq4_xs.  Fields h d; u16 high; u8 scales[4], q[128].  v = P(q,4,16);
+ * s[k] = field(scales[floor(k/2)], 4*(k mod 2), 4) + 16*field(high, 2k, 2) - 32;
+ * y[j] = M(M(d, s[floor(j/32)]), IQ4[v[j]]). */
+static void dec_iq4_xs(const uint8_t *b, float *y) {
+    uint32_t v[256];
+    float d = H(b);
+    uint32_t high = U(b + 2, 2);
+    P(b + 8, 128, 4, 16, v);
+    for (int j = 0; j < 256; ++j) {
+        int k = j / 32;
+        int32_t sc = (int32_t)field(b[4 + k / 2], 4 * (k % 2), 4) + 16 * (int32_t)field(high, 2 * k, 2) - 32;
+        y[j] = M(M(d, (float)sc), (float)OR_IQ4[v[j]]);
+    }
+}
+
+/* gguf:tq1_0.  Fields u8 q[48], high[4]; h d.  Three output sequences for
+ * (start, width, count) = (0,32,5), (32,16,5), (48,4,4), in that order; in
+ * each, p = 0..count-1 before j = 0..width-1; output
+ * M(d, floor(3*((b[start+j]*3^p) mod 256)/256) - 1). */
+static void dec_tq1_0(const uint8_t *b, float *y) {
+    static const int seq[3][3] = {{0, 32, 5}, {32, 16, 5}, {48, 4, 4}};
+    float d = H(b + 52);
+    int n = 0;
+    for (int t = 0; t < 3; ++t) {
+        uint32_t pw = 1;
+        for (int p = 0; p < seq[t][2]; ++p, pw *= 3u)
+            for (int j = 0; j < seq[t][1]; ++j) {
+                uint32_t r = (b[seq[t][0] + j] * pw) % 256u;
+                int32_t q = (int32_t)((3u * r) / 256u) - 1;
+                y[n++] = M(d, (float)q);
+            }
+    }
+}
+
+/* gguf:tq2_0.  Fields u8 q[64]; h d.  y[j] = M(d, v[j]-1), v = P(q,2,32). */
+static void dec_tq2_0(const uint8_t *b, float *y) {
+    uint32_t v[256];
+    float d = H(b + 64);
+    P(b, 64, 2, 32, v);
+    for (int j = 0; j < 256; ++j) y[j] = M(d, (float)((int32_t)v[j] - 1));
+}
+
+/* gguf:q1_0.  Fields h d; u8 q[16].  y[j] = d if bit(q[floor(j/8)], j mod 8)
+ * is one, else -d (no multiplication). */
+static void dec_q1_0(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int j = 0; j < 128; ++j) y[j] = ((b[2 + j / 8] >> (j % 8)) & 1u) ? d : -d;
+}
+
+/* gguf:q2_0.  Fields h d; u8 q[16].  y[j] = M(d, v[j]-1), v = P(q,2,1). */
+static void dec_q2_0(const uint8_t *b, float *y) {
+    uint32_t v[64];
+    float d = H(b);
+    P(b + 2, 16, 2, 1, v);
+    for (int j = 0; j < 64; ++j) y[j] = M(d, (float)((int32_t)v[j] - 1));
+}
+
+/* One block of format `name` (dw: nvfp4 divisor) to binary32. */
+static int or_decode_block(const char *name, const uint8_t *b, float dw, float *y) {
+    if (strcmp(name, "gguf:q8_0") == 0 || strcmp(name, "q8_g32_fp16") == 0) dec_q8_0(b, y);
+    else if (strcmp(name, "gguf:q4_0") == 0) dec_q4_0(b, y);
+    else if (strcmp(name, "gguf:iq4_nl") == 0) dec_iq4_nl(b, y);
+    else if (strcmp(name, "gguf:q4_k") == 0) dec_q4_k(b, y);
+    else if (strcmp(name, "gguf:q6_k") == 0) dec_q6_k(b, y);
+    else if (strcmp(name, "gguf:mxfp4") == 0) dec_mxfp4(b, y);
+    else if (strcmp(name, "gguf:nvfp4") == 0) dec_gguf_nvfp4(b, y);
+    else if (strcmp(name, "q4_g64_fp16") == 0) dec_q4_g64(b, y);
+    else if (strcmp(name, "nvfp4") == 0) dec_nvfp4(b, dw, y);
+    else if (strcmp(name, "gguf:q4_1") == 0) dec_q4_1(b, y);
+    else if (strcmp(name, "gguf:q5_0") == 0) dec_q5(b, 0, y);
+    else if (strcmp(name, "gguf:q5_1") == 0) dec_q5(b, 1, y);
+    else if (strcmp(name, "gguf:q8_1") == 0) dec_q8_1(b, y);
+    else if (strcmp(name, "gguf:q8_k") == 0) dec_q8_k(b, y);
+    else if (strcmp(name, "gguf:q2_k") == 0) dec_q2_k(b, y);
+    else if (strcmp(name, "gguf:q3_k") == 0) dec_q3_k(b, y);
+    else if (strcmp(name, "gguf:q5_k") == 0) dec_q5_k(b, y);
+    else if (strcmp(name, "gguf:iq4_xs") == 0) dec_iq4_xs(b, y);
+    else if (strcmp(name, "gguf:tq1_0") == 0) dec_tq1_0(b, y);
+    else if (strcmp(name, "gguf:tq2_0") == 0) dec_tq2_0(b, y);
+    else if (strcmp(name, "gguf:q1_0") == 0) dec_q1_0(b, y);
+    else if (strcmp(name, "gguf:q2_0") == 0) dec_q2_0(b, y);
+    else return OR_ERR_UNSUPPORTED_FORMAT;
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Top level: validation, block loop, single output cast.                    */
 /* ------------------------------------------------------------------------ */
@@ -471,22 +650,15 @@ int oracle_decode_range(const char *name, const int64_t *shape, int ndim, int ou
     uint64_t bpr = (uint64_t)shape[ndim - 1] / (uint64_t)f->B; /* blocks per row */
     for (uint64_t bi = b0; bi < b1; ++bi) {
         const uint8_t *b = x + bi * (uint64_t)f->S;
-        if (strcmp(name, "gguf:q8_0") == 0 || strcmp(name, "q8_g32_fp16") == 0) dec_q8_0(b, blk);
-        else if (strcmp(name, "gguf:q4_0") == 0) dec_q4_0(b, blk);
-        else if (strcmp(name, "gguf:iq4_nl") == 0) dec_iq4_nl(b, blk);
-        else if (strcmp(name, "gguf:q4_k") == 0) dec_q4_k(b, blk);
-        else if (strcmp(name, "gguf:q6_k") == 0) dec_q6_k(b, blk);
-        else if (strcmp(name, "gguf:mxfp4") == 0) dec_mxfp4(b, blk);
-        else if (strcmp(name, "gguf:nvfp4") == 0) dec_gguf_nvfp4(b, blk);
-        else if (strcmp(name, "q4_g64_fp16") == 0) dec_q4_g64(b, blk);
-        else if (strcmp(name, "nvfp4") == 0) {
+        float dw = 1.0f;
+        if (strcmp(name, "nvfp4") == 0) {
             /* row r uses divisor floor(r / (N / D)) ([NINF] section 3.3) */
             uint64_t row = bi / bpr;
             uint64_t di = row / (N / D);
-            float dw = or_f32(U(x + nb * 36u + 4u * di, 4));
-            dec_nvfp4(b, dw, blk);
-        } else
-            return OR_ERR_UNSUPPORTED_FORMAT;
+            dw = or_f32(U(x + nb * 36u + 4u * di, 4));
+        }
+        rc = or_decode_block(name, b, dw, blk);
+        if (rc != OR_OK) return rc;
         for (int j = 0; j < f->B; ++j)
             or_store(out_dtype, blk[j], y, (bi - b0) * (uint64_t)f->B + (uint64_t)j);
     }
@@ -508,17 +680,7 @@ int oracle_decode_block_f32(const char *name, const uint8_t *b, float dw, float 
     int fi = or_find(name);
     if (fi < 0) return OR_ERR_UNKNOWN_FORMAT;
     if (!b || !y) return OR_ERR_NULL;
-    if (strcmp(name, "gguf:q8_0") == 0 || strcmp(name, "q8_g32_fp16") == 0) dec_q8_0(b, y);
-    else if (strcmp(name, "gguf:q4_0") == 0) dec_q4_0(b, y);
-    else if (strcmp(name, "gguf:iq4_nl") == 0) dec_iq4_nl(b, y);
-    else if (strcmp(name, "gguf:q4_k") == 0) dec_q4_k(b, y);
-    else if (strcmp(name, "gguf:q6_k") == 0) dec_q6_k(b, y);
-    else if (strcmp(name, "gguf:mxfp4") == 0) dec_mxfp4(b, y);
-    else if (strcmp(name, "gguf:nvfp4") == 0) dec_gguf_nvfp4(b, y);
-    else if (strcmp(name, "q4_g64_fp16") == 0) dec_q4_g64(b, y);
-    else if (strcmp(name, "nvfp4") == 0) dec_nvfp4(b, dw, y);
-    else return OR_ERR_UNSUPPORTED_FORMAT;
-    return OR_OK;
+    return or_decode_block(name, b, dw, y);
 }
 
 /* Kiln group count ([KILN] "Quantization"): ceil(shape[axis]/g) times the

@@ -18,6 +18,10 @@ Field distributions follow the benchmark workloads:
     nonnegative finite word), code bytes uniform, one FP32 divisor
     d_w = binary32(2688 / binary32(amax)) with amax = 0.1 (448*6/amax);
   * gguf:nvfp4 -- scale bytes uniform over 0x00..0x7e, codes uniform;
+  * the other gguf formats (q4_1, q5_0, q5_1, q8_1, q8_k, q2_k, q3_k, q5_k,
+    iq4_xs, tq1_0, tq2_0, q1_0, q2_0) -- binary16 scales |N(0,0.02)|+1e-4,
+    minima |N(0,0.01)|, q8_k's binary32 scale likewise, codes in [-127, 127]
+    for q8_k, every other byte uniform;
   * "bytes" -- every byte uniform over 0..255 (exercises special scales:
     binary16 infinities/NaNs, E4M3FN NaN words, E8M0 extremes).
 
@@ -36,6 +40,19 @@ GEOMETRY = {
     "gguf:iq4_nl": (32, 18), "q4_g64_fp16": (64, 34), "gguf:q4_k": (256, 144),
     "gguf:q6_k": (256, 210), "gguf:mxfp4": (32, 17), "gguf:nvfp4": (64, 36),
     "nvfp4": (64, 36),
+    "gguf:q4_1": (32, 20), "gguf:q5_0": (32, 22), "gguf:q5_1": (32, 24), "gguf:q8_1": (32, 36),
+    "gguf:q8_k": (256, 292), "gguf:q2_k": (256, 84), "gguf:q3_k": (256, 110), "gguf:q5_k": (256, 176),
+    "gguf:iq4_xs": (256, 136), "gguf:tq1_0": (256, 54), "gguf:tq2_0": (256, 66), "gguf:q1_0": (128, 18),
+    "gguf:q2_0": (64, 18),
+}
+
+# Byte offsets of the binary16 scale fields of the other gguf formats; their
+# workload recipe draws these from |N(0,0.02)|+1e-4 (minima |N(0,0.01)|) and
+# every other byte uniformly.  q8_k's scale is one binary32 at offset 0.
+F16_SCALES = {
+    "gguf:q4_1": (0, 2), "gguf:q5_0": (0,), "gguf:q5_1": (0, 2), "gguf:q8_1": (0,), "gguf:q2_k": (80, 82),
+    "gguf:q3_k": (108,), "gguf:q5_k": (0, 2), "gguf:iq4_xs": (0,), "gguf:tq1_0": (52,), "gguf:tq2_0": (64,),
+    "gguf:q1_0": (0,), "gguf:q2_0": (0,),
 }
 
 NVFP4_AMAX = 0.1
@@ -108,6 +125,14 @@ def payload(fmt: str, shape, seed: int, dist: str = "workload", ndiv: int = 1) -
         blk[:, 0] = rng.integers(118, 131, size=nb, dtype=np.uint8)
     elif fmt in ("gguf:nvfp4", "nvfp4"):
         blk[:, 0:4] = rng.integers(0, 0x7F, size=(nb, 4), dtype=np.uint8)
+    elif fmt in F16_SCALES:
+        for i, off in enumerate(F16_SCALES[fmt]):
+            sd = 0.02 if i == 0 else 0.01
+            blk[:, off:off + 2] = _f16_bytes(np.abs(rng.normal(0.0, sd, size=nb)) + (1e-4 if i == 0 else 0.0))
+    elif fmt == "gguf:q8_k":
+        d = (np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4).astype("<f4")
+        blk[:, 0:4] = d.view(np.uint8).reshape(nb, 4)
+        blk[:, 4:260] = rng.integers(-127, 128, size=(nb, 256), dtype=np.int8).view(np.uint8)
     else:
         raise ValueError(fmt)
     out = blk.reshape(-1)

@@ -61,7 +61,10 @@ def test_grouped_format_readings_match_bits_per_weight(orc):
 def test_decoded_set(orc):
     decoded = {f for f in orc.formats() if orc.format_info(f)[2]}
     assert decoded == {"gguf:q8_0", "gguf:q4_0", "gguf:q4_k", "gguf:q6_k", "gguf:iq4_nl",
-                       "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16", "q8_g32_fp16"}
+                       "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16", "q8_g32_fp16",
+                       "gguf:q4_1", "gguf:q5_0", "gguf:q5_1", "gguf:q8_1", "gguf:q8_k", "gguf:q2_k",
+                       "gguf:q3_k", "gguf:q5_k", "gguf:iq4_xs", "gguf:tq1_0", "gguf:tq2_0", "gguf:q1_0",
+                       "gguf:q2_0"}
 
 
 @pytest.mark.parametrize("fmt,shape", [
