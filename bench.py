@@ -16,8 +16,12 @@ Printed (rank 0, one JSON line on stdout):
   roofline      the decode kernel against the measured HBM copy bandwidth;
   cpu_baseline  the CPU oracle on a bounded sample of the same workload;
   per_workload  the single-format workloads (q8_0, q4_0, q4_g64, q4_k, q6_k,
-                nvfp4, mxfp4, iq4_nl), each timed with an L2 flush between
-                repetitions.
+                nvfp4, mxfp4, iq4_nl), each timed back to back over buffer
+                sets larger than L2 and as one launch after an L2 eviction;
+  per_workload_next_formats
+                the same for the other simple gguf profiles (q4_1, q5_0,
+                q5_1, q8_1, q8_k, q2_k, q3_k, q5_k, iq4_xs, tq1_0, tq2_0,
+                q1_0, q2_0), each on one [14336,4096] tensor -> bf16.
 
 `--impl reference` times the CPU oracle (the parity reference) on the host
 cores instead, on a bounded sample of the same workload per step.
@@ -256,7 +260,7 @@ def profiled_traffic(profile_name: str):
     return None
 
 
-def time_single_workloads(torch, ndq, stream, peak):
+def time_single_workloads(torch, ndq, stream, peak, workloads):
     """Single-format workloads.
 
     Steady state: back-to-back launches rotating over enough copies of the
@@ -270,7 +274,7 @@ def time_single_workloads(torch, ndq, stream, peak):
     flush_sink = torch.empty((), dtype=torch.uint8, device="cuda")
     out = {}
     tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}
-    for label, fmt, shape, seed, od in synth.WORKLOADS:
+    for label, fmt, shape, seed, od in workloads:
         x_np = synth.payload(fmt, shape, seed)
         nbytes = x_np.size + int(np.prod(shape)) * torch.empty((), dtype=tdt[od]).element_size()
         nsets = int(min(64, max(2, -(-4 * l2 // nbytes))))
@@ -313,9 +317,10 @@ def time_single_workloads(torch, ndq, stream, peak):
 def run_only(args, torch, ndq):
     """One single-format workload, --warmup untimed then --steps timed
     launches (used for focused profiling of one format)."""
-    match = [w for w in synth.WORKLOADS if w[0] == args.only]
+    every = synth.WORKLOADS + synth.NEXT_WORKLOADS
+    match = [w for w in every if w[0] == args.only]
     if not match:
-        raise SystemExit(f"unknown workload {args.only!r}; choose from {[w[0] for w in synth.WORKLOADS]}")
+        raise SystemExit(f"unknown workload {args.only!r}; choose from {[w[0] for w in every]}")
     label, fmt, shape, seed, od = match[0]
     tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}[od]
     x_np = synth.payload(fmt, shape, seed)
@@ -524,9 +529,10 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = end_to_end(args, torch, ndq, work, x_host, x_dev, y_dev, stream, world, step_bytes)
 
-    per_workload = None
+    per_workload = per_workload_next = None
     if not args.no_workloads and rank == 0:
-        per_workload = time_single_workloads(torch, ndq, stream, peak)
+        per_workload = time_single_workloads(torch, ndq, stream, peak, synth.WORKLOADS)
+        per_workload_next = time_single_workloads(torch, ndq, stream, peak, synth.NEXT_WORKLOADS)
 
     cpu = None
     if not args.no_cpu and rank == 0:
@@ -554,7 +560,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "peak_source": peak_src,
                      "kernel": "k_decode (batched; step time includes the 2 KB descriptor-table upload kernel)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
-        "per_workload": per_workload,
+        "per_workload": per_workload, "per_workload_next_formats": per_workload_next,
     }
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -32,17 +32,17 @@ struct FormatRow {
 // formats.
 const FormatRow kFormats[NDQ_NUM_FORMATS] = {
     {"gguf:q4_0", 32, 18, ndq::KF_Q4_0},
-    {"gguf:q4_1", 32, 20, -1},
-    {"gguf:q5_0", 32, 22, -1},
-    {"gguf:q5_1", 32, 24, -1},
+    {"gguf:q4_1", 32, 20, ndq::KF_Q4_1},
+    {"gguf:q5_0", 32, 22, ndq::KF_Q5_0},
+    {"gguf:q5_1", 32, 24, ndq::KF_Q5_1},
     {"gguf:q8_0", 32, 34, ndq::KF_Q8_0},
-    {"gguf:q8_1", 32, 36, -1},
-    {"gguf:q2_k", 256, 84, -1},
-    {"gguf:q3_k", 256, 110, -1},
+    {"gguf:q8_1", 32, 36, ndq::KF_Q8_1},
+    {"gguf:q2_k", 256, 84, ndq::KF_Q2_K},
+    {"gguf:q3_k", 256, 110, ndq::KF_Q3_K},
     {"gguf:q4_k", 256, 144, ndq::KF_Q4_K},
-    {"gguf:q5_k", 256, 176, -1},
+    {"gguf:q5_k", 256, 176, ndq::KF_Q5_K},
     {"gguf:q6_k", 256, 210, ndq::KF_Q6_K},
-    {"gguf:q8_k", 256, 292, -1},
+    {"gguf:q8_k", 256, 292, ndq::KF_Q8_K},
     {"gguf:iq2_xxs", 256, 66, -1},
     {"gguf:iq2_xs", 256, 74, -1},
     {"gguf:iq3_xxs", 256, 98, -1},
@@ -50,14 +50,14 @@ const FormatRow kFormats[NDQ_NUM_FORMATS] = {
     {"gguf:iq4_nl", 32, 18, ndq::KF_IQ4_NL},
     {"gguf:iq3_s", 256, 110, -1},
     {"gguf:iq2_s", 256, 82, -1},
-    {"gguf:iq4_xs", 256, 136, -1},
+    {"gguf:iq4_xs", 256, 136, ndq::KF_IQ4_XS},
     {"gguf:iq1_m", 256, 56, -1},
-    {"gguf:tq1_0", 256, 54, -1},
-    {"gguf:tq2_0", 256, 66, -1},
+    {"gguf:tq1_0", 256, 54, ndq::KF_TQ1_0},
+    {"gguf:tq2_0", 256, 66, ndq::KF_TQ2_0},
     {"gguf:mxfp4", 32, 17, ndq::KF_MXFP4},
     {"gguf:nvfp4", 64, 36, ndq::KF_GGUF_NVFP4},
-    {"gguf:q1_0", 128, 18, -1},
-    {"gguf:q2_0", 64, 18, -1},
+    {"gguf:q1_0", 128, 18, ndq::KF_Q1_0},
+    {"gguf:q2_0", 64, 18, ndq::KF_Q2_0},
     {"nvfp4", 64, 36, ndq::KF_NVFP4},
     {"q4_g64_fp16", 64, 34, ndq::KF_Q4_G64},
     {"q8_g32_fp16", 32, 34, ndq::KF_Q8_0},

@@ -531,6 +531,316 @@ struct Fmt<KF_Q4_G64> {
 };
 
 // ---------------------------------------------------------------------------
+// The other simple gguf profiles ("Mathematical decoding rules").  Where a
+// rule adds or subtracts after an exact product (an fp16 scale times an
+// integer of at most 5 bits, or a 17-bit sub-scale product times at most 5
+// bits), the product and the sum are formed by one FMA: the product is exact
+// in binary32, so the single rounding is the rule's.
+// ---------------------------------------------------------------------------
+
+// 4 bits of `b` (bits 0..3) spread to bit 4 of each byte: the 5th code bit.
+__device__ __forceinline__ uint32_t spread4_b4(uint32_t b) { return ((b * 0x00204081u) & 0x01010101u) << 4; }
+
+// gguf:q4_1: v = P(q,4,16); y[j] = A(M(d, v[j]), m).
+template <>
+struct Fmt<KF_Q4_1> {
+    static constexpr int B = 32, S = 20, CE = 16, CPB = 2;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 1) * S;
+        const float d = h2f(lds_2<PH>(in, off)), m = h2f(lds_2<PH>(in, off + 2u));
+        const uint4 n = nib_plane16(lds_16<false>(in, off + 4u), c & 1u);
+        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
+        const float bias = 8388608.0f;  // 2^23
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[4 * q + 0] = __fmaf_rn(d, byte_minus<0>(w[q], bias), m);
+            v[4 * q + 1] = __fmaf_rn(d, byte_minus<1>(w[q], bias), m);
+            v[4 * q + 2] = __fmaf_rn(d, byte_minus<2>(w[q], bias), m);
+            v[4 * q + 3] = __fmaf_rn(d, byte_minus<3>(w[q], bias), m);
+        }
+    }
+};
+
+// gguf:q5_0 / q5_1: v = P(q,4,16) + 16*bit(U(high), j); Q5_0 y = M(d, v-16),
+// Q5_1 y = A(M(d, v), m).  Chunk c&1 = plane c&1, high bits 16*(c&1)...
+template <bool AFF>
+struct Q5Impl {
+    static constexpr int S = AFF ? 24 : 22;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v) {
+        const uint32_t off = ph + (c >> 1) * S, o = AFF ? 4u : 2u;
+        const float d = h2f(lds_2<PH>(in, off));
+        const float m = AFF ? h2f(lds_2<PH>(in, off + 2u)) : 0.0f;
+        const uint32_t hb = lds_4(in, off + o) >> (16u * (c & 1u));
+        const uint4 n = nib_plane16(lds_16<false>(in, off + o + 4u), c & 1u);
+        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t u = w[q] | spread4_b4((hb >> (4 * q)) & 15u);
+            if (AFF) {
+                const float bias = 8388608.0f;  // 2^23
+                v[4 * q + 0] = __fmaf_rn(d, byte_minus<0>(u, bias), m);
+                v[4 * q + 1] = __fmaf_rn(d, byte_minus<1>(u, bias), m);
+                v[4 * q + 2] = __fmaf_rn(d, byte_minus<2>(u, bias), m);
+                v[4 * q + 3] = __fmaf_rn(d, byte_minus<3>(u, bias), m);
+            } else {
+                mul4(d, u, 8388624.0f, v + 4 * q);  // 2^23 + 16
+            }
+        }
+    }
+};
+template <>
+struct Fmt<KF_Q5_0> {
+    static constexpr int B = 32, S = 22, CE = 16, CPB = 2;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        Q5Impl<false>::chunk<PH>(in, ph, c, v);
+    }
+};
+template <>
+struct Fmt<KF_Q5_1> {
+    static constexpr int B = 32, S = 24, CE = 16, CPB = 2;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        Q5Impl<true>::chunk<PH>(in, ph, c, v);
+    }
+};
+
+// gguf:q8_1 (h d, s; i8 q[32]) and gguf:q8_k (f d; i8 q[256]; i16 sums[16]):
+// y[j] = M(d, q[j]); the cached sum fields are never read.
+template <>
+struct Fmt<KF_Q8_1> {
+    static constexpr int B = 32, S = 36, CE = 16, CPB = 2;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 1) * S;
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint4 q = lds_16<false>(in, off + 4u + 16u * (c & 1u));
+        const float bias = 8388736.0f;  // 2^23 + 128
+        mul4(d, q.x ^ 0x80808080u, bias, v);
+        mul4(d, q.y ^ 0x80808080u, bias, v + 4);
+        mul4(d, q.z ^ 0x80808080u, bias, v + 8);
+        mul4(d, q.w ^ 0x80808080u, bias, v + 12);
+    }
+};
+template <>
+struct Fmt<KF_Q8_K> {
+    static constexpr int B = 256, S = 292, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S;
+        const float d = __uint_as_float(lds_4(in, off));
+        const uint4 q = lds_16<false>(in, off + 4u + 16u * (c & 15u));
+        const float bias = 8388736.0f;
+        mul4(d, q.x ^ 0x80808080u, bias, v);
+        mul4(d, q.y ^ 0x80808080u, bias, v + 4);
+        mul4(d, q.z ^ 0x80808080u, bias, v + 8);
+        mul4(d, q.w ^ 0x80808080u, bias, v + 12);
+    }
+};
+
+// 2-bit plane p of 16 code bytes, as bytes (P(q,2,32) layout).
+__device__ __forceinline__ uint4 plane2_16(uint4 q, uint32_t p) {
+    const uint32_t s = 2u * p;
+    return make_uint4((q.x >> s) & 0x03030303u, (q.y >> s) & 0x03030303u, (q.z >> s) & 0x03030303u,
+                      (q.w >> s) & 0x03030303u);
+}
+
+// Bit b of 16 mask bytes, as bytes (P(mask,1,32) layout).
+__device__ __forceinline__ uint4 plane1_16(uint4 q, uint32_t b) {
+    return make_uint4((q.x >> b) & 0x01010101u, (q.y >> b) & 0x01010101u, (q.z >> b) & 0x01010101u,
+                      (q.w >> b) & 0x01010101u);
+}
+
+// gguf:q2_k: v = P(q,2,32), s = scales[floor(j/16)];
+// y[j] = D(M(M(d, s mod 16), v[j]), M(dmin, floor(s/16))).  Chunk cc = scale
+// cc; code bytes 32*(cc>>3) + 16*(cc&1), plane (cc>>1)&3.
+template <>
+struct Fmt<KF_Q2_K> {
+    static constexpr int B = 256, S = 84, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
+        const uint32_t sc = in[off + cc];
+        const float d = h2f(lds_2<PH>(in, off + 80u)), dmin = h2f(lds_2<PH>(in, off + 82u));
+        const float ds = __fmul_rn(d, static_cast<float>(sc & 15u));
+        const float ndm = -__fmul_rn(dmin, static_cast<float>(sc >> 4));
+        const uint4 n = plane2_16(lds_16<false>(in, off + 16u + 32u * (cc >> 3) + 16u * (cc & 1u)), (cc >> 1) & 3u);
+        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
+        const float bias = 8388608.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[4 * q + 0] = __fmaf_rn(ds, byte_minus<0>(w[q], bias), ndm);
+            v[4 * q + 1] = __fmaf_rn(ds, byte_minus<1>(w[q], bias), ndm);
+            v[4 * q + 2] = __fmaf_rn(ds, byte_minus<2>(w[q], bias), ndm);
+            v[4 * q + 3] = __fmaf_rn(ds, byte_minus<3>(w[q], bias), ndm);
+        }
+    }
+};
+
+// gguf:q3_k: v = P(q,2,32), h = P(mask,1,32), l = P(b[96:104],4,8),
+// a = P(b[104:108],2,4); s = l[k] + 16 a[k] - 32 with k = floor(j/16);
+// y[j] = M(M(d, s), v[j] - 4*(1 - h[j])).  Chunk cc: scale k = cc; codes as
+// q2_k at byte 32; mask bit cc>>1 of mask bytes 16*(cc&1)...
+template <>
+struct Fmt<KF_Q3_K> {
+    static constexpr int B = 256, S = 110, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
+        const float d = h2f(lds_2<PH>(in, off + 108u));
+        const uint32_t l = (in[off + 96u + (cc & 7u)] >> (4u * (cc >> 3))) & 15u;
+        const uint32_t a = (in[off + 104u + (cc & 3u)] >> (2u * (cc >> 2))) & 3u;
+        const float ds = __fmul_rn(d, static_cast<float>(static_cast<int32_t>(l + 16u * a) - 32));
+        const uint4 vq = plane2_16(lds_16<false>(in, off + 32u + 32u * (cc >> 3) + 16u * (cc & 1u)), (cc >> 1) & 3u);
+        const uint4 hm = plane1_16(lds_16<false>(in, off + 16u * (cc & 1u)), cc >> 1);
+        // v - 4*(1 - h) = (v + 4h) - 4
+        mul4(ds, vq.x | (hm.x << 2), 8388612.0f, v);  // 2^23 + 4
+        mul4(ds, vq.y | (hm.y << 2), 8388612.0f, v + 4);
+        mul4(ds, vq.z | (hm.z << 2), 8388612.0f, v + 8);
+        mul4(ds, vq.w | (hm.w << 2), 8388612.0f, v + 12);
+    }
+};
+
+// gguf:q5_k: v = P(q,4,32) + 16*P(high,1,32); a, m as q4_k;
+// y[j] = D(M(M(d, a[k]), v[j]), M(dmin, m[k])).  Chunk cc: sub-block k = cc>>1,
+// codes 48 + 32*(cc>>2) + 16*(cc&1) plane k&1, high bit k of bytes 16 + 16*(cc&1).
+template <>
+struct Fmt<KF_Q5_K> {
+    static constexpr int B = 256, S = 176, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, k = cc >> 1;
+        const uint4 hdr = lds_16<!PH>(in, off);
+        const float d = h2f(hdr.x & 0xffffu), dmin = h2f(hdr.x >> 16);
+        const uint32_t j8 = 8u * (k & 3u);
+        const uint32_t b0 = (hdr.y >> j8) & 0xffu, b1 = (hdr.z >> j8) & 0xffu, b2 = (hdr.w >> j8) & 0xffu;
+        const bool lo = k < 4u;
+        const uint32_t sa = lo ? (b0 & 63u) : ((b2 & 15u) | ((b0 >> 6) << 4));
+        const uint32_t sm = lo ? (b1 & 63u) : ((b2 >> 4) | ((b1 >> 6) << 4));
+        const float da = __fmul_rn(d, static_cast<float>(sa));
+        const float ndm = -__fmul_rn(dmin, static_cast<float>(sm));
+        const uint4 n = nib_plane16(lds_16<!PH>(in, off + 48u + 32u * (cc >> 2) + 16u * (cc & 1u)), k & 1u);
+        const uint4 hb = plane1_16(lds_16<!PH>(in, off + 16u + 16u * (cc & 1u)), k);
+        const uint32_t w[4] = {n.x | (hb.x << 4), n.y | (hb.y << 4), n.z | (hb.z << 4), n.w | (hb.w << 4)};
+        const float bias = 8388608.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[4 * q + 0] = __fmaf_rn(da, byte_minus<0>(w[q], bias), ndm);
+            v[4 * q + 1] = __fmaf_rn(da, byte_minus<1>(w[q], bias), ndm);
+            v[4 * q + 2] = __fmaf_rn(da, byte_minus<2>(w[q], bias), ndm);
+            v[4 * q + 3] = __fmaf_rn(da, byte_minus<3>(w[q], bias), ndm);
+        }
+    }
+};
+
+// gguf:iq4_xs: v = P(q,4,16); s[k] = field(scales[k/2], 4(k mod 2), 4)
+// + 16*field(high, 2k, 2) - 32; y[j] = M(M(d, s[floor(j/32)]), IQ4[v[j]]).
+// Chunk cc: k = cc>>1, plane cc&1 of code bytes 16k...
+template <>
+struct Fmt<KF_IQ4_XS> {
+    static constexpr int B = 256, S = 136, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, k = cc >> 1;
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t high = lds_2<PH>(in, off + 2u);
+        const uint32_t lo4 = (in[off + 4u + (k >> 1)] >> (4u * (k & 1u))) & 15u;
+        const int32_t sc = static_cast<int32_t>(lo4 | (((high >> (2u * k)) & 3u) << 4)) - 32;
+        const float ds = __fmul_rn(d, static_cast<float>(sc));
+        const uint4 n = nib_plane16(lds_16<false>(in, off + 8u + 16u * k), cc & 1u);
+        const float* T = x.H->lut_iq4;
+        lut4(T, ds, n.x, v);
+        lut4(T, ds, n.y, v + 4);
+        lut4(T, ds, n.z, v + 8);
+        lut4(T, ds, n.w, v + 12);
+    }
+};
+
+// gguf:tq1_0: outputs in three sequences (start, width, count) = (0,32,5),
+// (32,16,5), (48,4,4), plane p before lane j: M(d, floor(3*((b*3^p) mod 256)
+// /256) - 1).  Chunks 0..9: p = cc>>1, bytes 16*(cc&1)...; 10..14: p = cc-10,
+// bytes 32..47; 15: element i has p = i/4 and byte 48 + i%4.
+template <>
+struct Fmt<KF_TQ1_0> {
+    static constexpr int B = 256, S = 54, CE = 16, CPB = 16;
+    __device__ __forceinline__ static float trit(uint32_t byte, uint32_t pw) {
+        const uint32_t t = ((((byte * pw) & 255u) * 3u) >> 8);  // 0, 1 or 2
+        return __fsub_rn(__uint_as_float(0x4B000000u | t), 8388609.0f);  // t - 1, exact
+    }
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
+        const float d = h2f(lds_2<PH>(in, off + 52u));
+        const uint32_t start = cc < 10u ? 16u * (cc & 1u) : (cc < 15u ? 32u : 48u);
+        const uint4 q = lds_16<false>(in, off + start);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        if (cc < 15u) {
+            const uint32_t p = cc < 10u ? (cc >> 1) : (cc - 10u);
+            const uint32_t pw = p == 0u ? 1u : p == 1u ? 3u : p == 2u ? 9u : p == 3u ? 27u : 81u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(d, trit((w[i >> 2] >> (8 * (i & 3))) & 255u, pw));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t pw = (i >> 2) == 0 ? 1u : (i >> 2) == 1 ? 3u : (i >> 2) == 2 ? 9u : 27u;
+                v[i] = __fmul_rn(d, trit((w[0] >> (8 * (i & 3))) & 255u, pw));
+            }
+        }
+    }
+};
+
+// gguf:tq2_0: y[j] = M(d, v[j] - 1), v = P(q,2,32) (q at byte 0, d at 64).
+template <>
+struct Fmt<KF_TQ2_0> {
+    static constexpr int B = 256, S = 66, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
+        const float d = h2f(lds_2<PH>(in, off + 64u));
+        const uint4 n = plane2_16(lds_16<false>(in, off + 32u * (cc >> 3) + 16u * (cc & 1u)), (cc >> 1) & 3u);
+        const float bias = 8388609.0f;  // 2^23 + 1
+        mul4(d, n.x, bias, v);
+        mul4(d, n.y, bias, v + 4);
+        mul4(d, n.z, bias, v + 8);
+        mul4(d, n.w, bias, v + 12);
+    }
+};
+
+// gguf:q1_0: y[j] = d if bit(q[floor(j/8)], j mod 8) else -d (no multiply).
+template <>
+struct Fmt<KF_Q1_0> {
+    static constexpr int B = 128, S = 18, CE = 16, CPB = 8;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 3) * S;
+        const float d = h2f(lds_2<PH>(in, off)), nd = -d;
+        const uint32_t bits = lds_2<PH>(in, off + 2u + 2u * (c & 7u));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = ((bits >> i) & 1u) ? d : nd;
+    }
+};
+
+// gguf:q2_0: y[j] = M(d, v[j] - 1), v = P(q,2,1): element j is bits 2*(j mod 4)
+// of byte floor(j/4), i.e. bits 2i of the chunk's 4 bytes.
+template <>
+struct Fmt<KF_Q2_0> {
+    static constexpr int B = 64, S = 18, CE = 16, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 2) * S;
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t w = lds_4(in, off + 2u + 4u * (c & 3u));
+        const float bias = 8388609.0f;  // 2^23 + 1
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = __fmul_rn(d, __fsub_rn(__uint_as_float(0x4B000000u | ((w >> (2 * i)) & 3u)), bias));
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Output stage: one RNE conversion per element; 16-byte stores when y is
 // 16-byte aligned (chunk offsets are multiples of 8 elements, so every chunk
 // then starts on a 16-byte boundary).
@@ -631,6 +941,19 @@ __device__ __noinline__ void decode_tile_slow(const StageInfo& si, const uint8_t
         case KF_MXFP4: decode_tile_slow_f<KF_MXFP4>(si, in, x, tid); break;
         case KF_GGUF_NVFP4: decode_tile_slow_f<KF_GGUF_NVFP4>(si, in, x, tid); break;
         case KF_NVFP4: decode_tile_slow_f<KF_NVFP4>(si, in, x, tid); break;
+        case KF_Q4_1: decode_tile_slow_f<KF_Q4_1>(si, in, x, tid); break;
+        case KF_Q5_0: decode_tile_slow_f<KF_Q5_0>(si, in, x, tid); break;
+        case KF_Q5_1: decode_tile_slow_f<KF_Q5_1>(si, in, x, tid); break;
+        case KF_Q8_1: decode_tile_slow_f<KF_Q8_1>(si, in, x, tid); break;
+        case KF_Q8_K: decode_tile_slow_f<KF_Q8_K>(si, in, x, tid); break;
+        case KF_Q2_K: decode_tile_slow_f<KF_Q2_K>(si, in, x, tid); break;
+        case KF_Q3_K: decode_tile_slow_f<KF_Q3_K>(si, in, x, tid); break;
+        case KF_Q5_K: decode_tile_slow_f<KF_Q5_K>(si, in, x, tid); break;
+        case KF_IQ4_XS: decode_tile_slow_f<KF_IQ4_XS>(si, in, x, tid); break;
+        case KF_TQ1_0: decode_tile_slow_f<KF_TQ1_0>(si, in, x, tid); break;
+        case KF_TQ2_0: decode_tile_slow_f<KF_TQ2_0>(si, in, x, tid); break;
+        case KF_Q1_0: decode_tile_slow_f<KF_Q1_0>(si, in, x, tid); break;
+        case KF_Q2_0: decode_tile_slow_f<KF_Q2_0>(si, in, x, tid); break;
         default: decode_tile_slow_f<KF_Q4_G64>(si, in, x, tid); break;
     }
 }
@@ -678,6 +1001,19 @@ __device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint
         case KF_MXFP4: decode_tile_fast_f<KF_MXFP4, OSEL>(si, in, x, tid); break;
         case KF_GGUF_NVFP4: decode_tile_fast_f<KF_GGUF_NVFP4, OSEL>(si, in, x, tid); break;
         case KF_NVFP4: decode_tile_fast_f<KF_NVFP4, OSEL>(si, in, x, tid); break;
+        case KF_Q4_1: decode_tile_fast_f<KF_Q4_1, OSEL>(si, in, x, tid); break;
+        case KF_Q5_0: decode_tile_fast_f<KF_Q5_0, OSEL>(si, in, x, tid); break;
+        case KF_Q5_1: decode_tile_fast_f<KF_Q5_1, OSEL>(si, in, x, tid); break;
+        case KF_Q8_1: decode_tile_fast_f<KF_Q8_1, OSEL>(si, in, x, tid); break;
+        case KF_Q8_K: decode_tile_fast_f<KF_Q8_K, OSEL>(si, in, x, tid); break;
+        case KF_Q2_K: decode_tile_fast_f<KF_Q2_K, OSEL>(si, in, x, tid); break;
+        case KF_Q3_K: decode_tile_fast_f<KF_Q3_K, OSEL>(si, in, x, tid); break;
+        case KF_Q5_K: decode_tile_fast_f<KF_Q5_K, OSEL>(si, in, x, tid); break;
+        case KF_IQ4_XS: decode_tile_fast_f<KF_IQ4_XS, OSEL>(si, in, x, tid); break;
+        case KF_TQ1_0: decode_tile_fast_f<KF_TQ1_0, OSEL>(si, in, x, tid); break;
+        case KF_TQ2_0: decode_tile_fast_f<KF_TQ2_0, OSEL>(si, in, x, tid); break;
+        case KF_Q1_0: decode_tile_fast_f<KF_Q1_0, OSEL>(si, in, x, tid); break;
+        case KF_Q2_0: decode_tile_fast_f<KF_Q2_0, OSEL>(si, in, x, tid); break;
         default: decode_tile_fast_f<KF_Q4_G64, OSEL>(si, in, x, tid); break;
     }
 }

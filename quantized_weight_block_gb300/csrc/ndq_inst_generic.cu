@@ -3,7 +3,17 @@
 #include "ndq_device.cuh"
 
 namespace ndq {
-KernelFn kernel_generic(int osel) { return kernel_row<-1>(osel); }
+// The generic kernels of each output type sit in their own translation units
+// (ndq_inst_generic_<type>.cu) so that they compile in parallel.
+KernelFn kernel_generic(int osel) {
+    switch (osel) {
+        case KO_F32: return kernel_generic_f32();
+        case KO_F16: return kernel_generic_f16();
+        case KO_BF16: return kernel_generic_bf16();
+        case KO_F64: return kernel_generic_f64();
+        default: return kernel_generic_any();
+    }
+}
 KernelFn kernel_kquant_mix(int osel) { return kernel_row<kFselKQuantMix>(osel); }
 
 size_t decode_smem_bytes(bool tab) {

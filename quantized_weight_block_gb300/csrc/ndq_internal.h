@@ -19,7 +19,20 @@ enum KFmt : int32_t {
     KF_GGUF_NVFP4 = 6,
     KF_NVFP4 = 7,
     KF_Q4_G64 = 8,
-    KF_COUNT = 9,
+    KF_Q4_1 = 9,
+    KF_Q5_0 = 10,
+    KF_Q5_1 = 11,
+    KF_Q8_1 = 12,
+    KF_Q8_K = 13,
+    KF_Q2_K = 14,
+    KF_Q3_K = 15,
+    KF_Q5_K = 16,
+    KF_IQ4_XS = 17,
+    KF_TQ1_0 = 18,
+    KF_TQ2_0 = 19,
+    KF_Q1_0 = 20,
+    KF_Q2_0 = 21,
+    KF_COUNT = 22,
 };
 
 // Format selector of a launch whose tensors mix only gguf:q8_0, gguf:q4_k and
@@ -35,10 +48,10 @@ enum KOut : int32_t { KO_F32 = 0, KO_F16 = 1, KO_BF16 = 2, KO_F64 = 3 };
 // so full tiles of a 16-byte-aligned payload are bulk-copyable.
 constexpr int kTileElems = 8192;
 constexpr int kThreads = 256;
-constexpr int kMaxTileBytes = 8704;  // gguf:q8_0: 256 blocks * 34 bytes
+constexpr int kMaxTileBytes = 9344;  // gguf:q8_k: 32 blocks * 292 bytes
 constexpr int kBlockThreads = kThreads + 32;  // consumer warps + one producer warp
 constexpr int kStages = 4;                    // staged tiles in flight per CTA
-constexpr int kInStride = 8832;               // tile bytes + phase + rounding + over-read
+constexpr int kInStride = 9472;               // tile bytes + phase + rounding + over-read
 constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
 // Resident CTAs per SM for launches that mix formats (the whole-model decode):
 // measured fastest at 2 even when registers and shared memory allow 3.
@@ -88,6 +101,24 @@ KernelFn kernel_mxfp4(int osel);
 KernelFn kernel_gguf_nvfp4(int osel);
 KernelFn kernel_nvfp4(int osel);
 KernelFn kernel_q4_g64(int osel);
+KernelFn kernel_q4_1(int osel);
+KernelFn kernel_q5_0(int osel);
+KernelFn kernel_q5_1(int osel);
+KernelFn kernel_q8_1(int osel);
+KernelFn kernel_q8_k(int osel);
+KernelFn kernel_q2_k(int osel);
+KernelFn kernel_q3_k(int osel);
+KernelFn kernel_q5_k(int osel);
+KernelFn kernel_iq4_xs(int osel);
+KernelFn kernel_tq1_0(int osel);
+KernelFn kernel_tq2_0(int osel);
+KernelFn kernel_q1_0(int osel);
+KernelFn kernel_q2_0(int osel);
+KernelFn kernel_generic_f32();
+KernelFn kernel_generic_f16();
+KernelFn kernel_generic_bf16();
+KernelFn kernel_generic_f64();
+KernelFn kernel_generic_any();
 KernelFn kernel_generic(int osel);
 KernelFn kernel_kquant_mix(int osel);
 

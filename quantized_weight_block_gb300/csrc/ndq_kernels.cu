@@ -43,6 +43,19 @@ KernelFn pick_kernel(int fsel, int osel) {
         case KF_GGUF_NVFP4: return kernel_gguf_nvfp4(osel);
         case KF_NVFP4: return kernel_nvfp4(osel);
         case KF_Q4_G64: return kernel_q4_g64(osel);
+        case KF_Q4_1: return kernel_q4_1(osel);
+        case KF_Q5_0: return kernel_q5_0(osel);
+        case KF_Q5_1: return kernel_q5_1(osel);
+        case KF_Q8_1: return kernel_q8_1(osel);
+        case KF_Q8_K: return kernel_q8_k(osel);
+        case KF_Q2_K: return kernel_q2_k(osel);
+        case KF_Q3_K: return kernel_q3_k(osel);
+        case KF_Q5_K: return kernel_q5_k(osel);
+        case KF_IQ4_XS: return kernel_iq4_xs(osel);
+        case KF_TQ1_0: return kernel_tq1_0(osel);
+        case KF_TQ2_0: return kernel_tq2_0(osel);
+        case KF_Q1_0: return kernel_q1_0(osel);
+        case KF_Q2_0: return kernel_q2_0(osel);
         default: return kernel_generic(osel);
     }
 }

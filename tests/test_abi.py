@@ -113,7 +113,7 @@ def test_validation_errors_return_before_any_launch():
     F = ndq.NDQ_FLOAT
     # invalid arguments never reach CUDA, so these run without a GPU
     assert ndq.ndq_dequantize_packed(99, (1, 32), F, 16, 18, 16) == 2
-    assert ndq.ndq_dequantize_packed(ndq.format_id("gguf:q2_k"), (1, 256), F, 16, 84, 16) == 3
+    assert ndq.ndq_dequantize_packed(ndq.format_id("gguf:iq2_xxs"), (1, 256), F, 16, 66, 16) == 3
     assert ndq.ndq_dequantize_packed(q40, (), F, 16, 0, 16) == 4
     assert ndq.ndq_dequantize_packed(q40, (1,) * 9 + (32,), F, 16, 18, 16) == 4
     assert ndq.ndq_dequantize_packed(q40, (-2, 32), F, 16, 0, 16) == 5

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 import quantized_weight_block_gb300 as ndq  # noqa: E402
 
 FORMATS = ["gguf:q8_0", "q8_g32_fp16", "gguf:q4_0", "gguf:iq4_nl", "gguf:q4_k", "gguf:q6_k",
-           "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16"]
+           "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16"] + synth.NEXT_FORMATS
 OUTS = ["float32", "float16", "bfloat16", "float64"]
 TORCH_OUT = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16,
              "float64": torch.float64}
@@ -133,21 +133,36 @@ def test_every_scale_byte(orc, fmt):
 
 
 def test_special_binary16_scales(orc):
-    # every binary16 scale pattern class: zeros, subnormals, max, inf, NaN
+    # every binary16 scale pattern class: zeros, subnormals, max, inf, NaN,
+    # placed in the first (d) and second (m / dmin) binary16 field
     specials = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x7C01,
                          0x3C00, 0xBC00], np.uint16)
-    for fmt in ("gguf:q8_0", "gguf:q4_0", "gguf:iq4_nl", "q4_g64_fp16", "gguf:q4_k", "gguf:q6_k"):
+    fields = {"gguf:q8_0": (0,), "gguf:q4_0": (0,), "gguf:iq4_nl": (0,), "q4_g64_fp16": (0,), "gguf:q4_k": (0, 2),
+              "gguf:q6_k": (208,), **synth.F16_SCALES}
+    for fmt, offs in fields.items():
         B, S = synth.GEOMETRY[fmt]
         nb = len(specials) ** 2
         x = synth.payload(fmt, (nb, B), seed=5, dist="bytes").reshape(nb, S).copy()
         a, b = np.meshgrid(specials, specials)
-        offs = {"gguf:q4_k": (0, 2), "gguf:q6_k": (208, 208)}.get(fmt, (0, 0))
         x[:, offs[0]:offs[0] + 2] = a.reshape(-1, 1).view(np.uint8).reshape(nb, 2)
-        if fmt == "gguf:q4_k":
-            x[:, 2:4] = b.reshape(-1, 1).view(np.uint8).reshape(nb, 2)
+        if len(offs) > 1:
+            x[:, offs[1]:offs[1] + 2] = b.reshape(-1, 1).view(np.uint8).reshape(nb, 2)
         x = x.reshape(-1)
         for out in OUTS:
             assert_bit_exact(gpu_decode(fmt, (nb, B), x, out), orc.decode(fmt, (nb, B), x, out), out, fmt)
+
+
+def test_special_binary32_scales_q8_k(orc):
+    # gguf:q8_k's scale is binary32: zeros, subnormals, max, inf, NaN
+    specials = np.array([0, 0x80000000, 1, 0x807FFFFF, 0x00800000, 0x7F7FFFFF, 0xFF7FFFFF, 0x7F800000,
+                         0xFF800000, 0x7FC00000, 0x7F800001, 0x3F800000, 0x477FE000, 0x5F800000], np.uint32)
+    nb = len(specials) * 4
+    x = synth.payload("gguf:q8_k", (nb, 256), seed=6, dist="bytes").reshape(nb, 292).copy()
+    x[:, 0:4] = np.repeat(specials, 4).astype("<u4").view(np.uint8).reshape(nb, 4)
+    x = x.reshape(-1)
+    for out in OUTS:
+        assert_bit_exact(gpu_decode("gguf:q8_k", (nb, 256), x, out), orc.decode("gguf:q8_k", (nb, 256), x, out), out,
+                         "q8_k")
 
 
 def test_batched_mixed(orc):
@@ -203,7 +218,7 @@ def check_sampled(orc, fmt, shape, x_np, y_t, out, seed=0):
     assert_bit_exact(got, want, out, f"{fmt} {shape} sampled")
 
 
-@pytest.mark.parametrize("label,fmt,shape,seed,out", synth.WORKLOADS)
+@pytest.mark.parametrize("label,fmt,shape,seed,out", synth.WORKLOADS + synth.NEXT_WORKLOADS)
 def test_full_size_workloads_sampled(orc, label, fmt, shape, seed, out):
     x = synth.payload(fmt, shape, seed)
     y = ndq.dequantize_packed(fmt, shape, torch.from_numpy(x).to(DEV), TORCH_OUT[out])
