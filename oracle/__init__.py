@@ -19,6 +19,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ndq_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# The IQ codebooks are page data kept as a cited text fixture; the oracle
+# expands them itself (oracle_set_codebook).
+CODEBOOKS_FILE = os.path.join(os.path.dirname(_HERE), "tests", "golden", "iq_codebooks.txt")
 
 # The oracle's own output-type codes (FLOAT, FLOAT16, BFLOAT16, DOUBLE).
 OUT_DTYPES = {"float32": 0, "float16": 1, "bfloat16": 2, "float64": 3}
@@ -85,8 +88,45 @@ def lib() -> ctypes.CDLL:
         L.oracle_encode_grouped.argtypes = [c.c_char_p, vp, c.c_uint64, c.c_uint64, vp]
         for fn in ("oracle_h2f_array", "oracle_f32_to_bf16_array", "oracle_f32_to_f16_array"):
             getattr(L, fn).argtypes = [vp, vp, c.c_uint64]
+        L.oracle_set_codebook.argtypes = [c.c_char_p, c.c_int, c.c_int, vp, c.c_int, vp, c.c_uint64]
+        L.oracle_codebook_row.argtypes = [c.c_char_p, c.c_int, vp]
+        L.oracle_codebook_rows.argtypes = [c.c_char_p]
+        for name, (width, bits, _rows, values, packed) in read_codebooks().items():
+            vals = np.array(values, np.int32)
+            rc = L.oracle_set_codebook(name.encode(), width, bits, _ptr(vals), len(vals), _ptr(packed), packed.size)
+            if rc:
+                raise OracleError(rc, f"codebook {name}")
         _lib = L
     return _lib
+
+
+def read_codebooks(path: str = CODEBOOKS_FILE) -> dict:
+    """{name: (width, bits, stated rows, values, packed bytes)} from the fixture."""
+    books, cur = {}, None
+    with open(path) as f:
+        for line in f:
+            tok = line.split("#", 1)[0].split()
+            if not tok:
+                continue
+            if tok[0] == "codebook":
+                cur = tok[1]
+                books[cur] = [int(tok[2]), int(tok[3]), int(tok[4]), [int(v) for v in tok[5].split(",")], []]
+            elif tok[0] == "hex":
+                books[cur][4].append(tok[1])
+    return {k: (w, b, r, v, np.frombuffer(bytes.fromhex("".join(h)), np.uint8).copy())
+            for k, (w, b, r, v, h) in books.items()}
+
+
+def codebook_rows(name: str) -> int:
+    return lib().oracle_codebook_rows(name.encode())
+
+
+def codebook_row(name: str, r: int) -> list[int]:
+    out = np.zeros(8, np.int32)
+    w = lib().oracle_codebook_row(name.encode(), r, _ptr(out))
+    if w < 0:
+        raise OracleError(-w, f"{name} row {r}")
+    return out[:w].tolist()
 
 
 def _shape_arg(shape):

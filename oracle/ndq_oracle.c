@@ -26,6 +26,10 @@
  *          (grouped_absmax canonical encoder), GGUF block table.
  *  [KILN]  gld-kiln "Quantization" spec: group-count formula, E8M0 byte 127.
  *
+ * The IQ codebooks ([DQP] "IQ codebooks") are page data; the test harness
+ * passes them in from a cited text fixture (oracle_set_codebook) and the
+ * IQ decoders report an unsupported format until they are loaded.
+ *
  * Readings where the pages leave a step open are marked READING and listed
  * in the design notes.
  *
@@ -74,11 +78,11 @@ static const or_format OR_FORMATS[] = {
     {"gguf:q2_k", 256, 84, 1},    {"gguf:q3_k", 256, 110, 1},
     {"gguf:q4_k", 256, 144, 1},   {"gguf:q5_k", 256, 176, 1},
     {"gguf:q6_k", 256, 210, 1},   {"gguf:q8_k", 256, 292, 1},
-    {"gguf:iq2_xxs", 256, 66, 0}, {"gguf:iq2_xs", 256, 74, 0},
-    {"gguf:iq3_xxs", 256, 98, 0}, {"gguf:iq1_s", 256, 50, 0},
-    {"gguf:iq4_nl", 32, 18, 1},   {"gguf:iq3_s", 256, 110, 0},
-    {"gguf:iq2_s", 256, 82, 0},   {"gguf:iq4_xs", 256, 136, 1},
-    {"gguf:iq1_m", 256, 56, 0},   {"gguf:tq1_0", 256, 54, 1},
+    {"gguf:iq2_xxs", 256, 66, 1}, {"gguf:iq2_xs", 256, 74, 1},
+    {"gguf:iq3_xxs", 256, 98, 1}, {"gguf:iq1_s", 256, 50, 1},
+    {"gguf:iq4_nl", 32, 18, 1},   {"gguf:iq3_s", 256, 110, 1},
+    {"gguf:iq2_s", 256, 82, 1},   {"gguf:iq4_xs", 256, 136, 1},
+    {"gguf:iq1_m", 256, 56, 1},   {"gguf:tq1_0", 256, 54, 1},
     {"gguf:tq2_0", 256, 66, 1},   {"gguf:mxfp4", 32, 17, 1},
     {"gguf:nvfp4", 64, 36, 1},    {"gguf:q1_0", 128, 18, 1},
     {"gguf:q2_0", 64, 18, 1},
@@ -533,6 +537,230 @@ static void dec_q2_0(const uint8_t *b, float *y) {
     for (int j = 0; j < 64; ++j) y[j] = M(d, (float)((int32_t)v[j] - 1));
 }
 
+/* ------------------------------------------------------------------------ */
+/* IQ2, IQ3 and IQ1 formats ([DQP] "Mathematical decoding rules", "IQ2,     */
+/* IQ3, and IQ1 formats"; tables from [DQP] "IQ codebooks").                 */
+/* ------------------------------------------------------------------------ */
+
+/* The six codebooks G(name, r).  Their contents are data printed on the
+ * page; the test harness passes each one in as the page's packed bytes
+ * (oracle_set_codebook), and this file expands them: entry k is the
+ * bits-wide field at bit bits*k of the byte stream (low bits of a byte
+ * first) used as an index into the value list, and row r is entries
+ * width*r .. width*r + width - 1. */
+#define OR_CB_COUNT 6
+#define OR_CB_MAX_ENTRIES (2048 * 8)
+static const char *const OR_CB_NAMES[OR_CB_COUNT] = {"iq2xxs_grid", "iq2xs_grid", "iq2s_grid",
+                                                     "iq3xxs_grid", "iq3s_grid", "iq1s_grid"};
+enum { CB_IQ2XXS, CB_IQ2XS, CB_IQ2S, CB_IQ3XXS, CB_IQ3S, CB_IQ1S };
+static int8_t OR_CB[OR_CB_COUNT][OR_CB_MAX_ENTRIES];
+static int OR_CB_WIDTH[OR_CB_COUNT], OR_CB_ROWS[OR_CB_COUNT];
+
+static int or_cb_find(const char *name) {
+    for (int i = 0; i < OR_CB_COUNT; ++i)
+        if (name && strcmp(OR_CB_NAMES[i], name) == 0) return i;
+    return -1;
+}
+
+int oracle_set_codebook(const char *name, int width, int bits, const int32_t *values, int nvalues,
+                        const uint8_t *packed, uint64_t nbytes) {
+    int ci = or_cb_find(name);
+    if (ci < 0) return OR_ERR_UNKNOWN_FORMAT;
+    if (!values || !packed) return OR_ERR_NULL;
+    if (width < 1 || bits < 1 || bits > 8 || 8 % bits != 0 || nvalues < 1) return OR_ERR_RANGE;
+    uint64_t entries = nbytes * 8u / (uint64_t)bits;
+    if (entries % (uint64_t)width != 0 || entries > OR_CB_MAX_ENTRIES) return OR_ERR_RANGE;
+    for (uint64_t k = 0; k < entries; ++k) {
+        uint64_t bit0 = k * (uint64_t)bits;
+        uint32_t idx = field(packed[bit0 / 8u], (int)(bit0 % 8u), bits);
+        if (idx >= (uint32_t)nvalues) return OR_ERR_RANGE;
+        OR_CB[ci][k] = (int8_t)values[idx];
+    }
+    OR_CB_WIDTH[ci] = width;
+    OR_CB_ROWS[ci] = (int)(entries / (uint64_t)width);
+    return OR_OK;
+}
+
+/* Row r of a loaded codebook into out[0..width-1]; returns the width, or a
+ * negative error. */
+int oracle_codebook_row(const char *name, int r, int32_t *out) {
+    int ci = or_cb_find(name);
+    if (ci < 0 || !out) return -OR_ERR_UNKNOWN_FORMAT;
+    if (r < 0 || r >= OR_CB_ROWS[ci]) return -OR_ERR_RANGE;
+    for (int j = 0; j < OR_CB_WIDTH[ci]; ++j) out[j] = OR_CB[ci][r * OR_CB_WIDTH[ci] + j];
+    return OR_CB_WIDTH[ci];
+}
+
+int oracle_codebook_rows(const char *name) {
+    int ci = or_cb_find(name);
+    return ci < 0 ? -OR_ERR_UNKNOWN_FORMAT : OR_CB_ROWS[ci];
+}
+
+/* G(name, r): row r of a codebook (NULL when the table is not loaded). */
+static const int8_t *G(int ci, uint32_t r) {
+    if ((int)r >= OR_CB_ROWS[ci]) return NULL;
+    return &OR_CB[ci][r * (uint32_t)OR_CB_WIDTH[ci]];
+}
+
+/* S(v): the eight signs 1 - 2*bit(v, j).  SP(v): signs 0..6 from the low
+ * seven bits of v and sign 7 from their parity. */
+static void S8(uint32_t v, float *s) {
+    for (int j = 0; j < 8; ++j) s[j] = 1.0f - 2.0f * (float)field(v, j, 1);
+}
+
+static void SP8(uint32_t v, float *s) {
+    uint32_t par = 0;
+    for (int j = 0; j < 7; ++j) par += field(v, j, 1);
+    S8((v & 127u) | ((par % 2u) << 7), s);
+}
+
+/* A block is eight groups g of four lanes l; lane i = 4g + l yields outputs
+ * 8i .. 8i+7.  For IQ2_XXS, IQ2_XS, IQ2_S, IQ3_XXS and IQ3_S each output is
+ * M(M(c, v[j]), s[j]) with the lane's codebook values v, signs s and scale
+ * c. */
+static void or_lane_signed(float c, const int8_t *v, const float *s, float *y) {
+    for (int j = 0; j < 8; ++j) y[j] = M(M(c, (float)v[j]), s[j]);
+}
+
+static int dec_iq2_xxs(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g) {
+        uint32_t a = U(b + 6 + 8 * g, 4);
+        float c = M(M(d, A(0.5f, (float)(a >> 28))), 0.25f);
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            const int8_t *v = G(CB_IQ2XXS, b[2 + 8 * g + l]);
+            float s[8];
+            if (!v) return OR_ERR_UNSUPPORTED_FORMAT;
+            SP8(field(a, 7 * l, 7), s);
+            or_lane_signed(c, v, s, y + 8 * i);
+        }
+    }
+    return OR_OK;
+}
+
+static int dec_iq2_xs(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g)
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            uint32_t a = U(b + 2 + 2 * i, 2);
+            uint32_t t = field(b[66 + g], 4 * (l / 2), 4);
+            float c = M(M(d, A(0.5f, (float)t)), 0.25f);
+            const int8_t *v = G(CB_IQ2XS, a % 512u);
+            float s[8];
+            if (!v) return OR_ERR_UNSUPPORTED_FORMAT;
+            SP8(a / 512u, s);
+            or_lane_signed(c, v, s, y + 8 * i);
+        }
+    return OR_OK;
+}
+
+static int dec_iq2_s(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g)
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            uint32_t r = b[2 + i] + 256u * field(b[66 + g], 2 * l, 2);
+            uint32_t t = field(b[74 + g], 4 * (l / 2), 4);
+            float c = M(M(d, A(0.5f, (float)t)), 0.25f);
+            const int8_t *v = G(CB_IQ2S, r);
+            float s[8];
+            if (!v) return OR_ERR_UNSUPPORTED_FORMAT;
+            S8(b[34 + i], s);
+            or_lane_signed(c, v, s, y + 8 * i);
+        }
+    return OR_OK;
+}
+
+static int dec_iq3_xxs(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g) {
+        uint32_t a = U(b + 66 + 4 * g, 4);
+        float c = M(M(d, A(0.5f, (float)(a >> 28))), 0.5f);
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            const int8_t *v0 = G(CB_IQ3XXS, b[2 + 2 * i]), *v1 = G(CB_IQ3XXS, b[3 + 2 * i]);
+            int8_t v[8];
+            float s[8];
+            if (!v0 || !v1) return OR_ERR_UNSUPPORTED_FORMAT;
+            for (int j = 0; j < 4; ++j) {
+                v[j] = v0[j];
+                v[4 + j] = v1[j];
+            }
+            SP8(field(a, 7 * l, 7), s);
+            or_lane_signed(c, v, s, y + 8 * i);
+        }
+    }
+    return OR_OK;
+}
+
+static int dec_iq3_s(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g) {
+        float c = M(d, (float)(1u + 2u * field(b[106 + g / 2], 4 * (g % 2), 4)));
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            int8_t v[8];
+            float s[8];
+            for (int t = 0; t < 2; ++t) {
+                uint32_t r = b[2 + 2 * i + t] + 256u * field(b[66 + g], 2 * l + t, 1);
+                const int8_t *row = G(CB_IQ3S, r);
+                if (!row) return OR_ERR_UNSUPPORTED_FORMAT;
+                for (int j = 0; j < 4; ++j) v[4 * t + j] = row[j];
+            }
+            S8(b[74 + i], s);
+            or_lane_signed(c, v, s, y + 8 * i);
+        }
+    }
+    return OR_OK;
+}
+
+/* IQ1_S and IQ1_M: y[8i+j] = M(c, A(v[j], delta)) with v = G(iq1s_grid, r). */
+static int or_lane_shifted(float c, uint32_t r, float delta, float *y) {
+    const int8_t *v = G(CB_IQ1S, r);
+    if (!v) return OR_ERR_UNSUPPORTED_FORMAT;
+    for (int j = 0; j < 8; ++j) y[j] = M(c, A((float)v[j], delta));
+    return OR_OK;
+}
+
+static int dec_iq1_s(const uint8_t *b, float *y) {
+    float d = H(b);
+    for (int g = 0; g < 8; ++g) {
+        uint32_t a = U(b + 34 + 2 * g, 2);
+        float c = M(d, (float)(2u * field(a, 12, 3) + 1u));
+        float delta = field(a, 15, 1) ? -0.125f : 0.125f;
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            uint32_t r = b[2 + i] + 256u * field(a, 3 * l, 3);
+            int rc = or_lane_shifted(c, r, delta, y + 8 * i);
+            if (rc != OR_OK) return rc;
+        }
+    }
+    return OR_OK;
+}
+
+static int dec_iq1_m(const uint8_t *b, float *y) {
+    uint32_t w[4], dbits = 0;
+    for (int k = 0; k < 4; ++k) {
+        w[k] = U(b + 48 + 2 * k, 2);
+        dbits += (w[k] >> 12) << (4 * k); /* floor(w[k]/2^12) * 2^(4k) */
+    }
+    float d = oracle_h2f((uint16_t)dbits);
+    for (int g = 0; g < 8; ++g)
+        for (int l = 0; l < 4; ++l) {
+            int i = 4 * g + l;
+            uint32_t a = field(b[32 + i / 2], 4 * (i % 2), 4);
+            uint32_t r = b[i] + 256u * (a % 8u);
+            uint32_t t = field(w[g / 2], 6 * (g % 2) + 3 * (l / 2), 3);
+            float c = M(d, (float)(2u * t + 1u));
+            float delta = field(a, 3, 1) ? -0.125f : 0.125f;
+            int rc = or_lane_shifted(c, r, delta, y + 8 * i);
+            if (rc != OR_OK) return rc;
+        }
+    return OR_OK;
+}
+
 /* One block of format `name` (dw: nvfp4 divisor) to binary32. */
 static int or_decode_block(const char *name, const uint8_t *b, float dw, float *y) {
     if (strcmp(name, "gguf:q8_0") == 0 || strcmp(name, "q8_g32_fp16") == 0) dec_q8_0(b, y);
@@ -557,6 +785,13 @@ static int or_decode_block(const char *name, const uint8_t *b, float dw, float *
     else if (strcmp(name, "gguf:tq2_0") == 0) dec_tq2_0(b, y);
     else if (strcmp(name, "gguf:q1_0") == 0) dec_q1_0(b, y);
     else if (strcmp(name, "gguf:q2_0") == 0) dec_q2_0(b, y);
+    else if (strcmp(name, "gguf:iq2_xxs") == 0) return dec_iq2_xxs(b, y);
+    else if (strcmp(name, "gguf:iq2_xs") == 0) return dec_iq2_xs(b, y);
+    else if (strcmp(name, "gguf:iq2_s") == 0) return dec_iq2_s(b, y);
+    else if (strcmp(name, "gguf:iq3_xxs") == 0) return dec_iq3_xxs(b, y);
+    else if (strcmp(name, "gguf:iq3_s") == 0) return dec_iq3_s(b, y);
+    else if (strcmp(name, "gguf:iq1_s") == 0) return dec_iq1_s(b, y);
+    else if (strcmp(name, "gguf:iq1_m") == 0) return dec_iq1_m(b, y);
     else return OR_ERR_UNSUPPORTED_FORMAT;
     return OR_OK;
 }

@@ -19,7 +19,9 @@ Field distributions follow the benchmark workloads:
     d_w = binary32(2688 / binary32(amax)) with amax = 0.1 (448*6/amax);
   * gguf:nvfp4 -- scale bytes uniform over 0x00..0x7e, codes uniform;
   * the other gguf formats (q4_1, q5_0, q5_1, q8_1, q8_k, q2_k, q3_k, q5_k,
-    iq4_xs, tq1_0, tq2_0, q1_0, q2_0) -- binary16 scales |N(0,0.02)|+1e-4,
+    iq4_xs, tq1_0, tq2_0, q1_0, q2_0, iq2_xxs, iq2_xs, iq2_s, iq3_xxs, iq3_s,
+    iq1_s, iq1_m) -- binary16 scales |N(0,0.02)|+1e-4 (iq1_m: its scale's
+    four nibbles in the top bits of the four 16-bit words at byte 48),
     minima |N(0,0.01)|, q8_k's binary32 scale likewise, codes in [-127, 127]
     for q8_k, every other byte uniform;
   * "bytes" -- every byte uniform over 0..255 (exercises special scales:
@@ -44,6 +46,8 @@ GEOMETRY = {
     "gguf:q8_k": (256, 292), "gguf:q2_k": (256, 84), "gguf:q3_k": (256, 110), "gguf:q5_k": (256, 176),
     "gguf:iq4_xs": (256, 136), "gguf:tq1_0": (256, 54), "gguf:tq2_0": (256, 66), "gguf:q1_0": (128, 18),
     "gguf:q2_0": (64, 18),
+    "gguf:iq2_xxs": (256, 66), "gguf:iq2_xs": (256, 74), "gguf:iq2_s": (256, 82), "gguf:iq3_xxs": (256, 98),
+    "gguf:iq3_s": (256, 110), "gguf:iq1_s": (256, 50), "gguf:iq1_m": (256, 56),
 }
 
 # Byte offsets of the binary16 scale fields of the other gguf formats; their
@@ -53,6 +57,8 @@ F16_SCALES = {
     "gguf:q4_1": (0, 2), "gguf:q5_0": (0,), "gguf:q5_1": (0, 2), "gguf:q8_1": (0,), "gguf:q2_k": (80, 82),
     "gguf:q3_k": (108,), "gguf:q5_k": (0, 2), "gguf:iq4_xs": (0,), "gguf:tq1_0": (52,), "gguf:tq2_0": (64,),
     "gguf:q1_0": (0,), "gguf:q2_0": (0,),
+    "gguf:iq2_xxs": (0,), "gguf:iq2_xs": (0,), "gguf:iq2_s": (0,), "gguf:iq3_xxs": (0,), "gguf:iq3_s": (0,),
+    "gguf:iq1_s": (0,),
 }
 
 NVFP4_AMAX = 0.1
@@ -129,6 +135,12 @@ def payload(fmt: str, shape, seed: int, dist: str = "workload", ndiv: int = 1) -
         for i, off in enumerate(F16_SCALES[fmt]):
             sd = 0.02 if i == 0 else 0.01
             blk[:, off:off + 2] = _f16_bytes(np.abs(rng.normal(0.0, sd, size=nb)) + (1e-4 if i == 0 else 0.0))
+    elif fmt == "gguf:iq1_m":
+        # the binary16 block scale is split over the top 4 bits of the four
+        # 16-bit words at byte 48 (nibble k of the scale in word k)
+        h = (np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4).astype(np.float16).view(np.uint16).astype(np.uint32)
+        for k in range(4):
+            blk[:, 49 + 2 * k] = (blk[:, 49 + 2 * k] & 0x0F) | (((h >> (4 * k)) & 15) << 4).astype(np.uint8)
     elif fmt == "gguf:q8_k":
         d = (np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4).astype("<f4")
         blk[:, 0:4] = d.view(np.uint8).reshape(nb, 4)

@@ -64,7 +64,9 @@ def test_decoded_set(orc):
                        "gguf:mxfp4", "gguf:nvfp4", "nvfp4", "q4_g64_fp16", "q8_g32_fp16",
                        "gguf:q4_1", "gguf:q5_0", "gguf:q5_1", "gguf:q8_1", "gguf:q8_k", "gguf:q2_k",
                        "gguf:q3_k", "gguf:q5_k", "gguf:iq4_xs", "gguf:tq1_0", "gguf:tq2_0", "gguf:q1_0",
-                       "gguf:q2_0"}
+                       "gguf:q2_0", "gguf:iq2_xxs", "gguf:iq2_xs", "gguf:iq2_s", "gguf:iq3_xxs", "gguf:iq3_s",
+                       "gguf:iq1_s", "gguf:iq1_m"}
+    assert decoded == set(orc.formats())
 
 
 @pytest.mark.parametrize("fmt,shape", [
