@@ -43,15 +43,15 @@ const FormatRow kFormats[NDQ_NUM_FORMATS] = {
     {"gguf:q5_k", 256, 176, ndq::KF_Q5_K},
     {"gguf:q6_k", 256, 210, ndq::KF_Q6_K},
     {"gguf:q8_k", 256, 292, ndq::KF_Q8_K},
-    {"gguf:iq2_xxs", 256, 66, -1},
-    {"gguf:iq2_xs", 256, 74, -1},
-    {"gguf:iq3_xxs", 256, 98, -1},
-    {"gguf:iq1_s", 256, 50, -1},
+    {"gguf:iq2_xxs", 256, 66, ndq::KF_IQ2_XXS},
+    {"gguf:iq2_xs", 256, 74, ndq::KF_IQ2_XS},
+    {"gguf:iq3_xxs", 256, 98, ndq::KF_IQ3_XXS},
+    {"gguf:iq1_s", 256, 50, ndq::KF_IQ1_S},
     {"gguf:iq4_nl", 32, 18, ndq::KF_IQ4_NL},
-    {"gguf:iq3_s", 256, 110, -1},
-    {"gguf:iq2_s", 256, 82, -1},
+    {"gguf:iq3_s", 256, 110, ndq::KF_IQ3_S},
+    {"gguf:iq2_s", 256, 82, ndq::KF_IQ2_S},
     {"gguf:iq4_xs", 256, 136, ndq::KF_IQ4_XS},
-    {"gguf:iq1_m", 256, 56, -1},
+    {"gguf:iq1_m", 256, 56, ndq::KF_IQ1_M},
     {"gguf:tq1_0", 256, 54, ndq::KF_TQ1_0},
     {"gguf:tq2_0", 256, 66, ndq::KF_TQ2_0},
     {"gguf:mxfp4", 32, 17, ndq::KF_MXFP4},

@@ -251,6 +251,7 @@ struct Ctx {
     const uint8_t* divs;
     uint64_t block0;
     uint64_t blocks_per_div;
+    const IqGrids* grids;  // IQ codebooks
 };
 
 // 16 bytes at byte offset `off` of a 16-byte-aligned stage (ALIGNED: off is a
@@ -841,6 +842,204 @@ struct Fmt<KF_Q2_0> {
 };
 
 // ---------------------------------------------------------------------------
+// IQ2, IQ3 and IQ1 formats ("Mathematical decoding rules", "IQ2, IQ3, and IQ1
+// formats").  A block is 8 groups g of 4 lanes l; lane i = 4g + l gives
+// outputs 8i..8i+7, so chunk cc (16 outputs) is lanes 2cc and 2cc+1 of group
+// cc>>1.  Codebook rows are read from the device copy of the codebooks
+// through the read-only cache.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 ldg_row8(const uint64_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+
+// SP(v): the low seven bits of v, completed by their parity as bit 7.
+__device__ __forceinline__ uint32_t sp_signs(uint32_t v7) { return v7 | ((__popc(v7) & 1u) << 7); }
+
+// Four outputs M(M(c, v), s) from codebook bytes w (value j in byte j) and
+// sign bits sg (bit j set: s = -1).  With s = +-1 the outer product only sets
+// the sign, so it is applied to the sign bit of M(c, v).
+__device__ __forceinline__ void signed4(float c, uint32_t w, uint32_t sg, float* v) {
+    const float z = 8388608.0f;  // 2^23
+    v[0] = __uint_as_float(__float_as_uint(__fmul_rn(c, byte_minus<0>(w, z))) ^ ((sg << 31) & 0x80000000u));
+    v[1] = __uint_as_float(__float_as_uint(__fmul_rn(c, byte_minus<1>(w, z))) ^ ((sg << 30) & 0x80000000u));
+    v[2] = __uint_as_float(__float_as_uint(__fmul_rn(c, byte_minus<2>(w, z))) ^ ((sg << 29) & 0x80000000u));
+    v[3] = __uint_as_float(__float_as_uint(__fmul_rn(c, byte_minus<3>(w, z))) ^ ((sg << 28) & 0x80000000u));
+}
+
+__device__ __forceinline__ void lane8_signed(float c, uint2 row, uint32_t sg, float* v) {
+    signed4(c, row.x, sg, v);
+    signed4(c, row.y, sg >> 4, v + 4);
+}
+
+// IQ1 lane: y[j] = M(c, A(v[j], delta)) with v = stored/8 - 1 and
+// delta = +-1/8.  8*A(v, delta) = stored - (8 -+ 1) is an exact integer, and
+// M(c, x) = M(c/8, 8x) exactly (c/8 is exact: c is a binary16 scale times an
+// odd integer), so y = M(c8, stored - bias) with bias = 2^23 + 7 or 2^23 + 9.
+__device__ __forceinline__ void lane8_shifted(float c8, uint2 row, float bias, float* v) {
+    mul4(c8, row.x, bias, v);
+    mul4(c8, row.y, bias, v + 4);
+}
+
+// c = M(M(d, 0.5 + t), q) of IQ2_XXS / IQ2_XS / IQ2_S (q = 1/4) and IQ3_XXS
+// (q = 1/2).
+__device__ __forceinline__ float iq_half_scale(float d, uint32_t t, float q) {
+    return __fmul_rn(__fmul_rn(d, __fadd_rn(0.5f, static_cast<float>(t))), q);
+}
+
+// gguf:iq2_xxs: a = U(b[6+8g:10+8g]); v = G(iq2xxs_grid, b[2+8g+l]),
+// s = SP(field(a,7l,7)), c = M(M(d, 0.5 + a>>28), 0.25).
+template <>
+struct Fmt<KF_IQ2_XXS> {
+    static constexpr int B = 256, S = 66, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1, l0 = 2u * (cc & 1u);
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t idx = lds_2<PH>(in, off + 2u + 8u * g + l0);
+        const uint32_t a = lds_4(in, off + 6u + 8u * g);
+        const float cs = iq_half_scale(d, a >> 28, 0.25f);
+        const uint64_t* G = x.grids->iq2xxs;
+        lane8_signed(cs, ldg_row8(G + (idx & 255u)), sp_signs((a >> (7u * l0)) & 127u), v);
+        lane8_signed(cs, ldg_row8(G + (idx >> 8)), sp_signs((a >> (7u * l0 + 7u)) & 127u), v + 8);
+    }
+};
+
+// gguf:iq2_xs: a = U(b[2+2i:4+2i]), t = field(b[66+g], 4*floor(l/2), 4);
+// v = G(iq2xs_grid, a mod 512), s = SP(floor(a/512)), c = M(M(d, 0.5+t), 0.25).
+template <>
+struct Fmt<KF_IQ2_XS> {
+    static constexpr int B = 256, S = 74, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1;
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t qa = lds_4(in, off + 2u + 4u * cc);
+        const uint32_t t = (in[off + 66u + g] >> (4u * (cc & 1u))) & 15u;
+        const float cs = iq_half_scale(d, t, 0.25f);
+        const uint64_t* G = x.grids->iq2xs;
+        lane8_signed(cs, ldg_row8(G + (qa & 511u)), sp_signs((qa >> 9) & 127u), v);
+        lane8_signed(cs, ldg_row8(G + ((qa >> 16) & 511u)), sp_signs(qa >> 25), v + 8);
+    }
+};
+
+// gguf:iq2_s: r = b[2+i] + 256*field(b[66+g], 2l, 2), t = field(b[74+g],
+// 4*floor(l/2), 4); v = G(iq2s_grid, r), s = S(b[34+i]), c = M(M(d,0.5+t),0.25).
+template <>
+struct Fmt<KF_IQ2_S> {
+    static constexpr int B = 256, S = 82, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1, l0 = 2u * (cc & 1u);
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t qs = lds_2<PH>(in, off + 2u + 2u * cc);
+        const uint32_t qh = in[off + 66u + g] >> (2u * l0);
+        const uint32_t t = (in[off + 74u + g] >> (4u * (cc & 1u))) & 15u;
+        const uint32_t sg = lds_2<PH>(in, off + 34u + 2u * cc);
+        const float cs = iq_half_scale(d, t, 0.25f);
+        const uint64_t* G = x.grids->iq2s;
+        lane8_signed(cs, ldg_row8(G + ((qs & 255u) | ((qh & 3u) << 8))), sg & 255u, v);
+        lane8_signed(cs, ldg_row8(G + ((qs >> 8) | (((qh >> 2) & 3u) << 8))), sg >> 8, v + 8);
+    }
+};
+
+// gguf:iq3_xxs: a = U(b[66+4g:70+4g]); v = G(iq3xxs_grid, b[2+2i]) followed
+// by G(iq3xxs_grid, b[3+2i]), s = SP(field(a,7l,7)), c = M(M(d, 0.5 + a>>28), 0.5).
+template <>
+struct Fmt<KF_IQ3_XXS> {
+    static constexpr int B = 256, S = 98, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1, l0 = 2u * (cc & 1u);
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t q = lds_4(in, off + 2u + 4u * cc);
+        const uint32_t a = lds_4(in, off + 66u + 4u * g);
+        const float cs = iq_half_scale(d, a >> 28, 0.5f);
+        const uint32_t* G = x.grids->iq3xxs;
+        const uint2 r0 = make_uint2(__ldg(G + (q & 255u)), __ldg(G + ((q >> 8) & 255u)));
+        const uint2 r1 = make_uint2(__ldg(G + ((q >> 16) & 255u)), __ldg(G + (q >> 24)));
+        lane8_signed(cs, r0, sp_signs((a >> (7u * l0)) & 127u), v);
+        lane8_signed(cs, r1, sp_signs((a >> (7u * l0 + 7u)) & 127u), v + 8);
+    }
+};
+
+// gguf:iq3_s: r[t] = b[2+2i+t] + 256*bit(b[66+g], 2l+t); v = G(iq3s_grid,
+// r[0]) followed by G(iq3s_grid, r[1]), s = S(b[74+i]),
+// c = M(d, 1 + 2*field(b[106+floor(g/2)], 4*(g mod 2), 4)).
+template <>
+struct Fmt<KF_IQ3_S> {
+    static constexpr int B = 256, S = 110, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1, l0 = 2u * (cc & 1u);
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t q = lds_4(in, off + 2u + 4u * cc);
+        const uint32_t qh = in[off + 66u + g] >> (2u * l0);  // bits t, lane order: r0, r1, r0', r1'
+        const uint32_t sg = lds_2<PH>(in, off + 74u + 2u * cc);
+        const uint32_t sc = (in[off + 106u + (g >> 1)] >> (4u * (g & 1u))) & 15u;
+        const float cs = __fmul_rn(d, static_cast<float>(1u + 2u * sc));
+        const uint32_t* G = x.grids->iq3s;
+        const uint2 r0 = make_uint2(__ldg(G + ((q & 255u) | ((qh & 1u) << 8))),
+                                    __ldg(G + (((q >> 8) & 255u) | (((qh >> 1) & 1u) << 8))));
+        const uint2 r1 = make_uint2(__ldg(G + (((q >> 16) & 255u) | (((qh >> 2) & 1u) << 8))),
+                                    __ldg(G + ((q >> 24) | (((qh >> 3) & 1u) << 8))));
+        lane8_signed(cs, r0, sg & 255u, v);
+        lane8_signed(cs, r1, sg >> 8, v + 8);
+    }
+};
+
+// gguf:iq1_s: a = U(b[34+2g:36+2g]), r = b[2+i] + 256*field(a,3l,3),
+// c = M(d, 2*field(a,12,3)+1), delta = -1/8 if bit(a,15) else 1/8;
+// y = M(c, A(G(iq1s_grid, r)[j], delta)).
+template <>
+struct Fmt<KF_IQ1_S> {
+    static constexpr int B = 256, S = 50, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1, l0 = 2u * (cc & 1u);
+        const float d = h2f(lds_2<PH>(in, off));
+        const uint32_t qs = lds_2<PH>(in, off + 2u + 2u * cc);
+        const uint32_t a = lds_2<PH>(in, off + 34u + 2u * g);
+        const float c8 = __fmul_rn(__fmul_rn(d, static_cast<float>(2u * ((a >> 12) & 7u) + 1u)), 0.125f);
+        const float bias = (a >> 15) ? 8388617.0f : 8388615.0f;  // 2^23 + 9 / 2^23 + 7
+        const uint32_t hi = a >> (3u * l0);
+        const uint64_t* G = x.grids->iq1s;
+        lane8_shifted(c8, ldg_row8(G + ((qs & 255u) | ((hi & 7u) << 8))), bias, v);
+        lane8_shifted(c8, ldg_row8(G + ((qs >> 8) | (((hi >> 3) & 7u) << 8))), bias, v + 8);
+    }
+};
+
+// gguf:iq1_m: w[k] = U(b[48+2k:50+2k]); d is the binary16 whose nibble k is
+// floor(w[k]/2^12); a = field(b[32+floor(i/2)], 4*(i mod 2), 4),
+// r = b[i] + 256*(a mod 8), t = field(w[floor(g/2)], 6*(g mod 2)+3*floor(l/2), 3),
+// c = M(d, 2t+1), delta = -1/8 if bit(a,3) else 1/8.
+template <>
+struct Fmt<KF_IQ1_M> {
+    static constexpr int B = 256, S = 56, CE = 16, CPB = 16;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, g = cc >> 1;
+        const uint2 w = lds_8(in, off + 48u);  // w[0] | w[1] << 16, w[2] | w[3] << 16
+        const uint32_t hb = ((w.x >> 12) & 0x000Fu) | ((w.x >> 24) & 0x00F0u) | ((w.y >> 4) & 0x0F00u) |
+                            ((w.y >> 16) & 0xF000u);
+        const float d = h2f(hb);
+        const uint32_t ww = (g & 4u) ? w.y : w.x;  // holds w[floor(g/2)] in its half (g>>1)&1
+        const uint32_t t = (ww >> (16u * ((g >> 1) & 1u) + 6u * (g & 1u) + 3u * (cc & 1u))) & 7u;
+        const float c8 = __fmul_rn(__fmul_rn(d, static_cast<float>(2u * t + 1u)), 0.125f);
+        const uint32_t qs = lds_2<PH>(in, off + 2u * cc);
+        const uint32_t qh = in[off + 32u + cc];
+        const uint64_t* G = x.grids->iq1s;
+        lane8_shifted(c8, ldg_row8(G + ((qs & 255u) | ((qh & 7u) << 8))), (qh & 8u) ? 8388617.0f : 8388615.0f, v);
+        lane8_shifted(c8, ldg_row8(G + ((qs >> 8) | (((qh >> 4) & 7u) << 8))), (qh & 128u) ? 8388617.0f : 8388615.0f,
+                      v + 8);
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Output stage: one RNE conversion per element; 16-byte stores when y is
 // 16-byte aligned (chunk offsets are multiples of 8 elements, so every chunk
 // then starts on a 16-byte boundary).
@@ -954,6 +1153,13 @@ __device__ __noinline__ void decode_tile_slow(const StageInfo& si, const uint8_t
         case KF_TQ2_0: decode_tile_slow_f<KF_TQ2_0>(si, in, x, tid); break;
         case KF_Q1_0: decode_tile_slow_f<KF_Q1_0>(si, in, x, tid); break;
         case KF_Q2_0: decode_tile_slow_f<KF_Q2_0>(si, in, x, tid); break;
+        case KF_IQ2_XXS: decode_tile_slow_f<KF_IQ2_XXS>(si, in, x, tid); break;
+        case KF_IQ2_XS: decode_tile_slow_f<KF_IQ2_XS>(si, in, x, tid); break;
+        case KF_IQ2_S: decode_tile_slow_f<KF_IQ2_S>(si, in, x, tid); break;
+        case KF_IQ3_XXS: decode_tile_slow_f<KF_IQ3_XXS>(si, in, x, tid); break;
+        case KF_IQ3_S: decode_tile_slow_f<KF_IQ3_S>(si, in, x, tid); break;
+        case KF_IQ1_S: decode_tile_slow_f<KF_IQ1_S>(si, in, x, tid); break;
+        case KF_IQ1_M: decode_tile_slow_f<KF_IQ1_M>(si, in, x, tid); break;
         default: decode_tile_slow_f<KF_Q4_G64>(si, in, x, tid); break;
     }
 }
@@ -1014,6 +1220,13 @@ __device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint
         case KF_TQ2_0: decode_tile_fast_f<KF_TQ2_0, OSEL>(si, in, x, tid); break;
         case KF_Q1_0: decode_tile_fast_f<KF_Q1_0, OSEL>(si, in, x, tid); break;
         case KF_Q2_0: decode_tile_fast_f<KF_Q2_0, OSEL>(si, in, x, tid); break;
+        case KF_IQ2_XXS: decode_tile_fast_f<KF_IQ2_XXS, OSEL>(si, in, x, tid); break;
+        case KF_IQ2_XS: decode_tile_fast_f<KF_IQ2_XS, OSEL>(si, in, x, tid); break;
+        case KF_IQ2_S: decode_tile_fast_f<KF_IQ2_S, OSEL>(si, in, x, tid); break;
+        case KF_IQ3_XXS: decode_tile_fast_f<KF_IQ3_XXS, OSEL>(si, in, x, tid); break;
+        case KF_IQ3_S: decode_tile_fast_f<KF_IQ3_S, OSEL>(si, in, x, tid); break;
+        case KF_IQ1_S: decode_tile_fast_f<KF_IQ1_S, OSEL>(si, in, x, tid); break;
+        case KF_IQ1_M: decode_tile_fast_f<KF_IQ1_M, OSEL>(si, in, x, tid); break;
         default: decode_tile_fast_f<KF_Q4_G64, OSEL>(si, in, x, tid); break;
     }
 }
@@ -1155,17 +1368,18 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
         const uint8_t* in = inbuf + s * kInStride;
         const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
         if (si.phase != 0u || (nv && !si.nv_tab)) {
-            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div},
+            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids},
                              tid);
         } else {
-            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, nullptr, 0, 1}, tid);
+            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, nullptr, 0, 1, p.grids}, tid);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&H.empty[s]);
     }
 }
 
-// Kernel of format F for output type `osel`.
+// Kernel of format F for output type `osel` (launches that mix output types
+// use the generic kernel, so there is no per-format one for them).
 template <int F>
 KernelFn kernel_row(int osel) {
     switch (osel) {
@@ -1173,7 +1387,7 @@ KernelFn kernel_row(int osel) {
         case KO_F16: return k_decode<F, KO_F16>;
         case KO_BF16: return k_decode<F, KO_BF16>;
         case KO_F64: return k_decode<F, KO_F64>;
-        default: return k_decode<F, -1>;
+        default: return nullptr;
     }
 }
 

@@ -32,7 +32,14 @@ enum KFmt : int32_t {
     KF_TQ2_0 = 19,
     KF_Q1_0 = 20,
     KF_Q2_0 = 21,
-    KF_COUNT = 22,
+    KF_IQ2_XXS = 22,
+    KF_IQ2_XS = 23,
+    KF_IQ2_S = 24,
+    KF_IQ3_XXS = 25,
+    KF_IQ3_S = 26,
+    KF_IQ1_S = 27,
+    KF_IQ1_M = 28,
+    KF_COUNT = 29,
 };
 
 // Format selector of a launch whose tensors mix only gguf:q8_0, gguf:q4_k and
@@ -75,6 +82,19 @@ struct DevTensor {
 };
 static_assert(sizeof(DevTensor) == 64, "DevTensor layout");
 
+// Codebook rows of the IQ2 / IQ3 / IQ1 formats in the layout the kernels
+// read: row r of an 8-wide table in one 64-bit word, of a 4-wide table in one
+// 32-bit word, entry j in byte j.  iq1s_grid's entries v in {-1, 0, 1} are
+// stored as 8 * (v + 1).  One copy per device (see launch_decode).
+struct IqGrids {
+    uint64_t iq2xxs[256];  // 8, 25 or 43
+    uint64_t iq2xs[512];
+    uint64_t iq2s[1024];
+    uint32_t iq3xxs[256];  // 4, 12, ..., 52, 62
+    uint32_t iq3s[512];    // 1, 3, ..., 15
+    uint64_t iq1s[2048];   // 0, 8 or 16
+};
+
 // Kernel parameters.  A single-tensor launch carries its descriptor inline
 // (table == nullptr, n == 1); a batched launch points at a device table of n
 // descriptors sorted by tile_begin.
@@ -87,6 +107,7 @@ struct KParams {
     int32_t fsel;      // KFmt shared by every tensor of the launch, kFselKQuantMix, or -1
     int32_t osel;      // KOut shared by every tensor of the launch, or -1
     unsigned int* fault;  // device fault word (set by the launcher)
+    const IqGrids* grids;  // IQ codebooks (set by the launcher)
 };
 
 using KernelFn = void (*)(KParams);
@@ -114,6 +135,13 @@ KernelFn kernel_tq1_0(int osel);
 KernelFn kernel_tq2_0(int osel);
 KernelFn kernel_q1_0(int osel);
 KernelFn kernel_q2_0(int osel);
+KernelFn kernel_iq2_xxs(int osel);
+KernelFn kernel_iq2_xs(int osel);
+KernelFn kernel_iq2_s(int osel);
+KernelFn kernel_iq3_xxs(int osel);
+KernelFn kernel_iq3_s(int osel);
+KernelFn kernel_iq1_s(int osel);
+KernelFn kernel_iq1_m(int osel);
 KernelFn kernel_generic_f32();
 KernelFn kernel_generic_f16();
 KernelFn kernel_generic_bf16();

@@ -9,11 +9,15 @@
 #include <cstdint>
 
 #include "ndq_internal.h"
+#include "ndq_iq_codebooks.h"
 
 namespace ndq {
 
 // Set by a kernel whose bounded wait gave up (see ndq_get_device_fault).
 __device__ unsigned int g_fault_word;
+
+// The IQ codebooks, expanded at compile time.
+__device__ const IqGrids g_iq_grids = iqcb::make_iq_grids();
 
 namespace {
 
@@ -56,6 +60,13 @@ KernelFn pick_kernel(int fsel, int osel) {
         case KF_TQ2_0: return kernel_tq2_0(osel);
         case KF_Q1_0: return kernel_q1_0(osel);
         case KF_Q2_0: return kernel_q2_0(osel);
+        case KF_IQ2_XXS: return kernel_iq2_xxs(osel);
+        case KF_IQ2_XS: return kernel_iq2_xs(osel);
+        case KF_IQ2_S: return kernel_iq2_s(osel);
+        case KF_IQ3_XXS: return kernel_iq3_xxs(osel);
+        case KF_IQ3_S: return kernel_iq3_s(osel);
+        case KF_IQ1_S: return kernel_iq1_s(osel);
+        case KF_IQ1_M: return kernel_iq1_m(osel);
         default: return kernel_generic(osel);
     }
 }
@@ -74,8 +85,10 @@ DeviceInfo g_dev[kMaxDevices];
 
 size_t smem_bytes(bool tab) { return decode_smem_bytes(tab); }
 
-// Device address of the fault word, resolved once per device.
+// Device addresses of the fault word and the IQ codebooks, resolved once per
+// device.
 unsigned int* g_fault_addr[kMaxDevices];
+const IqGrids* g_grids_addr[kMaxDevices];
 
 }  // namespace
 
@@ -90,6 +103,7 @@ int launch_decode(const KParams& p, void* stream) {
     const int fsel = ((p.fsel >= 0 && p.fsel < KF_COUNT) || p.fsel == kFselKQuantMix) ? p.fsel : -1;
     const int osel = (p.osel >= 0 && p.osel <= KO_F64) ? p.osel : -1;
     const KernelFn fn = pick_kernel(fsel, osel);
+    if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     DeviceInfo& di = g_dev[dev];
     // Benign race: concurrent first calls compute and store the same values.
     if (di.sms == 0) {
@@ -114,8 +128,15 @@ int launch_decode(const KParams& p, void* stream) {
         if (e != cudaSuccess) return static_cast<int>(e);
         g_fault_addr[dev] = static_cast<unsigned int*>(addr);
     }
+    if (!g_grids_addr[dev]) {
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_iq_grids);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        g_grids_addr[dev] = static_cast<const IqGrids*>(addr);
+    }
     KParams q = p;
     q.fault = g_fault_addr[dev];
+    q.grids = g_grids_addr[dev];
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
     void* args[] = {&q};

@@ -72,7 +72,8 @@ def test_supported_set(orc):
     # every format the GPU decodes has an oracle decoder to be checked against
     sup = {ndq.ndq_format_name(i) for i in range(ndq.NDQ_NUM_FORMATS) if ndq.ndq_format_supported(i) == 1}
     decoded = {f for f in orc.formats() if orc.format_info(f)[2]}
-    assert sup <= decoded and len(sup) >= 10
+    # every registered format is decoded by both the library and the oracle
+    assert sup == decoded == set(orc.formats())
     assert ndq.ndq_format_supported(99) == -1
 
 
@@ -113,7 +114,6 @@ def test_validation_errors_return_before_any_launch():
     F = ndq.NDQ_FLOAT
     # invalid arguments never reach CUDA, so these run without a GPU
     assert ndq.ndq_dequantize_packed(99, (1, 32), F, 16, 18, 16) == 2
-    assert ndq.ndq_dequantize_packed(ndq.format_id("gguf:iq2_xxs"), (1, 256), F, 16, 66, 16) == 3
     assert ndq.ndq_dequantize_packed(q40, (), F, 16, 0, 16) == 4
     assert ndq.ndq_dequantize_packed(q40, (1,) * 9 + (32,), F, 16, 18, 16) == 4
     assert ndq.ndq_dequantize_packed(q40, (-2, 32), F, 16, 0, 16) == 5

@@ -165,6 +165,22 @@ def test_special_binary32_scales_q8_k(orc):
                          "q8_k")
 
 
+def test_special_binary16_scales_iq1_m(orc):
+    # gguf:iq1_m's binary16 scale is the top nibbles of the four 16-bit words
+    # at byte 48 (nibble k in word k)
+    specials = [0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x7C01, 0x3C00, 0xBC00]
+    nb = len(specials) * 3
+    x = synth.payload("gguf:iq1_m", (nb, 256), seed=7, dist="bytes").reshape(nb, 56).copy()
+    for r in range(nb):
+        h = specials[r % len(specials)]
+        for k in range(4):
+            x[r, 49 + 2 * k] = (x[r, 49 + 2 * k] & 0x0F) | (((h >> (4 * k)) & 15) << 4)
+    x = x.reshape(-1)
+    for out in OUTS:
+        assert_bit_exact(gpu_decode("gguf:iq1_m", (nb, 256), x, out), orc.decode("gguf:iq1_m", (nb, 256), x, out),
+                         out, "iq1_m")
+
+
 def test_batched_mixed(orc):
     specs = []
     rng = np.random.default_rng(0)
