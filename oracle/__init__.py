@@ -252,11 +252,12 @@ def grouped_absmax_group(x, qmin: int, qmax: int) -> tuple[int, np.ndarray]:
 
 
 def encode_grouped(name: str, x: np.ndarray) -> np.ndarray:
-    """Encode a [rows, K] float32 matrix into a q4_g64_fp16 / q8_g32_fp16 payload."""
+    """Encode a [rows, K] float32 matrix into a q4/q5/q6_g64_fp16 or
+    q8_g32_fp16 payload (grouped_absmax, NInfer section 7.2)."""
     a = np.ascontiguousarray(x, dtype=np.float32)
     rows, K = a.shape
-    G = 64 if name == "q4_g64_fp16" else 32
-    out = np.zeros(rows * (K // G) * 34, dtype=np.uint8)
+    G, S, _ = format_info(name)
+    out = np.zeros(rows * (K // G) * S, dtype=np.uint8)
     rc = lib().oracle_encode_grouped(name.encode(), _ptr(a), rows, K, _ptr(out))
     if rc:
         raise OracleError(rc, name)

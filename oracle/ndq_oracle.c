@@ -94,6 +94,17 @@ static const or_format OR_FORMATS[] = {
     {"nvfp4", 64, 36, 1},
     {"q4_g64_fp16", 64, 34, 1},
     {"q8_g32_fp16", 32, 34, 1},
+    /* READING: q2/q5/q6_g64_fp16 and t2_g128_fp16 follow q4_g64_fp16: one
+     * binary16 scale, then the group's codes as an LSB-first bit stream
+     * (S = 2 + G*b/8).  The row-scaled FP8 formats are a code plane of
+     * N*K E4M3FN bytes (row-major) followed by a plane of N little-endian
+     * 16-bit row multipliers; a "block" is one code (B = S = 1). */
+    {"q2_g64_fp16", 64, 18, 1},
+    {"q5_g64_fp16", 64, 42, 1},
+    {"q6_g64_fp16", 64, 50, 1},
+    {"t2_g128_fp16", 128, 34, 1},
+    {"fp8_e4m3fn_row_bf16", 1, 1, 1},
+    {"fp8_e4m3fn_row_fp16", 1, 1, 1},
 };
 #define OR_NFORMATS ((int)(sizeof(OR_FORMATS) / sizeof(OR_FORMATS[0])))
 
@@ -761,7 +772,62 @@ static int dec_iq1_m(const uint8_t *b, float *y) {
     return OR_OK;
 }
 
-/* One block of format `name` (dw: nvfp4 divisor) to binary32. */
+/* ------------------------------------------------------------------------ */
+/* The other NInfer grouped schemes and the row-scaled FP8 formats          */
+/* ([NINF] sections 4-6.2, 3.4 and the fp8_e4m3fn_row_* description).       */
+/* ------------------------------------------------------------------------ */
+
+/* Signed code of a `width`-bit logical word u ([NINF] section 5): u when
+ * u < 2^(width-1), else u - 2^width. */
+static int32_t or_twos(uint32_t u, int width) {
+    return (u < (1u << (width - 1))) ? (int32_t)u : (int32_t)u - (int32_t)(1u << width);
+}
+
+/* Logical word k of a packed code plane: bits [width*k, width*k + width) of
+ * the little-endian bit stream at `a` (READING: the page gives the words,
+ * not their bytes; this is the LSB-first packing of q4_g64_fp16 extended to
+ * every width, so fields of 5 and 6 bits may straddle bytes). */
+static uint32_t or_stream_word(const uint8_t *a, int k, int width) {
+    uint32_t v = 0;
+    for (int t = 0; t < width; ++t) {
+        int bitpos = width * k + t;
+        v |= (uint32_t)field(a[bitpos / 8], bitpos % 8, 1) << t;
+    }
+    return v;
+}
+
+/* q5_g64_fp16 / q6_g64_fp16 / t2_g128_fp16 (READING: a binary16 scale, then
+ * the group's codes as a packed plane): w_hat = binary32(s32 * binary32(q))
+ * ([NINF] section 6.2) with q the two's-complement code.  t2's word 0b10
+ * (-2) is outside the valid artifact language; decoding stays total and
+ * gives -2 * s. */
+static void dec_grouped_twos(const uint8_t *b, int G, int width, float *y) {
+    float s32 = H(b);
+    for (int k = 0; k < G; ++k) y[k] = M(s32, (float)or_twos(or_stream_word(b + 2, k, width), width));
+}
+
+/* q2_g64_fp16 ([NINF] section 5): the GSQ Q2_0 grid, q = u - 1 for the
+ * unsigned 2-bit word u; w_hat = binary32(s32 * binary32(q)). */
+static void dec_q2_g64(const uint8_t *b, float *y) {
+    float s32 = H(b);
+    for (int k = 0; k < 64; ++k) y[k] = M(s32, (float)((int32_t)or_stream_word(b + 2, k, 2) - 1));
+}
+
+/* fp8_e4m3fn_row_bf16 / _fp16: one E4M3FN code per element and one row
+ * multiplier s32 (already expanded from BF16 or binary16 by the caller):
+ * w_hat = binary32(c32 * s32).  A "block" here is one code. */
+static void dec_fp8_row(const uint8_t *b, float s32, float *y) { y[0] = M(oracle_e4m3fn(b[0]), s32); }
+
+/* BF16 -> binary32: the 16 bits are the high half of the binary32 pattern
+ * ([NINF] section 3.1), exact. */
+static float or_bf16_to_f32(uint32_t w) { return or_f32(w << 16); }
+
+static int or_is_fp8_row(const char *name) {
+    return strcmp(name, "fp8_e4m3fn_row_bf16") == 0 || strcmp(name, "fp8_e4m3fn_row_fp16") == 0;
+}
+
+/* One block of format `name` to binary32.  dw is the nvfp4 divisor, or the
+ * expanded row multiplier of an fp8_e4m3fn_row_* code. */
 static int or_decode_block(const char *name, const uint8_t *b, float dw, float *y) {
     if (strcmp(name, "gguf:q8_0") == 0 || strcmp(name, "q8_g32_fp16") == 0) dec_q8_0(b, y);
     else if (strcmp(name, "gguf:q4_0") == 0) dec_q4_0(b, y);
@@ -792,6 +858,11 @@ static int or_decode_block(const char *name, const uint8_t *b, float dw, float *
     else if (strcmp(name, "gguf:iq3_s") == 0) return dec_iq3_s(b, y);
     else if (strcmp(name, "gguf:iq1_s") == 0) return dec_iq1_s(b, y);
     else if (strcmp(name, "gguf:iq1_m") == 0) return dec_iq1_m(b, y);
+    else if (strcmp(name, "q2_g64_fp16") == 0) dec_q2_g64(b, y);
+    else if (strcmp(name, "q5_g64_fp16") == 0) dec_grouped_twos(b, 64, 5, y);
+    else if (strcmp(name, "q6_g64_fp16") == 0) dec_grouped_twos(b, 64, 6, y);
+    else if (strcmp(name, "t2_g128_fp16") == 0) dec_grouped_twos(b, 128, 2, y);
+    else if (or_is_fp8_row(name)) dec_fp8_row(b, dw, y);
     else return OR_ERR_UNSUPPORTED_FORMAT;
     return OR_OK;
 }
@@ -848,6 +919,10 @@ int oracle_geometry(const char *name, const int64_t *shape, int ndim, uint64_t x
         if (x_len < bytes || (x_len - bytes) % 4 != 0) return OR_ERR_LENGTH_MISMATCH;
         D = (x_len - bytes) / 4;
         if (D < 1 || N % D != 0) return OR_ERR_LENGTH_MISMATCH;
+    } else if (or_is_fp8_row(name) && nb > 0) {
+        /* READING: the N row multipliers follow the code plane */
+        if (x_len != bytes + 2u * N) return OR_ERR_LENGTH_MISMATCH;
+        D = N;
     } else if (x_len != bytes) {
         return OR_ERR_LENGTH_MISMATCH;
     }
@@ -891,6 +966,11 @@ int oracle_decode_range(const char *name, const int64_t *shape, int ndim, int ou
             uint64_t row = bi / bpr;
             uint64_t di = row / (N / D);
             dw = or_f32(U(x + nb * 36u + 4u * di, 4));
+        } else if (or_is_fp8_row(name)) {
+            /* code bi belongs to row floor(bi / K); its multiplier is word
+             * `row` of the plane after the codes */
+            uint32_t w = U(x + nb + 2u * (bi / bpr), 2);
+            dw = strcmp(name, "fp8_e4m3fn_row_bf16") == 0 ? or_bf16_to_f32(w) : oracle_h2f((uint16_t)w);
         }
         rc = or_decode_block(name, b, dw, blk);
         if (rc != OR_OK) return rc;
@@ -980,28 +1060,35 @@ int oracle_grouped_absmax_group(const float *x, int G, int qmin, int qmax,
  * payload under this oracle's byte-layout READING.  K must be a multiple of
  * the group size. */
 int oracle_encode_grouped(const char *name, const float *x, uint64_t rows, uint64_t K, uint8_t *out) {
-    int is4 = name && strcmp(name, "q4_g64_fp16") == 0;
-    int is8 = name && strcmp(name, "q8_g32_fp16") == 0;
-    if (!is4 && !is8) return OR_ERR_UNSUPPORTED_FORMAT;
-    uint64_t G = is4 ? 64u : 32u;
+    /* qmax of the reference encoder per scheme ([NINF] section 5 table;
+     * q8's interval is [-127, 127]) and the code width */
+    int width, qmin, qmax;
+    uint64_t G = 64u;
+    if (!name) return OR_ERR_NULL;
+    if (strcmp(name, "q4_g64_fp16") == 0) { width = 4; qmin = -8; qmax = 7; }
+    else if (strcmp(name, "q5_g64_fp16") == 0) { width = 5; qmin = -16; qmax = 15; }
+    else if (strcmp(name, "q6_g64_fp16") == 0) { width = 6; qmin = -32; qmax = 31; }
+    else if (strcmp(name, "q8_g32_fp16") == 0) { width = 8; qmin = -127; qmax = 127; G = 32u; }
+    else return OR_ERR_UNSUPPORTED_FORMAT;
     if (K % G != 0) return OR_ERR_NOT_BLOCK_ALIGNED;
+    uint64_t S = 2u + G * (uint64_t)width / 8u;
     int32_t codes[64];
     uint64_t nb = rows * (K / G);
     for (uint64_t bi = 0; bi < nb; ++bi) {
         uint16_t s16;
-        int rc = oracle_grouped_absmax_group(x + bi * G, (int)G, is4 ? -8 : -127, is4 ? 7 : 127,
-                                             &s16, codes);
+        int rc = oracle_grouped_absmax_group(x + bi * G, (int)G, qmin, qmax, &s16, codes);
         if (rc != OR_OK) return rc;
-        uint8_t *b = out + bi * 34u;
+        uint8_t *b = out + bi * S;
+        memset(b, 0, (size_t)S);
         b[0] = (uint8_t)(s16 & 0xffu);
         b[1] = (uint8_t)(s16 >> 8);
-        if (is4) {
-            for (int k = 0; k < 32; ++k) {
-                uint32_t lo = (uint32_t)codes[2 * k] & 15u, hi = (uint32_t)codes[2 * k + 1] & 15u;
-                b[2 + k] = (uint8_t)(lo | (hi << 4));
+        /* codes as width-bit two's-complement words, LSB-first bit stream */
+        for (int k = 0; k < (int)G; ++k) {
+            uint32_t u = (uint32_t)codes[k] & ((1u << width) - 1u);
+            for (int t = 0; t < width; ++t) {
+                int bitpos = width * k + t;
+                b[2 + bitpos / 8] |= (uint8_t)(((u >> t) & 1u) << (bitpos % 8));
             }
-        } else {
-            for (int k = 0; k < 32; ++k) b[2 + k] = (uint8_t)(codes[k] & 0xff);
         }
     }
     return OR_OK;

@@ -20,10 +20,14 @@ Field distributions follow the benchmark workloads:
   * gguf:nvfp4 -- scale bytes uniform over 0x00..0x7e, codes uniform;
   * the other gguf formats (q4_1, q5_0, q5_1, q8_1, q8_k, q2_k, q3_k, q5_k,
     iq4_xs, tq1_0, tq2_0, q1_0, q2_0, iq2_xxs, iq2_xs, iq2_s, iq3_xxs, iq3_s,
-    iq1_s, iq1_m) -- binary16 scales |N(0,0.02)|+1e-4 (iq1_m: its scale's
+    iq1_s, iq1_m, and NInfer's q2/q5/q6_g64_fp16, t2_g128_fp16) -- binary16
+    scales |N(0,0.02)|+1e-4 (t2: only the valid words 0, 1, 3; iq1_m: its scale's
     four nibbles in the top bits of the four 16-bit words at byte 48),
     minima |N(0,0.01)|, q8_k's binary32 scale likewise, codes in [-127, 127]
     for q8_k, every other byte uniform;
+  * fp8_e4m3fn_row_bf16 / _fp16 -- codes uniform over the 254 non-NaN
+    E4M3FN words, then one positive row multiplier |N(0,0.02)|+1e-4 per
+    row (BF16 or binary16);
   * "bytes" -- every byte uniform over 0..255 (exercises special scales:
     binary16 infinities/NaNs, E4M3FN NaN words, E8M0 extremes).
 
@@ -48,7 +52,12 @@ GEOMETRY = {
     "gguf:q2_0": (64, 18),
     "gguf:iq2_xxs": (256, 66), "gguf:iq2_xs": (256, 74), "gguf:iq2_s": (256, 82), "gguf:iq3_xxs": (256, 98),
     "gguf:iq3_s": (256, 110), "gguf:iq1_s": (256, 50), "gguf:iq1_m": (256, 56),
+    "q2_g64_fp16": (64, 18), "q5_g64_fp16": (64, 42), "q6_g64_fp16": (64, 50), "t2_g128_fp16": (128, 34),
+    "fp8_e4m3fn_row_bf16": (1, 1), "fp8_e4m3fn_row_fp16": (1, 1),
 }
+# Formats whose payload ends with one 16-bit multiplier per row (after the
+# row-major code plane).
+ROW_SCALED = ("fp8_e4m3fn_row_bf16", "fp8_e4m3fn_row_fp16")
 
 # Byte offsets of the binary16 scale fields of the other gguf formats; their
 # workload recipe draws these from |N(0,0.02)|+1e-4 (minima |N(0,0.01)|) and
@@ -107,10 +116,13 @@ def payload(fmt: str, shape, seed: int, dist: str = "workload", ndiv: int = 1) -
     nb = _nblocks(fmt, shape)
     B, S = GEOMETRY[fmt]
     blk = _u8(rng, (nb, S))
+    rows = int(np.prod(shape[:-1], dtype=np.int64))
     if dist == "bytes":
         out = blk.reshape(-1)
         if fmt == "nvfp4" and nb:
             out = np.concatenate([out, nvfp4_divisors(ndiv, seed).astype("<f4").view(np.uint8)])
+        if fmt in ROW_SCALED and nb:
+            out = np.concatenate([out, _u8(rng, 2 * rows)])
         return out
     if dist != "workload":
         raise ValueError(dist)
@@ -141,6 +153,22 @@ def payload(fmt: str, shape, seed: int, dist: str = "workload", ndiv: int = 1) -
         h = (np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4).astype(np.float16).view(np.uint16).astype(np.uint32)
         for k in range(4):
             blk[:, 49 + 2 * k] = (blk[:, 49 + 2 * k] & 0x0F) | (((h >> (4 * k)) & 15) << 4).astype(np.uint8)
+    elif fmt in ("q2_g64_fp16", "q5_g64_fp16", "q6_g64_fp16", "t2_g128_fp16"):
+        blk[:, 0:2] = _f16_bytes(np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4)
+        if fmt == "t2_g128_fp16":  # valid ternary words only: 0, 1, 3 (0b10 is outside the format)
+            w = rng.choice(np.array([0, 1, 3], np.uint8), size=(nb, 32, 4))
+            blk[:, 2:34] = w[..., 0] | (w[..., 1] << 2) | (w[..., 2] << 4) | (w[..., 3] << 6)
+    elif fmt in ROW_SCALED:
+        # every valid E4M3FN word (0x7f and 0xff are NaN words), positive
+        # row multipliers |N(0,0.02)| + 1e-4 as BF16 or binary16
+        codes = rng.integers(0, 254, size=nb, dtype=np.uint8)
+        blk[:, 0] = np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)
+        sc = (np.abs(rng.normal(0.0, 0.02, size=rows)) + 1e-4).astype(np.float32)
+        if fmt == "fp8_e4m3fn_row_fp16":
+            words = sc.astype(np.float16).view(np.uint16)
+        else:  # the high half of the binary32 pattern
+            words = (sc.view(np.uint32) >> 16).astype(np.uint16)
+        return np.concatenate([blk.reshape(-1), words.astype("<u2").view(np.uint8)]) if nb else blk.reshape(-1)
     elif fmt == "gguf:q8_k":
         d = (np.abs(rng.normal(0.0, 0.02, size=nb)) + 1e-4).astype("<f4")
         blk[:, 0:4] = d.view(np.uint8).reshape(nb, 4)

@@ -65,7 +65,8 @@ def test_decoded_set(orc):
                        "gguf:q4_1", "gguf:q5_0", "gguf:q5_1", "gguf:q8_1", "gguf:q8_k", "gguf:q2_k",
                        "gguf:q3_k", "gguf:q5_k", "gguf:iq4_xs", "gguf:tq1_0", "gguf:tq2_0", "gguf:q1_0",
                        "gguf:q2_0", "gguf:iq2_xxs", "gguf:iq2_xs", "gguf:iq2_s", "gguf:iq3_xxs", "gguf:iq3_s",
-                       "gguf:iq1_s", "gguf:iq1_m"}
+                       "gguf:iq1_s", "gguf:iq1_m", "q2_g64_fp16", "q5_g64_fp16", "q6_g64_fp16", "t2_g128_fp16",
+                       "fp8_e4m3fn_row_bf16", "fp8_e4m3fn_row_fp16"}
     assert decoded == set(orc.formats())
 
 
