@@ -59,7 +59,7 @@ extern "C" {
 
 /* Format identifiers: a closed enumeration.  0..26 are the 27 fixed GGUF
  * profiles of "Quantization formats", in the specification's table order;
- * 27..29 are formats of the NInfer "tensor-formats" registry. */
+ * 27..35 are formats of the NInfer "tensor-formats" registry. */
 #define NDQ_GGUF_Q4_0 0
 #define NDQ_GGUF_Q4_1 1
 #define NDQ_GGUF_Q5_0 2
@@ -103,7 +103,28 @@ extern "C" {
 /* q8_g32_fp16 (NInfer sections 4-6.2): 32-value blocks of 34 bytes: a
  * binary16 scale then 32 signed bytes (byte-identical to gguf:q8_0). */
 #define NDQ_Q8_G32_FP16 29
-#define NDQ_NUM_FORMATS 30
+/* The other grouped signed-integer schemes of NInfer sections 4-6.2.  Each
+ * block is one group: a binary16 scale, then the group's G codes of b bits as
+ * an LSB-first bit stream (code k in bits [b*k, b*k + b) of the bytes after
+ * the scale; a layout reading extending q4_g64_fp16's), so S = 2 + G*b/8.
+ * w = binary32(scale * code).
+ *   q2_g64_fp16: b = 2, G = 64, code = u - 1 (the Q2_0 grid; byte-identical
+ *                to gguf:q2_0);
+ *   q5_g64_fp16, q6_g64_fp16: b = 5 / 6, G = 64, two's complement;
+ *   t2_g128_fp16: b = 2, G = 128, two's complement (the word 0b10 = -2 is
+ *                outside the format and decodes as -2). */
+#define NDQ_Q2_G64_FP16 30
+#define NDQ_Q5_G64_FP16 31
+#define NDQ_Q6_G64_FP16 32
+#define NDQ_T2_G128_FP16 33
+/* Row-scaled FP8 (NInfer fp8_e4m3fn_row_bf16 / fp8_e4m3fn_row_fp16): one
+ * E4M3FN code per element and one multiplier per row, w = binary32(c * s).
+ * Layout (a reading): the N*K code bytes of the N = prod(shape[:-1]) rows
+ * (row-major), then N little-endian 16-bit multipliers (BF16 or binary16).
+ * B = S = 1 (a "block" is one code); x_len = N*K + 2*N, 0 when empty. */
+#define NDQ_FP8_E4M3FN_ROW_BF16 34
+#define NDQ_FP8_E4M3FN_ROW_FP16 35
+#define NDQ_NUM_FORMATS 36
 
 #define NDQ_MAX_RANK 8
 
@@ -132,10 +153,11 @@ const char *ndq_status_string(int status);
 /* Host-only validation of one payload under the length rule of "Signature
  * and storage": rank >= 1, nonnegative dims, shape[-1] % B == 0 and
  * x_len == prod(shape[:-1]) * (shape[-1] / B) * S (for nvfp4 plus 4*D bytes of
- * divisors, D >= 1 dividing the row count, none when the tensor is empty).
+ * divisors, D >= 1 dividing the row count; for the fp8 row formats plus 2
+ * bytes per row; no trailing words when the tensor is empty).
  * On success writes the block count, the element count and the number of
- * nvfp4 divisors (0 otherwise); any output pointer may be NULL.  Does not
- * touch the GPU. */
+ * trailing per-row words (nvfp4 divisors, fp8 row multipliers; 0 otherwise);
+ * any output pointer may be NULL.  Does not touch the GPU. */
 int ndq_payload_geometry(int format_id, const int64_t *shape, int ndim, uint64_t x_len,
                          uint64_t *nblocks, uint64_t *nelements, uint64_t *ndivisors);
 

@@ -33,7 +33,7 @@ STATUS = {
 }
 NDQ_FLOAT, NDQ_FLOAT16, NDQ_DOUBLE, NDQ_BFLOAT16 = 1, 10, 11, 16
 NDQ_MAX_RANK = 8
-NDQ_NUM_FORMATS = 30
+NDQ_NUM_FORMATS = 36
 NDQ_NOALLOC_MAX_TENSORS = 1024
 
 

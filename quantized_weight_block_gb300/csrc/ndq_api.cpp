@@ -61,9 +61,17 @@ const FormatRow kFormats[NDQ_NUM_FORMATS] = {
     {"nvfp4", 64, 36, ndq::KF_NVFP4},
     {"q4_g64_fp16", 64, 34, ndq::KF_Q4_G64},
     {"q8_g32_fp16", 32, 34, ndq::KF_Q8_0},
+    {"q2_g64_fp16", 64, 18, ndq::KF_Q2_0},
+    {"q5_g64_fp16", 64, 42, ndq::KF_Q5_G64},
+    {"q6_g64_fp16", 64, 50, ndq::KF_Q6_G64},
+    {"t2_g128_fp16", 128, 34, ndq::KF_T2_G128},
+    {"fp8_e4m3fn_row_bf16", 1, 1, ndq::KF_FP8_ROW_BF16},
+    {"fp8_e4m3fn_row_fp16", 1, 1, ndq::KF_FP8_ROW_FP16},
 };
 
 bool valid_id(int id) { return id >= 0 && id < NDQ_NUM_FORMATS; }
+
+bool fp8_row(int id) { return id == NDQ_FP8_E4M3FN_ROW_BF16 || id == NDQ_FP8_E4M3FN_ROW_FP16; }
 
 int out_code(int out_dtype, int* size) {
     switch (out_dtype) {
@@ -105,6 +113,10 @@ int geometry(int id, const int64_t* shape, int ndim, uint64_t x_len, Geometry* g
         if (x_len < bytes || (x_len - bytes) % 4 != 0) return NDQ_ERR_LENGTH_MISMATCH;
         D = (x_len - bytes) / 4;
         if (D < 1 || N % D != 0) return NDQ_ERR_LENGTH_MISMATCH;
+    } else if (fp8_row(id) && nb > 0) {
+        // the code plane, then one 16-bit multiplier per row
+        if (x_len != bytes + 2u * N) return NDQ_ERR_LENGTH_MISMATCH;
+        D = N;
     } else if (x_len != bytes) {
         return NDQ_ERR_LENGTH_MISMATCH;
     }
@@ -141,6 +153,16 @@ int prepare(int id, const int64_t* shape, int ndim, int out_dtype, const uint8_t
         const uint64_t bpr = static_cast<uint64_t>(shape[ndim - 1]) / 64u;
         t->divs = x + g->nblocks * 36u;
         t->blocks_per_div = bpr * (g->rows / g->ndiv);
+    }
+    if (fp8_row(id)) {
+        // The kernel reads the code plane in 16-code units (the last one may
+        // be partial); the row multipliers follow the codes.
+        t->nblocks = (g->nelements + 15u) / 16u;
+        t->S = 16;
+        t->B = 16;
+        t->bpt = static_cast<uint16_t>(ndq::kTileElems / 16);
+        t->divs = x + g->nelements;
+        t->blocks_per_div = static_cast<uint64_t>(shape[ndim - 1]);
     }
     return NDQ_OK;
 }

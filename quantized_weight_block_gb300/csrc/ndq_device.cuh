@@ -252,7 +252,18 @@ struct Ctx {
     uint64_t block0;
     uint64_t blocks_per_div;
     const IqGrids* grids;  // IQ codebooks
+    uint64_t n_el;         // fp8 rows: codes in the tensor (the last 16-code unit may be partial)
 };
+
+__host__ __device__ constexpr bool is_fp8_row(int f) { return f == KF_FP8_ROW_BF16 || f == KF_FP8_ROW_FP16; }
+
+// Codes of an fp8 row tensor: its row multipliers start right after the code
+// plane.  0 for every other format.
+__device__ __forceinline__ uint64_t code_count(const DevTensor& t) {
+    return is_fp8_row(t.fmt) ? static_cast<uint64_t>(reinterpret_cast<uintptr_t>(t.divs) -
+                                                      reinterpret_cast<uintptr_t>(t.x))
+                             : 0u;
+}
 
 // 16 bytes at byte offset `off` of a 16-byte-aligned stage (ALIGNED: off is a
 // multiple of 16, one 16-byte load).
@@ -1040,6 +1051,137 @@ struct Fmt<KF_IQ1_M> {
 };
 
 // ---------------------------------------------------------------------------
+// NInfer grouped schemes q5_g64_fp16, q6_g64_fp16, t2_g128_fp16 (q2_g64_fp16
+// is byte-identical to gguf:q2_0) and the row-scaled FP8 formats
+// ("tensor-formats" sections 4-6.2 and fp8_e4m3fn_row_*).  Grouped blocks:
+// a binary16 scale, then the codes as an LSB-first bit stream;
+// w = binary32(s32 * binary32(q)).
+// ---------------------------------------------------------------------------
+
+// 16 codes of W bits from the bit stream held in q (bits [0, 16W)), as
+// two's-complement values: v[i] = M(d, q_i).  The word u becomes the float
+// 2^23 + (u XOR 2^(W-1)) by one bitwise operation; subtracting 2^23 + 2^(W-1)
+// leaves the signed code exactly.
+template <int W>
+__device__ __forceinline__ void twos16(float d, uint4 q, float* v) {
+    const uint32_t w[5] = {q.x, q.y, q.z, q.w, 0u};
+    constexpr uint32_t mask = (1u << W) - 1u, flip = 0x4B000000u | (1u << (W - 1));
+    constexpr float bias = 8388608.0f + static_cast<float>(1u << (W - 1));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int bit = W * i;
+        const uint32_t u = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) & mask;
+        v[i] = __fmul_rn(d, __fsub_rn(__uint_as_float(u ^ flip), bias));
+    }
+}
+
+// q5_g64_fp16 / q6_g64_fp16: B = 64, 4 chunks per block; chunk c&3 holds
+// bits [16W*(c&3), 16W*(c&3+1)) of the stream, i.e. 2W bytes at 2 + 2W*(c&3).
+template <int W, int S_>
+struct GroupedTwos {
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v) {
+        const uint32_t off = ph + (c >> 2) * S_;
+        const float d = h2f(lds_2<PH>(in, off));
+        twos16<W>(d, lds_16<false>(in, off + 2u + 2u * W * (c & 3u)), v);
+    }
+};
+template <>
+struct Fmt<KF_Q5_G64> {
+    static constexpr int B = 64, S = 42, CE = 16, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        GroupedTwos<5, 42>::chunk<PH>(in, ph, c, v);
+    }
+};
+template <>
+struct Fmt<KF_Q6_G64> {
+    static constexpr int B = 64, S = 50, CE = 16, CPB = 4;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        GroupedTwos<6, 50>::chunk<PH>(in, ph, c, v);
+    }
+};
+
+// t2_g128_fp16: B = 128, 8 chunks per block of 4 code bytes each.
+template <>
+struct Fmt<KF_T2_G128> {
+    static constexpr int B = 128, S = 34, CE = 16, CPB = 8;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
+        const uint32_t off = ph + (c >> 3) * S;
+        const float d = h2f(lds_2<PH>(in, off));
+        twos16<2>(d, make_uint4(lds_4(in, off + 2u + 4u * (c & 7u)), 0u, 0u, 0u), v);
+    }
+};
+
+// E4M3FN word to binary32 (bias 7; 0x7f / 0xff NaN; sign on every word):
+// the exponent and fraction bits placed at binary32's fraction top give
+// 2^(e-127)(1+m/8) (or m*2^-129 for e = 0), and the exact factor 2^120
+// rebiases them to 2^(e-7)(1+m/8) (or m*2^-9).
+__device__ __forceinline__ float e4m3fn_word(uint32_t b) {
+    const float m = __fmul_rn(__uint_as_float(((b & 0x7Fu) << 20) | ((b & 0x80u) << 24)), 0x1p120f);
+    return ((b & 0x7Fu) == 0x7Fu) ? __uint_as_float(0x7FC00000u) : m;
+}
+
+// Row multiplier `row` of an fp8 row tensor (16-bit little-endian words,
+// any alignment): BF16 (the high half of a binary32) or binary16.
+template <bool BF>
+__device__ __forceinline__ float row_multiplier(const uint8_t* plane, uint64_t row) {
+    const uint8_t* p = plane + 2u * row;
+    const uint32_t w = static_cast<uint32_t>(__ldg(p)) | (static_cast<uint32_t>(__ldg(p + 1)) << 8);
+    return BF ? __uint_as_float(w << 16) : h2f(w);
+}
+
+// fp8_e4m3fn_row_*: the kernel sees 16-code units (B = S = 16); y = M(c32, s32)
+// with s32 the multiplier of the code's row (element e is in row e / K).
+template <bool BF>
+struct Fp8Row {
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v,
+                                                 const Ctx& x) {
+        const uint4 q = lds_16<!PH>(in, ph + 16u * c);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        const uint64_t K = x.blocks_per_div;
+        const uint64_t e0 = (x.block0 + c) * 16u;
+        uint64_t row = e0 / K, col = e0 - row * K;
+        float s = row_multiplier<BF>(x.divs, row);
+        if (col + 16u <= K) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(e4m3fn_word((w[i >> 2] >> (8 * (i & 3))) & 255u), s);
+        } else {
+            // the unit crosses a row boundary (K not a multiple of 16)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (col == K) {
+                    ++row;
+                    col = 0;
+                    if (e0 + i < x.n_el) s = row_multiplier<BF>(x.divs, row);
+                }
+                v[i] = __fmul_rn(e4m3fn_word((w[i >> 2] >> (8 * (i & 3))) & 255u), s);
+                ++col;
+            }
+        }
+    }
+};
+template <>
+struct Fmt<KF_FP8_ROW_BF16> {
+    static constexpr int B = 16, S = 16, CE = 16, CPB = 1;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx& x) {
+        Fp8Row<true>::chunk<PH>(in, ph, c, v, x);
+    }
+};
+template <>
+struct Fmt<KF_FP8_ROW_FP16> {
+    static constexpr int B = 16, S = 16, CE = 16, CPB = 1;
+    template <bool PH>
+    __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx& x) {
+        Fp8Row<false>::chunk<PH>(in, ph, c, v, x);
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Output stage: one RNE conversion per element; 16-byte stores when y is
 // 16-byte aligned (chunk offsets are multiples of 8 elements, so every chunk
 // then starts on a 16-byte boundary).
@@ -1096,6 +1238,18 @@ __device__ __forceinline__ void store_chunk(void* y, uint64_t e0, const float* v
     }
 }
 
+// The last 16 codes of an fp8 row tensor may be fewer than 16: one scalar
+// store per valid element.
+template <int O>
+__device__ __forceinline__ void store_partial(void* y, uint64_t e0, const float* v, uint32_t n) {
+    for (uint32_t i = 0; i < n; ++i) {
+        if (O == KO_F32) static_cast<float*>(y)[e0 + i] = v[i];
+        else if (O == KO_F64) static_cast<double*>(y)[e0 + i] = static_cast<double>(v[i]);
+        else if (O == KO_BF16) static_cast<__nv_bfloat16*>(y)[e0 + i] = __float2bfloat16_rn(v[i]);
+        else static_cast<__half*>(y)[e0 + i] = __float2half_rn(v[i]);
+    }
+}
+
 template <int F, int O, bool PH>
 __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
     using Fm = Fmt<F>;
@@ -1111,7 +1265,11 @@ __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8
         if (c < nch) {
             float v[Fm::CE];
             Fm::template chunk<PH>(in, ph, c, v, x);
-            store_chunk<O, Fm::CE>(y, e_base + static_cast<uint64_t>(Fm::CE) * c, v, vec);
+            const uint64_t e0 = e_base + static_cast<uint64_t>(Fm::CE) * c;
+            if (is_fp8_row(F) && e0 + Fm::CE > x.n_el)
+                store_partial<O>(y, e0, v, static_cast<uint32_t>(x.n_el - e0));
+            else
+                store_chunk<O, Fm::CE>(y, e0, v, vec);
         }
     }
 }
@@ -1160,6 +1318,11 @@ __device__ __noinline__ void decode_tile_slow(const StageInfo& si, const uint8_t
         case KF_IQ3_S: decode_tile_slow_f<KF_IQ3_S>(si, in, x, tid); break;
         case KF_IQ1_S: decode_tile_slow_f<KF_IQ1_S>(si, in, x, tid); break;
         case KF_IQ1_M: decode_tile_slow_f<KF_IQ1_M>(si, in, x, tid); break;
+        case KF_Q5_G64: decode_tile_slow_f<KF_Q5_G64>(si, in, x, tid); break;
+        case KF_Q6_G64: decode_tile_slow_f<KF_Q6_G64>(si, in, x, tid); break;
+        case KF_T2_G128: decode_tile_slow_f<KF_T2_G128>(si, in, x, tid); break;
+        case KF_FP8_ROW_BF16: decode_tile_slow_f<KF_FP8_ROW_BF16>(si, in, x, tid); break;
+        case KF_FP8_ROW_FP16: decode_tile_slow_f<KF_FP8_ROW_FP16>(si, in, x, tid); break;
         default: decode_tile_slow_f<KF_Q4_G64>(si, in, x, tid); break;
     }
 }
@@ -1227,6 +1390,11 @@ __device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint
         case KF_IQ3_S: decode_tile_fast_f<KF_IQ3_S, OSEL>(si, in, x, tid); break;
         case KF_IQ1_S: decode_tile_fast_f<KF_IQ1_S, OSEL>(si, in, x, tid); break;
         case KF_IQ1_M: decode_tile_fast_f<KF_IQ1_M, OSEL>(si, in, x, tid); break;
+        case KF_Q5_G64: decode_tile_fast_f<KF_Q5_G64, OSEL>(si, in, x, tid); break;
+        case KF_Q6_G64: decode_tile_fast_f<KF_Q6_G64, OSEL>(si, in, x, tid); break;
+        case KF_T2_G128: decode_tile_fast_f<KF_T2_G128, OSEL>(si, in, x, tid); break;
+        case KF_FP8_ROW_BF16: decode_tile_fast_f<KF_FP8_ROW_BF16, OSEL>(si, in, x, tid); break;
+        case KF_FP8_ROW_FP16: decode_tile_fast_f<KF_FP8_ROW_FP16, OSEL>(si, in, x, tid); break;
         default: decode_tile_fast_f<KF_Q4_G64, OSEL>(si, in, x, tid); break;
     }
 }
@@ -1256,7 +1424,13 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
         const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
         const uint8_t* src = t.x + b0 * t.S;
         const uint32_t phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-        const uint32_t bytes = (phase + nb * t.S + 15u) & ~15u;
+        uint32_t span = nb * t.S;
+        if (t.fmt == KF_FP8_ROW_BF16 || t.fmt == KF_FP8_ROW_FP16) {
+            // stop at the end of the code plane (the row multipliers follow it)
+            const uint64_t plane = reinterpret_cast<uintptr_t>(t.divs) - reinterpret_cast<uintptr_t>(src);
+            if (plane < span) span = static_cast<uint32_t>(plane);
+        }
+        const uint32_t bytes = (phase + span + 15u) & ~15u;
         si.block0 = b0;
         si.nb = nb;
         si.phase = phase;
@@ -1368,10 +1542,10 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
         const uint8_t* in = inbuf + s * kInStride;
         const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
         if (si.phase != 0u || (nv && !si.nv_tab)) {
-            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids},
+            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t)},
                              tid);
         } else {
-            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, nullptr, 0, 1, p.grids}, tid);
+            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t)}, tid);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&H.empty[s]);

@@ -1,0 +1,6 @@
+// Decode kernels specialised for fp8_e4m3fn_row_bf16 (one per output type).
+#include "ndq_device.cuh"
+
+namespace ndq {
+KernelFn kernel_fp8_row_bf16(int osel) { return kernel_row<KF_FP8_ROW_BF16>(osel); }
+}  // namespace ndq

@@ -39,7 +39,12 @@ enum KFmt : int32_t {
     KF_IQ3_S = 26,
     KF_IQ1_S = 27,
     KF_IQ1_M = 28,
-    KF_COUNT = 29,
+    KF_Q5_G64 = 29,
+    KF_Q6_G64 = 30,
+    KF_T2_G128 = 31,
+    KF_FP8_ROW_BF16 = 32,
+    KF_FP8_ROW_FP16 = 33,
+    KF_COUNT = 34,
 };
 
 // Format selector of a launch whose tensors mix only gguf:q8_0, gguf:q4_k and
@@ -71,8 +76,8 @@ struct DevTensor {
     void* y;                  // output
     uint64_t nblocks;         // blocks in the payload
     uint64_t tile_begin;      // first global tile index of this tensor
-    const uint8_t* divs;      // nvfp4: FP32 divisor words (may be unaligned)
-    uint64_t blocks_per_div;  // nvfp4: blocks sharing one divisor
+    const uint8_t* divs;      // nvfp4: FP32 divisor words; fp8 rows: the row multipliers (may be unaligned)
+    uint64_t blocks_per_div;  // nvfp4: blocks sharing one divisor; fp8 rows: elements per row
     int32_t fmt;              // KFmt
     int32_t out;              // KOut
     uint16_t S;               // bytes per block
@@ -142,6 +147,11 @@ KernelFn kernel_iq3_xxs(int osel);
 KernelFn kernel_iq3_s(int osel);
 KernelFn kernel_iq1_s(int osel);
 KernelFn kernel_iq1_m(int osel);
+KernelFn kernel_q5_g64(int osel);
+KernelFn kernel_q6_g64(int osel);
+KernelFn kernel_t2_g128(int osel);
+KernelFn kernel_fp8_row_bf16(int osel);
+KernelFn kernel_fp8_row_fp16(int osel);
 KernelFn kernel_generic_f32();
 KernelFn kernel_generic_f16();
 KernelFn kernel_generic_bf16();

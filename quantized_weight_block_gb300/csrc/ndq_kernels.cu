@@ -67,6 +67,11 @@ KernelFn pick_kernel(int fsel, int osel) {
         case KF_IQ3_S: return kernel_iq3_s(osel);
         case KF_IQ1_S: return kernel_iq1_s(osel);
         case KF_IQ1_M: return kernel_iq1_m(osel);
+        case KF_Q5_G64: return kernel_q5_g64(osel);
+        case KF_Q6_G64: return kernel_q6_g64(osel);
+        case KF_T2_G128: return kernel_t2_g128(osel);
+        case KF_FP8_ROW_BF16: return kernel_fp8_row_bf16(osel);
+        case KF_FP8_ROW_FP16: return kernel_fp8_row_fp16(osel);
         default: return kernel_generic(osel);
     }
 }

@@ -230,10 +230,12 @@ WORKLOADS = [
     ("iq4_nl[8192,28672]->bf16", "gguf:iq4_nl", (8192, 28672), 7, "bfloat16"),
 ]
 
-# The other gguf formats, each on one Llama-3-8B FFN-shaped tensor
+# The other gguf and NInfer formats, each on one Llama-3-8B FFN-shaped tensor
 # [14336, 4096] decoded to bf16; seeds 100 + index.
 NEXT_FORMATS = ["gguf:q4_1", "gguf:q5_0", "gguf:q5_1", "gguf:q8_1", "gguf:q8_k", "gguf:q2_k", "gguf:q3_k",
                 "gguf:q5_k", "gguf:iq4_xs", "gguf:tq1_0", "gguf:tq2_0", "gguf:q1_0", "gguf:q2_0",
-                "gguf:iq2_xxs", "gguf:iq2_xs", "gguf:iq2_s", "gguf:iq3_xxs", "gguf:iq3_s", "gguf:iq1_s", "gguf:iq1_m"]
-NEXT_WORKLOADS = [(f"{f[5:]}[14336,4096]->bf16", f, (14336, 4096), 100 + i, "bfloat16")
+                "gguf:iq2_xxs", "gguf:iq2_xs", "gguf:iq2_s", "gguf:iq3_xxs", "gguf:iq3_s", "gguf:iq1_s", "gguf:iq1_m",
+                "q2_g64_fp16", "q5_g64_fp16", "q6_g64_fp16", "t2_g128_fp16", "fp8_e4m3fn_row_bf16",
+                "fp8_e4m3fn_row_fp16"]
+NEXT_WORKLOADS = [(f"{f.split(':')[-1]}[14336,4096]->bf16", f, (14336, 4096), 100 + i, "bfloat16")
                   for i, f in enumerate(NEXT_FORMATS)]

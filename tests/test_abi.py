@@ -59,13 +59,20 @@ def test_format_table_matches_onnx_table():
     assert ndq.ndq_format_geometry(ndq.format_id("q8_g32_fp16")) == (32, 34)
 
 
+def test_ninfer_geometry_matches_oracle(orc):
+    for i in range(27, ndq.NDQ_NUM_FORMATS):
+        name = ndq.ndq_format_name(i)
+        assert ndq.ndq_format_geometry(i) == orc.format_info(name)[:2], name
+
+
 def test_identifiers_are_closed_and_case_sensitive():
     for bad in ("gguf:Q4_0", "q4_0", "gguf:q4_0 ", "gguf:q4_0(32)", "", "NVFP4"):
         assert ndq.ndq_format_from_name(bad) == -1
     assert ndq.ndq_format_from_name(None) == -1
-    assert ndq.ndq_format_name(-1) is None and ndq.ndq_format_name(30) is None
+    n = ndq.NDQ_NUM_FORMATS
+    assert ndq.ndq_format_name(-1) is None and ndq.ndq_format_name(n) is None
     with pytest.raises(ndq.NdqError):
-        ndq.ndq_format_geometry(30)
+        ndq.ndq_format_geometry(n)
 
 
 def test_supported_set(orc):

@@ -138,7 +138,8 @@ def test_special_binary16_scales(orc):
     specials = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x7C01,
                          0x3C00, 0xBC00], np.uint16)
     fields = {"gguf:q8_0": (0,), "gguf:q4_0": (0,), "gguf:iq4_nl": (0,), "q4_g64_fp16": (0,), "gguf:q4_k": (0, 2),
-              "gguf:q6_k": (208,), **synth.F16_SCALES}
+              "gguf:q6_k": (208,), **synth.F16_SCALES, "q2_g64_fp16": (0,), "q5_g64_fp16": (0,), "q6_g64_fp16": (0,),
+              "t2_g128_fp16": (0,)}
     for fmt, offs in fields.items():
         B, S = synth.GEOMETRY[fmt]
         nb = len(specials) ** 2
@@ -179,6 +180,32 @@ def test_special_binary16_scales_iq1_m(orc):
     for out in OUTS:
         assert_bit_exact(gpu_decode("gguf:iq1_m", (nb, 256), x, out), orc.decode("gguf:iq1_m", (nb, 256), x, out),
                          out, "iq1_m")
+
+
+@pytest.mark.parametrize("fmt", synth.ROW_SCALED)
+def test_fp8_rows_every_code_and_special_multipliers(orc, fmt):
+    # 256 codes per row (every E4M3FN word), one special multiplier per row:
+    # zeros, subnormals, largest finite, infinities, NaN, negative
+    words = [0x0000, 0x8000, 0x0001, 0x8001, 0x3F80, 0xBF80, 0x7F7F, 0x7F80, 0xFF80, 0x7FC0, 0x0080, 0x4B00] \
+        if fmt == "fp8_e4m3fn_row_bf16" else \
+        [0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x3C00, 0xBC00, 0x7BFF, 0x7C00, 0xFC00, 0x7E00, 0x5A00]
+    N = len(words)
+    x = np.concatenate([np.tile(np.arange(256, dtype=np.uint8), N), np.array(words, "<u2").view(np.uint8)])
+    for out in OUTS:
+        assert_bit_exact(gpu_decode(fmt, (N, 256), x, out), orc.decode(fmt, (N, 256), x, out), out, fmt)
+
+
+@pytest.mark.parametrize("fmt", synth.ROW_SCALED)
+@pytest.mark.parametrize("shape", [(7, 1), (3, 5), (2, 15), (4, 16), (3, 17), (1, 8191), (2, 8193), (1000, 13),
+                                   (9, 4097), (2, 3, 11), (37,)])
+def test_fp8_rows_cross_units_and_tiles(orc, fmt, shape):
+    # rows that are not a multiple of 16 codes: 16-code units straddle rows,
+    # and a partial last unit
+    x = synth.payload(fmt, shape, seed=sum(shape), dist="workload")
+    for out in ("float32", "bfloat16"):
+        for x_off, y_off in ((0, 0), (3, 1)):
+            assert_bit_exact(gpu_decode(fmt, shape, x, out, x_offset=x_off, y_offset=y_off),
+                             orc.decode(fmt, shape, x, out), out, f"{fmt} {shape} x+{x_off} y+{y_off}")
 
 
 def test_batched_mixed(orc):
