@@ -88,7 +88,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_encode_grouped.argtypes = [c.c_char_p, vp, c.c_uint64, c.c_uint64, vp]
         for fn in ("oracle_h2f_array", "oracle_f32_to_bf16_array", "oracle_f32_to_f16_array"):
             getattr(L, fn).argtypes = [vp, vp, c.c_uint64]
-        L.oracle_matmul_packed.argtypes = [c.c_char_p, c.c_uint64, c.c_uint64, vp, c.c_uint64, vp, c.c_uint64, vp, vp]
+        L.oracle_matmul_packed.argtypes = [c.c_char_p, c.c_uint64, c.c_uint64, vp, c.c_uint64, vp, c.c_uint64,
+                                           c.c_int, vp, vp]
         L.oracle_set_codebook.argtypes = [c.c_char_p, c.c_int, c.c_int, vp, c.c_int, vp, c.c_uint64]
         L.oracle_codebook_row.argtypes = [c.c_char_p, c.c_int, vp]
         L.oracle_codebook_rows.argtypes = [c.c_char_p]
@@ -118,17 +119,19 @@ def read_codebooks(path: str = CODEBOOKS_FILE) -> dict:
             for k, (w, b, r, v, h) in books.items()}
 
 
-def matmul_packed(name: str, N: int, K: int, w: np.ndarray, x_bf16: np.ndarray):
+def matmul_packed(name: str, N: int, K: int, w: np.ndarray, x_bf16: np.ndarray, weights: str = "bfloat16"):
     """Reference of the fused decode + product: (y, yabs), both float64 [M, N].
 
-    y[m, n] = sum_k X[m, k] * W[n, k] with W the payload decoded to bfloat16
-    and X given as bfloat16 bit patterns [M, K]; yabs is sum_k |X W|."""
+    y[m, n] = sum_k X[m, k] * W[n, k] with W the payload decoded to
+    `weights` ("float32": the exact binary32 decode, or "bfloat16") and X
+    given as bfloat16 bit patterns [M, K]; yabs is sum_k |X W|."""
     w = np.ascontiguousarray(w, dtype=np.uint8)
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1, K) if K else np.zeros((len(x_bf16), 0), np.uint16)
     M = x.shape[0]
     y = np.zeros((M, N), np.float64)
     yabs = np.zeros((M, N), np.float64)
-    rc = lib().oracle_matmul_packed(name.encode(), N, K, _ptr(w), w.size, _ptr(x), M, _ptr(y), _ptr(yabs))
+    rc = lib().oracle_matmul_packed(name.encode(), N, K, _ptr(w), w.size, _ptr(x), M, OUT_DTYPES[weights],
+                                    _ptr(y), _ptr(yabs))
     if rc:
         raise OracleError(rc, name)
     return y, yabs

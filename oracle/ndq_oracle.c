@@ -1112,38 +1112,41 @@ void oracle_f32_to_f16_array(const uint32_t *in, uint16_t *out, uint64_t n) {
 /* product, choosing its own staging, reduction order and intermediate       */
 /* precision; its result is qualified against an independent oracle).       */
 /*                                                                          */
-/* READING: the weight operand is DequantizePacked(w, [N, K], BFLOAT16) --   */
-/* the decoded weights rounded once to bfloat16, i.e. exactly what a         */
-/* decode-to-bf16 followed by a bf16 matrix product consumes -- and the      */
+/* READING: the weight operand is DequantizePacked(w, [N, K], T) with T     */
+/* FLOAT (the exact binary32 decode) or BFLOAT16 (rounded once to bfloat16, */
+/* what a decode-to-bf16 followed by a bf16 product consumes), and the      */
 /* activations X are bfloat16 [M, K].  The reference sums the exact products */
 /* in binary64:                                                             */
 /*     y[m*N + n] = sum_k X[m,k] * W[n,k],   yabs[...] = sum_k |X[m,k] W[n,k]| */
-/* (every product of two bfloat16 values is exact in binary64; yabs bounds  */
-/* the rounding error of any binary32 evaluation order).                   */
+/* (every product of a bfloat16 and a binary32 value is exact in binary64;  */
+/* yabs bounds the rounding error of any binary32 evaluation order).        */
 /* ------------------------------------------------------------------------ */
 static double or_bf16_to_f64(uint16_t h) { return (double)or_f32((uint32_t)h << 16); }
 
 int oracle_matmul_packed(const char *name, uint64_t N, uint64_t K, const uint8_t *w, uint64_t w_len,
-                         const uint16_t *x_bf16, uint64_t M, double *y, double *yabs) {
+                         const uint16_t *x_bf16, uint64_t M, int weight_dtype, double *y, double *yabs) {
     int64_t shape[2] = {(int64_t)N, (int64_t)K};
     uint64_t nb = 0;
     int rc = oracle_geometry(name, shape, 2, w_len, &nb, NULL, NULL);
     if (rc != OR_OK) return rc;
     if (M == 0 || N == 0) return OR_OK;
+    if (weight_dtype != 0 && weight_dtype != 2) return OR_ERR_BAD_DTYPE; /* FLOAT or BFLOAT16 */
     if (!x_bf16 || !y || !yabs || (K > 0 && !w)) return OR_ERR_NULL;
     int fi = or_find(name);
     uint64_t bpr = K / (uint64_t)OR_FORMATS[fi].B; /* blocks per weight row */
-    uint16_t *row = (uint16_t *)malloc((size_t)(K ? K : 1) * sizeof(uint16_t));
+    float *row = (float *)malloc((size_t)(K ? K : 1) * sizeof(float));
     if (!row) return OR_ERR_NULL;
     for (uint64_t n = 0; n < N; ++n) {
         if (K > 0) {
-            rc = oracle_decode_range(name, shape, 2, 2 /* BFLOAT16 */, w, w_len, n * bpr, (n + 1) * bpr, row);
+            rc = oracle_decode_range(name, shape, 2, weight_dtype, w, w_len, n * bpr, (n + 1) * bpr, row);
             if (rc != OR_OK) break;
+            if (weight_dtype == 2) /* bfloat16 bit patterns, expanded in place from the top */
+                for (uint64_t k = K; k-- > 0;) row[k] = or_f32((uint32_t)((uint16_t *)row)[k] << 16);
         }
         for (uint64_t m = 0; m < M; ++m) {
             double s = 0.0, a = 0.0;
             for (uint64_t k = 0; k < K; ++k) {
-                double p = or_bf16_to_f64(x_bf16[m * K + k]) * or_bf16_to_f64(row[k]);
+                double p = or_bf16_to_f64(x_bf16[m * K + k]) * (double)row[k];
                 s += p;
                 a += fabs(p);
             }

@@ -1,7 +1,7 @@
 """Pins for the oracle's fused decode + product reference (CPU only).
 
-y[m, n] = sum_k X[m, k] * W[n, k] with W = DequantizePacked(w, [N, K],
-BFLOAT16) and bfloat16 activations X, summed exactly enough in binary64.
+y[m, n] = sum_k X[m, k] * W[n, k] with W = DequantizePacked(w, [N, K], T),
+T FLOAT or BFLOAT16, and bfloat16 activations X, summed in binary64.
 
 * One-hot activation rows pick single decoded weights (the index wiring:
   W is [N, K], the product contracts K).
@@ -28,16 +28,18 @@ def bf16_values(bits):
 
 
 @pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q6_k", "gguf:iq2_xs", "nvfp4", "fp8_e4m3fn_row_fp16"])
-def test_one_hot_rows_pick_decoded_weights(orc, fmt):
+@pytest.mark.parametrize("weights", ["bfloat16", "float32"])
+def test_one_hot_rows_pick_decoded_weights(orc, fmt, weights):
     B = synth.GEOMETRY[fmt][0]
     N, K = 5, 2 * max(B, 32)
     w = synth.payload(fmt, (N, K), seed=3)
-    W = bf16_values(orc.decode(fmt, (N, K), w, "bfloat16")).astype(np.float64)
+    dec = orc.decode(fmt, (N, K), w, weights)
+    W = (bf16_values(dec) if weights == "bfloat16" else dec).astype(np.float64)
     ks = [0, 1, K // 2 + 3, K - 1]
     x = np.zeros((len(ks), K), np.uint16)
     for m, k in enumerate(ks):
         x[m, k] = BF16_ONE
-    y, yabs = orc.matmul_packed(fmt, N, K, w, x)
+    y, yabs = orc.matmul_packed(fmt, N, K, w, x, weights)
     for m, k in enumerate(ks):
         assert np.array_equal(y[m], W[:, k]), (fmt, k)
         assert np.array_equal(yabs[m], np.abs(W[:, k]))
@@ -56,8 +58,9 @@ def test_integer_case_is_numpy_int_matmul(orc, fmt, lo, hi):
         q = blk[:, 2:].astype(np.int64)
         codes = np.concatenate([q & 15, q >> 4], axis=1).reshape(N, K) - 8
     xi = rng.integers(-8, 9, size=(M, K))
-    y, _ = orc.matmul_packed(fmt, N, K, blk.reshape(-1), bf16_bits(xi))
-    assert np.array_equal(y, (xi @ codes.T).astype(np.float64))
+    for weights in ("bfloat16", "float32"):
+        y, _ = orc.matmul_packed(fmt, N, K, blk.reshape(-1), bf16_bits(xi), weights)
+        assert np.array_equal(y, (xi @ codes.T).astype(np.float64))
 
 
 def test_rows_of_x_are_independent(orc):
