@@ -194,6 +194,31 @@ typedef struct ndq_tensor_desc {
     void *y;
 } ndq_tensor_desc;
 
+/* Decode fused into a matrix product (the consumer-side use of a packed
+ * weight: NInfer "tensor-formats" lets a consuming kernel fuse decode into
+ * its product with its own staging, reduction order and precision):
+ *
+ *     Y[m, n] = sum_k X[m, k] * W[n, k]      (m < M, n < N, k < K)
+ *
+ *   format_id     any supported format (the fp8 row formats need K % 16 == 0)
+ *   w, w_len      device payload of the weight matrix [N, K] under the same
+ *                 length rule as ndq_dequantize_packed
+ *   x_bf16        device bfloat16 activations [M, K], row-major
+ *   weight_dtype  NDQ_FLOAT: W is the payload decoded exactly as
+ *                 ndq_dequantize_packed decodes it to FLOAT; NDQ_BFLOAT16: W
+ *                 is that decode rounded once to bfloat16 (the operand of an
+ *                 unfused decode-to-bf16 and bf16 product)
+ *   y             device output [M, N], row-major, NDQ_FLOAT or NDQ_BFLOAT16
+ * Products and sums are binary32 (fused multiply-adds) in an unspecified
+ * but fixed order, so repeated calls give identical bits; each output is
+ * within 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then
+ * rounded once to out_dtype.  Rows of X are processed in passes of up to 8
+ * (each pass reads the payload once).  Same ownership, asynchrony and error
+ * rules as ndq_dequantize_packed; M, N or K of 0 is valid (K == 0 writes
+ * zeros); NDQ_ERR_BAD_DTYPE for other weight or output types. */
+int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t *w, size_t w_len, const void *x_bf16,
+                      int64_t M, int weight_dtype, int out_dtype, void *y, void *stream);
+
 /* Device workspace bytes the batched call needs for n tensors (a table of
  * per-tensor launch descriptors), or 0 when n < 0. */
 size_t ndq_batched_workspace_bytes(int n);

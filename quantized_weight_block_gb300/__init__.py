@@ -72,12 +72,15 @@ _lib.ndq_dequantize_packed_batched.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c
                                                _c.c_void_p]
 _lib.ndq_get_device_fault.argtypes = [_c.POINTER(_c.c_uint32)]
 _lib.ndq_dequantize_packed_batched_noalloc.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p]
+_lib.ndq_matmul_packed.argtypes = [_c.c_int, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_size_t, _c.c_void_p,
+                                   _c.c_int64, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p]
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = (
     "ndq_format_from_name", "ndq_format_name", "ndq_format_geometry", "ndq_format_supported",
     "ndq_status_string", "ndq_payload_geometry", "ndq_dequantize_packed", "ndq_batched_workspace_bytes",
     "ndq_dequantize_packed_batched", "ndq_get_device_fault", "ndq_dequantize_packed_batched_noalloc",
+    "ndq_matmul_packed",
 )
 
 
@@ -143,6 +146,12 @@ def ndq_dequantize_packed_batched_noalloc(descs, stream: int = 0) -> int:
     library's own device array); returns the status code."""
     arr = (ndq_tensor_desc * max(1, len(descs)))(*descs)
     return _lib.ndq_dequantize_packed_batched_noalloc(arr, len(descs), stream)
+
+
+def ndq_matmul_packed(format_id: int, N: int, K: int, w_ptr: int, w_len: int, x_ptr: int, M: int,
+                      weight_dtype: int, out_dtype: int, y_ptr: int, stream: int = 0) -> int:
+    """Raw call of the fused decode + product; returns the status code."""
+    return _lib.ndq_matmul_packed(format_id, N, K, w_ptr, w_len, x_ptr, M, weight_dtype, out_dtype, y_ptr, stream)
 
 
 def ndq_get_device_fault() -> int:
@@ -227,6 +236,25 @@ def dequantize_packed_batched(items, workspace=None, stream=None):
     if rc:
         raise NdqError(rc)
     return workspace
+
+
+def matmul_packed(fmt, w, N: int, K: int, x, out_dtype=None, y=None, stream=None, weight_dtype=None):
+    """Y = X @ W^T with W [N, K] decoded from the CUDA uint8 payload `w`
+    (binary32, or rounded to bfloat16 when weight_dtype is torch.bfloat16)
+    and X a CUDA bfloat16 tensor [M, K]; returns Y [M, N]."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.float32
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[-1] != K:
+        raise ValueError("x must be a contiguous bfloat16 tensor [M, K]")
+    M = x.numel() // K if K else x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=w.device)
+    wcode = out_dtype_code(weight_dtype or torch.float32)
+    rc = ndq_matmul_packed(format_id(fmt), N, K, w.data_ptr(), w.numel(), x.data_ptr(), M, wcode,
+                           out_dtype_code(y.dtype), y.data_ptr(), _stream_handle(stream))
+    if rc:
+        raise NdqError(rc, str(fmt))
+    return y
 
 
 def get_device_fault() -> int:

@@ -247,6 +247,51 @@ int ndq_dequantize_packed(int format_id, const int64_t* shape, int ndim, int out
     return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
 }
 
+int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, size_t w_len, const void* x_bf16,
+                      int64_t M, int weight_dtype, int out_dtype, void* y, void* stream) {
+    if (!valid_id(format_id)) return NDQ_ERR_UNKNOWN_FORMAT;
+    if (N < 0 || K < 0 || M < 0) return NDQ_ERR_NEGATIVE_DIM;
+    if (out_dtype != NDQ_FLOAT && out_dtype != NDQ_BFLOAT16) return NDQ_ERR_BAD_DTYPE;
+    if (weight_dtype != NDQ_FLOAT && weight_dtype != NDQ_BFLOAT16) return NDQ_ERR_BAD_DTYPE;
+    // the fp8 row formats decode in 16-code units, which must not cross rows here
+    if (fp8_row(format_id) && K % 16 != 0) return NDQ_ERR_NOT_BLOCK_ALIGNED;
+    const int64_t shape[2] = {N, K};
+    ndq::MvParams p;
+    std::memset(&p, 0, sizeof(p));
+    Geometry g;
+    // (the weight descriptor's output pointer is unused by the fused kernel)
+    const int rc = prepare(format_id, shape, 2, NDQ_FLOAT, w, w_len, const_cast<uint8_t*>(w), &p.w, &g);
+    if (rc != NDQ_OK) return rc;
+    uint64_t mn = 0, ybytes = 0;
+    const uint64_t osize = out_dtype == NDQ_FLOAT ? 4u : 2u;
+    if (mul_ovf(static_cast<uint64_t>(M), static_cast<uint64_t>(N), &mn) || mul_ovf(mn, osize, &ybytes) ||
+        ybytes > static_cast<uint64_t>(INT64_MAX))
+        return NDQ_ERR_OVERFLOW;
+    if (mn == 0) return NDQ_OK;
+    if (!y || (K > 0 && !x_bf16)) return NDQ_ERR_NULL;
+    if (K == 0)  // empty sums
+        return cudaMemsetAsync(y, 0, ybytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NDQ_OK : NDQ_ERR_CUDA;
+    p.n_rows = static_cast<uint64_t>(N);
+    p.K = static_cast<uint64_t>(K);
+    p.bpr = p.w.nblocks / static_cast<uint64_t>(N);
+    const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+    p.xvec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && K % 8 == 0;
+    p.wbf16 = weight_dtype == NDQ_BFLOAT16;
+    // whole rows per staged unit: up to 8192 decoded elements and 8 row groups
+    p.rows_per_stage = 1;
+    while (p.rows_per_stage < ndq::kConsumerWarpsPerCta &&
+           static_cast<int64_t>(p.rows_per_stage) * 2 * K <= ndq::kTileElems)
+        p.rows_per_stage *= 2;
+    p.out_bf16 = out_dtype == NDQ_BFLOAT16;
+    for (int64_t m0 = 0; m0 < M; m0 += ndq::kMvMaxRows) {
+        p.x = x + static_cast<uint64_t>(m0) * static_cast<uint64_t>(K);
+        p.y = static_cast<uint8_t*>(y) + static_cast<uint64_t>(m0) * static_cast<uint64_t>(N) * osize;
+        p.m = static_cast<int32_t>(M - m0 < ndq::kMvMaxRows ? M - m0 : ndq::kMvMaxRows);
+        if (ndq::launch_matvec(p, stream) != 0) return NDQ_ERR_CUDA;
+    }
+    return NDQ_OK;
+}
+
 size_t ndq_batched_workspace_bytes(int n) {
     if (n < 0) return 0;
     return (static_cast<size_t>(n) * sizeof(ndq::DevTensor) + kWorkspaceAlign - 1) / kWorkspaceAlign *

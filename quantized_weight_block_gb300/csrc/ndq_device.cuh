@@ -1288,6 +1288,17 @@ __device__ __forceinline__ void decode_tile_slow_f(const StageInfo& si, const ui
     }
 }
 
+// Slow path of a kernel specialised for format F (and output type O when
+// O >= 0): only that decoder, so the specialised kernel's register budget is
+// not set by the other formats' slow paths.
+template <int F, int O>
+__device__ __noinline__ void decode_tile_slow_one(const StageInfo& si, const uint8_t* in, const Ctx x, uint32_t tid) {
+    if (O >= 0)
+        decode_tile_fop<F, (O >= 0 ? O : 0), true>(si, in, x, tid);
+    else
+        decode_tile_slow_f<F>(si, in, x, tid);
+}
+
 __device__ __noinline__ void decode_tile_slow(const StageInfo& si, const uint8_t* in, const Ctx x, uint32_t tid) {
     switch (si.t.fmt) {
         case KF_Q8_0: decode_tile_slow_f<KF_Q8_0>(si, in, x, tid); break;
@@ -1542,8 +1553,12 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
         const uint8_t* in = inbuf + s * kInStride;
         const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
         if (si.phase != 0u || (nv && !si.nv_tab)) {
-            decode_tile_slow(si, in, Ctx{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t)},
-                             tid);
+            const Ctx xs{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids,
+                         code_count(si.t)};
+            if (FSEL >= 0)
+                decode_tile_slow_one<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, xs, tid);
+            else
+                decode_tile_slow(si, in, xs, tid);
         } else {
             decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t)}, tid);
         }

@@ -1,6 +1,7 @@
-// Decode kernels specialised for gguf:iq3_xxs (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for gguf:iq3_xxs (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_iq3_xxs(int osel) { return kernel_row<KF_IQ3_XXS>(osel); }
+MvKernelFn matvec_iq3_xxs(int variant) { return matvec_kernel<KF_IQ3_XXS>(variant); }
 }  // namespace ndq

@@ -1,0 +1,102 @@
+// Launcher of the fused decode + product kernels (one per decode family,
+// instantiated beside each family's decode kernels).
+#include <cuda_runtime.h>
+
+#include "ndq_matvec.cuh"
+
+namespace ndq {
+
+MvKernelFn matvec_for(int kfmt, int variant) {
+    switch (kfmt) {
+        case KF_FP8_ROW_BF16: return matvec_fp8_row_bf16(variant);
+        case KF_FP8_ROW_FP16: return matvec_fp8_row_fp16(variant);
+        case KF_GGUF_NVFP4: return matvec_gguf_nvfp4(variant);
+        case KF_IQ1_M: return matvec_iq1_m(variant);
+        case KF_IQ1_S: return matvec_iq1_s(variant);
+        case KF_IQ2_S: return matvec_iq2_s(variant);
+        case KF_IQ2_XS: return matvec_iq2_xs(variant);
+        case KF_IQ2_XXS: return matvec_iq2_xxs(variant);
+        case KF_IQ3_S: return matvec_iq3_s(variant);
+        case KF_IQ3_XXS: return matvec_iq3_xxs(variant);
+        case KF_IQ4_NL: return matvec_iq4_nl(variant);
+        case KF_IQ4_XS: return matvec_iq4_xs(variant);
+        case KF_MXFP4: return matvec_mxfp4(variant);
+        case KF_NVFP4: return matvec_nvfp4(variant);
+        case KF_Q1_0: return matvec_q1_0(variant);
+        case KF_Q2_0: return matvec_q2_0(variant);
+        case KF_Q2_K: return matvec_q2_k(variant);
+        case KF_Q3_K: return matvec_q3_k(variant);
+        case KF_Q4_0: return matvec_q4_0(variant);
+        case KF_Q4_1: return matvec_q4_1(variant);
+        case KF_Q4_G64: return matvec_q4_g64(variant);
+        case KF_Q4_K: return matvec_q4_k(variant);
+        case KF_Q5_0: return matvec_q5_0(variant);
+        case KF_Q5_1: return matvec_q5_1(variant);
+        case KF_Q5_G64: return matvec_q5_g64(variant);
+        case KF_Q5_K: return matvec_q5_k(variant);
+        case KF_Q6_G64: return matvec_q6_g64(variant);
+        case KF_Q6_K: return matvec_q6_k(variant);
+        case KF_Q8_0: return matvec_q8_0(variant);
+        case KF_Q8_1: return matvec_q8_1(variant);
+        case KF_Q8_K: return matvec_q8_k(variant);
+        case KF_T2_G128: return matvec_t2_g128(variant);
+        case KF_TQ1_0: return matvec_tq1_0(variant);
+        case KF_TQ2_0: return matvec_tq2_0(variant);
+        default: return nullptr;
+    }
+}
+
+namespace {
+struct MvDeviceInfo {
+    int sms = 0;
+    int ctas_per_sm[KF_COUNT][3] = {};  // per decode family and variant; 0 = not yet queried
+};
+MvDeviceInfo g_mv_dev[64];
+}  // namespace
+
+int launch_matvec(const MvParams& p0, void* stream) {
+    if (p0.n_rows == 0 || p0.m <= 0) return 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    MvParams p = p0;
+    const int se = device_symbols(dev, &p.fault, &p.grids);
+    if (se != 0) return se;
+    const int f = p.w.fmt;
+    // every unit starts on a 16-byte boundary when the payload does and a
+    // unit's rows (or a row, when rows are segmented) span whole lines;
+    // segments of a row are whole tiles, which always do
+    const uint64_t unit_rows = static_cast<uint64_t>(p.rows_per_stage);
+    const bool aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (unit_rows * p.bpr * p.w.S) % 16u == 0;
+    const int variant = aligned ? (p.m == 1 ? 0 : 1) : 2;
+    const MvKernelFn fn = (f >= 0 && f < KF_COUNT) ? matvec_for(f, variant) : nullptr;
+    if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    const size_t smem = static_cast<size_t>(kStages * kInStride + kHdrBytes + kMvExtraBytes);
+    MvDeviceInfo& di = g_mv_dev[dev];
+    if (di.sms == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        di.sms = sms;
+    }
+    int& cps = di.ctas_per_sm[f][variant];
+    if (cps == 0) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        cps = n > 0 ? n : 1;
+    }
+    const uint64_t R = static_cast<uint64_t>(p.rows_per_stage);
+    const uint64_t units = (p.n_rows + R - 1) / R;
+    const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
+    const unsigned grid = static_cast<unsigned>(units < resident ? units : resident);
+    void* args[] = {&p};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
+                         static_cast<cudaStream_t>(stream));
+    return static_cast<int>(e);
+}
+
+}  // namespace ndq

@@ -1,6 +1,7 @@
-// Decode kernels specialised for gguf:q3_k (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for gguf:q3_k (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_q3_k(int osel) { return kernel_row<KF_Q3_K>(osel); }
+MvKernelFn matvec_q3_k(int variant) { return matvec_kernel<KF_Q3_K>(variant); }
 }  // namespace ndq

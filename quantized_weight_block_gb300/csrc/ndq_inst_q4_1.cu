@@ -1,6 +1,7 @@
-// Decode kernels specialised for gguf:q4_1 (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for gguf:q4_1 (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_q4_1(int osel) { return kernel_row<KF_Q4_1>(osel); }
+MvKernelFn matvec_q4_1(int variant) { return matvec_kernel<KF_Q4_1>(variant); }
 }  // namespace ndq

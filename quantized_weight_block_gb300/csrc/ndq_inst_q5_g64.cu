@@ -1,6 +1,7 @@
-// Decode kernels specialised for q5_g64_fp16 (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for q5_g64_fp16 (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_q5_g64(int osel) { return kernel_row<KF_Q5_G64>(osel); }
+MvKernelFn matvec_q5_g64(int variant) { return matvec_kernel<KF_Q5_G64>(variant); }
 }  // namespace ndq

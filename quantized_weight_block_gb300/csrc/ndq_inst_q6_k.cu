@@ -1,6 +1,7 @@
-// Decode kernels specialised for KF_Q6_K (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for KF_Q6_K (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_q6_k(int osel) { return kernel_row<KF_Q6_K>(osel); }
+MvKernelFn matvec_q6_k(int variant) { return matvec_kernel<KF_Q6_K>(variant); }
 }  // namespace ndq

@@ -1,6 +1,7 @@
-// Decode kernels specialised for t2_g128_fp16 (one per output type).
-#include "ndq_device.cuh"
+// Decode kernels specialised for t2_g128_fp16 (one per output type) and its fused product kernel.
+#include "ndq_matvec.cuh"
 
 namespace ndq {
 KernelFn kernel_t2_g128(int osel) { return kernel_row<KF_T2_G128>(osel); }
+MvKernelFn matvec_t2_g128(int variant) { return matvec_kernel<KF_T2_G128>(variant); }
 }  // namespace ndq

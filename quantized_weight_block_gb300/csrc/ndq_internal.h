@@ -62,6 +62,7 @@ constexpr int kTileElems = 8192;
 constexpr int kThreads = 256;
 constexpr int kMaxTileBytes = 9344;  // gguf:q8_k: 32 blocks * 292 bytes
 constexpr int kBlockThreads = kThreads + 32;  // consumer warps + one producer warp
+constexpr int kConsumerWarpsPerCta = kThreads / 32;
 constexpr int kStages = 4;                    // staged tiles in flight per CTA
 constexpr int kInStride = 9472;               // tile bytes + phase + rounding + over-read
 constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
@@ -116,6 +117,72 @@ struct KParams {
 };
 
 using KernelFn = void (*)(KParams);
+
+// Decode fused into a product with few activation rows (ndq_matvec.cuh):
+// Y[m, n] = sum_k X[m, k] * W[n, k] for m < m_rows <= kMvMaxRows.
+constexpr int kMvMaxRows = 8;
+struct MvParams {
+    DevTensor w;          // the weight payload as a decode descriptor (y unused)
+    const uint16_t* x;    // bfloat16 activations [m, K], row-major
+    void* y;              // outputs [m, N], row-major (FLOAT or BFLOAT16)
+    uint64_t n_rows;      // N
+    uint64_t K;
+    uint64_t bpr;         // payload blocks per weight row
+    int32_t m;            // activation rows of this launch (1..kMvMaxRows)
+    int32_t xvec;         // 1 if every 16-element slice of x is 16-byte aligned
+    int32_t rows_per_stage;  // R in {1, 2, 4, 8}: whole rows per staged unit (K <= 8192/R), 1 = segments
+    int32_t wbf16;        // 1: round the decoded weights to bfloat16 before the product
+    int32_t out_bf16;     // 1: y is bfloat16, else binary32
+    int32_t pad_;
+    unsigned int* fault;  // device fault word (set by the launcher)
+    const IqGrids* grids;  // IQ codebooks (set by the launcher)
+};
+
+using MvKernelFn = void (*)(MvParams);
+
+// Fused kernels, one per decode family (defined in the instantiation files).
+MvKernelFn matvec_fp8_row_bf16(int variant);
+MvKernelFn matvec_fp8_row_fp16(int variant);
+MvKernelFn matvec_gguf_nvfp4(int variant);
+MvKernelFn matvec_iq1_m(int variant);
+MvKernelFn matvec_iq1_s(int variant);
+MvKernelFn matvec_iq2_s(int variant);
+MvKernelFn matvec_iq2_xs(int variant);
+MvKernelFn matvec_iq2_xxs(int variant);
+MvKernelFn matvec_iq3_s(int variant);
+MvKernelFn matvec_iq3_xxs(int variant);
+MvKernelFn matvec_iq4_nl(int variant);
+MvKernelFn matvec_iq4_xs(int variant);
+MvKernelFn matvec_mxfp4(int variant);
+MvKernelFn matvec_nvfp4(int variant);
+MvKernelFn matvec_q1_0(int variant);
+MvKernelFn matvec_q2_0(int variant);
+MvKernelFn matvec_q2_k(int variant);
+MvKernelFn matvec_q3_k(int variant);
+MvKernelFn matvec_q4_0(int variant);
+MvKernelFn matvec_q4_1(int variant);
+MvKernelFn matvec_q4_g64(int variant);
+MvKernelFn matvec_q4_k(int variant);
+MvKernelFn matvec_q5_0(int variant);
+MvKernelFn matvec_q5_1(int variant);
+MvKernelFn matvec_q5_g64(int variant);
+MvKernelFn matvec_q5_k(int variant);
+MvKernelFn matvec_q6_g64(int variant);
+MvKernelFn matvec_q6_k(int variant);
+MvKernelFn matvec_q8_0(int variant);
+MvKernelFn matvec_q8_1(int variant);
+MvKernelFn matvec_q8_k(int variant);
+MvKernelFn matvec_t2_g128(int variant);
+MvKernelFn matvec_tq1_0(int variant);
+MvKernelFn matvec_tq2_0(int variant);
+MvKernelFn matvec_for(int kfmt, int variant);
+
+// Launch one fused product.  Returns 0 or a CUDA error code.
+int launch_matvec(const MvParams& p, void* stream);
+
+// Device addresses of the fault word and the IQ codebooks on the current
+// device (resolved once per device).  Returns 0 or a CUDA error code.
+int device_symbols(int dev, unsigned int** fault, const IqGrids** grids);
 
 // Kernel getters, one per instantiation file (osel: KOut, or -1 for any).
 KernelFn kernel_q8_0(int osel);

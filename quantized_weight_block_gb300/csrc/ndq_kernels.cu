@@ -127,27 +127,34 @@ int launch_decode(const KParams& p, void* stream) {
         if (fsel < 0 && n > kMixedCtasPerSm) n = kMixedCtasPerSm;
         cps = n > 0 ? n : 1;
     }
-    if (!g_fault_addr[dev]) {
-        void* addr = nullptr;
-        e = cudaGetSymbolAddress(&addr, g_fault_word);
-        if (e != cudaSuccess) return static_cast<int>(e);
-        g_fault_addr[dev] = static_cast<unsigned int*>(addr);
-    }
-    if (!g_grids_addr[dev]) {
-        void* addr = nullptr;
-        e = cudaGetSymbolAddress(&addr, g_iq_grids);
-        if (e != cudaSuccess) return static_cast<int>(e);
-        g_grids_addr[dev] = static_cast<const IqGrids*>(addr);
-    }
     KParams q = p;
-    q.fault = g_fault_addr[dev];
-    q.grids = g_grids_addr[dev];
+    const int se = device_symbols(dev, &q.fault, &q.grids);
+    if (se != 0) return se;
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
     void* args[] = {&q};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
                          static_cast<cudaStream_t>(stream));
     return static_cast<int>(e);
+}
+
+int device_symbols(int dev, unsigned int** fault, const IqGrids** grids) {
+    if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+    if (!g_fault_addr[dev]) {
+        void* addr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&addr, g_fault_word);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        g_fault_addr[dev] = static_cast<unsigned int*>(addr);
+    }
+    if (!g_grids_addr[dev]) {
+        void* addr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&addr, g_iq_grids);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        g_grids_addr[dev] = static_cast<const IqGrids*>(addr);
+    }
+    *fault = g_fault_addr[dev];
+    *grids = g_grids_addr[dev];
+    return 0;
 }
 
 int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream) {

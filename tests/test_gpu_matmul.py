@@ -1,0 +1,143 @@
+"""GPU tests of the fused decode + product (ndq_matmul_packed) against the
+oracle's binary64 reference.
+
+Y[m, n] = sum_k X[m, k] * W[n, k] with W the payload decoded to binary32
+(or that decode rounded to bfloat16).  The kernel sums the exact products
+(bfloat16 times binary32) with binary32 fused multiply-adds: each term passes through at most K + 13 roundings (its
+thread's running sum, 5 warp-shuffle additions, 8 per-warp partials), so
+|Y - Y_ref| <= (K + 16) * 2^-24 * sum_k |X W| (the standard recursive
+summation bound, doubled for margin below); a bfloat16 output adds one
+rounding of at most 2^-8 |Y|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+import quantized_weight_block_gb300 as ndq  # noqa: E402
+
+DEV = "cuda"
+FORMATS = ["gguf:q8_0", "gguf:q4_0", "gguf:iq4_nl", "gguf:q4_k", "gguf:q6_k", "gguf:mxfp4", "gguf:nvfp4", "nvfp4",
+           "q4_g64_fp16", "q8_g32_fp16"] + synth.NEXT_FORMATS
+
+
+def _x_bf16(M, K, seed):
+    x = torch.from_numpy(np.random.default_rng(seed).standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    return x, x.view(torch.int16).numpy().view(np.uint16)
+
+
+def _run(fmt, N, K, M, w_np, x_t, out_dtype=torch.float32, w_off=0, x_off=0, weights="float32"):
+    wbuf = torch.zeros(w_np.size + w_off + 16, dtype=torch.uint8, device=DEV)
+    wbuf[w_off:w_off + w_np.size] = torch.from_numpy(w_np).to(DEV)
+    w = wbuf[w_off:w_off + w_np.size]
+    xbuf = torch.zeros(M * K + x_off + 8, dtype=torch.bfloat16, device=DEV)
+    xbuf[x_off:x_off + M * K] = x_t.reshape(-1).to(DEV)
+    x = xbuf[x_off:x_off + M * K]
+    y = torch.full((M, N), float("nan"), dtype=out_dtype, device=DEV)
+    wcode = ndq.NDQ_FLOAT if weights == "float32" else ndq.NDQ_BFLOAT16
+    rc = ndq.ndq_matmul_packed(ndq.format_id(fmt), N, K, w.data_ptr(), w_np.size, x.data_ptr(), M, wcode,
+                               ndq.out_dtype_code(out_dtype), y.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, ndq.ndq_status_string(rc)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def _check(got, ref, yabs, K, bf16_out=False, what=""):
+    tol = 2.0 * (K + 16) * 2.0 ** -24 * yabs + 1e-30
+    if bf16_out:
+        tol = tol + 2.0 ** -8 * np.abs(ref)
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), what
+    assert (err <= tol).all(), f"{what}: worst {np.max(err / tol):.3g} of the bound"
+
+
+@pytest.fixture(autouse=True)
+def _no_device_fault():
+    yield
+    assert ndq.get_device_fault() == 0
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("weights", ["float32", "bfloat16"])
+def test_matmul_against_oracle(orc, fmt, weights):
+    N, K, M = 37, 12288, 3  # rows of two segments (8192 + 4096 elements)
+    w = synth.payload(fmt, (N, K), seed=11)
+    x_t, x_bits = _x_bf16(M, K, 12)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+    _check(_run(fmt, N, K, M, w, x_t, weights=weights), ref, yabs, K, what=f"{fmt} {weights}")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q8_0", "gguf:mxfp4", "gguf:iq3_s", "nvfp4", "fp8_e4m3fn_row_fp16"])
+@pytest.mark.parametrize("N,K", [(37, 4096), (13, 2048), (9, 1024), (17, 512), (5, 256), (130, 8192), (3, 12800)])
+def test_matmul_whole_rows_per_stage(orc, fmt, N, K):
+    # K <= 4096 stages 2..8 whole rows at a time (a partial last unit when N
+    # is not a multiple); larger K splits rows into segments
+    B = synth.GEOMETRY[fmt][0]
+    if K % max(B, 16):
+        pytest.skip("K not a multiple of the block")
+    w = synth.payload(fmt, (N, K), seed=K + N)
+    x_t, x_bits = _x_bf16(2, K, N)
+    for weights in ("float32", "bfloat16"):
+        ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+        _check(_run(fmt, N, K, 2, w, x_t, weights=weights), ref, yabs, K, what=f"{fmt} {N}x{K} {weights}")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q6_k", "gguf:q8_0", "gguf:iq2_xs", "nvfp4", "fp8_e4m3fn_row_bf16"])
+@pytest.mark.parametrize("M", [1, 8, 11])
+def test_matmul_rows_of_x_and_bf16_output(orc, fmt, M):
+    B = synth.GEOMETRY[fmt][0]
+    N, K = 64, 2048 // max(B, 16) * max(B, 16)
+    w = synth.payload(fmt, (N, K), seed=M)
+    x_t, x_bits = _x_bf16(M, K, 100 + M)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
+    _check(_run(fmt, N, K, M, w, x_t), ref, yabs, K, what=f"{fmt} M={M}")
+    _check(_run(fmt, N, K, M, w, x_t, out_dtype=torch.bfloat16), ref, yabs, K, bf16_out=True, what=f"{fmt} M={M} bf16")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q5_0", "gguf:mxfp4", "q6_g64_fp16"])
+@pytest.mark.parametrize("w_off,x_off", [(1, 0), (7, 3), (0, 1)])
+def test_matmul_unaligned_operands(orc, fmt, w_off, x_off):
+    B = synth.GEOMETRY[fmt][0]
+    N, K = 19, 3 * 1024 // max(B, 16) * max(B, 16)
+    w = synth.payload(fmt, (N, K), seed=w_off)
+    x_t, x_bits = _x_bf16(2, K, x_off)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
+    _check(_run(fmt, N, K, 2, w, x_t, w_off=w_off, x_off=x_off), ref, yabs, K, what=f"{fmt} +{w_off}/+{x_off}")
+
+
+def test_matmul_nvfp4_several_divisors(orc):
+    N, K = 12, 64 * 40
+    w = synth.payload("nvfp4", (N, K), seed=4, ndiv=4)
+    x_t, x_bits = _x_bf16(2, K, 5)
+    ref, yabs = orc.matmul_packed("nvfp4", N, K, w, x_bits, "float32")
+    _check(_run("nvfp4", N, K, 2, w, x_t), ref, yabs, K, what="nvfp4 D=4")
+
+
+def test_matmul_is_deterministic():
+    fmt, N, K, M = "gguf:q4_k", 256, 4096, 4
+    w = synth.payload(fmt, (N, K), seed=1)
+    x_t, _ = _x_bf16(M, K, 2)
+    a = _run(fmt, N, K, M, w, x_t)
+    b = _run(fmt, N, K, M, w, x_t)
+    assert np.array_equal(a, b)
+
+
+def test_matmul_validation_and_empty():
+    q4k = ndq.format_id("gguf:q4_k")
+    F = ndq.NDQ_FLOAT
+    assert ndq.ndq_matmul_packed(q4k, 2, 256, 16, 288, 16, 1, F, ndq.NDQ_FLOAT16, 16) == 9
+    assert ndq.ndq_matmul_packed(q4k, 2, 256, 16, 288, 16, 1, ndq.NDQ_FLOAT16, F, 16) == 9
+    assert ndq.ndq_matmul_packed(q4k, -1, 256, 16, 0, 16, 1, F, F, 16) == 5
+    assert ndq.ndq_matmul_packed(q4k, 2, 100, 16, 0, 16, 1, F, F, 16) == 6
+    assert ndq.ndq_matmul_packed(q4k, 2, 256, 16, 287, 16, 1, F, F, 16) == 7
+    assert ndq.ndq_matmul_packed(ndq.format_id("fp8_e4m3fn_row_fp16"), 2, 24, 16, 52, 16, 1, F, F, 16) == 6
+    assert ndq.ndq_matmul_packed(99, 2, 256, 16, 288, 16, 1, F, F, 16) == 2
+    assert ndq.ndq_matmul_packed(q4k, 2, 256, 16, 288, 16, 0, F, F, 0) == 0  # M = 0
+    y = torch.full((3, 5), 7.0, dtype=torch.float32, device=DEV)
+    assert ndq.ndq_matmul_packed(q4k, 5, 0, 0, 0, 0, 3, F, F, y.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream) == 0  # K = 0: zeros
+    torch.cuda.synchronize()
+    assert not y.any()
