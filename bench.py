@@ -19,9 +19,11 @@ Printed (rank 0, one JSON line on stdout):
                 nvfp4, mxfp4, iq4_nl), each timed back to back over buffer
                 sets larger than L2 and as one launch after an L2 eviction;
   per_workload_next_formats
-                the same for the other simple gguf profiles (q4_1, q5_0,
-                q5_1, q8_1, q8_k, q2_k, q3_k, q5_k, iq4_xs, tq1_0, tq2_0,
-                q1_0, q2_0), each on one [14336,4096] tensor -> bf16.
+                the same for every other gguf and NInfer format, each on one
+                [14336,4096] tensor -> bf16;
+  fused_matmul  decode fused into its consumer (ndq_matmul_packed) against
+                decode-to-bf16 + cuBLAS: one whole-model generation step
+                (M = 1) and single tensors at M = 1 and 8.
 
 `--impl reference` times the CPU oracle (the parity reference) on the host
 cores instead, on a bounded sample of the same workload per step.
@@ -63,6 +65,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-groups", type=int, default=32, help="tensor groups pipelined in the end-to-end leg")
     ap.add_argument("--no-workloads", action="store_true", help="skip the single-format workload table")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused decode + product figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-fraction", type=int, default=1,
@@ -314,6 +317,89 @@ def time_single_workloads(torch, ndq, stream, peak, workloads):
     return out
 
 
+def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
+    """Decode fused into its consumer (ndq_matmul_packed), M = 1 activation
+    row: one generation step of the whole model (one fused product per
+    weight tensor, 225 launches replayed as a CUDA graph) against the
+    unfused path on the same payloads (the batched decode to bf16, then one
+    cuBLAS bf16 product per tensor, also as a graph).  Also single tensors
+    at M = 1 and M = 8.  Weight operand: the exact binary32 decode."""
+    specs = work.specs
+    ks = sorted({s.shape[1] for s in specs})
+    xs = {k: torch.randn(1, k, device="cuda").to(torch.bfloat16) for k in ks}
+    n_out = sum(s.shape[0] for s in specs)
+    y_f = torch.empty(n_out, dtype=torch.float32, device="cuda")
+    y_u = torch.empty(n_out, dtype=torch.bfloat16, device="cuda")
+    views, wviews = [], []
+    o = 0
+    for i, s in enumerate(specs):
+        N, K = s.shape
+        views.append((s.fmt, x_dev[work.x_off[i]:work.x_off[i] + work.x_len[i]], N, K, y_f[o:o + N].view(1, N),
+                      y_u[o:o + N].view(1, N)))
+        wviews.append(y_dev[work.y_off[i] // 2:work.y_off[i] // 2 + work.nel[i]].view(N, K))
+        o += N
+
+    def fused():
+        for fmt, w, N, K, yf, _ in views:
+            ndq.matmul_packed(fmt, w, N, K, xs[K], y=yf)
+
+    def gemvs():
+        for (fmt, w, N, K, _, yu), wb in zip(views, wviews):
+            torch.matmul(xs[K], wb.t(), out=yu)
+
+    def decode():
+        ndq.dequantize_packed_batched([(s.fmt, s.shape, views[i][1], wviews[i]) for i, s in enumerate(specs)])
+
+    def graph_of(fn):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def timed(fn, n=reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / n
+
+    g_fused, g_gemv = graph_of(fused), graph_of(gemvs)
+    t_f = timed(g_fused.replay)
+    t_g = timed(g_gemv.replay)
+    t_d = timed(decode)
+    whole = {"fused_ms": round(t_f, 4), "unfused_ms": round(t_d + t_g, 4), "unfused_decode_ms": round(t_d, 4),
+             "unfused_cublas_ms": round(t_g, 4), "speedup": round((t_d + t_g) / t_f, 3),
+             "launches": len(specs), "payload_GB/s": round(work.bytes_in / (t_f * 1e-3) / 1e9, 1),
+             "weights/s": float(f"{work.elements / (t_f * 1e-3):.4g}"),
+             "what": "one generation step (M=1) over all 225 weight tensors, each a CUDA graph of per-tensor launches"}
+
+    single = {}
+    for fmt, N, K in (("gguf:q4_k", 4096, 4096), ("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336),
+                      ("gguf:q8_0", 128256, 4096)):
+        i = next(j for j, s in enumerate(specs) if s.fmt == fmt and s.shape == (N, K))
+        w, wb = views[i][1], wviews[i]
+        for M in (1, 8):
+            x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            yf = torch.empty(M, N, device="cuda")
+            yb = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            tf = timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf))
+            tu = timed(lambda: (ndq.dequantize_packed(fmt, (N, K), w, torch.bfloat16, y=wb),
+                                torch.matmul(x, wb.t(), out=yb)))
+            single[f"{fmt.split(':')[-1]}[{N},{K}] M={M}"] = {"fused_us": round(tf * 1e3, 1),
+                                                                "unfused_us": round(tu * 1e3, 1),
+                                                                "speedup": round(tu / tf, 3)}
+    return {"whole_model_m1": whole, "single": single,
+            "l2": "payloads of 5.9 GB per step (whole model); single tensors back to back (the 33-560 MB payload "
+                  "and its decoded copy partly stay in L2)"}
+
+
 def run_only(args, torch, ndq):
     """One single-format workload, --warmup untimed then --steps timed
     launches (used for focused profiling of one format)."""
@@ -529,10 +615,12 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = end_to_end(args, torch, ndq, work, x_host, x_dev, y_dev, stream, world, step_bytes)
 
-    per_workload = per_workload_next = None
+    per_workload = per_workload_next = fused = None
     if not args.no_workloads and rank == 0:
         per_workload = time_single_workloads(torch, ndq, stream, peak, synth.WORKLOADS)
         per_workload_next = time_single_workloads(torch, ndq, stream, peak, synth.NEXT_WORKLOADS)
+    if not args.no_fused and rank == 0 and not (args.layers != 32 or args.no_embedding):
+        fused = time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev)
 
     cpu = None
     if not args.no_cpu and rank == 0:
@@ -560,7 +648,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "peak_source": peak_src,
                      "kernel": "k_decode (batched; step time includes the 2 KB descriptor-table upload kernel)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
-        "per_workload": per_workload, "per_workload_next_formats": per_workload_next,
+        "per_workload": per_workload, "per_workload_next_formats": per_workload_next, "fused_matmul": fused,
     }
     if world > 1:
         torch.distributed.destroy_process_group()
