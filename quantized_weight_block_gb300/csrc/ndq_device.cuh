@@ -65,7 +65,10 @@ struct StageInfo {
     uint32_t nb;      // blocks in the tile
     uint32_t phase;   // byte offset of the first block within the stage (0..15)
     uint32_t nv_tab;  // nvfp4: the whole tile uses the divisor the shared table was built for
-    uint32_t pad[11];
+    uint32_t pad_;
+    uint64_t row0;    // fp8 rows: row and column of the tile's first code
+    uint64_t col0;
+    uint32_t pad[6];
 };
 static_assert(sizeof(StageInfo) == 128, "StageInfo layout");
 
@@ -253,6 +256,8 @@ struct Ctx {
     uint64_t blocks_per_div;
     const IqGrids* grids;  // IQ codebooks
     uint64_t n_el;         // fp8 rows: codes in the tensor (the last 16-code unit may be partial)
+    uint64_t row0;         // fp8 rows: row and column of the code at block0
+    uint64_t col0;
 };
 
 __host__ __device__ constexpr bool is_fp8_row(int f) { return f == KF_FP8_ROW_BF16 || f == KF_FP8_ROW_FP16; }
@@ -1144,7 +1149,17 @@ struct Fp8Row {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         const uint64_t K = x.blocks_per_div;
         const uint64_t e0 = (x.block0 + c) * 16u;
-        uint64_t row = e0 / K, col = e0 - row * K;
+        // row and column from the tile's first code (row0, col0): the offset
+        // exceeds K only by a few rows, found by a 32-bit division when
+        // everything fits in 32 bits
+        uint64_t row = x.row0, col = x.col0 + 16u * c;
+        if (col >= K) {
+            const uint64_t q = ((col | K) >> 32) == 0 ? static_cast<uint64_t>(static_cast<uint32_t>(col) /
+                                                                             static_cast<uint32_t>(K))
+                                                      : col / K;
+            row += q;
+            col -= q * K;
+        }
         float s = row_multiplier<BF>(x.divs, row);
         if (col + 16u <= K) {
 #pragma unroll
@@ -1442,6 +1457,11 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
             if (plane < span) span = static_cast<uint32_t>(plane);
         }
         const uint32_t bytes = (phase + span + 15u) & ~15u;
+        if (t.fmt == KF_FP8_ROW_BF16 || t.fmt == KF_FP8_ROW_FP16) {  // one division per tile
+            const uint64_t e0 = b0 * 16u;
+            si.row0 = e0 / t.blocks_per_div;
+            si.col0 = e0 - si.row0 * t.blocks_per_div;
+        }
         si.block0 = b0;
         si.nb = nb;
         si.phase = phase;
@@ -1554,13 +1574,13 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
         const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
         if (si.phase != 0u || (nv && !si.nv_tab)) {
             const Ctx xs{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids,
-                         code_count(si.t)};
+                         code_count(si.t), si.row0, si.col0};
             if (FSEL >= 0)
                 decode_tile_slow_one<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, xs, tid);
             else
                 decode_tile_slow(si, in, xs, tid);
         } else {
-            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t)}, tid);
+            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t), si.row0, si.col0}, tid);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&H.empty[s]);

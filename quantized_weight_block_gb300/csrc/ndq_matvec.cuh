@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_matvec(const MvParams p) {
 
     const uint32_t lane = tid & 31u, warp = tid >> 5;
     const DevTensor& t = p.w;
-    const Ctx base{&H, nullptr, t.divs, 0, t.blocks_per_div, p.grids, code_count(t)};
+    const Ctx base{&H, nullptr, t.divs, 0, t.blocks_per_div, p.grids, code_count(t), 0, 0};
     const uint64_t R = static_cast<uint64_t>(p.rows_per_stage);
     const uint64_t seg = R > 1 ? p.bpr : static_cast<uint64_t>(t.bpt);
     const uint64_t units = (p.n_rows + R - 1) / R;
@@ -211,6 +211,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_matvec(const MvParams p) {
             const uint8_t* in = inbuf + s * kInStride;
             Ctx x = base;
             x.block0 = st.block0;
+            x.row0 = st.row;  // fp8 rows: the unit's first code is at (row, k0)
+            x.col0 = st.k0;
             mv_tile<F, !ALIGNED, MT>(st, in, x, tid, p, acc);
             if (st.last && g < st.nrows) {
                 // warp partials, then the last warp of the row group adds the
