@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--e2e-groups", type=int, default=32, help="tensor groups pipelined in the end-to-end leg")
     ap.add_argument("--no-workloads", action="store_true", help="skip the single-format workload table")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused decode + product figures")
+    ap.add_argument("--only-fused", default=None, metavar="FMT,N,K,M",
+                    help="time one fused decode + product (weights FMT [N,K], M activation rows) for --steps "
+                         "launches and exit (for focused profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-fraction", type=int, default=1,
@@ -400,6 +403,30 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
                   "and its decoded copy partly stay in L2)"}
 
 
+def run_only_fused(args, torch, ndq):
+    """One fused decode + product, --warmup untimed then --steps timed launches."""
+    fmt, N, K, M = args.only_fused.split(",")
+    N, K, M = int(N), int(K), int(M)
+    w = torch.from_numpy(synth.payload(fmt, (N, K), 3)).cuda()
+    x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    y = torch.empty(M, N, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ndq.matmul_packed(fmt, w, N, K, x, y=y)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        ndq.matmul_packed(fmt, w, N, K, x, y=y)
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"fused": args.only_fused, "us_per_launch": round(ms * 1e3, 2),
+                      "weights/s": float(f"{N * K / (ms * 1e-3):.4g}"),
+                      "payload_GB/s": round(w.numel() / (ms * 1e-3) / 1e9, 1), "steps": args.steps,
+                      "l2": "back-to-back launches on one payload"}), flush=True)
+
+
 def run_only(args, torch, ndq):
     """One single-format workload, --warmup untimed then --steps timed
     launches (used for focused profiling of one format)."""
@@ -552,6 +579,8 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_src = measured_peaks()
     if args.only:
         return run_only(args, torch, ndq)
+    if args.only_fused:
+        return run_only_fused(args, torch, ndq)
     specs = synth.llama3_8b_tensors()
     if args.layers != 32 or args.no_embedding:
         specs = [t for t in specs if (t.name.startswith("layers.") and int(t.name.split(".")[1]) < args.layers)
