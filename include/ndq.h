@@ -209,11 +209,14 @@ typedef struct ndq_tensor_desc {
  *                 is that decode rounded once to bfloat16 (the operand of an
  *                 unfused decode-to-bf16 and bf16 product)
  *   y             device output [M, N], row-major, NDQ_FLOAT or NDQ_BFLOAT16
- * Products and sums are binary32 (fused multiply-adds) in an unspecified
- * but fixed order, so repeated calls give identical bits; each output is
- * within 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then
- * rounded once to out_dtype.  Rows of X are processed in passes of up to 8
- * (each pass reads the payload once).  Same ownership, asynchrony and error
+ * Products and sums are binary32 in an unspecified but fixed order, so
+ * repeated calls give identical bits; each output is within
+ * 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then rounded once
+ * to out_dtype.  Up to 8 rows of X are processed per pass on the CUDA cores
+ * (fused multiply-adds; each pass reads the payload once); with
+ * NDQ_BFLOAT16 weights, more than 8 rows, X 16-byte aligned and K % 8 == 0
+ * the product runs on the tensor cores (tcgen05, binary32 accumulation in
+ * tensor memory) in one pass.  Same ownership, asynchrony and error
  * rules as ndq_dequantize_packed; M, N or K of 0 is valid (K == 0 writes
  * zeros); NDQ_ERR_BAD_DTYPE for other weight or output types. */
 int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t *w, size_t w_len, const void *x_bf16,

@@ -283,6 +283,27 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
            static_cast<int64_t>(p.rows_per_stage) * 2 * K <= ndq::kTileElems)
         p.rows_per_stage *= 2;
     p.out_bf16 = out_dtype == NDQ_BFLOAT16;
+    // More activation rows than one CUDA-core pass takes, with bfloat16
+    // weights: the tensor-core (tcgen05) product, when X is 16-byte aligned
+    // and K % 8 == 0.
+    if (weight_dtype == NDQ_BFLOAT16 && M > ndq::kMvMaxRows && p.xvec && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+        static_cast<uint64_t>(M) <= UINT32_MAX) {
+        ndq::MmaParams q;
+        std::memset(&q, 0, sizeof(q));
+        q.w = p.w;
+        q.x = x;
+        q.y = y;
+        q.n_rows = p.n_rows;
+        q.K = p.K;
+        q.bpr = p.bpr;
+        q.m_rows = static_cast<uint64_t>(M);
+        q.bn = 16;
+        while (q.bn < 256 && q.bn < static_cast<uint64_t>(M)) q.bn *= 2;
+        q.span_elems = p.w.B > 64 ? p.w.B : 64;
+        q.span_bytes = q.span_elems / p.w.B * p.w.S;
+        q.out_bf16 = p.out_bf16;
+        return ndq::launch_mma(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    }
     for (int64_t m0 = 0; m0 < M; m0 += ndq::kMvMaxRows) {
         p.x = x + static_cast<uint64_t>(m0) * static_cast<uint64_t>(K);
         p.y = static_cast<uint8_t*>(y) + static_cast<uint64_t>(m0) * static_cast<uint64_t>(N) * osize;

@@ -1,7 +1,9 @@
-// Decode kernels specialised for KF_GGUF_NVFP4 (one per output type) and its fused product kernel.
+// Decode kernels specialised for KF_GGUF_NVFP4 (one per output type) and its fused product kernels.
 #include "ndq_matvec.cuh"
+#include "ndq_mma.cuh"
 
 namespace ndq {
 KernelFn kernel_gguf_nvfp4(int osel) { return kernel_row<KF_GGUF_NVFP4>(osel); }
 MvKernelFn matvec_gguf_nvfp4(int variant) { return matvec_kernel<KF_GGUF_NVFP4>(variant); }
+MmaKernelFn mma_gguf_nvfp4() { return mma_kernel<KF_GGUF_NVFP4>(); }
 }  // namespace ndq

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include "ndq_matvec.cuh"
+#include "ndq_mma.cuh"
 
 namespace ndq {
 
@@ -95,6 +96,69 @@ int launch_matvec(const MvParams& p0, void* stream) {
     const unsigned grid = static_cast<unsigned>(units < resident ? units : resident);
     void* args[] = {&p};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
+                         static_cast<cudaStream_t>(stream));
+    return static_cast<int>(e);
+}
+
+MmaKernelFn mma_for(int kfmt) {
+    switch (kfmt) {
+        case KF_FP8_ROW_BF16: return mma_fp8_row_bf16();
+        case KF_FP8_ROW_FP16: return mma_fp8_row_fp16();
+        case KF_GGUF_NVFP4: return mma_gguf_nvfp4();
+        case KF_IQ1_M: return mma_iq1_m();
+        case KF_IQ1_S: return mma_iq1_s();
+        case KF_IQ2_S: return mma_iq2_s();
+        case KF_IQ2_XS: return mma_iq2_xs();
+        case KF_IQ2_XXS: return mma_iq2_xxs();
+        case KF_IQ3_S: return mma_iq3_s();
+        case KF_IQ3_XXS: return mma_iq3_xxs();
+        case KF_IQ4_NL: return mma_iq4_nl();
+        case KF_IQ4_XS: return mma_iq4_xs();
+        case KF_MXFP4: return mma_mxfp4();
+        case KF_NVFP4: return mma_nvfp4();
+        case KF_Q1_0: return mma_q1_0();
+        case KF_Q2_0: return mma_q2_0();
+        case KF_Q2_K: return mma_q2_k();
+        case KF_Q3_K: return mma_q3_k();
+        case KF_Q4_0: return mma_q4_0();
+        case KF_Q4_1: return mma_q4_1();
+        case KF_Q4_G64: return mma_q4_g64();
+        case KF_Q4_K: return mma_q4_k();
+        case KF_Q5_0: return mma_q5_0();
+        case KF_Q5_1: return mma_q5_1();
+        case KF_Q5_G64: return mma_q5_g64();
+        case KF_Q5_K: return mma_q5_k();
+        case KF_Q6_G64: return mma_q6_g64();
+        case KF_Q6_K: return mma_q6_k();
+        case KF_Q8_0: return mma_q8_0();
+        case KF_Q8_1: return mma_q8_1();
+        case KF_Q8_K: return mma_q8_k();
+        case KF_T2_G128: return mma_t2_g128();
+        case KF_TQ1_0: return mma_tq1_0();
+        case KF_TQ2_0: return mma_tq2_0();
+        default: return nullptr;
+    }
+}
+
+int launch_mma(const MmaParams& p0, void* stream) {
+    if (p0.n_rows == 0 || p0.m_rows == 0) return 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    MmaParams p = p0;
+    const int se = device_symbols(dev, &p.fault, &p.grids);
+    if (se != 0) return se;
+    const int f = p.w.fmt;
+    const MmaKernelFn fn = (f >= 0 && f < KF_COUNT) ? mma_for(f) : nullptr;
+    if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    const size_t smem = mma_smem_bytes(p.bn, p.span_bytes);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    const dim3 grid(static_cast<unsigned>((p.n_rows + kMmaRows - 1) / kMmaRows),
+                    static_cast<unsigned>((p.m_rows + p.bn - 1) / p.bn));
+    void* args[] = {&p};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), grid, dim3(kMmaThreads), args, smem,
                          static_cast<cudaStream_t>(stream));
     return static_cast<int>(e);
 }

@@ -1,7 +1,9 @@
-// Decode kernels specialised for KF_Q4_G64 (one per output type) and its fused product kernel.
+// Decode kernels specialised for KF_Q4_G64 (one per output type) and its fused product kernels.
 #include "ndq_matvec.cuh"
+#include "ndq_mma.cuh"
 
 namespace ndq {
 KernelFn kernel_q4_g64(int osel) { return kernel_row<KF_Q4_G64>(osel); }
 MvKernelFn matvec_q4_g64(int variant) { return matvec_kernel<KF_Q4_G64>(variant); }
+MmaKernelFn mma_q4_g64() { return mma_kernel<KF_Q4_G64>(); }
 }  // namespace ndq

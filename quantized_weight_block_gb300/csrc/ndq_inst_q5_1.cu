@@ -1,7 +1,9 @@
-// Decode kernels specialised for gguf:q5_1 (one per output type) and its fused product kernel.
+// Decode kernels specialised for gguf:q5_1 (one per output type) and its fused product kernels.
 #include "ndq_matvec.cuh"
+#include "ndq_mma.cuh"
 
 namespace ndq {
 KernelFn kernel_q5_1(int osel) { return kernel_row<KF_Q5_1>(osel); }
 MvKernelFn matvec_q5_1(int variant) { return matvec_kernel<KF_Q5_1>(variant); }
+MmaKernelFn mma_q5_1() { return mma_kernel<KF_Q5_1>(); }
 }  // namespace ndq

@@ -1,7 +1,9 @@
-// Decode kernels specialised for gguf:tq1_0 (one per output type) and its fused product kernel.
+// Decode kernels specialised for gguf:tq1_0 (one per output type) and its fused product kernels.
 #include "ndq_matvec.cuh"
+#include "ndq_mma.cuh"
 
 namespace ndq {
 KernelFn kernel_tq1_0(int osel) { return kernel_row<KF_TQ1_0>(osel); }
 MvKernelFn matvec_tq1_0(int variant) { return matvec_kernel<KF_TQ1_0>(variant); }
+MmaKernelFn mma_tq1_0() { return mma_kernel<KF_TQ1_0>(); }
 }  // namespace ndq

@@ -140,6 +140,61 @@ struct MvParams {
 
 using MvKernelFn = void (*)(MvParams);
 
+// Decode fused into a tensor-core (tcgen05) product (ndq_mma.cuh): tiles of
+// 128 weight rows by bn activation rows, the weights rounded to bfloat16.
+struct MmaParams {
+    DevTensor w;          // the weight payload as a decode descriptor (y unused)
+    const uint16_t* x;    // bfloat16 activations [m_rows, K], 16-byte aligned, K % 8 == 0
+    void* y;              // outputs [m_rows, N]
+    uint64_t n_rows;      // N
+    uint64_t K;
+    uint64_t bpr;         // payload blocks per weight row
+    uint64_t m_rows;      // M
+    uint32_t bn;          // activation rows per CTA: 16, 32, 64, 128 or 256
+    uint32_t span_elems;  // weights per staged span: max(B, 64), whole blocks
+    uint32_t span_bytes;  // payload bytes of a full span
+    int32_t out_bf16;
+    unsigned int* fault;
+    const IqGrids* grids;
+};
+using MmaKernelFn = void (*)(MmaParams);
+MmaKernelFn mma_fp8_row_bf16();
+MmaKernelFn mma_fp8_row_fp16();
+MmaKernelFn mma_gguf_nvfp4();
+MmaKernelFn mma_iq1_m();
+MmaKernelFn mma_iq1_s();
+MmaKernelFn mma_iq2_s();
+MmaKernelFn mma_iq2_xs();
+MmaKernelFn mma_iq2_xxs();
+MmaKernelFn mma_iq3_s();
+MmaKernelFn mma_iq3_xxs();
+MmaKernelFn mma_iq4_nl();
+MmaKernelFn mma_iq4_xs();
+MmaKernelFn mma_mxfp4();
+MmaKernelFn mma_nvfp4();
+MmaKernelFn mma_q1_0();
+MmaKernelFn mma_q2_0();
+MmaKernelFn mma_q2_k();
+MmaKernelFn mma_q3_k();
+MmaKernelFn mma_q4_0();
+MmaKernelFn mma_q4_1();
+MmaKernelFn mma_q4_g64();
+MmaKernelFn mma_q4_k();
+MmaKernelFn mma_q5_0();
+MmaKernelFn mma_q5_1();
+MmaKernelFn mma_q5_g64();
+MmaKernelFn mma_q5_k();
+MmaKernelFn mma_q6_g64();
+MmaKernelFn mma_q6_k();
+MmaKernelFn mma_q8_0();
+MmaKernelFn mma_q8_1();
+MmaKernelFn mma_q8_k();
+MmaKernelFn mma_t2_g128();
+MmaKernelFn mma_tq1_0();
+MmaKernelFn mma_tq2_0();
+MmaKernelFn mma_for(int kfmt);
+int launch_mma(const MmaParams& p, void* stream);
+
 // Fused kernels, one per decode family (defined in the instantiation files).
 MvKernelFn matvec_fp8_row_bf16(int variant);
 MvKernelFn matvec_fp8_row_fp16(int variant);

@@ -141,3 +141,45 @@ def test_matmul_validation_and_empty():
                                  torch.cuda.current_stream().cuda_stream) == 0  # K = 0: zeros
     torch.cuda.synchronize()
     assert not y.any()
+
+
+# ---- the tensor-core (tcgen05) path: bfloat16 weights and M > 8 -----------
+TC_FORMATS = ["gguf:q8_0", "gguf:q4_0", "gguf:q4_k", "gguf:q6_k", "gguf:iq4_nl", "gguf:mxfp4", "nvfp4",
+              "gguf:q2_k", "gguf:iq2_xs", "gguf:iq1_m", "q4_g64_fp16", "q5_g64_fp16", "t2_g128_fp16",
+              "fp8_e4m3fn_row_bf16"]
+
+
+@pytest.mark.parametrize("fmt", TC_FORMATS)
+@pytest.mark.parametrize("M", [9, 16, 37, 256, 300])
+def test_tensor_core_product(orc, fmt, M):
+    # N not a multiple of the 128-row tile; M across the 16..256 activation
+    # tiles with partial tiles; K = 1280 spans several staged blocks
+    N, K = 200, 1280
+    w = synth.payload(fmt, (N, K), seed=M)
+    x_t, x_bits = _x_bf16(M, K, 7 * M)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "bfloat16")
+    _check(_run(fmt, N, K, M, w, x_t, weights="bfloat16"), ref, yabs, K, what=f"{fmt} M={M}")
+
+
+@pytest.mark.parametrize("fmt,K", [("gguf:q8_0", 96), ("gguf:q4_0", 32), ("q8_g32_fp16", 8192 + 32),
+                                   ("gguf:q4_k", 256), ("gguf:q6_k", 14336), ("fp8_e4m3fn_row_fp16", 48)])
+def test_tensor_core_ragged_k(orc, fmt, K):
+    # K not a multiple of the 64-weight k-step (zero-filled tail), and long K
+    N, M = 130, 20
+    w = synth.payload(fmt, (N, K), seed=K)
+    x_t, x_bits = _x_bf16(M, K, K)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "bfloat16")
+    _check(_run(fmt, N, K, M, w, x_t, weights="bfloat16"), ref, yabs, K, what=f"{fmt} K={K}")
+    _check(_run(fmt, N, K, M, w, x_t, weights="bfloat16", out_dtype=torch.bfloat16), ref, yabs, K, bf16_out=True,
+           what=f"{fmt} K={K} bf16 out")
+
+
+def test_tensor_core_unaligned_payload_and_determinism(orc):
+    fmt, N, K, M = "gguf:q6_k", 256, 2048, 64
+    w = synth.payload(fmt, (N, K), seed=3)
+    x_t, x_bits = _x_bf16(M, K, 3)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "bfloat16")
+    a = _run(fmt, N, K, M, w, x_t, weights="bfloat16", w_off=5)
+    _check(a, ref, yabs, K, what="q6_k w+5")
+    b = _run(fmt, N, K, M, w, x_t, weights="bfloat16", w_off=5)
+    assert np.array_equal(a, b)
