@@ -66,9 +66,9 @@ def parse_args():
     ap.add_argument("--e2e-groups", type=int, default=32, help="tensor groups pipelined in the end-to-end leg")
     ap.add_argument("--no-workloads", action="store_true", help="skip the single-format workload table")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused decode + product figures")
-    ap.add_argument("--only-fused", default=None, metavar="FMT,N,K,M",
-                    help="time one fused decode + product (weights FMT [N,K], M activation rows) for --steps "
-                         "launches and exit (for focused profiling)")
+    ap.add_argument("--only-fused", default=None, metavar="FMT,N,K,M[,bf16]",
+                    help="time one fused decode + product (weights FMT [N,K], M activation rows; binary32 "
+                         "weights, or bfloat16 with ',bf16') for --steps launches and exit (for focused profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-fraction", type=int, default=1,
@@ -405,19 +405,20 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
 
 def run_only_fused(args, torch, ndq):
     """One fused decode + product, --warmup untimed then --steps timed launches."""
-    fmt, N, K, M = args.only_fused.split(",")
+    fmt, N, K, M, *wt = args.only_fused.split(",")
     N, K, M = int(N), int(K), int(M)
+    wdt = torch.bfloat16 if wt and wt[0] == "bf16" else torch.float32
     w = torch.from_numpy(synth.payload(fmt, (N, K), 3)).cuda()
     x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
     y = torch.empty(M, N, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        ndq.matmul_packed(fmt, w, N, K, x, y=y)
+        ndq.matmul_packed(fmt, w, N, K, x, y=y, weight_dtype=wdt)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(args.steps):
-        ndq.matmul_packed(fmt, w, N, K, x, y=y)
+        ndq.matmul_packed(fmt, w, N, K, x, y=y, weight_dtype=wdt)
     b.record(stream)
     b.synchronize()
     ms = a.elapsed_time(b) / args.steps

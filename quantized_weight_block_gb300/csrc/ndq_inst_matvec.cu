@@ -152,14 +152,36 @@ int launch_mma(const MmaParams& p0, void* stream) {
     const int f = p.w.fmt;
     const MmaKernelFn fn = (f >= 0 && f < KF_COUNT) ? mma_for(f) : nullptr;
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
     const size_t smem = mma_smem_bytes(p.bn, p.span_bytes);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
-    const dim3 grid(static_cast<unsigned>((p.n_rows + kMmaRows - 1) / kMmaRows),
-                    static_cast<unsigned>((p.m_rows + p.bn - 1) / p.bn));
+    const uint64_t tiles_n = (p.n_rows + kMmaRows - 1) / kMmaRows;
+    const uint64_t tiles_m = (p.m_rows + p.bn - 1) / p.bn;
+    // Split K over a cluster of up to 8 CTAs until the CTAs cover every SM
+    // (partial tiles of 128 x bn <= 128 binary32 fit over the operand stages);
+    // every CTA keeps at least two spans.
+    const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
+    unsigned split = 1;
+    while (split < 8 && p.bn <= 128 && tiles_n * tiles_m * split < static_cast<uint64_t>(sms) &&
+           spans >= 4u * split)
+        split *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), split);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = split;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     void* args[] = {&p};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), grid, dim3(kMmaThreads), args, smem,
-                         static_cast<cudaStream_t>(stream));
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
     return static_cast<int>(e);
 }
 

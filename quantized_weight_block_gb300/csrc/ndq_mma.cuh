@@ -8,45 +8,70 @@
 // accumulates in binary32 in TMEM.
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M) by BN activation
-// rows (the MMA's N, 16..256) over all of K, in k-steps of 64:
-//   * its 256 threads stage the packed bytes of the tile's rows for a span of
-//     max(B, 64) weights (whole blocks) into shared memory, 16-byte lines at a
-//     time (every line read holds payload bytes), then decode 64-weight slices
-//     of that span with the same Fmt<F> decoders, round them to bfloat16 and
-//     write them as the A operand in the 128-byte-swizzled K-major layout;
-//   * they copy the X slice [BN x 64] as the B operand in the same layout;
+// rows (the MMA's N, 16..256) over its share of K, in k-steps of 64:
+//   * a producer warp bulk-copies, for each span of max(B, 64) weights (whole
+//     blocks), the packed bytes of the tile's 128 rows into a two-stage ring
+//     (one copy per row, rounded out to 16-byte lines that all hold payload
+//     bytes; full/empty mbarriers);
+//   * 8 consumer warps decode 64-weight slices of the staged span with the
+//     same Fmt<F> decoders, round them to bfloat16 and write them as the A
+//     operand in the 128-byte-swizzled K-major layout, and copy the X slice
+//     [BN x 64] as the B operand in the same layout;
 //   * one thread issues four tcgen05.mma (K = 16 each) and commits them to an
 //     mbarrier; two operand stages let the next slice be decoded while the
 //     tensor core works on the current one;
 //   * the epilogue reads the accumulator back with tcgen05.ld (warp w reads
-//     TMEM lanes 32*(w%4).., half of the columns each) and stores Y.
-// Every wait is bounded; a wait that gives up sets the fault word, and the
-// CTA still frees its TMEM before it returns.
+//     TMEM lanes 32*(w%4).., half of the columns each).  With split-K
+//     (gridDim.z > 1, one thread-block cluster per tile) each CTA parks its
+//     partial tile in shared memory and the cluster's rank-0 CTA adds them
+//     in rank order through distributed shared memory, so the result does
+//     not depend on timing.
+// Every wait is bounded; a wait that gives up sets the fault word, the
+// consumers leave their loops together, and the CTA still reaches the
+// cluster barriers and frees its TMEM.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "ndq_device.cuh"
 
 namespace ndq {
+namespace cg = cooperative_groups;
 namespace {
 
-constexpr int kMmaThreads = 256;
-constexpr int kMmaRows = 128;        // weight rows per CTA (MMA M)
-constexpr int kMmaK = 64;            // weights per k-step (one 128-byte swizzle atom of bf16)
+constexpr int kMmaConsumers = 256;               // 8 warps: decode, operands, MMA issue, epilogue
+constexpr int kMmaThreads = kMmaConsumers + 32;  // + one bulk-copy producer warp
+constexpr int kMmaRows = 128;                    // weight rows per CTA (MMA M)
+constexpr int kMmaK = 64;                        // weights per k-step (one 128-byte swizzle atom of bf16)
 constexpr int kMmaATile = kMmaRows * kMmaK * 2;  // 16 KB
-constexpr int kMmaStages = 2;
+constexpr int kMmaStages = 2;                    // operand stages (A, B)
+constexpr int kMmaSpanStages = 2;                // staged packed spans
 
 struct MmaShared {
-    uint64_t mma_bar[kMmaStages];
+    uint64_t full[kMmaSpanStages];   // packed span staged (bulk copies complete)
+    uint64_t empty[kMmaSpanStages];  // every consumer warp is done decoding the span
+    uint64_t mma_bar[kMmaStages];    // the MMAs reading an operand stage are done
     uint32_t tmem;
     uint32_t pad[3];
 };
 
-// Dynamic shared memory: [A x2][B x2][packed rows], each 1024-byte aligned.
+// Dynamic shared memory: [A x2][B x2][packed spans x2][MmaShared], 1024-byte
+// aligned pieces.  After the k-loop the A and B region holds the partial tile
+// (128 x bn binary32) of a split-K reduction.
 __host__ __device__ constexpr uint32_t mma_b_tile(uint32_t bn) { return bn * 128u; }
-__host__ __device__ constexpr uint32_t mma_row_stride(uint32_t span) { return (span + 15u + 15u + 16u) & ~15u; }
+// Staged row stride: room for the span, its byte phase and the decoders'
+// over-read, rounded to an odd number of 16-byte units so that the rows a
+// warp decodes at once spread over the shared-memory banks.
+__host__ __device__ constexpr uint32_t mma_row_stride(uint32_t span) {
+    return (((span + 15u + 15u + 16u) & ~15u) / 16u % 2u == 0u) ? ((span + 15u + 15u + 16u) & ~15u) + 16u
+                                                               : ((span + 15u + 15u + 16u) & ~15u);
+}
+__host__ __device__ constexpr uint32_t mma_span_stage(uint32_t span) {
+    return (kMmaRows * mma_row_stride(span) + 1023u) & ~1023u;
+}
 __host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span) {
-    return 1024u + kMmaStages * kMmaATile + kMmaStages * mma_b_tile(bn) +
-           ((kMmaRows * mma_row_stride(span) + 1023u) & ~1023u) + 1024u;
+    return 1024u + kMmaStages * kMmaATile + kMmaStages * mma_b_tile(bn) + kMmaSpanStages * mma_span_stage(span) +
+           1024u;
 }
 
 // K-major 128-byte swizzle: row r, 16-byte unit u (8 units per 128-byte row).
@@ -80,18 +105,93 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Barrier of the 256 consumer threads (named barrier 1) that also ORs a
+// fault flag across them, so that they all leave a loop together.
+__device__ __forceinline__ bool consumers_sync_or(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
+        "bar.red.or.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(flag ? 1u : 0u), "n"(kMmaConsumers)
+        : "memory");
+    return r != 0;
+}
+
+// TMEM -> registers: 8 consecutive binary32 columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// The span range [sp0, sp1) of packed spans this CTA covers (split-K over
+// blockIdx.z).
+__device__ __forceinline__ void mma_span_range(const MmaParams& p, uint64_t& sp0, uint64_t& sp1) {
+    const uint64_t ns = (p.K + p.span_elems - 1) / p.span_elems;
+    sp0 = ns * blockIdx.z / gridDim.z;
+    sp1 = ns * (blockIdx.z + 1) / gridDim.z;
+}
+
+__device__ void mma_producer(const MmaParams& p, MmaShared& S, uint8_t* sP, uint32_t rstride, uint32_t stage_bytes) {
+    const DevTensor& t = p.w;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
+    uint64_t sp0, sp1;
+    mma_span_range(p, sp0, sp1);
+    int issued = 0;
+    bool fault = false;
+    for (uint64_t sp = sp0; sp < sp1; ++sp, ++issued) {
+        const int s = issued % kMmaSpanStages;
+        if (issued >= kMmaSpanStages &&
+            !mbar_wait_bounded(&S.empty[s], static_cast<uint32_t>(((issued / kMmaSpanStages) - 1) & 1))) {
+            fault = true;
+            break;
+        }
+        const uint64_t k0 = sp * p.span_elems;
+        const uint64_t kleft = p.K - k0;
+        const uint32_t span = static_cast<uint32_t>((kleft < p.span_elems ? kleft : p.span_elems) / t.B * t.S);
+        uint32_t mine = 0;
+        for (uint32_t r = lane; r < kMmaRows; r += 32) {
+            const uint64_t n = n0 + r;
+            if (n < p.n_rows) {
+                const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
+                mine += (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u) + span + 15u) & ~15u;
+            }
+        }
+        const uint32_t total = __reduce_add_sync(0xffffffffu, mine);
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[s], total);
+        __syncwarp();
+        for (uint32_t r = lane; r < kMmaRows; r += 32) {
+            const uint64_t n = n0 + r;
+            if (n < p.n_rows) {
+                const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
+                const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+                bulk_load(sP + s * stage_bytes + r * rstride, src - ph, (ph + span + 15u) & ~15u, &S.full[s]);
+            }
+        }
+    }
+    if (fault) {
+        if (lane == 0) atomicOr(p.fault, 1u);
+        for (int j = issued - kMmaSpanStages; j < issued; ++j)
+            if (j >= 0) mbar_wait_bounded(&S.full[j % kMmaSpanStages], static_cast<uint32_t>((j / kMmaSpanStages) & 1));
+    }
+}
+
 template <int F>
 __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     using Fm = Fmt<F>;
     constexpr int CE = Fm::CE;
     extern __shared__ __align__(1024) uint8_t mma_smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023u) & ~uintptr_t(1023));
-    const uint32_t bn = static_cast<uint32_t>(p.bn);
+    const uint32_t bn = p.bn;
     uint8_t* sA = base;
     uint8_t* sB = base + kMmaStages * kMmaATile;
     uint8_t* sP = sB + kMmaStages * mma_b_tile(bn);
     const uint32_t rstride = mma_row_stride(p.span_bytes);
-    MmaShared& S = *reinterpret_cast<MmaShared*>(sP + ((kMmaRows * rstride + 1023u) & ~1023u));
+    const uint32_t stage_bytes = mma_span_stage(p.span_bytes);
+    MmaShared& S = *reinterpret_cast<MmaShared*>(sP + kMmaSpanStages * stage_bytes);
     __shared__ SmemHdr H;  // the decoders' 16-entry tables
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
@@ -102,6 +202,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
+        for (int s = 0; s < kMmaSpanStages; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], kMmaConsumers / 32);
+        }
         for (int s = 0; s < kMmaStages; ++s) mbar_init(&S.mma_bar[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -113,114 +217,131 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem;
+    bool fault = false;
+    bool issued_any = false;  // this CTA issued at least one MMA (its accumulator is defined)
 
-    const DevTensor& t = p.w;
+    if (tid >= kMmaConsumers) {
+        mma_producer(p, S, sP, rstride, stage_bytes);
+    } else {
+        const DevTensor& t = p.w;
+        const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
+        const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
+        const uint32_t r = tid & (kMmaRows - 1);  // this thread's weight row in the tile
+        const uint32_t half = tid >> 7;           // which half of the row's chunks it decodes
+        const uint64_t n = n0 + r;
+        const bool row_ok = n < p.n_rows;
+        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) | ((kMmaRows >> 4) << 24);
+        Ctx x{&H, nullptr, t.divs, 0, t.blocks_per_div, p.grids, code_count(t), n, 0};
+        uint64_t sp0, sp1;
+        mma_span_range(p, sp0, sp1);
+        uint64_t kbi = 0;  // k-steps issued by this CTA
+        constexpr uint32_t kChunks = kMmaK / CE;
+        const uint32_t xunits = bn * 8u;  // 16-byte units of the X slice
+        for (uint64_t sp = sp0; sp < sp1 && !fault; ++sp) {
+            const uint64_t i = sp - sp0;
+            const int s = static_cast<int>(i % kMmaSpanStages);
+            const bool ok = mbar_wait_bounded(&S.full[s], static_cast<uint32_t>((i / kMmaSpanStages) & 1u));
+            if (consumers_sync_or(!ok)) {
+                fault = true;
+                break;
+            }
+            const uint64_t k0s = sp * p.span_elems;
+            const uint64_t kend = (k0s + p.span_elems < p.K) ? k0s + p.span_elems : p.K;
+            const uint8_t* row_in = sP + s * stage_bytes + r * rstride;
+            const uint32_t ph = static_cast<uint32_t>(
+                reinterpret_cast<uintptr_t>(t.x + (n * p.bpr + k0s / t.B) * t.S) & 15u);
+            x.block0 = n * p.bpr + k0s / t.B;
+            x.col0 = k0s;
+            for (uint64_t k0 = k0s; k0 < kend; k0 += kMmaK, ++kbi) {
+                const int b = static_cast<int>(kbi & 1u);
+                bool okb = true;
+                if (kbi >= kMmaStages)  // the MMAs that read operand stage b two k-steps ago are done
+                    okb = mbar_wait_bounded(&S.mma_bar[b], static_cast<uint32_t>(((kbi - kMmaStages) >> 1) & 1u));
+                // the activation slice X[m0 .. m0+bn, k0 .. k0+64) into B[b] by
+                // asynchronous 16-byte copies (zero-filled outside X), which
+                // complete while the weights are decoded
+                uint8_t* bS = sB + b * mma_b_tile(bn);
+                for (uint32_t iu = tid; iu < xunits; iu += kMmaConsumers) {
+                    const uint64_t m = m0 + (iu >> 3), kk = k0 + 8u * (iu & 7u);
+                    const bool in = m < p.m_rows && kk < p.K;
+                    const uint16_t* src = in ? p.x + m * p.K + kk : p.x;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(bS + sw128(iu >> 3, iu & 7u))),
+                                 "l"(src), "r"(in ? 16u : 0u)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                // decode this k-step's 64 weights of row r into A[b] (bf16, swizzled)
+                uint8_t* aS = sA + b * kMmaATile;
+                const uint32_t c_first = static_cast<uint32_t>((k0 - k0s) / CE);
+                for (uint32_t j = half; j < kChunks; j += 2) {
+                    const uint64_t kc = k0 + static_cast<uint64_t>(j) * CE;
+                    uint32_t wb[CE / 2];
+                    if (row_ok && kc < p.K) {
+                        float v[CE];
+                        Fm::template chunk<true>(row_in, ph, c_first + j, v, x);
+#pragma unroll
+                        for (int e = 0; e < CE / 2; ++e) wb[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < CE / 2; ++e) wb[e] = 0u;
+                    }
+#pragma unroll
+                    for (int q = 0; q < CE / 8; ++q)
+                        *reinterpret_cast<uint4*>(aS + sw128(r, j * (CE / 8) + q)) =
+                            make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
+                }
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_fence_before();
+                if (consumers_sync_or(!okb)) {
+                    fault = true;
+                    break;
+                }
+                tc_fence_after();
+                if (tid == 0) {
+                    const uint32_t a0 = smem_addr(aS), b0 = smem_addr(bS);
+#pragma unroll
+                    for (uint32_t q = 0; q < kMmaK / 16; ++q)
+                        mma_bf16(tmem, mma_sdesc(a0 + 32u * q), mma_sdesc(b0 + 32u * q), idesc,
+                                 (kbi > 0 || q > 0) ? 1u : 0u);
+                    mma_commit(&S.mma_bar[b]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[s]);  // this warp no longer reads the span
+        }
+        // the last commit covers every MMA of the CTA
+        if (!fault && kbi > 0) {
+            const uint64_t kl = kbi - 1;
+            const bool ok = mbar_wait_bounded(&S.mma_bar[kl & 1u], static_cast<uint32_t>((kl >> 1) & 1u));
+            fault = consumers_sync_or(!ok);
+        }
+        tc_fence_after();
+        if (fault && lane == 0) atomicOr(p.fault, 4u);
+        issued_any = kbi > 0;
+    }
+
+    // Epilogue.  Warp w < 8 reads TMEM lanes 32*(w%4).. (weight rows) and half
+    // of the columns (activation rows).  With one CTA per tile it stores Y;
+    // with a split-K cluster every CTA parks its partial tile in shared
+    // memory and the cluster's rank-0 CTA adds them in rank order.
+    const bool split = gridDim.z > 1;
+    float* part = reinterpret_cast<float*>(base);  // [128][bn] binary32, over the operand stages
     const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
     const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
-    const uint32_t r = tid & (kMmaRows - 1);  // this thread's weight row in the tile
-    const uint32_t half = tid >> 7;           // which half of the row's chunks it decodes
-    const uint64_t n = n0 + r;
-    const bool row_ok = n < p.n_rows;
-    const uint64_t kspan = static_cast<uint64_t>(p.span_elems);  // weights per staged span (whole blocks)
-    const uint64_t ksteps = (p.K + kMmaK - 1) / kMmaK;
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) | ((kMmaRows >> 4) << 24);
-    Ctx x{&H, nullptr, t.divs, 0, t.blocks_per_div, p.grids, code_count(t), n, 0};
-    uint32_t phase_row = 0;  // byte phase of this row's staged span
-    bool fault = false;
-
-    for (uint64_t kb = 0; kb < ksteps && !fault; ++kb) {
-        const int s = static_cast<int>(kb & 1u);
-        const uint64_t k0 = kb * kMmaK;
-        bool ok = true;
-        if (kb >= kMmaStages)  // the MMAs that read stage s two steps ago are done
-            ok = mbar_wait_bounded(&S.mma_bar[s], static_cast<uint32_t>(((kb - kMmaStages) >> 1) & 1u));
-        if (__syncthreads_or(!ok)) {  // every thread leaves together
-            fault = true;
-            break;
-        }
-        if (k0 % kspan == 0) {  // stage the packed span [k0, k0 + kspan) of every row
-            __syncthreads();    // every thread is done decoding the previous span
-            const uint64_t kleft = p.K - k0;
-            const uint64_t blocks = (kleft < kspan ? kleft : kspan) / t.B;  // whole blocks (K % B == 0)
-            if (row_ok) {
-                const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
-                const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-                const uint32_t lines = (ph + static_cast<uint32_t>(blocks * t.S) + 15u) >> 4;
-                const uint4* gl = reinterpret_cast<const uint4*>(src - ph);
-                uint4* sl = reinterpret_cast<uint4*>(sP + r * rstride);
-                for (uint32_t i = half; i < lines; i += 2) sl[i] = __ldg(gl + i);
-                phase_row = ph;
-            }
-            x.block0 = n * p.bpr + k0 / t.B;
-            x.col0 = k0;
-            __syncthreads();
-        }
-        // decode this k-step's 64 weights of row r into A[s] (bf16, swizzled)
-        uint8_t* aS = sA + s * kMmaATile;
-        const uint32_t c_first = static_cast<uint32_t>((k0 % kspan) / CE);
-        constexpr uint32_t kChunks = kMmaK / CE;        // 4 (CE = 16) or 8 (CE = 8)
-        for (uint32_t j = half; j < kChunks; j += 2) {
-            const uint64_t kc = k0 + static_cast<uint64_t>(j) * CE;
-            uint32_t wb[CE / 2];
-            if (row_ok && kc < p.K) {
-                float v[CE];
-                Fm::template chunk<true>(sP + r * rstride, phase_row, c_first + j, v, x);
-#pragma unroll
-                for (int i = 0; i < CE / 2; ++i) wb[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < CE / 2; ++i) wb[i] = 0u;
-            }
-#pragma unroll
-            for (int q = 0; q < CE / 8; ++q)
-                *reinterpret_cast<uint4*>(aS + sw128(r, j * (CE / 8) + q)) =
-                    make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
-        }
-        // the activation slice X[m0 .. m0+bn, k0 .. k0+64] into B[s]
-        uint8_t* bS = sB + s * mma_b_tile(bn);
-        for (uint32_t i = tid; i < bn * 8u; i += kMmaThreads) {
-            const uint32_t rr = i >> 3, u = i & 7u;
-            const uint64_t m = m0 + rr, kk = k0 + 8u * u;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (m < p.m_rows && kk < p.K) v = __ldg(reinterpret_cast<const uint4*>(p.x + m * p.K + kk));
-            *reinterpret_cast<uint4*>(bS + sw128(rr, u)) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t a0 = smem_addr(aS), b0 = smem_addr(bS);
-#pragma unroll
-            for (uint32_t q = 0; q < kMmaK / 16; ++q)
-                mma_bf16(tmem, mma_sdesc(a0 + 32u * q), mma_sdesc(b0 + 32u * q), idesc, (kb > 0 || q > 0) ? 1u : 0u);
-            mma_commit(&S.mma_bar[s]);
-        }
-    }
-    // the last commit covers every MMA of the CTA
-    if (!fault && ksteps > 0) {
-        const uint64_t kl = ksteps - 1;
-        const bool ok = mbar_wait_bounded(&S.mma_bar[kl & 1u], static_cast<uint32_t>((kl >> 1) & 1u));
-        fault = __syncthreads_or(!ok) != 0;
-    }
-    tc_fence_after();
-    if (fault) {
-        if (lane == 0) atomicOr(p.fault, 4u);
-    } else {
-        // epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows), columns
-        // [half*bn/2, (half+1)*bn/2) (activation rows)
-        const uint32_t quarter = warp & 3u, wh = warp >> 2;
-        const uint64_t nn = n0 + 32u * quarter + lane;
-        const uint32_t cbeg = wh * (bn / 2u), cend = cbeg + bn / 2u;
+    const uint32_t quarter = warp & 3u, wh = (warp >> 2) & 1u;
+    const uint32_t row = 32u * quarter + lane;
+    const uint32_t cbeg = wh * (bn / 2u), cend = cbeg + bn / 2u;
+    if (tid < kMmaConsumers) {
+        const uint64_t nn = n0 + row;
         for (uint32_t c0 = cbeg; c0 < cend; c0 += 8) {
             uint32_t v[8];
-            const uint32_t taddr = tmem + ((32u * quarter) << 16) + c0;
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (nn < p.n_rows) {
+            tmem_ld8(tmem + ((32u * quarter) << 16) + c0, v);
+            if (split) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    part[row * bn + c0 + j] = (fault || !issued_any) ? 0.0f : __uint_as_float(v[j]);
+            } else if (!fault && issued_any && nn < p.n_rows) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint64_t m = m0 + c0 + j;
@@ -234,6 +355,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
                 }
             }
         }
+    }
+    if (split) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every CTA's partial tile is in its shared memory
+        if (cluster.block_rank() == 0 && tid < kMmaConsumers) {
+            const uint64_t nn = n0 + row;
+            for (uint32_t c = cbeg; c < cend; ++c) {
+                float sum = part[row * bn + c];
+                for (uint32_t rk = 1; rk < cluster.num_blocks(); ++rk)
+                    sum = __fadd_rn(sum, cluster.map_shared_rank(part, rk)[row * bn + c]);
+                const uint64_t m = m0 + c;
+                if (nn < p.n_rows && m < p.m_rows) {
+                    const uint64_t o = m * p.n_rows + nn;
+                    if (p.out_bf16)
+                        static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(sum);
+                    else
+                        static_cast<float*>(p.y)[o] = sum;
+                }
+            }
+        }
+        cluster.sync();  // rank 0 has read every partial before any CTA exits
     }
     tc_fence_before();
     __syncthreads();
