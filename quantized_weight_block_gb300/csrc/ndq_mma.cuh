@@ -9,10 +9,11 @@
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M) by BN activation
 // rows (the MMA's N, 16..256) over its share of K, in k-steps of 64:
-//   * a producer warp bulk-copies, for each span of max(B, 64) weights (whole
+//   * a producer warp copies, for each span of max(B, 64) weights (whole
 //     blocks), the packed bytes of the tile's 128 rows into a two-stage ring
-//     (one copy per row, rounded out to 16-byte lines that all hold payload
-//     bytes; full/empty mbarriers);
+//     with asynchronous 16-byte copies (rounded out to 16-byte lines that all
+//     hold payload bytes; full/empty mbarriers, each lane's copies counted on
+//     the full barrier as they land);
 //   * 8 consumer warps decode 64-weight slices of the staged span with the
 //     same Fmt<F> decoders, round them to bfloat16 and write them as the A
 //     operand in the 128-byte-swizzled K-major layout, and copy the X slice
@@ -152,25 +153,23 @@ __device__ void mma_producer(const MmaParams& p, MmaShared& S, uint8_t* sP, uint
         const uint64_t k0 = sp * p.span_elems;
         const uint64_t kleft = p.K - k0;
         const uint32_t span = static_cast<uint32_t>((kleft < p.span_elems ? kleft : p.span_elems) / t.B * t.S);
-        uint32_t mine = 0;
-        for (uint32_t r = lane; r < kMmaRows; r += 32) {
-            const uint64_t n = n0 + r;
-            if (n < p.n_rows) {
-                const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
-                mine += (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u) + span + 15u) & ~15u;
-            }
-        }
-        const uint32_t total = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(&S.full[s], total);
-        __syncwarp();
+        // every lane copies the 16-byte lines of rows lane, lane + 32, ...
+        // (asynchronous copies; the lines all hold payload bytes), then has
+        // the full barrier count its arrival once they have landed
         for (uint32_t r = lane; r < kMmaRows; r += 32) {
             const uint64_t n = n0 + r;
             if (n < p.n_rows) {
                 const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
                 const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-                bulk_load(sP + s * stage_bytes + r * rstride, src - ph, (ph + span + 15u) & ~15u, &S.full[s]);
+                const uint32_t lines = (ph + span + 15u) >> 4;
+                const uint8_t* g = src - ph;
+                const uint32_t d = smem_addr(sP + s * stage_bytes + r * rstride);
+                for (uint32_t i = 0; i < lines; ++i)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16u * i), "l"(g + 16u * i)
+                                 : "memory");
             }
         }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&S.full[s])) : "memory");
     }
     if (fault) {
         if (lane == 0) atomicOr(p.fault, 1u);
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     }
     if (tid == 0) {
         for (int s = 0; s < kMmaSpanStages; ++s) {
-            mbar_init(&S.full[s], 1);
+            mbar_init(&S.full[s], 32);  // one arrival per producer lane (cp.async completion)
             mbar_init(&S.empty[s], kMmaConsumers / 32);
         }
         for (int s = 0; s < kMmaStages; ++s) mbar_init(&S.mma_bar[s], 1);
