@@ -155,19 +155,44 @@ int launch_mma(const MmaParams& p0, void* stream) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return static_cast<int>(e);
+    // 256 activation rows per tile unless those tiles fill fewer than half of
+    // the SMs; then 128 (twice the decode per activation row, but K can split)
+    if (p.bn > 128 &&
+        2u * ((p.n_rows + kMmaRows - 1) / kMmaRows) * ((p.m_rows + 255u) / 256u) < static_cast<uint64_t>(sms))
+        p.bn = 128;
     const size_t smem = mma_smem_bytes(p.bn, p.span_bytes);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
     const uint64_t tiles_n = (p.n_rows + kMmaRows - 1) / kMmaRows;
     const uint64_t tiles_m = (p.m_rows + p.bn - 1) / p.bn;
-    // Split K over a cluster of up to 8 CTAs until the CTAs cover every SM
-    // (partial tiles of 128 x bn <= 128 binary32 fit over the operand stages);
-    // every CTA keeps at least two spans.
+    // Split K over a thread-block cluster of up to 8 CTAs (partial tiles of
+    // 128 x bn <= 128 binary32 fit over the operand stages; every CTA keeps
+    // at least two spans): the largest split whose clusters are all resident
+    // at once, as the occupancy calculator counts them for this footprint.
     const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
+    const uint64_t tiles = tiles_n * tiles_m;
     unsigned split = 1;
-    while (split < 8 && p.bn <= 128 && tiles_n * tiles_m * split < static_cast<uint64_t>(sms) &&
-           spans >= 4u * split)
-        split *= 2;
+    for (unsigned c = 2; c <= 8 && p.bn <= 128 && spans >= 2u * c; c *= 2) {
+        cudaLaunchConfig_t probe = {};
+        probe.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), c);
+        probe.blockDim = dim3(kMmaThreads);
+        probe.dynamicSmemBytes = smem;
+        cudaLaunchAttribute pa[1];
+        pa[0].id = cudaLaunchAttributeClusterDimension;
+        pa[0].val.clusterDim.x = 1;
+        pa[0].val.clusterDim.y = 1;
+        pa[0].val.clusterDim.z = c;
+        probe.attrs = pa;
+        probe.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(fn), &probe) != cudaSuccess) {
+            (void)cudaGetLastError();
+            break;
+        }
+        if (tiles > static_cast<uint64_t>(clusters)) break;  // more clusters than fit in one wave
+        split = c;
+    }
+    (void)sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), split);
     cfg.blockDim = dim3(kMmaThreads);

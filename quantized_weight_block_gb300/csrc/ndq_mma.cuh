@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
         const DevTensor& t = p.w;
         const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
         const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
-        const uint32_t r = tid & (kMmaRows - 1);  // this thread's weight row in the tile
-        const uint32_t half = tid >> 7;           // which half of the row's chunks it decodes
+        // two adjacent threads per weight row, so that a warp touches 16 rows
+        // at a time (fewer shared-memory bank conflicts than 32)
+        const uint32_t r = tid >> 1;      // this thread's weight row in the tile
+        const uint32_t half = tid & 1u;   // which half of the row's chunks it decodes
         const uint64_t n = n0 + r;
         const bool row_ok = n < p.n_rows;
         const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) | ((kMmaRows >> 4) << 24);
