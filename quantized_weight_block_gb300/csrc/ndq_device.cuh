@@ -1493,6 +1493,12 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
     float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
     const uint32_t tid = threadIdx.x;
+    // Programmatic dependent launch: this grid may have started before the
+    // previous kernel of the stream finished; wait for it (and the
+    // visibility of its writes) before touching global memory, then let the
+    // next launch start placing its CTAs as this grid's CTAs finish.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {

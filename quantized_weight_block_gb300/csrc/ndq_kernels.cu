@@ -133,8 +133,20 @@ int launch_decode(const KParams& p, void* stream) {
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
     void* args[] = {&q};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
-                         static_cast<cudaStream_t>(stream));
+    // programmatic stream serialization: the kernel waits on the previous
+    // grid itself (griddepcontrol.wait), so its CTAs may be placed as soon as
+    // the previous grid's CTAs retire
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kBlockThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
     return static_cast<int>(e);
 }
 
