@@ -214,7 +214,7 @@ typedef struct ndq_tensor_desc {
  * 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then rounded once
  * to out_dtype.  Up to 8 rows of X are processed per pass on the CUDA cores
  * (fused multiply-adds; each pass reads the payload once); with
- * NDQ_BFLOAT16 weights, more than 8 rows, X 16-byte aligned and K % 8 == 0
+ * NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte aligned and K % 8 == 0
  * the product runs on the tensor cores (tcgen05, binary32 accumulation in
  * tensor memory) in one pass.  Same ownership, asynchrony and error
  * rules as ndq_dequantize_packed; M, N or K of 0 is valid (K == 0 writes

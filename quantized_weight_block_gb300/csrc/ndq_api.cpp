@@ -171,6 +171,9 @@ uint64_t tiles_of(const ndq::DevTensor& t) { return (t.nblocks + t.bpt - 1) / t.
 
 constexpr size_t kWorkspaceAlign = 16;
 
+// Activation rows from which bfloat16-weight products run on the tensor cores.
+constexpr int64_t kTensorCoreMinRows = 6;
+
 }  // namespace
 
 extern "C" {
@@ -283,10 +286,11 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
            static_cast<int64_t>(p.rows_per_stage) * 2 * K <= ndq::kTileElems)
         p.rows_per_stage *= 2;
     p.out_bf16 = out_dtype == NDQ_BFLOAT16;
-    // More activation rows than one CUDA-core pass takes, with bfloat16
-    // weights: the tensor-core (tcgen05) product, when X is 16-byte aligned
-    // and K % 8 == 0.
-    if (weight_dtype == NDQ_BFLOAT16 && M > ndq::kMvMaxRows && p.xvec && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+    // Six or more activation rows with bfloat16 weights: the tensor-core
+    // (tcgen05) product (measured faster than the CUDA-core passes from M = 6
+    // on), when X is 16-byte aligned and K % 8 == 0.
+    if (weight_dtype == NDQ_BFLOAT16 && M >= kTensorCoreMinRows && p.xvec &&
+        (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
         static_cast<uint64_t>(M) <= UINT32_MAX) {
         ndq::MmaParams q;
         std::memset(&q, 0, sizeof(q));

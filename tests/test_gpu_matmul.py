@@ -143,12 +143,12 @@ def test_matmul_validation_and_empty():
     assert not y.any()
 
 
-# ---- the tensor-core (tcgen05) path: bfloat16 weights and M > 8 -----------
+# ---- the tensor-core (tcgen05) path: bfloat16 weights and M >= 6 ----------
 TC_FORMATS = FORMATS
 
 
 @pytest.mark.parametrize("fmt", TC_FORMATS)
-@pytest.mark.parametrize("M", [9, 37, 300])
+@pytest.mark.parametrize("M", [6, 37, 300])
 def test_tensor_core_product(orc, fmt, M):
     # N not a multiple of the 128-row tile; M across the 16..256 activation
     # tiles with partial tiles; K = 1280 spans several staged blocks
