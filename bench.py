@@ -398,7 +398,22 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
             single[f"{fmt.split(':')[-1]}[{N},{K}] M={M}"] = {"fused_us": round(tf * 1e3, 1),
                                                                 "unfused_us": round(tu * 1e3, 1),
                                                                 "speedup": round(tu / tf, 3)}
-    return {"whole_model_m1": whole, "single": single,
+    # bfloat16 weights on the tensor cores (tcgen05) for more activation rows
+    tensor = {}
+    for fmt, N, K in (("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336)):
+        i = next(j for j, s in enumerate(specs) if s.fmt == fmt and s.shape == (N, K))
+        w, wb = views[i][1], wviews[i]
+        for M in (16, 64, 256):
+            x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            yf = torch.empty(M, N, device="cuda")
+            yb = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            tf = timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf, weight_dtype=torch.bfloat16))
+            tu = timed(lambda: (ndq.dequantize_packed(fmt, (N, K), w, torch.bfloat16, y=wb),
+                                torch.matmul(x, wb.t(), out=yb)))
+            tensor[f"{fmt.split(':')[-1]}[{N},{K}] M={M}"] = {
+                "fused_us": round(tf * 1e3, 1), "unfused_us": round(tu * 1e3, 1), "speedup": round(tu / tf, 3),
+                "TFLOP/s": round(2 * M * N * K / (tf * 1e-3) / 1e12, 1)}
+    return {"whole_model_m1": whole, "single": single, "tensor_core_bf16_weights": tensor,
             "l2": "payloads of 5.9 GB per step (whole model); single tensors back to back (the 33-560 MB payload "
                   "and its decoded copy partly stay in L2)"}
 
