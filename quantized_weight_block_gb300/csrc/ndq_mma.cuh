@@ -47,6 +47,7 @@ constexpr int kMmaK = 64;                        // weights per k-step (one 128-
 constexpr int kMmaATile = kMmaRows * kMmaK * 2;  // 16 KB
 constexpr int kMmaStages = 2;                    // operand stages (A, B)
 constexpr int kMmaSpanStages = 2;                // staged packed spans
+constexpr uint32_t kMaxMmaSplit = 8;             // CTAs of a split-K cluster (portable cluster size)
 
 struct MmaShared {
     uint64_t full[kMmaSpanStages];   // packed span staged (bulk copies complete)
@@ -323,11 +324,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     }
 
     // Epilogue.  Warp w < 8 reads TMEM lanes 32*(w%4).. (weight rows) and half
-    // of the columns (activation rows).  With one CTA per tile it stores Y;
-    // with a split-K cluster every CTA parks its partial tile in shared
-    // memory and the cluster's rank-0 CTA adds them in rank order.
+    // of the columns (activation rows).  With one CTA per tile it stores Y.
+    // With a split-K cluster every CTA parks its partial tile in shared
+    // memory, column-major (part[c * 128 + row], so a warp's 32 rows are one
+    // conflict-free line), and rank r then reduces columns
+    // [r*bn/c, (r+1)*bn/c) of every rank's partial, adding them in rank
+    // order so that the result does not depend on timing.
     const bool split = gridDim.z > 1;
-    float* part = reinterpret_cast<float*>(base);  // [128][bn] binary32, over the operand stages
+    float* part = reinterpret_cast<float*>(base);  // [bn][128] binary32, over the operand stages
     const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
     const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
     const uint32_t quarter = warp & 3u, wh = (warp >> 2) & 1u;
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
             if (split) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    part[row * bn + c0 + j] = (fault || !issued_any) ? 0.0f : __uint_as_float(v[j]);
+                    part[(c0 + j) * kMmaRows + row] = (fault || !issued_any) ? 0.0f : __uint_as_float(v[j]);
             } else if (!fault && issued_any && nn < p.n_rows) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -360,23 +364,46 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     if (split) {
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();  // every CTA's partial tile is in its shared memory
-        if (cluster.block_rank() == 0 && tid < kMmaConsumers) {
-            const uint64_t nn = n0 + row;
-            for (uint32_t c = cbeg; c < cend; ++c) {
-                float sum = part[row * bn + c];
-                for (uint32_t rk = 1; rk < cluster.num_blocks(); ++rk)
-                    sum = __fadd_rn(sum, cluster.map_shared_rank(part, rk)[row * bn + c]);
-                const uint64_t m = m0 + c;
-                if (nn < p.n_rows && m < p.m_rows) {
-                    const uint64_t o = m * p.n_rows + nn;
-                    if (p.out_bf16)
-                        static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(sum);
-                    else
-                        static_cast<float*>(p.y)[o] = sum;
+        const uint32_t nr = cluster.num_blocks(), rank = cluster.block_rank();
+        const uint32_t cs = bn * rank / nr, ce = bn * (rank + 1u) / nr;
+        const uint32_t units = (ce - cs) * (kMmaRows / 4u);  // float4 units of this rank's columns
+        if (tid < kMmaConsumers) {
+            const float4* src[kMaxMmaSplit];
+#pragma unroll
+            for (uint32_t rk = 0; rk < kMaxMmaSplit; ++rk)
+                src[rk] = reinterpret_cast<const float4*>(cluster.map_shared_rank(part, rk < nr ? rk : 0u)) +
+                          cs * (kMmaRows / 4u);
+            for (uint32_t u = tid; u < units; u += kMmaConsumers) {
+                float4 pv[kMaxMmaSplit];
+#pragma unroll
+                for (uint32_t rk = 0; rk < kMaxMmaSplit; ++rk)
+                    if (rk < nr) pv[rk] = src[rk][u];
+                float4 s = pv[0];
+#pragma unroll
+                for (uint32_t rk = 1; rk < kMaxMmaSplit; ++rk)
+                    if (rk < nr) {
+                        s.x = __fadd_rn(s.x, pv[rk].x);
+                        s.y = __fadd_rn(s.y, pv[rk].y);
+                        s.z = __fadd_rn(s.z, pv[rk].z);
+                        s.w = __fadd_rn(s.w, pv[rk].w);
+                    }
+                const uint64_t m = m0 + cs + u / (kMmaRows / 4u);
+                const uint64_t nb = n0 + 4u * (u % (kMmaRows / 4u));
+                const float sv[4] = {s.x, s.y, s.z, s.w};
+                if (m < p.m_rows) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (nb + j < p.n_rows) {
+                            const uint64_t o = m * p.n_rows + nb + j;
+                            if (p.out_bf16)
+                                static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(sv[j]);
+                            else
+                                static_cast<float*>(p.y)[o] = sv[j];
+                        }
                 }
             }
         }
-        cluster.sync();  // rank 0 has read every partial before any CTA exits
+        cluster.sync();  // every rank has read the partials before any CTA exits
     }
     tc_fence_before();
     __syncthreads();
