@@ -1265,6 +1265,144 @@ __device__ __forceinline__ void store_partial(void* y, uint64_t e0, const float*
     }
 }
 
+// ---------------------------------------------------------------------------
+// Byte-table decode of nvfp4 to a 16-bit output.  The output of an element
+// depends only on its group's scale byte s, its 4-bit code c and the tile's
+// divisor, so each CTA tabulates the 16-bit result of (s, c) for the codes
+// c < 8 once, computed by the format's own rule (one division) and cast
+// once: row s (16 bytes) holds their high bytes, then their low bytes.  A
+// code c | 8 decodes to the negated value of c: E2M1 word 8 + m is
+// -e2m1(m) (word 8 is -0), the product with the scale is exact, and RNE
+// division and the RNE cast are odd-symmetric.  Decoding is then pure data
+// movement: one prmt looks up 4 codes' high (or low) bytes in the row, the
+// sign bit is flipped from each code's bit 3, and two more prmts pair low
+// and high bytes into output words.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// The table for divisor dw and output type O (row s in words 4s..4s+3 of
+// L), written by threads tid, tid + nthr, ...
+template <int O>
+__device__ __forceinline__ void build_lut16(uint32_t* L, float dw, uint32_t tid, uint32_t nthr) {
+    for (uint32_t i = tid; i < 512u; i += nthr) {
+        const uint32_t s = i >> 1, c0 = 4u * (i & 1u);
+        uint32_t hi = 0, lo = 0;
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j) {
+            const uint32_t c = c0 + j;
+            const float w = __fdiv_rn(__fmul_rn(e2m1(c), e4m3fn(s)), dw);
+            const uint32_t h = (O == KO_BF16) ? (pack_bf16(w, 0.0f) & 0xffffu) : (pack_f16(w, 0.0f) & 0xffffu);
+            hi |= (h >> 8) << (8u * j);
+            lo |= (h & 0xffu) << (8u * j);
+        }
+        L[4u * s + (i & 1u)] = hi;
+        L[4u * s + 2u + (i & 1u)] = lo;
+    }
+}
+
+// Eight codes (the nibbles of q, low nibble first) through table row r.
+// The nibbles of q are codes of elements e0, f0, e1, f1, e2, f2, e3, f3,
+// where e and f are two runs of 4 consecutive outputs: a0 and a1 receive
+// (e0, e1) and (e2, e3), b0 and b1 receive (f0, f1) and (f2, f3), as pairs
+// of 16-bit words (the first element in the low half).
+__device__ __forceinline__ void lut16_word(uint32_t q, uint4 r, uint32_t& a0, uint32_t& a1, uint32_t& b0, uint32_t& b1) {
+    // 0x80 in output byte i where the code in selector nibble i has bit 3
+    // set: prmt's sign-replicating selectors copy the top bit of a source
+    // byte, and the top bits of q << 4 and q are the codes' bit 3.
+    const uint32_t t = q << 4;
+    const uint32_t ma = prmt(t, q, 0xD9C8u) & 0x80808080u, mb = prmt(t, q, 0xFBEAu) & 0x80808080u;
+    const uint32_t sa = q & 0x7777u, sb = (q >> 16) & 0x7777u;  // codes mod 8
+    uint32_t h = prmt(r.x, r.y, sa) ^ ma, l = prmt(r.z, r.w, sa);
+    a0 = prmt(l, h, 0x6240u);
+    b0 = prmt(l, h, 0x7351u);
+    h = prmt(r.x, r.y, sb) ^ mb;
+    l = prmt(r.z, r.w, sb);
+    a1 = prmt(l, h, 0x6240u);
+    b1 = prmt(l, h, 0x7351u);
+}
+
+template <int N>
+__device__ __forceinline__ void store_words16(uint16_t* p, const uint32_t* w, bool vec) {
+    if (vec) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) reinterpret_cast<uint4*>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            p[2 * i] = static_cast<uint16_t>(w[i] & 0xffffu);
+            p[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+        }
+    }
+}
+
+// Formats whose decode is limited by instruction issue rather than by memory
+// (measured): the lane-pair exchange of store16_pairs costs them more than
+// whole-sector stores gain.
+__host__ __device__ constexpr bool issue_bound(int f) {
+    return f == KF_TQ1_0 || f == KF_IQ2_XXS || f == KF_IQ2_XS || f == KF_IQ2_S || f == KF_IQ3_XXS || f == KF_IQ3_S ||
+           f == KF_IQ1_S || f == KF_IQ1_M;
+}
+
+// Stores 16 consecutive 16-bit outputs (words w[0..7]) at element e0 of a
+// 16-byte-aligned y.  Every lane of the warp calls it.  When pair_ok, lanes
+// 2j and 2j+1 hold adjacent chunks (odd: this lane holds the later one) and
+// swap halves so that each store instruction of the pair fills one whole
+// 32-byte sector: lane 2j stores bytes [0,16) then [32,48) of the pair's 64
+// bytes, lane 2j+1 bytes [16,32) then [48,64).  A lane writing its own 32
+// bytes as two 16-byte stores leaves every sector half written per
+// instruction, which on GB300 caps the write rate near 3.8 TB/s (6.5 TB/s
+// with whole sectors).  Otherwise a lane with ok stores its own chunk.
+__device__ __forceinline__ void store16_pairs(uint16_t* y, uint64_t e0, const uint32_t* w, bool odd, bool ok,
+                                              bool pair_ok) {
+    uint32_t ra[4], rb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ra[i] = __shfl_xor_sync(0xffffffffu, w[i], 1);
+        rb[i] = __shfl_xor_sync(0xffffffffu, w[4 + i], 1);
+    }
+    if (pair_ok) {
+        uint16_t* p = y + e0 - (odd ? 8u : 0u);
+        reinterpret_cast<uint4*>(p)[0] = odd ? make_uint4(rb[0], rb[1], rb[2], rb[3]) : make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(p + 16)[0] = odd ? make_uint4(w[4], w[5], w[6], w[7]) : make_uint4(ra[0], ra[1], ra[2], ra[3]);
+    } else if (ok) {
+        reinterpret_cast<uint4*>(y + e0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(y + e0)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// A 16-byte-aligned nvfp4 stage through the table (row s at L[s]).  One
+// group of 16 outputs per chunk: scale byte g of the block, then 8 code
+// bytes whose low nibbles are outputs 0..7 and high nibbles outputs 8..15
+// (the blocks' 36-byte stride keeps them 4-byte aligned).
+__device__ __forceinline__ void decode_tile_lut16(const StageInfo& si, const uint8_t* in, const uint4* L, uint32_t tid) {
+    uint16_t* y = static_cast<uint16_t*>(si.t.y);
+    const bool vec = si.t.yvec != 0;
+    const uint32_t nch = si.nb * 4u;
+#pragma unroll
+    for (int k = 0; k < kTileElems / 16 / kThreads; ++k) {
+        const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
+        const bool ok = c < nch;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (ok) {
+            const uint32_t off = (c >> 2) * 36u, g = c & 3u;
+            const uint32_t s = in[off + g];
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(in + off + 4u + 8u * g);
+            const uint4 r = L[s];
+            lut16_word(qw[0], r, w[0], w[1], w[4], w[5]);
+            lut16_word(qw[1], r, w[2], w[3], w[6], w[7]);
+        }
+        const uint64_t e0 = si.block0 * 64u + 16u * c;
+        if (vec)  // (uniform over the warp)
+            store16_pairs(y, e0, w, c & 1u, ok, (c | 1u) < nch);
+        else if (ok)
+            store_words16<8>(y + e0, w, false);
+    }
+}
+
 template <int F, int O, bool PH>
 __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8_t* in, const Ctx& x, uint32_t tid) {
     using Fm = Fmt<F>;
@@ -1274,10 +1412,32 @@ __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8
     void* y = si.t.y;
     const uint32_t ph = PH ? si.phase : 0u;
     constexpr int kPerThread = kTileElems / Fm::CE / kThreads;  // chunks per thread per tile
+    constexpr bool kPair = (O == KO_BF16 || O == KO_F16) && Fm::CE == 16 && !issue_bound(F);
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) {
         const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
-        if (c < nch) {
+        if (kPair && vec) {
+            // adjacent lanes hold adjacent chunks: store them as sector pairs
+            const bool ok = c < nch;
+            float v[16];
+            if (ok) {
+                Fm::template chunk<PH>(in, ph, c, v, x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+            }
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+            const uint32_t cp = c | 1u;  // the later chunk of the pair
+            bool pair_ok = cp < nch;
+            if (is_fp8_row(F)) pair_ok = pair_ok && e_base + 16ull * cp + 16u <= x.n_el;
+            const uint64_t e0 = e_base + 16ull * c;
+            const bool part = is_fp8_row(F) && ok && e0 + 16u > x.n_el;  // a partial last fp8 unit
+            store16_pairs(static_cast<uint16_t*>(y), e0, w, c & 1u, ok && !part, pair_ok);
+            if (part) store_partial<O>(y, e0, v, static_cast<uint32_t>(x.n_el - e0));
+        } else if (c < nch) {
             float v[Fm::CE];
             Fm::template chunk<PH>(in, ph, c, v, x);
             const uint64_t e0 = e_base + static_cast<uint64_t>(Fm::CE) * c;
@@ -1433,6 +1593,11 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
     int32_t di = 0;   // current tensor (tiles of a CTA increase, so it only moves forward)
     int issued = 0;   // tiles staged so far
     bool fault = false;
+    // nvfp4: the last divisor compared with the shared tables' (tensor,
+    // index), so that a tile whose divisor was seen before issues no load
+    int32_t nv_di = -1;
+    uint64_t nv_d = 0;
+    uint32_t nv_same = 0;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
         const int s = issued % kStages;
         if (issued >= kStages &&
@@ -1468,7 +1633,12 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
         uint32_t nv_tab = 0;
         if (t.fmt == KF_NVFP4 && H.tab_valid) {
             const uint64_t d0 = b0 / t.blocks_per_div, d1 = (b0 + nb - 1u) / t.blocks_per_div;
-            nv_tab = d0 == d1 && __float_as_uint(load_f32_bytes(t.divs + 4u * d0)) == H.tab_bits;
+            if (d0 != nv_d || di != nv_di) {
+                nv_same = __float_as_uint(load_f32_bytes(t.divs + 4u * d0)) == H.tab_bits;
+                nv_d = d0;
+                nv_di = di;
+            }
+            nv_tab = d0 == d1 && nv_same;
         }
         si.nv_tab = nv_tab;
         mbar_arrive_expect_tx(&H.full[s], bytes);
@@ -1493,6 +1663,22 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
     float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
     const uint32_t tid = threadIdx.x;
+    constexpr bool kLut = uses_lut16(FSEL, OSEL);
+
+    // Shared-memory set-up that reads nothing another kernel writes runs
+    // before the wait below, overlapping the previous kernel's tail.
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&H.full[s], 1);
+            mbar_init(&H.empty[s], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < 16) {
+        H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
+        H.lut_v[tid] = static_cast<float>(c_v[tid]);
+    }
+
     // Programmatic dependent launch: this grid may have started before the
     // previous kernel of the stream finished; wait for it (and the
     // visibility of its writes) before touching global memory, then let the
@@ -1500,27 +1686,30 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // nvfp4: the tables are built for the first divisor of the first nvfp4
+    // tensor of the launch; tiles with another divisor divide per element.
+    float dw = 0.0f;
+    if (p.nv_index >= 0) dw = load_f32_bytes((p.table ? p.table[p.nv_index] : p.single).divs);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&H.full[s], 1);
-            mbar_init(&H.empty[s], kConsumerWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        H.tab_valid = 0;
+        H.tab_bits = __float_as_uint(dw);
+        H.tab_valid = p.nv_index >= 0;
     }
-    if (tid < 16) {
-        H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
-        H.lut_v[tid] = static_cast<float>(c_v[tid]);
+    __syncthreads();
+
+    if (tid >= kThreads) {  // producer warp: starts staging while the consumers build the tables
+        if (tid == kThreads) producer(p, H, inbuf);
+        return;
     }
-    // nvfp4: build the quotient table for the first divisor of the first
-    // nvfp4 tensor of the launch; tiles with another divisor divide per element.
-    // Entry 16*s + c is e2m1(c) * e4m3fn(s) / d_w; only codes 0..7 divide: the
-    // entry of c | 8 is the same quotient with the sign bit flipped (RNE
-    // division is odd-symmetric, and (-0)*s/d_w is the negated (+0)*s/d_w).
-    if (p.nv_index >= 0) {
-        const DevTensor& t = p.table ? p.table[p.nv_index] : p.single;
-        const float dw = load_f32_bytes(t.divs);
-        for (uint32_t i = tid; i < kTabEntries / 2; i += kBlockThreads) {
+
+    // Consumer warps only from here; they meet at named barrier 1.
+    if constexpr (kLut) {
+        build_lut16<OSEL>(reinterpret_cast<uint32_t*>(tab), dw, tid, kThreads);
+    } else if (p.nv_index >= 0) {
+        // Entry 16*s + c is e2m1(c) * e4m3fn(s) / d_w; only codes 0..7
+        // divide: the entry of c | 8 is the same quotient with the sign bit
+        // flipped (RNE division is odd-symmetric, and (-0)*s/d_w is the
+        // negated (+0)*s/d_w).
+        for (uint32_t i = tid; i < kTabEntries / 2; i += kThreads) {
             const uint32_t sb = i >> 3, c = i & 7u;
             const float q = __fdiv_rn(__fmul_rn(e2m1(c), e4m3fn(sb)), dw);
             tab[16u * sb + c] = q;
@@ -1538,14 +1727,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
                                         __float_as_uint(scale) | ((tid & 8u) ? 0x80000000u : 0u));
         }
         if (tid < 8) H.nv_ok[tid] = 0u;
-        if (tid == 0) {
-            H.tab_bits = __float_as_uint(dw);
-            H.tab_valid = 1;
-        }
-    }
-    __syncthreads();
-    if (p.nv_index >= 0) {  // verify the per-scale form against the table, scale byte by scale byte
-        for (uint32_t sb = tid; sb < 256u; sb += kBlockThreads) {
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+        // verify the per-scale form against the table, scale byte by scale byte
+        for (uint32_t sb = tid; sb < 256u; sb += kThreads) {
             const float2 q = H.nv_q[sb];
             bool ok = true;
             for (uint32_t c = 0; c < 16u; ++c) {
@@ -1558,12 +1742,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
             if (ok) atomicOr(&H.nv_ok[sb >> 5], 1u << (sb & 31u));
         }
     }
-    __syncthreads();
-
-    if (tid >= kThreads) {  // producer warp
-        if (tid == kThreads) producer(p, H, inbuf);
-        return;
-    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 
     // consumer warps
     const uint64_t grid = gridDim.x;
@@ -1571,7 +1750,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     int it = 0;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
         const int s = it % kStages;
-        if (!mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1))) {
+        // (decided by the whole warp: the decoders shuffle between lanes)
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1)))) {
             if (lane == 0) atomicOr(p.fault, 2u);
             return;
         }
@@ -1579,12 +1759,15 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
         const uint8_t* in = inbuf + s * kInStride;
         const bool nv = (FSEL < 0 || FSEL == KF_NVFP4) && si.t.fmt == KF_NVFP4;
         if (si.phase != 0u || (nv && !si.nv_tab)) {
-            const Ctx xs{&H, si.nv_tab ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div, p.grids,
-                         code_count(si.t), si.row0, si.col0};
+            // (the byte-table kernels hold no quotient table: nvfp4 divides)
+            const Ctx xs{&H, (!kLut && si.nv_tab) ? tab : nullptr, si.t.divs, si.block0, si.t.blocks_per_div,
+                         p.grids, code_count(si.t), si.row0, si.col0};
             if (FSEL >= 0)
                 decode_tile_slow_one<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, xs, tid);
             else
                 decode_tile_slow(si, in, xs, tid);
+        } else if constexpr (kLut) {
+            decode_tile_lut16(si, in, reinterpret_cast<const uint4*>(tab), tid);
         } else {
             decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t), si.row0, si.col0}, tid);
         }

@@ -66,6 +66,20 @@ constexpr int kConsumerWarpsPerCta = kThreads / 32;
 constexpr int kStages = 4;                    // staged tiles in flight per CTA
 constexpr int kInStride = 9472;               // tile bytes + phase + rounding + over-read
 constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
+
+// Launches whose tensors are all nvfp4 with one 16-bit output type decode by
+// byte-table lookup: the 16-bit output of every (scale byte, code) pair,
+// built per CTA in the shared-memory region of the nvfp4 quotient table (4 KB
+// of its 16 KB).  (gguf:nvfp4 and gguf:mxfp4 have the same structure without
+// the division and measured as fast with their 16-entry value table.)
+#if defined(__CUDACC__)
+#define NDQ_HOST_DEVICE __host__ __device__
+#else
+#define NDQ_HOST_DEVICE
+#endif
+NDQ_HOST_DEVICE constexpr bool uses_lut16(int fsel, int osel) {
+    return fsel == KF_NVFP4 && (osel == KO_F16 || osel == KO_BF16);
+}
 // Resident CTAs per SM for launches that mix formats (the whole-model decode):
 // measured fastest at 2 even when registers and shared memory allow 3.
 // Single-format launches use every CTA the occupancy calculator allows.

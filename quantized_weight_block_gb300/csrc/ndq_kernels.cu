@@ -103,10 +103,10 @@ int launch_decode(const KParams& p, void* stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return static_cast<int>(e);
     if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
-    const bool tab = p.nv_index >= 0;
-    const size_t smem = smem_bytes(tab);
     const int fsel = ((p.fsel >= 0 && p.fsel < KF_COUNT) || p.fsel == kFselKQuantMix) ? p.fsel : -1;
     const int osel = (p.osel >= 0 && p.osel <= KO_F64) ? p.osel : -1;
+    const bool tab = p.nv_index >= 0 || uses_lut16(fsel, osel);
+    const size_t smem = smem_bytes(tab);
     const KernelFn fn = pick_kernel(fsel, osel);
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     DeviceInfo& di = g_dev[dev];

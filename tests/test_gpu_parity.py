@@ -116,10 +116,11 @@ def test_nvfp4_every_scale_code_pair(orc):
     for s in range(256):
         blocks.append(np.concatenate([np.full(4, s, np.uint8), codes]))
     blk = np.concatenate(blocks)
-    for dw in (1.0, 26880.0, 3.0, 1e-30, 3e38):
+    for dw in (1.0, 26880.0, 3.0, 1e-30, 3e38, -0.75):
         x = np.concatenate([blk, np.array([dw], "<f4").view(np.uint8)])
-        assert_bit_exact(gpu_decode("nvfp4", (256, 64), x, "float32"), orc.decode("nvfp4", (256, 64), x, "float32"),
-                         "float32", f"dw={dw}")
+        for out in ("float32", "bfloat16", "float16"):
+            assert_bit_exact(gpu_decode("nvfp4", (256, 64), x, out), orc.decode("nvfp4", (256, 64), x, out),
+                             out, f"dw={dw}")
 
 
 @pytest.mark.parametrize("fmt", ["gguf:mxfp4", "gguf:nvfp4"])
