@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import ctypes
 import hashlib
 import json
 import os
@@ -287,15 +288,28 @@ def time_single_workloads(torch, ndq, stream, peak, workloads):
         x0 = torch.from_numpy(x_np).cuda()
         xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
         ys = [torch.empty(shape, dtype=tdt[od], device="cuda") for _ in range(nsets)]
+        # the C ABI with prepared arguments, so that host overhead per call
+        # stays below the kernel time even for the 10 us launches
+        call = ndq._lib.ndq_dequantize_packed
+        fid, oc = ndq.format_id(fmt), ndq.out_dtype_code(tdt[od])
+        sa = (ctypes.c_int64 * len(shape))(*shape)
+        sh = int(stream.cuda_stream)
+        args = [(fid, sa, len(shape), oc, xs[i].data_ptr(), x_np.size, ys[i].data_ptr(), sh) for i in range(nsets)]
+
+        def launch(i):
+            rc = call(*args[i])
+            if rc:
+                raise ndq.NdqError(rc)
+
         for i in range(nsets):
-            ndq.dequantize_packed(fmt, shape, xs[i], tdt[od], y=ys[i])
+            launch(i)
         reps = max(40, 2 * nsets)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for r in range(reps):
-            ndq.dequantize_packed(fmt, shape, xs[r % nsets], tdt[od], y=ys[r % nsets])
+            launch(r % nsets)
         b.record(stream)
         b.synchronize()
         ms = a.elapsed_time(b) / reps
@@ -303,7 +317,7 @@ def time_single_workloads(torch, ndq, stream, peak, workloads):
         for r in range(12):
             flush_sink.copy_(flush.max())
             a.record(stream)
-            ndq.dequantize_packed(fmt, shape, xs[r % nsets], tdt[od], y=ys[r % nsets])
+            launch(r % nsets)
             b.record(stream)
             b.synchronize()
             single.append(a.elapsed_time(b))
