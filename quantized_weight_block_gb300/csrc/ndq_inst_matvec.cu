@@ -172,7 +172,16 @@ int launch_mma(const MmaParams& p0, void* stream) {
     const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
     const uint64_t tiles = tiles_n * tiles_m;
     unsigned split = 1;
-    for (unsigned c = 2; c <= 8 && p.bn <= 128 && spans >= 2u * c; c *= 2) {
+    if (p.bn <= 16) {
+        // Tiles of 16 activation rows: split K until the clusters hold up to
+        // two CTAs per SM.  Measured on GB300: q4_k [14336,4096] 77 -> 59 us
+        // (split 2), q6_k [4096,14336] 78 -> 60 us (split 8).  For wider
+        // tiles the measurements disagreed between shapes (q6_k
+        // [4096,14336] with 64 rows: 84 us at split 4, 131 us at split 8), so
+        // they keep the one-wave rule below.
+        while (split < 8 && spans >= 4u * split && tiles * 2u * split <= 2u * static_cast<uint64_t>(sms)) split *= 2;
+    }
+    for (unsigned c = 2 * split; c <= 8 && p.bn <= 128 && spans >= 2u * c && split == 1; c *= 2) {
         cudaLaunchConfig_t probe = {};
         probe.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), c);
         probe.blockDim = dim3(kMmaThreads);
@@ -192,7 +201,6 @@ int launch_mma(const MmaParams& p0, void* stream) {
         if (tiles > static_cast<uint64_t>(clusters)) break;  // more clusters than fit in one wave
         split = c;
     }
-    (void)sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), split);
     cfg.blockDim = dim3(kMmaThreads);

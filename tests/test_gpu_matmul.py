@@ -181,3 +181,15 @@ def test_tensor_core_unaligned_payload_and_determinism(orc):
     _check(a, ref, yabs, K, what="q6_k w+5")
     b = _run(fmt, N, K, M, w, x_t, weights="bfloat16", w_off=5)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt,N,K", [("gguf:q4_k", 1000, 4096), ("gguf:q6_k", 300, 14336), ("gguf:iq4_nl", 1000, 2048)])
+def test_tensor_core_split_k_16_rows(orc, fmt, N, K):
+    # 16 activation rows per tile: K splits over clusters of up to 8 CTAs
+    M = 16
+    w = synth.payload(fmt, (N, K), seed=N)
+    x_t, x_bits = _x_bf16(M, K, K)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "bfloat16")
+    a = _run(fmt, N, K, M, w, x_t, weights="bfloat16")
+    _check(a, ref, yabs, K, what=f"{fmt} [{N},{K}] M=16")
+    assert np.array_equal(a, _run(fmt, N, K, M, w, x_t, weights="bfloat16"))
