@@ -183,6 +183,24 @@ __device__ __forceinline__ uint32_t lds_4(const uint8_t* base, uint32_t off) {
     return __funnelshift_r(w[0], w[1], (off & 3u) * 8u);
 }
 
+// prmt.b32 (byte permute of {b, a} by the 4-bit selectors in sel[15:0]; a
+// selector's bit 3 replicates the selected byte's top bit).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Two floats to one RNE pair of 16-bit outputs (the first in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // Exact binary16 -> binary32 (the specification's H).
 __device__ __forceinline__ float h2f(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
@@ -807,6 +825,42 @@ struct Fmt<KF_TQ1_0> {
             }
         }
     }
+    // The same chunk as 16-bit outputs of type O (pairs in w[0..7]).  A
+    // block has three outputs, cast(M(d, -1)), cast(M(d, +0)) and
+    // cast(M(d, 1)), held as a 6-byte table; each group of 4 codes (4 bytes
+    // sharing one power 3^p) gets its trits two at a time in 16-bit lanes,
+    // ((b * 3^p) mod 256) * 3 >> 8 (b * 81 < 2^16, so lanes do not carry),
+    // and one prmt per output pair looks up the table.
+    template <bool PH, int O>
+    __device__ __forceinline__ static void chunk16(const uint8_t* in, uint32_t ph, uint32_t c, uint32_t* w,
+                                                   const Ctx&) {
+        const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
+        const float d = h2f(lds_2<PH>(in, off + 52u));
+        const uint32_t start = cc < 10u ? 16u * (cc & 1u) : (cc < 15u ? 32u : 48u);
+        const uint4 q = lds_16<false>(in, off + start);
+        const uint32_t p = cc < 10u ? (cc >> 1) : (cc - 10u);
+        const uint32_t pw = p == 0u ? 1u : p == 1u ? 3u : p == 2u ? 9u : p == 3u ? 27u : 81u;
+        const float dm = __fmul_rn(d, -1.0f), d0 = __fmul_rn(d, 0.0f), d1 = __fmul_rn(d, 1.0f);
+        const uint32_t ta = (O == KO_BF16) ? pack_bf16(dm, d0) : pack_f16(dm, d0);
+        const uint32_t tb = (O == KO_BF16) ? pack_bf16(d1, 0.0f) : pack_f16(d1, 0.0f);
+        const bool last = cc == 15u;  // element i: byte 48 + i%4, power 3^(i/4)
+        const uint32_t g[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t W = last ? q.x : g[k];
+            const uint32_t P = last ? (k == 0 ? 1u : k == 1 ? 3u : k == 2 ? 9u : 27u) : pw;
+            const uint32_t lo = ((W & 0x00FF00FFu) * P) & 0x00FF00FFu;         // bytes 0, 2
+            const uint32_t hi = (((W >> 8) & 0x00FF00FFu) * P) & 0x00FF00FFu;  // bytes 1, 3
+            const uint32_t t = prmt(lo * 3u, hi * 3u, 0x7351u);  // trits of bytes 0..3, one per byte
+            w[2 * k] = prmt(ta, tb, t * 0x22u + 0x1010u);
+            w[2 * k + 1] = prmt(ta, tb, (t >> 16) * 0x22u + 0x1010u);
+        }
+    }
+};
+
+template <int F>
+struct has_chunk16 {
+    static constexpr bool value = F == KF_TQ1_0;
 };
 
 // gguf:tq2_0: y[j] = M(d, v[j] - 1), v = P(q,2,32) (q at byte 0, d at 64).
@@ -1201,14 +1255,6 @@ struct Fmt<KF_FP8_ROW_FP16> {
 // 16-byte aligned (chunk offsets are multiples of 8 elements, so every chunk
 // then starts on a 16-byte boundary).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 template <int O, int N>
 __device__ __forceinline__ void store_chunk(void* y, uint64_t e0, const float* v, bool vec) {
@@ -1278,12 +1324,6 @@ __device__ __forceinline__ void store_partial(void* y, uint64_t e0, const float*
 // sign bit is flipped from each code's bit 3, and two more prmts pair low
 // and high bytes into output words.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
 // The table for divisor dw and output type O (row s in words 4s..4s+3 of
 // L), written by threads tid, tid + nthr, ...
 template <int O>
@@ -1343,8 +1383,8 @@ __device__ __forceinline__ void store_words16(uint16_t* p, const uint32_t* w, bo
 // (measured): the lane-pair exchange of store16_pairs costs them more than
 // whole-sector stores gain.
 __host__ __device__ constexpr bool issue_bound(int f) {
-    return f == KF_TQ1_0 || f == KF_IQ2_XXS || f == KF_IQ2_XS || f == KF_IQ2_S || f == KF_IQ3_XXS || f == KF_IQ3_S ||
-           f == KF_IQ1_S || f == KF_IQ1_M;
+    return f == KF_IQ2_XXS || f == KF_IQ2_XS || f == KF_IQ2_S || f == KF_IQ3_XXS || f == KF_IQ3_S || f == KF_IQ1_S ||
+           f == KF_IQ1_M;
 }
 
 // Stores 16 consecutive 16-bit outputs (words w[0..7]) at element e0 of a
@@ -1420,16 +1460,22 @@ __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8
             // adjacent lanes hold adjacent chunks: store them as sector pairs
             const bool ok = c < nch;
             float v[16];
-            if (ok) {
-                Fm::template chunk<PH>(in, ph, c, v, x);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-            }
             uint32_t w[8];
+            if constexpr (has_chunk16<F>::value) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+                for (int i = 0; i < 8; ++i) w[i] = 0u;
+                if (ok) Fm::template chunk16<PH, O>(in, ph, c, w, x);
+            } else {
+                if (ok) {
+                    Fm::template chunk<PH>(in, ph, c, v, x);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+            }
             const uint32_t cp = c | 1u;  // the later chunk of the pair
             bool pair_ok = cp < nch;
             if (is_fp8_row(F)) pair_ok = pair_ok && e_base + 16ull * cp + 16u <= x.n_el;
