@@ -43,6 +43,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -858,10 +859,7 @@ struct Fmt<KF_TQ1_0> {
     }
 };
 
-template <int F>
-struct has_chunk16 {
-    static constexpr bool value = F == KF_TQ1_0;
-};
+
 
 // gguf:tq2_0: y[j] = M(d, v[j] - 1), v = P(q,2,32) (q at byte 0, d at 64).
 template <>
@@ -1232,6 +1230,43 @@ struct Fp8Row {
             }
         }
     }
+    // The same unit as 16-bit outputs of type O (pairs in w[0..7]).  Every
+    // E4M3FN word, NaN included, is exactly a binary16 value, so the
+    // hardware pair conversion gives the code's value; its binary32 product
+    // with the multiplier is then rounded once, as above.  A unit that
+    // crosses a row boundary takes the element-wise form.
+    template <bool PH, int O>
+    __device__ __forceinline__ static void chunk16(const uint8_t* in, uint32_t ph, uint32_t c, uint32_t* w,
+                                                   const Ctx& x) {
+        const uint64_t K = x.blocks_per_div;
+        uint64_t row = x.row0, col = x.col0 + 16u * c;
+        if (col >= K) {
+            const uint64_t q = ((col | K) >> 32) == 0 ? static_cast<uint64_t>(static_cast<uint32_t>(col) /
+                                                                             static_cast<uint32_t>(K))
+                                                      : col / K;
+            row += q;
+            col -= q * K;
+        }
+        if (col + 16u > K) {
+            float v[16];
+            chunk<PH>(in, ph, c, v, x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+            return;
+        }
+        const uint4 q = lds_16<!PH>(in, ph + 16u * c);
+        const uint32_t cw[4] = {q.x, q.y, q.z, q.w};
+        const float s = row_multiplier<BF>(x.divs, row);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((cw[i >> 1] >> (16 * (i & 1))) & 0xffffu), __NV_E4M3);
+            const float a = __fmul_rn(__half2float(__ushort_as_half(h.x)), s);
+            const float b = __fmul_rn(__half2float(__ushort_as_half(h.y)), s);
+            w[i] = (O == KO_BF16) ? pack_bf16(a, b) : pack_f16(a, b);
+        }
+    }
 };
 template <>
 struct Fmt<KF_FP8_ROW_BF16> {
@@ -1239,6 +1274,11 @@ struct Fmt<KF_FP8_ROW_BF16> {
     template <bool PH>
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx& x) {
         Fp8Row<true>::chunk<PH>(in, ph, c, v, x);
+    }
+    template <bool PH, int O>
+    __device__ __forceinline__ static void chunk16(const uint8_t* in, uint32_t ph, uint32_t c, uint32_t* w,
+                                                   const Ctx& x) {
+        Fp8Row<true>::template chunk16<PH, O>(in, ph, c, w, x);
     }
 };
 template <>
@@ -1248,6 +1288,17 @@ struct Fmt<KF_FP8_ROW_FP16> {
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx& x) {
         Fp8Row<false>::chunk<PH>(in, ph, c, v, x);
     }
+    template <bool PH, int O>
+    __device__ __forceinline__ static void chunk16(const uint8_t* in, uint32_t ph, uint32_t c, uint32_t* w,
+                                                   const Ctx& x) {
+        Fp8Row<false>::template chunk16<PH, O>(in, ph, c, w, x);
+    }
+};
+
+// Decoders that also produce 16-bit outputs directly (chunk16).
+template <int F>
+struct has_chunk16 {
+    static constexpr bool value = F == KF_TQ1_0 || F == KF_FP8_ROW_BF16 || F == KF_FP8_ROW_FP16;
 };
 
 // ---------------------------------------------------------------------------
@@ -1482,7 +1533,10 @@ __device__ __forceinline__ void decode_tile_fop(const StageInfo& si, const uint8
             const uint64_t e0 = e_base + 16ull * c;
             const bool part = is_fp8_row(F) && ok && e0 + 16u > x.n_el;  // a partial last fp8 unit
             store16_pairs(static_cast<uint16_t*>(y), e0, w, c & 1u, ok && !part, pair_ok);
-            if (part) store_partial<O>(y, e0, v, static_cast<uint32_t>(x.n_el - e0));
+            if (part) {
+                if constexpr (has_chunk16<F>::value) Fm::template chunk<PH>(in, ph, c, v, x);
+                store_partial<O>(y, e0, v, static_cast<uint32_t>(x.n_el - e0));
+            }
         } else if (c < nch) {
             float v[Fm::CE];
             Fm::template chunk<PH>(in, ph, c, v, x);
