@@ -167,40 +167,19 @@ int launch_mma(const MmaParams& p0, void* stream) {
     const uint64_t tiles_m = (p.m_rows + p.bn - 1) / p.bn;
     // Split K over a thread-block cluster of up to 8 CTAs (partial tiles of
     // 128 x bn <= 128 binary32 fit over the operand stages; every CTA keeps
-    // at least two spans): the largest split whose clusters are all resident
-    // at once, as the occupancy calculator counts them for this footprint.
+    // at least two spans): the largest split whose CTAs number at most one
+    // per SM, or two per SM for tiles of 16 activation rows.  A sweep of
+    // splits 1-8 on GB300 picked these in five of six cases (q4_k
+    // [14336,4096] at 16 rows: 77 -> 59 us with split 2; q6_k [4096,14336]:
+    // 60 us with split 8 at 16 rows, 84 us with split 4 at 64 rows).  Asking
+    // the occupancy calculator for co-resident clusters instead gave
+    // different splits on different boxes (q6_k [4096,14336] at 64 rows:
+    // split 2 and 155 us on one of them).
     const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
     const uint64_t tiles = tiles_n * tiles_m;
+    const uint64_t max_ctas = (p.bn <= 16 ? 2u : 1u) * static_cast<uint64_t>(sms);
     unsigned split = 1;
-    if (p.bn <= 16) {
-        // Tiles of 16 activation rows: split K until the clusters hold up to
-        // two CTAs per SM.  Measured on GB300: q4_k [14336,4096] 77 -> 59 us
-        // (split 2), q6_k [4096,14336] 78 -> 60 us (split 8).  For wider
-        // tiles the measurements disagreed between shapes (q6_k
-        // [4096,14336] with 64 rows: 84 us at split 4, 131 us at split 8), so
-        // they keep the one-wave rule below.
-        while (split < 8 && spans >= 4u * split && tiles * 2u * split <= 2u * static_cast<uint64_t>(sms)) split *= 2;
-    }
-    for (unsigned c = 2 * split; c <= 8 && p.bn <= 128 && spans >= 2u * c && split == 1; c *= 2) {
-        cudaLaunchConfig_t probe = {};
-        probe.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), c);
-        probe.blockDim = dim3(kMmaThreads);
-        probe.dynamicSmemBytes = smem;
-        cudaLaunchAttribute pa[1];
-        pa[0].id = cudaLaunchAttributeClusterDimension;
-        pa[0].val.clusterDim.x = 1;
-        pa[0].val.clusterDim.y = 1;
-        pa[0].val.clusterDim.z = c;
-        probe.attrs = pa;
-        probe.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(fn), &probe) != cudaSuccess) {
-            (void)cudaGetLastError();
-            break;
-        }
-        if (tiles > static_cast<uint64_t>(clusters)) break;  // more clusters than fit in one wave
-        split = c;
-    }
+    while (split < kMaxMmaSplit && p.bn <= 128 && spans >= 4u * split && tiles * 2u * split <= max_ctas) split *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), split);
     cfg.blockDim = dim3(kMmaThreads);
