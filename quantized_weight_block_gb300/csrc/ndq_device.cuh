@@ -14,12 +14,17 @@
 //    contiguous span) into shared memory with the Tensor Memory Accelerator
 //    (cp.async.bulk, completing on a "full" mbarrier), running up to kStages
 //    tiles ahead; it copies the tile's tensor descriptor next to the bytes;
-//  * eight consumer warps decode 8-element chunks straight from shared
+//  * eight consumer warps decode 16-element chunks straight from shared
 //    memory (the odd block strides of 17, 18, 34, 36 and 210 bytes are
 //    resolved with aligned 32-bit shared loads and funnel shifts), write
-//    each chunk with 16-byte vector stores (a warp covers 512 contiguous
-//    bytes per instruction), and release the stage on an "empty" mbarrier.
-//    Consumers never meet at a CTA-wide barrier inside the loop;
+//    them with 16-byte vector stores arranged so that each store
+//    instruction fills whole 32-byte sectors (adjacent lanes exchange chunk
+//    halves, or decode interleaved runs), and release the stage on an
+//    "empty" mbarrier.  Consumers never meet at a CTA-wide barrier inside
+//    the loop;
+//  * nvfp4 to a 16-bit output looks each (scale byte, code) pair up in a
+//    per-CTA table of its cast decode; tq1_0 and the FP8 row formats decode
+//    16-bit outputs in packed form;
 //  * a span that does not start on a 16-byte boundary (an unaligned payload,
 //    a ragged last tile) is staged from the 16-byte boundary below it to the
 //    one above its end, and decoded at its byte phase within the stage; the
