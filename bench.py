@@ -724,10 +724,12 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.build()
-    fraction = 4096
-    specs = synth.llama3_8b_tensors()
     # a bounded sample with the same field distributions: for every tensor,
-    # 1/fraction of its rows (at least one), generated from the tensor's seed
+    # 1/fraction of its rows (at least one), generated from the tensor's seed;
+    # 1/16 keeps the 225 calls' fixed cost small against the decode itself
+    # (at 1/4096 it was nearly all of a step)
+    fraction = 16
+    specs = synth.llama3_8b_tensors()
     sample = []
     for s in specs:
         rows = max(1, s.shape[0] // fraction)
