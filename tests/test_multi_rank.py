@@ -48,3 +48,26 @@ def test_reference_arm_does_nothing_on_other_ranks(capsys):
         steps, warmup = 1, 0
     bench.run_reference(A(), rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line():
+    # rank 0 runs the CPU oracle on the bounded sample and prints one JSON
+    # line with the contract's keys; its value, cpu_baseline and e2e agree
+    import json
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+                         cwd=bench.ROOT, capture_output=True, text=True, timeout=600, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["vs_baseline"] is None
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["tensors"] == 225
