@@ -235,6 +235,32 @@ def test_batched_mixed(orc):
         assert_bit_exact(got, orc.decode(fmt, shape, x, out), out, f"batched {fmt} {out}")
 
 
+def test_batched_nvfp4_divisors(orc):
+    # one launch of nvfp4 tensors to a 16-bit output (the byte-table kernel):
+    # the table serves the first tensor's divisor, tensors with another
+    # divisor (or several) divide per element, and a tensor whose divisor
+    # equals the first one's uses the table again
+    specs = []
+    for i, (dw, ndiv) in enumerate(((26880.0, 1), (3.0, 1), (26880.0, 1), (0.5, 1), (None, 3))):
+        shape = (3 * (i + 1), 64 * 70)
+        x = synth.payload("nvfp4", shape, seed=60 + i, ndiv=ndiv).copy()
+        if dw is not None:
+            x[-4:] = np.array([dw], "<f4").view(np.uint8)
+        specs.append((shape, x))
+    for out in ("bfloat16", "float16"):
+        items, ys = [], []
+        for shape, x in specs:
+            y = torch.empty(shape, dtype=TORCH_OUT[out], device=DEV)
+            items.append(("nvfp4", shape, torch.from_numpy(x).to(DEV), y))
+            ys.append(y)
+        ws = ndq.dequantize_packed_batched(items)
+        torch.cuda.synchronize()
+        del ws
+        for (shape, x), y in zip(specs, ys):
+            got = y.cpu().view(torch.uint16).numpy()
+            assert_bit_exact(got, orc.decode("nvfp4", shape, x, out), out, f"batched nvfp4 {shape} {out}")
+
+
 def test_repeat_is_deterministic():
     fmt, shape = "gguf:q6_k", (64, 4096)
     x = torch.from_numpy(synth.payload(fmt, shape, seed=1)).to(DEV)
