@@ -17,8 +17,11 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "ndq_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# NDQ_ORACLE_SRC / NDQ_ORACLE_LIB point the oracle at another source and
+# library path; only the mutation tests use them, to check that the pins
+# fail on oracles with planted mistakes.
+_SRC = os.environ.get("NDQ_ORACLE_SRC") or os.path.join(_HERE, "ndq_oracle.c")
+_LIB_PATH = os.environ.get("NDQ_ORACLE_LIB") or os.path.join(_HERE, "_build", "liboracle.so")
 # The IQ codebooks are page data kept as a cited text fixture; the oracle
 # expands them itself (oracle_set_codebook).
 CODEBOOKS_FILE = os.path.join(os.path.dirname(_HERE), "tests", "golden", "iq_codebooks.txt")
