@@ -1,10 +1,11 @@
 """The oracle's pins catch planted mistakes.
 
 Each mutant below is a copy of the oracle's C source with one plausible
-mistake: a wrong exponent bias or scale, a wrong table entry, a transposed
-loop order, a wrong index or offset, a dropped sign, a rounding tie broken
-the wrong way, a reciprocal multiply in place of a division, a dropped
-validation rule.  For each, the oracle's own pin tests (tables, scalars,
+mistake, in the shared helpers or in one format's decoder: a wrong
+exponent bias or scale, a wrong table entry, a transposed loop or bit
+order, a wrong index, offset or sign, a dropped term or parity, a rounding
+tie broken the wrong way, a reciprocal multiply in place of a division, a
+dropped validation rule.  For each, the oracle's own pin tests (tables, scalars,
 formats and the other families) run against the mutant in a subprocess and
 must fail.  CPU only: the mistakes are planted in the oracle, never in the
 CUDA library.
@@ -54,6 +55,38 @@ MUTANTS = [
      "if (0) return OR_ERR_NOT_BLOCK_ALIGNED;"),
     ("nvfp4 divisor count must divide the rows", "if (D < 1 || N % D != 0) return OR_ERR_LENGTH_MISMATCH;",
      "if (D < 1) return OR_ERR_LENGTH_MISMATCH;"),
+    # the other gguf formats
+    ("q4_1 minimum subtracted", "y[j] = A(M(d, (float)v[j]), m);", "y[j] = D(M(d, (float)v[j]), m);"),
+    ("q5_0 offset", "M(d, (float)((int32_t)vj - 16))", "M(d, (float)((int32_t)vj - 15))"),
+    ("q5 high bits in the wrong order", "16u * ((high >> j) & 1u)", "16u * ((high >> (j ^ 1)) & 1u)"),
+    ("q8_1 codes read over the cached sum", "for (int j = 0; j < 32; ++j) y[j] = M(d, (float)signed8(b[4 + j]));",
+     "for (int j = 0; j < 32; ++j) y[j] = M(d, (float)signed8(b[2 + j]));"),
+    ("q8_k scale read as binary16", "float d = or_f32(U(b, 4));", "float d = H(b);"),
+    ("q2_k minimum from the low nibble", "M(dmin, (float)(sc / 16u))", "M(dmin, (float)(sc % 16u))"),
+    ("q3_k mask sense", "4 * (1 - (int32_t)h[j])", "4 * (int32_t)h[j]"),
+    ("q5_k high bit weight", "(float)(v[j] + 16u * hb[j])", "(float)(v[j] + 8u * hb[j])"),
+    ("iq4_xs scale offset", "16 * (int32_t)field(high, 2 * k, 2) - 32;", "16 * (int32_t)field(high, 2 * k, 2) - 31;"),
+    ("tq1_0 trit divisor", "(int32_t)((3u * r) / 256u) - 1", "(int32_t)((3u * r) / 255u) - 1"),
+    ("tq2_0 offset", "for (int j = 0; j < 256; ++j) y[j] = M(d, (float)((int32_t)v[j] - 1));",
+     "for (int j = 0; j < 256; ++j) y[j] = M(d, (float)((int32_t)v[j] - 2));"),
+    ("q1_0 bit sense", "? d : -d;", "? -d : d;"),
+    ("q2_0 plane grouping", "P(b + 2, 16, 2, 1, v);", "P(b + 2, 16, 2, 16, v);"),
+    # the IQ formats
+    ("IQ sign parity dropped", "S8((v & 127u) | ((par % 2u) << 7), s);", "S8((v & 127u) | (0u * par), s);"),
+    ("iq2_xxs scale factor", "A(0.5f, (float)(a >> 28))), 0.25f)", "A(0.5f, (float)(a >> 28))), 0.125f)"),
+    ("iq3_s odd multiplier", "(float)(1u + 2u * field(b[106 + g / 2], 4 * (g % 2), 4))",
+     "(float)(2u * field(b[106 + g / 2], 4 * (g % 2), 4))"),
+    ("iq1_s shift sign", "float delta = field(a, 15, 1) ? -0.125f : 0.125f;",
+     "float delta = field(a, 15, 1) ? 0.125f : -0.125f;"),
+    ("iq1_m scale nibble order", "dbits += (w[k] >> 12) << (4 * k);", "dbits += (w[k] >> 12) << (4 * (3 - k));"),
+    # the other NInfer formats
+    ("grouped two's complement range", "(int32_t)u - (int32_t)(1u << width)",
+     "(int32_t)u - (int32_t)(1u << (width - 1))"),
+    ("grouped bit stream order", "v |= (uint32_t)field(a[bitpos / 8], bitpos % 8, 1) << t;",
+     "v |= (uint32_t)field(a[bitpos / 8], bitpos % 8, 1) << (width - 1 - t);"),
+    ("q2_g64 grid offset", "or_stream_word(b + 2, k, 2) - 1", "or_stream_word(b + 2, k, 2) - 2"),
+    ("fp8 row multiplier dropped", "y[0] = M(oracle_e4m3fn(b[0]), s32);", "y[0] = oracle_e4m3fn(b[0]) + 0.0f * s32;"),
+    ("BF16 multiplier bits", "or_f32(w << 16)", "or_f32(w << 15)"),
 ]
 
 
