@@ -87,6 +87,13 @@ MUTANTS = [
     ("q2_g64 grid offset", "or_stream_word(b + 2, k, 2) - 1", "or_stream_word(b + 2, k, 2) - 2"),
     ("fp8 row multiplier dropped", "y[0] = M(oracle_e4m3fn(b[0]), s32);", "y[0] = oracle_e4m3fn(b[0]) + 0.0f * s32;"),
     ("BF16 multiplier bits", "or_f32(w << 16)", "or_f32(w << 15)"),
+    # the fused-product reference
+    ("product activation index transposed", "or_bf16_to_f64(x_bf16[m * K + k]) * (double)row[k]",
+     "or_bf16_to_f64(x_bf16[k * M + m]) * (double)row[k]"),
+    ("product output index transposed", "y[m * N + n] = s;", "y[n * M + m] = s;"),
+    ("product weight row offset", "w, w_len, n * bpr, (n + 1) * bpr, row);", "w, w_len, n * K, n * K + bpr, row);"),
+    ("product bfloat16 weights not rounded", "if (weight_dtype == 2) /* bfloat16 bit patterns",
+     "if (weight_dtype == 3) /* bfloat16 bit patterns"),
 ]
 
 
