@@ -71,3 +71,10 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["tensors"] == 225
+
+
+def test_batched_launch_count_matches_the_library():
+    # a batched decode of n tensors: ceil(n / 128) launch-table uploads, one decode
+    assert [bench.batched_launches(n) for n in (1, 128, 129, 225)] == [2, 2, 3, 3]
+    src = open(os.path.join(bench.ROOT, "quantized_weight_block_gb300", "csrc", "ndq_kernels.cu")).read()
+    assert f"constexpr int kUploadChunk = {bench.UPLOAD_CHUNK};" in src
