@@ -78,6 +78,8 @@ def parse_args():
                     help="time one fused decode + product (weights FMT [N,K], M activation rows; binary32 "
                          "weights, or bfloat16 with ',bf16') for --steps launches and exit (for focused profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle comparisons of the timed outputs and the payload digests")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-fraction", type=int, default=1,
                     help="CPU baseline decodes 1/N of every tensor's blocks")
@@ -217,35 +219,130 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-# CPU oracle baseline
+# CPU oracle: timed baseline, parity and payload digests
 # --------------------------------------------------------------------------
-def cpu_oracle_sample(work: ModelWorkload, x_host_np, fraction: int, cores: int):
-    """Decode the first 1/fraction of every tensor's blocks with the oracle,
-    one piece per thread (the oracle itself is single-threaded C; ctypes
-    releases the GIL).  Returns (seconds, bytes in+out, elements)."""
+_OUT_BYTES = {"float32": 4, "float16": 2, "bfloat16": 2, "float64": 8}
+_BITS = {"float32": np.uint32, "float64": np.uint64, "float16": np.uint16, "bfloat16": np.uint16}
+
+
+def oracle_pieces(tensors, fraction: int, cores: int, out: str = "bfloat16", per_core: int = 8):
+    """Disjoint block ranges of about equal size covering the first
+    1/fraction of every tensor's blocks (at least one block each), so that
+    `cores` threads, each running the single-threaded oracle on one range at
+    a time, finish together.  tensors: [(fmt, shape, payload)].  Returns
+    (pieces [(fmt, shape, x, b0, b1)], bytes in+out, elements)."""
+    rows = []
+    for fmt, shape, x in tensors:
+        B, S = synth.GEOMETRY[fmt]
+        take = max(1, synth._nblocks(fmt, shape) // fraction)
+        rows.append((fmt, shape, x, take, B, S))
+    total = sum(take * B for (_, _, _, take, B, _) in rows)
+    target = max(1, total // (cores * per_core))
+    pieces, nbytes, nel = [], 0, 0
+    for fmt, shape, x, take, B, S in rows:
+        step = max(1, target // B)
+        for b0 in range(0, take, step):
+            b1 = min(take, b0 + step)
+            pieces.append((fmt, shape, x, b0, b1))
+        nbytes += take * (S + _OUT_BYTES[out] * B)
+        nel += take * B
+    return pieces, nbytes, nel
+
+
+def time_oracle(pieces, threads: int, out: str = "bfloat16") -> float:
+    """Seconds for the oracle, unchanged, to decode every piece: one thread
+    per piece at a time on `threads` host threads (ctypes releases the GIL
+    during each call)."""
     import oracle
 
     oracle.build()
-    pieces = []
-    for i, s in enumerate(work.specs):
-        B, S = synth.GEOMETRY[s.fmt]
-        nb = work.x_len[i] // S
-        take = max(1, nb // fraction)
-        x = x_host_np[work.x_off[i]:work.x_off[i] + work.x_len[i]]
-        step = max(1, take // 4)
-        for b0 in range(0, take, step):
-            pieces.append((s.fmt, s.shape, x, b0, min(take, b0 + step), B, S))
-    nbytes = sum((b1 - b0) * (S + 2 * B) for (_, _, _, b0, b1, B, S) in pieces)
-    nel = sum((b1 - b0) * B for (_, _, _, b0, b1, B, S) in pieces)
 
     def run(p):
-        fmt, shape, x, b0, b1, B, S = p
-        oracle.decode_range(fmt, shape, x, b0, b1, "bfloat16")
+        fmt, shape, x, b0, b1 = p
+        oracle.decode_range(fmt, shape, x, b0, b1, out)
 
     t0 = time.perf_counter()
-    with cf.ThreadPoolExecutor(cores) as ex:
-        list(ex.map(run, pieces))
-    return time.perf_counter() - t0, nbytes, nel
+    if threads == 1:
+        for p in pieces:
+            run(p)
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, pieces))
+    return time.perf_counter() - t0
+
+
+def oracle_figures(tensors, cores: int, out: str, one_core_elements: int = 1 << 24):
+    """The oracle timed on `cores` threads over all of `tensors`, and on one
+    core over a leading sample of about `one_core_elements` elements."""
+    pieces, nbytes, nel = oracle_pieces(tensors, 1, cores, out)
+    secs = time_oracle(pieces, cores, out)
+    total = sum(int(np.prod(shape)) for (_, shape, _) in tensors)
+    frac1 = max(1, total // one_core_elements)
+    p1, b1, n1 = oracle_pieces(tensors, frac1, 1, out, per_core=1)
+    s1 = time_oracle(p1, 1, out)
+    return {"cores": cores, "GB/s": round(nbytes / secs / 1e9, 3), "elements/s": float(f"{nel / secs:.4g}"),
+            "seconds": round(secs, 3),
+            "1_core": {"GB/s": round(b1 / s1 / 1e9, 3), "elements/s": float(f"{n1 / s1:.4g}"),
+                       "seconds": round(s1, 3),
+                       "sample": f"first 1/{frac1} of every tensor's blocks ({n1} elements)"}}
+
+
+def nan_mask(bits: np.ndarray, out: str) -> np.ndarray:
+    if out == "float32":
+        return (bits & 0x7F800000 == 0x7F800000) & (bits & 0x007FFFFF != 0)
+    if out == "float64":
+        return (bits & 0x7FF0000000000000 == 0x7FF0000000000000) & (bits & 0x000FFFFFFFFFFFFF != 0)
+    if out == "float16":
+        return (bits & 0x7C00 == 0x7C00) & (bits & 0x03FF != 0)
+    return (bits & 0x7F80 == 0x7F80) & (bits & 0x007F != 0)
+
+
+def count_mismatches(got: np.ndarray, want: np.ndarray, out: str) -> int:
+    """Elements whose bits differ (NaN only needs to be NaN: its payload is
+    unspecified)."""
+    g, w = got.reshape(-1).view(_BITS[out]), want.reshape(-1).view(_BITS[out])
+    if g.shape != w.shape:
+        return max(g.size, w.size)
+    if np.array_equal(g, w):
+        return 0
+    gn, wn = nan_mask(g, out), nan_mask(w, out)
+    return int(((gn != wn) | (~wn & (g != w))).sum())
+
+
+def parity_against_oracle(pool, tensors, fetch, out: str, cores: int):
+    """Every element of every tensor's GPU output against the oracle's
+    decode of the same payload, one tensor at a time (host memory holds one
+    decoded tensor); each tensor's blocks are split over the pool.
+    tensors: [(fmt, shape, payload)]; fetch(i) returns tensor i's GPU output
+    bits as a flat numpy array."""
+    import oracle
+
+    oracle.build()
+    total = bad = 0
+    bad_tensors = []
+    for i, (fmt, shape, x) in enumerate(tensors):
+        got = fetch(i)
+        B, _ = synth.GEOMETRY[fmt]
+        pieces, _, _ = oracle_pieces([(fmt, shape, x)], 1, cores, out, per_core=2)
+
+        def check(p, got=got, B=B):
+            f, shp, xx, b0, b1 = p
+            want = oracle.decode_range(f, shp, xx, b0, b1, out)
+            return count_mismatches(got[b0 * B:b1 * B], want, out)
+
+        m = sum(pool.map(check, pieces))
+        total += got.size
+        bad += m
+        if m:
+            bad_tensors.append(i)
+    return {"bit_exact": bad == 0, "elements": total, "mismatches": bad, "tensors": len(tensors),
+            "tensors_with_mismatches": bad_tensors[:16]}
+
+
+def payload_digests(pool, payloads):
+    """SHA-256 of every payload, and of the list of those digests (in order)."""
+    digs = list(pool.map(lambda x: hashlib.sha256(memoryview(np.ascontiguousarray(x))).hexdigest(), payloads))
+    return digs, hashlib.sha256("".join(digs).encode()).hexdigest()
 
 
 # --------------------------------------------------------------------------
@@ -274,14 +371,25 @@ def profiled_traffic(profile_name: str):
     return None
 
 
-def time_single_workloads(torch, ndq, stream, peak, workloads):
+def host_bits(torch, y):
+    """A device tensor's bits as a flat host numpy array."""
+    t = y.reshape(-1).cpu()
+    if t.element_size() == 2:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def time_single_workloads(torch, ndq, stream, peak, workloads, pool=None, cores=1, oracle_legs=True):
     """Single-format workloads.
 
     Steady state: back-to-back launches rotating over enough copies of the
     payload and output that the rotation's working set exceeds 4x L2, so no
     launch finds its data in L2.  Single launch: one launch after L2 was
     evicted by a 512 MB read (L2 left full of clean lines), which adds the
-    launch and pipeline-fill latency.
+    launch and pipeline-fill latency.  With oracle_legs: the payload's
+    SHA-256, the parity of the whole GPU output against the oracle, and the
+    oracle itself timed on the same payload (all host cores, and one core on
+    a sample).
     """
     l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or 132 << 20)
     flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
@@ -329,13 +437,20 @@ def time_single_workloads(torch, ndq, stream, peak, workloads):
             b.synchronize()
             single.append(a.elapsed_time(b))
         ms1 = statistics.median(single)
+        extra = {}
+        if oracle_legs and pool is not None:
+            torch.cuda.synchronize()
+            tensors = [(fmt, shape, x_np)]
+            extra["payload_sha256"] = hashlib.sha256(memoryview(x_np)).hexdigest()
+            extra["parity"] = parity_against_oracle(pool, tensors, lambda i: host_bits(torch, ys[0]), od, cores)
+            extra["oracle"] = oracle_figures(tensors, cores, od)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[label] = {"GB/s": round(gbs, 1), "ms": round(ms, 5), "elements/s": float(f"{np.prod(shape) / (ms * 1e-3):.4g}"),
                       "frac_of_8TBs": round(gbs / 8000.0, 4), "frac_of_measured": round(gbs / peak, 4),
                       "bytes": nbytes,
                       "l2": f"back to back over {nsets} buffer sets ({nsets * nbytes / 1e6:.0f} MB > 4x L2)",
                       "single_launch_ms": round(ms1, 5),
-                      "single_launch_GB/s": round(nbytes / (ms1 * 1e-3) / 1e9, 1)}
+                      "single_launch_GB/s": round(nbytes / (ms1 * 1e-3) / 1e9, 1), **extra}
         del xs, ys, x0
     del flush, flush_sink
     return out
@@ -676,6 +791,29 @@ def run_ours(args, rank, world, local_rank):
     if ndq.get_device_fault():
         raise RuntimeError("device fault word set during the timed region")
 
+    cores = os.cpu_count() or 1
+    pool = cf.ThreadPoolExecutor(cores)
+    x_np = x_host.numpy()
+    model_tensors = [(s.fmt, s.shape, x_np[work.x_off[i]:work.x_off[i] + work.x_len[i]])
+                     for i, s in enumerate(work.specs)]
+    # ---- outside the timed region: the timed launch's whole output against
+    # the oracle, and the payloads' digests ----
+    parity = digests = None
+    if not args.no_parity and rank == 0:
+        t0 = time.time()
+        digs, combined = payload_digests(pool, [t[2] for t in model_tensors])
+        digests = {"whole_model": combined, "tensors": len(digs),
+                   "what": "SHA-256 of the concatenated hex SHA-256 digests of every payload, in tensor order",
+                   "first": digs[0], "embedding": digs[-1]}
+
+        def fetch(i):
+            return host_bits(torch, y_dev[work.y_off[i] // 2:work.y_off[i] // 2 + work.nel[i]])
+
+        parity = parity_against_oracle(pool, model_tensors, fetch, "bfloat16", cores)
+        parity["what"] = ("every element of every tensor decoded by the last timed launch, against the oracle's "
+                          "decode of the same payload (bf16 bits; NaN only needs to be NaN)")
+        log(f"[bench] parity {parity['bit_exact']} ({parity['mismatches']} mismatches) in {time.time() - t0:.1f}s")
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -683,20 +821,28 @@ def run_ours(args, rank, world, local_rank):
 
     per_workload = per_workload_next = fused = None
     if not args.no_workloads and rank == 0:
-        per_workload = time_single_workloads(torch, ndq, stream, peak, synth.WORKLOADS)
-        per_workload_next = time_single_workloads(torch, ndq, stream, peak, synth.NEXT_WORKLOADS)
+        legs = not args.no_parity
+        per_workload = time_single_workloads(torch, ndq, stream, peak, synth.WORKLOADS, pool, cores, legs)
+        per_workload_next = time_single_workloads(torch, ndq, stream, peak, synth.NEXT_WORKLOADS, pool, cores, legs)
     if not args.no_fused and rank == 0 and not (args.layers != 32 or args.no_embedding):
         fused = time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev)
 
     cpu = None
     if not args.no_cpu and rank == 0:
-        cores = os.cpu_count() or 1
-        secs, nbytes, nel = cpu_oracle_sample(work, x_host.numpy(), args.cpu_fraction, cores)
+        pieces, nbytes, nel = oracle_pieces(model_tensors, args.cpu_fraction, cores)
+        secs = time_oracle(pieces, cores)
+        frac1 = max(1, work.elements // (1 << 26))
+        p1, b1, n1 = oracle_pieces(model_tensors, frac1, 1, per_core=1)
+        s1 = time_oracle(p1, 1)
         cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "elements/s": float(f"{nel / secs:.4g}"), "seconds": round(secs, 2),
                "sample": f"first 1/{args.cpu_fraction} of every tensor's blocks of the same whole-model "
                          f"payloads ({nel} elements, {nbytes / 1e9:.3f} GB in+out), decoded to bf16, "
-                         f"{cores} threads over disjoint block ranges"}
+                         f"{cores} threads over {len(pieces)} disjoint block ranges of about equal size",
+               "1_core": {"value": round(b1 / s1 / 1e9, 4), "unit": "GB/s", "elements/s": float(f"{n1 / s1:.4g}"),
+                          "seconds": round(s1, 2),
+                          "sample": f"first 1/{frac1} of every tensor's blocks ({n1} elements), one thread"}}
+    pool.shutdown()
 
     traffic = profiled_traffic("k_decode_whole_model.json")
     res = {
@@ -713,6 +859,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
                      "traffic": traffic, "peak_source": peak_src,
                      "kernel": "k_decode (batched; step time includes the launch-table upload kernels, 225 x 64 B)"},
+        "parity": parity, "payload_sha256": digests,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": batched_launches(len(items)) * args.steps, "clocks": clocks,
         "per_workload": per_workload, "per_workload_next_formats": per_workload_next, "fused_matmul": fused,
     }
@@ -742,18 +889,19 @@ def run_reference(args, rank, world):
         rows = max(1, s.shape[0] // fraction)
         shp = (rows,) + tuple(s.shape[1:])
         sample.append((s.fmt, shp, synth.payload(s.fmt, shp, s.seed)))
-    nbytes = sum(x.size + 2 * int(np.prod(shp)) for (_, shp, x) in sample)
-    nel = sum(int(np.prod(shp)) for (_, shp, _) in sample)
     cores = os.cpu_count() or 1
+    # disjoint block ranges of about equal size, so that every host thread
+    # stays busy to the end of each step (not one thread on the largest tensor)
+    pieces, nbytes, nel = oracle_pieces(sample, 1, cores)
 
-    def one(item):
-        fmt, shp, x = item
-        oracle.decode(fmt, shp, x, "bfloat16")
+    def one(p):
+        fmt, shp, x, b0, b1 = p
+        oracle.decode_range(fmt, shp, x, b0, b1, "bfloat16")
 
     ex = cf.ThreadPoolExecutor(cores)
 
     def step():
-        list(ex.map(one, sample))
+        list(ex.map(one, pieces))
 
     for _ in range(args.warmup):
         step()
@@ -772,7 +920,8 @@ def run_reference(args, rank, world):
                    "out_dtype": "bf16"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"1/{fraction} of every tensor's rows (same field distributions and seeds), "
-                                   f"{nel} elements per step, {cores} threads"},
+                                   f"{nel} elements per step, {cores} threads over {len(pieces)} disjoint block "
+                                   f"ranges of about equal size"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(res), flush=True)

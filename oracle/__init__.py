@@ -208,6 +208,44 @@ def decode_range(name: str, shape, x: np.ndarray, b0: int, b1: int, out_dtype: s
     return y
 
 
+def decode_range_into(name: str, shape, x: np.ndarray, b0: int, b1: int, out_dtype: str, y: np.ndarray) -> None:
+    """Decode blocks [b0, b1) of a payload into the contiguous array y
+    ((b1-b0)*B elements of the output type; 16-bit outputs as uint16)."""
+    assert y.flags.c_contiguous and y.dtype == _NP_OUT[out_dtype]
+    B, _, _ = format_info(name)
+    assert y.size == (b1 - b0) * B
+    sa, nd = _shape_arg(shape)
+    rc = lib().oracle_decode_range(name.encode(), sa, nd, OUT_DTYPES[out_dtype], _ptr(x), x.size, b0, b1, _ptr(y))
+    if rc:
+        raise OracleError(rc, name)
+
+
+def decode_parallel(name: str, shape, x: np.ndarray, out_dtype: str = "float32", threads: int | None = None,
+                    pool=None) -> np.ndarray:
+    """The same result as decode(), with the block range split into disjoint
+    pieces decoded by host threads (each piece by the unchanged
+    single-threaded C decoder; ctypes releases the GIL during the call)."""
+    import concurrent.futures as cf
+
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    nb, _, _ = geometry(name, shape, x.size)
+    B, _, _ = format_info(name)
+    y = np.empty(nb * B, dtype=_NP_OUT[out_dtype])
+    threads = threads or os.cpu_count() or 1
+    step = max(1, -(-nb // (4 * threads)))
+    ranges = [(b0, min(nb, b0 + step)) for b0 in range(0, nb, step)]
+
+    def run(r):
+        decode_range_into(name, shape, x, r[0], r[1], out_dtype, y[r[0] * B:r[1] * B])
+
+    if pool is not None:
+        list(pool.map(run, ranges))
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, ranges))
+    return y.reshape(tuple(int(s) for s in shape))
+
+
 def decode_block_f32(name: str, block: bytes | np.ndarray, dw: float = 1.0) -> np.ndarray:
     """One block to binary32 values (no cast)."""
     B, S, _ = format_info(name)

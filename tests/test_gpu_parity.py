@@ -269,49 +269,107 @@ def test_repeat_is_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-# ---- full-size workloads: sampled blocks against the oracle --------------
-def _sample_blocks(nb, rng, k=1500):
-    idx = np.unique(np.concatenate([rng.integers(0, nb, size=k), [0, 1, nb - 1, nb - 2],
-                                    np.arange(0, nb, max(1, nb // 50))]))
-    return idx[idx < nb]
-
-
-def check_sampled(orc, fmt, shape, x_np, y_t, out, seed=0):
-    B, _ = synth.GEOMETRY[fmt]
-    nb = int(np.prod(shape[:-1], dtype=np.int64)) * (shape[-1] // B)
-    rng = np.random.default_rng(seed)
-    idx = _sample_blocks(nb, rng)
-    yflat = y_t.reshape(-1)
-    got_rows = yflat.view(-1, B)[torch.from_numpy(idx).to(yflat.device)].cpu()
-    got = got_rows.view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
-    want = np.stack([orc.decode_range(fmt, shape, x_np, int(b), int(b) + 1, out) for b in idx])
-    assert_bit_exact(got, want, out, f"{fmt} {shape} sampled")
+# ---- full-size workloads: every output element against the oracle -------
+# The oracle decodes these with its block range split over the host cores
+# (oracle.decode_parallel: the unchanged single-threaded decoder per piece).
+def _bits_of(y, out):
+    return y.cpu().view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
 
 
 @pytest.mark.parametrize("label,fmt,shape,seed,out", synth.WORKLOADS + synth.NEXT_WORKLOADS)
-def test_full_size_workloads_sampled(orc, label, fmt, shape, seed, out):
+def test_full_size_workloads(orc, label, fmt, shape, seed, out):
+    """Each single-format workload at its full size, in the launch the
+    benchmark times (one ndq_dequantize_packed call), compared whole."""
     x = synth.payload(fmt, shape, seed)
     y = ndq.dequantize_packed(fmt, shape, torch.from_numpy(x).to(DEV), TORCH_OUT[out])
     torch.cuda.synchronize()
-    check_sampled(orc, fmt, shape, x, y, out, seed)
-    if int(np.prod(shape)) <= 1 << 24:  # small enough for the whole-output check
-        got = y.cpu().view(torch.uint16 if out in ("float16", "bfloat16") else TORCH_OUT[out]).numpy()
-        assert_bit_exact(got, orc.decode(fmt, shape, x, out), out, label)
+    assert_bit_exact(_bits_of(y, out), orc.decode_parallel(fmt, shape, x, out), out, label)
 
 
-def test_whole_model_batched_sampled(orc):
+def _whole_model_payloads(specs):
+    import concurrent.futures as cf
+
+    with cf.ThreadPoolExecutor(8) as ex:
+        return list(ex.map(lambda s: synth.payload(s.fmt, s.shape, s.seed), specs))
+
+
+def test_whole_model_batched_full(orc):
     """The whole-model workload in the launch configuration the benchmark
-    times (one batched launch over 225 tensors), sampled per tensor."""
+    times (one batched launch over all 225 tensors, the q8_0 / q4_k / q6_k
+    kernel), every element of every tensor compared with the oracle, one
+    tensor at a time so that host memory holds one decoded tensor at most."""
+    import concurrent.futures as cf
+
     specs = synth.llama3_8b_tensors()
-    xs_np, items = [], []
-    for s in specs:
-        x = synth.payload(s.fmt, s.shape, s.seed)
-        xs_np.append(x)
+    xs_np = _whole_model_payloads(specs)
+    items = []
+    for s, x in zip(specs, xs_np):
         items.append((s.fmt, s.shape, torch.from_numpy(x).to(DEV),
-                      torch.empty(s.shape, dtype=torch.bfloat16, device=DEV)))
+                      torch.full(s.shape, float("nan"), dtype=torch.bfloat16, device=DEV)))
     ws = ndq.dequantize_packed_batched(items)
     torch.cuda.synchronize()
     del ws
-    for i in list(range(0, len(specs), 7)) + [len(specs) - 1]:
-        s = specs[i]
-        check_sampled(orc, s.fmt, s.shape, xs_np[i], items[i][3], "bfloat16", seed=i)
+    with cf.ThreadPoolExecutor() as pool:
+        for s, x, it in zip(specs, xs_np, items):
+            want = orc.decode_parallel(s.fmt, s.shape, x, "bfloat16", pool=pool)
+            assert_bit_exact(_bits_of(it[3], "bfloat16"), want, "bfloat16", f"whole model {s.name}")
+
+
+def _batch_and_check(orc, specs, what):
+    """One batched call over specs = [(fmt, shape, out, payload)], every
+    output compared whole."""
+    items, ys = [], []
+    for fmt, shape, out, x in specs:
+        y = torch.full(shape, float("nan"), dtype=TORCH_OUT[out], device=DEV)
+        items.append((fmt, shape, torch.from_numpy(x).to(DEV), y))
+        ys.append(y)
+    ws = ndq.dequantize_packed_batched(items)
+    torch.cuda.synchronize()
+    del ws
+    for (fmt, shape, out, x), y in zip(specs, ys):
+        assert_bit_exact(_bits_of(y, out), orc.decode_parallel(fmt, shape, x, out), out, f"{what} {fmt} {shape}")
+
+
+def _ring_wrapping_tiles():
+    # more tiles than every resident CTA can hold in its staging ring, twice
+    # over, so every CTA reuses each stage several times
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return sms * 3 * 4 * 2
+
+
+@pytest.mark.parametrize("out", OUTS)
+def test_batched_kquant_mix_ring_wraps(orc, out):
+    """A batch of only gguf:q8_0 / q4_k / q6_k tensors (the whole-model
+    kernel) of one output type, large enough that the staging ring of every
+    CTA wraps several times, with ragged row counts; compared whole."""
+    tiles = _ring_wrapping_tiles()
+    rng = np.random.default_rng(11)
+    specs, n = [], 0
+    i = 0
+    while n < tiles * 8192:
+        fmt = ("gguf:q8_0", "gguf:q4_k", "gguf:q6_k")[i % 3]
+        shape = (int(rng.integers(50, 700)), int(rng.choice([1024, 4096, 2816])))
+        specs.append((fmt, shape, out, synth.payload(fmt, shape, seed=300 + i)))
+        n += shape[0] * shape[1]
+        i += 1
+    _batch_and_check(orc, specs, f"k-quant mix {out}")
+
+
+@pytest.mark.parametrize("outs", [["bfloat16"], OUTS])
+def test_batched_all_formats_ring_wraps(orc, outs):
+    """Every format in one batched launch (one output type: the all-format
+    kernel of that type; mixed types: the generic kernel), each CTA's ring
+    wrapping several times."""
+    tiles = _ring_wrapping_tiles()
+    per = -(-tiles * 8192 // len(FORMATS))
+    rng = np.random.default_rng(12)
+    specs = []
+    for i, fmt in enumerate(FORMATS):
+        B, _ = synth.GEOMETRY[fmt]
+        k = int(rng.integers(8, 40)) * max(B, 64)
+        rows = max(1, per // k)
+        if fmt == "nvfp4":
+            rows = rows // 6 * 6 or 6
+        specs.append((fmt, (rows, k), outs[i % len(outs)],
+                      synth.payload(fmt, (rows, k), seed=400 + i, ndiv=3 if fmt == "nvfp4" else 1)))
+    _batch_and_check(orc, specs, "all formats")
