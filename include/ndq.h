@@ -275,6 +275,22 @@ int ndq_dequantize_packed_batched(const ndq_tensor_desc *descs, int n, void *wor
  * validation and errors as ndq_dequantize_packed_batched (minus workspace). */
 int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc *descs, int n, void *stream);
 
+/* Failure-path check (not part of the pages' contract): makes the NEXT decode
+ * launch issued by the calling host thread (ndq_dequantize_packed or a
+ * batched call) exercise its device-side failure path without any GPU fault.
+ * That launch withholds the staging copy of global tile `tile` (the tiles of
+ * a launch are its tensors' 8192-element spans in order), so the decode
+ * warps waiting for that tile give up after `wait_limit_us` microseconds
+ * instead of the default 2 s, set their bits in the device fault word and
+ * stop; the CTA's producer then gives up too, waits for every copy it did
+ * issue, and stops.  Every other CTA decodes its tiles normally.  The
+ * request is consumed by that one launch (a launch of no tile does not
+ * consume it); tile = -1 cancels it.  Outputs of the affected CTA's tiles are
+ * unspecified; read the fault word with ndq_get_device_fault afterwards.
+ * Returns NDQ_ERR_BAD_COUNT when tile < -1 or wait_limit_us is 0 or above
+ * 2000000. */
+int ndq_test_withhold_copy(int64_t tile, uint32_t wait_limit_us);
+
 /* Read and clear the library's device fault word on the current device.
  * A kernel sets a nonzero bit when one of its bounded waits for staged
  * payload data gives up (it then stops decoding instead of hanging the GPU).

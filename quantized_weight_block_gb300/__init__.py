@@ -71,6 +71,7 @@ _lib.ndq_batched_workspace_bytes.restype = _c.c_size_t
 _lib.ndq_dequantize_packed_batched.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p, _c.c_size_t,
                                                _c.c_void_p]
 _lib.ndq_get_device_fault.argtypes = [_c.POINTER(_c.c_uint32)]
+_lib.ndq_test_withhold_copy.argtypes = [_c.c_int64, _c.c_uint32]
 _lib.ndq_dequantize_packed_batched_noalloc.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p]
 _lib.ndq_matmul_packed.argtypes = [_c.c_int, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_size_t, _c.c_void_p,
                                    _c.c_int64, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p]
@@ -80,7 +81,7 @@ EXPORTS = (
     "ndq_format_from_name", "ndq_format_name", "ndq_format_geometry", "ndq_format_supported",
     "ndq_status_string", "ndq_payload_geometry", "ndq_dequantize_packed", "ndq_batched_workspace_bytes",
     "ndq_dequantize_packed_batched", "ndq_get_device_fault", "ndq_dequantize_packed_batched_noalloc",
-    "ndq_matmul_packed",
+    "ndq_matmul_packed", "ndq_test_withhold_copy",
 )
 
 
@@ -152,6 +153,13 @@ def ndq_matmul_packed(format_id: int, N: int, K: int, w_ptr: int, w_len: int, x_
                       weight_dtype: int, out_dtype: int, y_ptr: int, stream: int = 0) -> int:
     """Raw call of the fused decode + product; returns the status code."""
     return _lib.ndq_matmul_packed(format_id, N, K, w_ptr, w_len, x_ptr, M, weight_dtype, out_dtype, y_ptr, stream)
+
+
+def ndq_test_withhold_copy(tile: int, wait_limit_us: int) -> int:
+    """Raw call: the next decode launch of this host thread withholds one
+    tile's staging copy (a check of the device-side failure path); returns
+    the status code."""
+    return _lib.ndq_test_withhold_copy(tile, wait_limit_us)
 
 
 def ndq_get_device_fault() -> int:

@@ -365,7 +365,10 @@ int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc* descs, int n, v
     if (n > NDQ_NOALLOC_MAX_TENSORS) return NDQ_ERR_TOO_MANY_TENSORS;
     if (n == 0) return NDQ_OK;
     if (!descs) return NDQ_ERR_NULL;
-    ndq::DevTensor table[NDQ_NOALLOC_MAX_TENSORS];  // host stack, 64 KiB
+    // Pass 1: validate the whole batch (one bad entry rejects it) and size
+    // the launch.  Nothing is kept per tensor, so the host stack holds no
+    // table: callers may run on small thread stacks.
+    ndq::KernelSelect sel;
     int count = 0;
     uint64_t tiles = 0;
     int nv_index = -1;
@@ -376,13 +379,52 @@ int ndq_dequantize_packed_batched_noalloc(const ndq_tensor_desc* descs, int n, v
         const int rc = prepare(d.format_id, d.shape, d.ndim, d.out_dtype, d.x, d.x_len, d.y, &t, &g);
         if (rc != NDQ_OK) return rc;
         if (g.nblocks == 0) continue;
-        t.tile_begin = tiles;
-        tiles += tiles_of(t);
         if (nv_index < 0 && t.fmt == ndq::KF_NVFP4) nv_index = count;
-        table[count++] = t;
+        sel.add(t);
+        tiles += tiles_of(t);
+        ++count;
     }
     if (count == 0) return NDQ_OK;
-    return ndq::launch_batched_noalloc(table, count, tiles, nv_index, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    ndq::DevTensor* table = nullptr;
+    if (ndq::noalloc_table(&table) != 0) return NDQ_ERR_CUDA;
+    // Pass 2: the same descriptors again, written into the library's table
+    // one upload launch (kUploadChunk entries) at a time.
+    ndq::KParams p;
+    std::memset(&p, 0, sizeof(p));
+    ndq::UploadParams up;
+    up.dst = table;
+    up.n = 0;
+    uint64_t tile_begin = 0;
+    int k = 0;
+    for (int i = 0; i < n; ++i) {
+        const ndq_tensor_desc& d = descs[i];
+        ndq::DevTensor t;
+        Geometry g;
+        if (prepare(d.format_id, d.shape, d.ndim, d.out_dtype, d.x, d.x_len, d.y, &t, &g) != NDQ_OK) return NDQ_ERR_NULL;
+        if (g.nblocks == 0) continue;
+        t.tile_begin = tile_begin;
+        tile_begin += tiles_of(t);
+        if (k++ == 0) p.single = t;
+        up.d[up.n++] = t;
+        if (up.n == ndq::kUploadChunk) {
+            if (ndq::upload_chunk(up, stream) != 0) return NDQ_ERR_CUDA;
+            up.dst += up.n;
+            up.n = 0;
+        }
+    }
+    if (up.n > 0 && ndq::upload_chunk(up, stream) != 0) return NDQ_ERR_CUDA;
+    p.table = table;
+    p.n = count;
+    p.nv_index = nv_index;
+    p.total_tiles = tiles;
+    sel.get(&p.fsel, &p.osel);
+    return ndq::launch_decode(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+}
+
+int ndq_test_withhold_copy(int64_t tile, uint32_t wait_limit_us) {
+    if (tile < -1 || wait_limit_us == 0 || wait_limit_us > 2000000u) return NDQ_ERR_BAD_COUNT;
+    ndq::set_withhold_next(tile, static_cast<uint64_t>(wait_limit_us) * 1000u);
+    return NDQ_OK;
 }
 
 int ndq_get_device_fault(uint32_t* flags) {

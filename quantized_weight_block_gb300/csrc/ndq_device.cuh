@@ -140,12 +140,13 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Bounded wait: true once the phase with `parity` has completed, false after
-// kWaitLimitNs of global time.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// `limit_ns` (by default kWaitLimitNs) of global time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -1756,12 +1757,20 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
     int32_t nv_di = -1;
     uint64_t nv_d = 0;
     uint32_t nv_same = 0;
+    int withheld = -1;  // staging whose copy was withheld on request (never completes)
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
         const int s = issued % kStages;
         if (issued >= kStages &&
-            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1))) {
+            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1), p.wait_ns)) {
             fault = true;
             break;
+        }
+        if (static_cast<int64_t>(tile) == p.withhold_tile) {
+            // failure-path check requested by the host (ndq_test_withhold_copy):
+            // this tile's stage is never filled, so the consumers' bounded
+            // wait for it runs out
+            withheld = issued;
+            continue;
         }
         if (p.table)
             while (di + 1 < p.n && p.table[di + 1].tile_begin <= tile) ++di;
@@ -1802,12 +1811,15 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
         mbar_arrive_expect_tx(&H.full[s], bytes);
         bulk_load(inbuf + s * kInStride, src - phase, bytes, &H.full[s]);
     }
-    if (fault) {
-        atomicOr(p.fault, 1u);
-        // Wait (bounded) for every copy still in flight: the last kStages
-        // stagings, whose full phases are the latest ones of their stages.
+    if (fault) atomicOr(p.fault, 1u);
+    if (fault || withheld >= 0) {
+        // The consumers may have stopped early: wait (bounded) for every copy
+        // still in flight before the CTA can exit.  Only the last kStages
+        // stagings can be in flight (an older stage was reused only after the
+        // consumers released it); a withheld staging has no copy.
         for (int j = issued - kStages; j < issued; ++j)
-            if (j >= 0) mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+            if (j >= 0 && j != withheld)
+                mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
     }
 }
 
@@ -1909,7 +1921,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
         const int s = it % kStages;
         // (decided by the whole warp: the decoders shuffle between lanes)
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1)))) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1), p.wait_ns))) {
             if (lane == 0) atomicOr(p.fault, 2u);
             return;
         }

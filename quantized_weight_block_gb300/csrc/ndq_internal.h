@@ -128,6 +128,8 @@ struct KParams {
     int32_t osel;      // KOut shared by every tensor of the launch, or -1
     unsigned int* fault;  // device fault word (set by the launcher)
     const IqGrids* grids;  // IQ codebooks (set by the launcher)
+    uint64_t wait_ns;      // limit of the kernel's bounded waits (set by the launcher)
+    int64_t withhold_tile;  // tile whose copy the producer withholds, or -1 (set by the launcher)
 };
 
 using KernelFn = void (*)(KParams);
@@ -303,21 +305,54 @@ size_t decode_smem_bytes(bool tab);
 // Returns 0 or a CUDA error code.
 int launch_decode(const KParams& p, void* stream);
 
-// Copy n host descriptors into a device table with kernel launches on
-// `stream` (no host-blocking copy).  Returns 0 or a CUDA error code.
+// Failure-path check of the calling host thread's next decode launch: the
+// producer withholds the copy of `tile` and every bounded wait gives up
+// after `wait_ns`.  Consumed (reset) by that launch.
+void set_withhold_next(int64_t tile, uint64_t wait_ns);
+
+// Launch-table upload: descriptors travel to the device as the parameters of
+// a small kernel, kUploadChunk per launch (no host-blocking copy).
+constexpr int kUploadChunk = 128;
+struct UploadParams {
+    DevTensor* dst;  // device entries dst[0..n) are written
+    int32_t n;
+    DevTensor d[kUploadChunk];
+};
+
+// One upload launch on `stream`.  Returns 0 or a CUDA error code.
+int upload_chunk(const UploadParams& up, void* stream);
+
+// Copy n host descriptors into a device table with upload launches on
+// `stream`.  Returns 0 or a CUDA error code.
 int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream);
 
 // Capacity of the library-owned launch table of the no-allocation batched
 // call (64 bytes per entry: 64 KiB per device).
 constexpr int kNoAllocMaxTensors = 1024;
 
-// Batched decode whose launch table lives in the library's own static device
-// array instead of a caller workspace.  `table` is host memory (n entries,
-// tile_begin set).  Returns 0 or a CUDA error code.
-int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int nv_index, void* stream);
+// Device address of the library-owned launch table on the current device,
+// looked up with cudaGetSymbolAddress on the first call per device.  Returns
+// 0 or a CUDA error code.
+int noalloc_table(DevTensor** table);
 
-// Kernel selectors of a launch over tensors t[0..n): the shared format (or
-// kFselKQuantMix, or -1) and the shared output type (or -1).
+// Kernel selectors of a launch, accumulated over its tensors: the shared
+// format (or kFselKQuantMix, or -1) and the shared output type (or -1).
+struct KernelSelect {
+    int32_t fsel = -3;  // -3: no tensor yet
+    int32_t osel = -3;
+    bool kmix = true;   // every tensor is gguf:q8_0, q4_k or q6_k
+    void add(const DevTensor& t) {
+        fsel = (fsel == -3 || fsel == t.fmt) ? t.fmt : -1;
+        osel = (osel == -3 || osel == t.out) ? t.out : -1;
+        kmix = kmix && (t.fmt == KF_Q8_0 || t.fmt == KF_Q4_K || t.fmt == KF_Q6_K);
+    }
+    void get(int32_t* f, int32_t* o) const {
+        *f = (fsel < 0 && kmix) ? kFselKQuantMix : fsel;
+        *o = osel;
+    }
+};
+
+// Kernel selectors of a launch over tensors t[0..n).
 void select_kernel(const DevTensor* t, int n, int32_t* fsel, int32_t* osel);
 
 // Read and clear the device fault word of the current device.

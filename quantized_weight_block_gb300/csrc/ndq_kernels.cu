@@ -22,13 +22,6 @@ __device__ const IqGrids g_iq_grids = iqcb::make_iq_grids();
 namespace {
 
 // Writes n descriptors (kernel parameters) into a device table.
-constexpr int kUploadChunk = 128;
-struct UploadParams {
-    DevTensor* dst;
-    int32_t n;
-    DevTensor d[kUploadChunk];
-};
-
 __global__ void k_upload_table(const UploadParams p) {
     for (int i = threadIdx.x; i < p.n; i += blockDim.x) p.dst[i] = p.d[i];
 }
@@ -95,7 +88,18 @@ size_t smem_bytes(bool tab) { return decode_smem_bytes(tab); }
 unsigned int* g_fault_addr[kMaxDevices];
 const IqGrids* g_grids_addr[kMaxDevices];
 
+// Limit of the decode kernels' bounded waits (2 s), and the failure-path
+// check requested for this host thread's next launch (none: -1).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+thread_local uint64_t t_wait_ns = kDefaultWaitNs;
+thread_local int64_t t_withhold_tile = -1;
+
 }  // namespace
+
+void set_withhold_next(int64_t tile, uint64_t wait_ns) {
+    t_withhold_tile = tile;
+    t_wait_ns = wait_ns;
+}
 
 int launch_decode(const KParams& p, void* stream) {
     if (p.total_tiles == 0) return 0;
@@ -130,6 +134,10 @@ int launch_decode(const KParams& p, void* stream) {
     KParams q = p;
     const int se = device_symbols(dev, &q.fault, &q.grids);
     if (se != 0) return se;
+    q.wait_ns = t_wait_ns;
+    q.withhold_tile = t_withhold_tile;
+    t_wait_ns = kDefaultWaitNs;  // a requested failure-path check applies to one launch
+    t_withhold_tile = -1;
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(p.total_tiles < resident ? p.total_tiles : resident);
     void* args[] = {&q};
@@ -169,29 +177,33 @@ int device_symbols(int dev, unsigned int** fault, const IqGrids** grids) {
     return 0;
 }
 
+int upload_chunk(const UploadParams& up, void* stream) {
+    k_upload_table<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(up);
+    return static_cast<int>(cudaGetLastError());
+}
+
 int upload_table(DevTensor* dst, const DevTensor* src, int n, void* stream) {
     for (int i0 = 0; i0 < n; i0 += kUploadChunk) {
         UploadParams up;
         up.dst = dst + i0;
         up.n = (n - i0) < kUploadChunk ? (n - i0) : kUploadChunk;
         for (int i = 0; i < up.n; ++i) up.d[i] = src[i0 + i];
-        k_upload_table<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(up);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return static_cast<int>(e);
+        const int e = upload_chunk(up, stream);
+        if (e != 0) return e;
     }
     return 0;
 }
 
 // ---------------------------------------------------------------------------
-// Batched decode without any device allocation by the caller: the launch
-// table lives in a fixed file-scope device array (kNoAllocMaxTensors entries,
-// 64 KiB) that every GPU which loads this library holds until process exit.
-// The host cannot use the array's name as a device address, so its address
-// is looked up once per device with cudaGetSymbolAddress while that device is
-// current.  Every call overwrites entries [0, n) before the decode launch on
-// the same stream; nothing has to start at zero because the decode reads only
-// the n entries this call wrote.  Calls whose work overlaps on the GPU (other
-// streams, other host threads) share the array and race.
+// The launch table of the no-allocation batched call: a fixed file-scope
+// device array (kNoAllocMaxTensors entries, 64 KiB) that every GPU which
+// loads this library holds until process exit.  The host cannot use the
+// array's name as a device address, so its address is looked up once per
+// device with cudaGetSymbolAddress while that device is current.  Every call
+// overwrites entries [0, n) before its decode launch on the same stream;
+// nothing has to start at zero because the decode reads only the n entries
+// that call wrote.  Calls whose work overlaps on the GPU (other streams,
+// other host threads) share the array and race.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) DevTensor g_noalloc_table[kNoAllocMaxTensors];
 
@@ -199,8 +211,7 @@ namespace {
 DevTensor* g_noalloc_addr[kMaxDevices];  // per-device address, set once
 }
 
-int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, int nv_index, void* stream) {
-    if (n < 1 || n > kNoAllocMaxTensors) return static_cast<int>(cudaErrorInvalidValue);
+int noalloc_table(DevTensor** table) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return static_cast<int>(e);
@@ -211,29 +222,14 @@ int launch_batched_noalloc(const DevTensor* table, int n, uint64_t total_tiles, 
         if (e != cudaSuccess) return static_cast<int>(e);
         g_noalloc_addr[dev] = static_cast<DevTensor*>(addr);
     }
-    DevTensor* dev_table = g_noalloc_addr[dev];
-    const int rc = upload_table(dev_table, table, n, stream);
-    if (rc != 0) return rc;
-    KParams p;
-    p.single = table[0];
-    p.table = dev_table;
-    p.n = n;
-    p.nv_index = nv_index;
-    p.total_tiles = total_tiles;
-    select_kernel(table, n, &p.fsel, &p.osel);
-    return launch_decode(p, stream);
+    *table = g_noalloc_addr[dev];
+    return 0;
 }
 
 void select_kernel(const DevTensor* t, int n, int32_t* fsel, int32_t* osel) {
-    *fsel = t[0].fmt;
-    *osel = t[0].out;
-    bool kmix = true;
-    for (int i = 0; i < n; ++i) {
-        if (t[i].fmt != *fsel) *fsel = -1;
-        if (t[i].out != *osel) *osel = -1;
-        kmix = kmix && (t[i].fmt == KF_Q8_0 || t[i].fmt == KF_Q4_K || t[i].fmt == KF_Q6_K);
-    }
-    if (*fsel < 0 && kmix) *fsel = kFselKQuantMix;
+    KernelSelect sel;
+    for (int i = 0; i < n; ++i) sel.add(t[i]);
+    sel.get(fsel, osel);
 }
 
 int read_fault(uint32_t* flags) {

@@ -164,3 +164,13 @@ def test_status_strings():
     for code in ndq.STATUS:
         assert ndq.ndq_status_string(code)
     assert ndq.ndq_status_string(1234) == "unknown status"
+
+
+def test_failure_path_request_validation():
+    # ndq_test_withhold_copy only records a request for the next launch of
+    # this thread; out-of-range arguments are rejected
+    assert ndq.ndq_test_withhold_copy(-2, 1000) == 13  # NDQ_ERR_BAD_COUNT
+    assert ndq.ndq_test_withhold_copy(0, 0) == 13
+    assert ndq.ndq_test_withhold_copy(0, 2000001) == 13
+    assert ndq.ndq_test_withhold_copy(3, 1000) == 0
+    assert ndq.ndq_test_withhold_copy(-1, 1) == 0  # cancelled

@@ -76,5 +76,5 @@ def test_reference_arm_json_line():
 def test_batched_launch_count_matches_the_library():
     # a batched decode of n tensors: ceil(n / 128) launch-table uploads, one decode
     assert [bench.batched_launches(n) for n in (1, 128, 129, 225)] == [2, 2, 3, 3]
-    src = open(os.path.join(bench.ROOT, "quantized_weight_block_gb300", "csrc", "ndq_kernels.cu")).read()
+    src = open(os.path.join(bench.ROOT, "quantized_weight_block_gb300", "csrc", "ndq_internal.h")).read()
     assert f"constexpr int kUploadChunk = {bench.UPLOAD_CHUNK};" in src

@@ -6,9 +6,11 @@ framework's pool): it keeps the batched launch table in a fixed array inside
 the library instead of a caller-provided workspace.  Here it is called
 through the C ABI and must reproduce, bit for bit (NaN only needs to be
 NaN), what the workspace-based ndq_dequantize_packed_batched produces on the
-same batch, on two calls in a row with different batches (so the second call
-has to overwrite the table the first one left behind).  The file is named to
-be collected last.
+same batch, and what the CPU oracle decodes, on two calls in a row with
+different batches (so the second call has to overwrite the table the first
+one left behind).  One pair of calls uses more than 128 tensors, so the
+table is written by several upload launches, the second call shorter than
+the first.  The file is named to be collected last.
 """
 import numpy as np
 import pytest
@@ -38,6 +40,19 @@ def _batch(seed: int):
     return specs
 
 
+def _many_small(n: int, seed: int):
+    # n tensors of one or two blocks each, formats and output types mixed
+    rng = np.random.default_rng(seed)
+    specs = []
+    for i in range(n):
+        fmt = FORMATS[int(rng.integers(0, len(FORMATS)))]
+        B, _ = synth.GEOMETRY[fmt]
+        shape = (1, B * int(rng.integers(1, 3)))
+        out = list(TORCH_OUT)[int(rng.integers(0, 4))]
+        specs.append((fmt, shape, out, synth.payload(fmt, shape, seed=seed * 1000 + i, dist="bytes")))
+    return specs
+
+
 def _descs(specs):
     descs, ys, keep = [], [], []
     for fmt, shape, out, x in specs:
@@ -63,21 +78,32 @@ def _with_workspace(specs):
     return [_bits(y, s[2]) for y, s in zip(ys, specs)]
 
 
-def test_noalloc_matches_workspace_call_on_two_calls():
-    batches = [_batch(1), _batch(2)]
+def _two_calls_in_a_row(orc, batches):
     expected = [_with_workspace(b) for b in batches]
     stream = torch.cuda.current_stream().cuda_stream
     runs = []
-    for b in batches:  # two calls in a row on the same stream
+    for b in batches:  # calls in a row on the same stream
         descs, ys, keep = _descs(b)
         rc = ndq.ndq_dequantize_packed_batched_noalloc(descs, stream)
         assert rc == 0, ndq.ndq_status_string(rc)
         runs.append((ys, keep))
     torch.cuda.synchronize()
     for b, exp, (ys, _) in zip(batches, expected, runs):
-        for (fmt, shape, out, _), want, y in zip(b, exp, ys):
-            assert_bit_exact(_bits(y, out), want, out, f"no-alloc {fmt} {shape} {out}")
+        for (fmt, shape, out, x), want, y in zip(b, exp, ys):
+            got = _bits(y, out)
+            assert_bit_exact(got, want, out, f"no-alloc vs workspace call {fmt} {shape} {out}")
+            assert_bit_exact(got, orc.decode(fmt, shape, x, out), out, f"no-alloc vs oracle {fmt} {shape} {out}")
     assert ndq.get_device_fault() == 0
+
+
+def test_noalloc_matches_workspace_call_and_oracle_on_two_calls(orc):
+    _two_calls_in_a_row(orc, [_batch(1), _batch(2)])
+
+
+def test_noalloc_tables_of_several_upload_chunks(orc):
+    # 300 tensors (three upload launches), then 150 (two): the second call
+    # rewrites the first 150 entries and leaves the rest of the first table
+    _two_calls_in_a_row(orc, [_many_small(300, 3), _many_small(150, 4)])
 
 
 def test_noalloc_rejects_batches_beyond_its_table():
