@@ -61,6 +61,15 @@ namespace {
 constexpr int kConsumerWarps = kThreads / 32;     // 8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;             // 2 s
 
+// Decode kernel shared memory: decode_stages() payload stages, the header,
+// for 16-bit outputs each consumer warp's two output buffers (its 1024
+// outputs of a tile, written to global memory by bulk copies), then the
+// nvfp4 tables.
+constexpr int kWarpOut = kTileElems / kConsumerWarps;               // 1024 outputs per warp per tile
+constexpr int kOutBufBytes = kWarpOut * 2;                          // one warp's 16-bit outputs of a tile
+constexpr int kOutStageBytes = kConsumerWarps * 2 * kOutBufBytes;  // 32 KB
+constexpr int kLutBytes = 256 * 16;                                 // nvfp4 byte table (16 bytes per scale)
+
 static_assert(kInStride >= kMaxTileBytes + 15 + 15 + 12, "stage size");
 static_assert(kInStride % 128 == 0, "stage alignment");
 
@@ -161,6 +170,32 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// TMA bulk copy shared -> global of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's earlier shared-memory writes before later bulk copies
+// (the async proxy) that read them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory byte access and exact scalar constructions.
 // ---------------------------------------------------------------------------
@@ -218,6 +253,72 @@ __device__ __forceinline__ float h2f(uint32_t h) {
 template <int I>
 __device__ __forceinline__ float byte_minus(uint32_t w, float bias) {
     return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)), bias);
+}
+
+// A signed byte (given as its unsigned byte b) as an exact float.
+__device__ __forceinline__ float i8_float(uint32_t b) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | (b ^ 0x80u)), 8388736.0f);  // (b ^ 128) - 128
+}
+
+// A small unsigned integer u (< 2^23) as an exact float.
+__device__ __forceinline__ float small_uint(uint32_t u) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | u), 8388608.0f);
+}
+
+// Pairs of binary32 values for Blackwell's two-lane FP32 instructions: each
+// lane of {sub,mul,fma}.rn.f32x2 is the correctly rounded scalar operation
+// (round to nearest even, subnormals kept), so a pair operation gives the
+// bits of two __fsub_rn / __fmul_rn / __fmaf_rn at half the issue cost.
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 r;
+    asm("{.reg .b64 a, b, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 r, a, b;\n\t"
+        "mov.b64 {%0, %1}, r;}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{.reg .b64 a, b, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 r, a, b;\n\t"
+        "mov.b64 {%0, %1}, r;}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{.reg .b64 a, b, c, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 r, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, r;}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// Bytes I and I+1 of w as the floats 2^23 + byte, minus `bias` (2^23 + code
+// offset): exact.
+template <int I>
+__device__ __forceinline__ float2 bytes_minus2(uint32_t w, float bias) {
+    return sub2(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)),
+                            __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (I + 1)))),
+                make_float2(bias, bias));
+}
+
+// Byte I of a and byte I of b, likewise.
+template <int I>
+__device__ __forceinline__ float2 bytes_minus2(uint32_t a, uint32_t b, float bias) {
+    return sub2(make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540u | I)),
+                            __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7540u | I))),
+                make_float2(bias, bias));
 }
 
 // MXFP4 half scale: the FLOAT with bit pattern 0x00200000 * 2^e for e < 2,
@@ -310,16 +411,34 @@ __device__ __forceinline__ uint4 lds_16(const uint8_t* base, uint32_t off) {
 // Four bytes of w (values < 256) as exact floats minus the code offset, times
 // d: v[i] = M(d, byte_i - offset) with bias = 2^23 + offset.
 __device__ __forceinline__ void mul4(float d, uint32_t w, float bias, float* v) {
-    v[0] = __fmul_rn(d, byte_minus<0>(w, bias));
-    v[1] = __fmul_rn(d, byte_minus<1>(w, bias));
-    v[2] = __fmul_rn(d, byte_minus<2>(w, bias));
-    v[3] = __fmul_rn(d, byte_minus<3>(w, bias));
+    const float2 dd = make_float2(d, d);
+    const float2 a = mul2(dd, bytes_minus2<0>(w, bias)), b = mul2(dd, bytes_minus2<2>(w, bias));
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = b.x;
+    v[3] = b.y;
+}
+
+// v[i] = fma(a, byte_i - offset, c): one rounding of a * byte + c, used only
+// where the product is exact in binary32.
+__device__ __forceinline__ void fma4(float a, uint32_t w, float bias, float c, float* v) {
+    const float2 aa = make_float2(a, a), cc = make_float2(c, c);
+    const float2 x = fma2(aa, bytes_minus2<0>(w, bias), cc), y = fma2(aa, bytes_minus2<2>(w, bias), cc);
+    v[0] = x.x;
+    v[1] = x.y;
+    v[2] = y.x;
+    v[3] = y.y;
 }
 
 // Table lookup of four nibbles (bytes of w) scaled by d: v[i] = M(d, T[n_i]).
 __device__ __forceinline__ void lut4(const float* T, float d, uint32_t w, float* v) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(d, T[(w >> (8 * i)) & 15u]);
+    const float2 dd = make_float2(d, d);
+    const float2 a = mul2(dd, make_float2(T[w & 15u], T[(w >> 8) & 15u]));
+    const float2 b = mul2(dd, make_float2(T[(w >> 16) & 15u], T[(w >> 24) & 15u]));
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = b.x;
+    v[3] = b.y;
 }
 
 template <int F>
@@ -499,22 +618,18 @@ struct Fmt<KF_Q4_K> {
         const bool lo = k < 4u;
         const uint32_t sa = lo ? (b0 & 63u) : ((b2 & 15u) | ((b0 >> 6) << 4));
         const uint32_t sm = lo ? (b1 & 63u) : ((b2 >> 4) | ((b1 >> 6) << 4));
-        const float da = __fmul_rn(d, static_cast<float>(sa));
-        const float ndm = -__fmul_rn(dmin, static_cast<float>(sm));
+        const float da = __fmul_rn(d, small_uint(sa));
+        const float ndm = -__fmul_rn(dmin, small_uint(sm));
         const uint4 n = nib_plane16(lds_16<!PH>(in, off + 16u + 32u * (cc >> 2) + 16u * (cc & 1u)), k & 1u);
         // D(M(da, v), dm) as one fused multiply-add: da = M(d, a) has at most
         // 17 significant bits and v at most 4, so M(da, v) is exact in
         // binary32 and the FMA rounds the same exact difference once (the
         // product cannot overflow, and inf/NaN/zero cases match term by term).
         const float bias = 8388608.0f;  // 2^23
-        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[4 * q + 0] = __fmaf_rn(da, byte_minus<0>(w[q], bias), ndm);
-            v[4 * q + 1] = __fmaf_rn(da, byte_minus<1>(w[q], bias), ndm);
-            v[4 * q + 2] = __fmaf_rn(da, byte_minus<2>(w[q], bias), ndm);
-            v[4 * q + 3] = __fmaf_rn(da, byte_minus<3>(w[q], bias), ndm);
-        }
+        fma4(da, n.x, bias, ndm, v);
+        fma4(da, n.y, bias, ndm, v + 4);
+        fma4(da, n.z, bias, ndm, v + 8);
+        fma4(da, n.w, bias, ndm, v + 12);
     }
 };
 
@@ -529,8 +644,7 @@ struct Fmt<KF_Q6_K> {
     __device__ __forceinline__ static void chunk(const uint8_t* in, uint32_t ph, uint32_t c, float* v, const Ctx&) {
         const uint32_t off = ph + (c >> 4) * S, cc = c & 15u, gi = cc >> 3;
         const float d = h2f(lds_2<PH>(in, off + 208u));
-        const int32_t sc = static_cast<int8_t>(in[off + 192u + cc]);
-        const float ds = __fmul_rn(d, static_cast<float>(sc));
+        const float ds = __fmul_rn(d, i8_float(in[off + 192u + cc]));
         const uint4 lo = lds_16<false>(in, off + 64u * gi + 16u * (cc & 3u));
         const uint4 hi = lds_16<false>(in, off + 128u + 32u * gi + 16u * (cc & 1u));
         const uint32_t pl = 4u * ((cc >> 2) & 1u), phh = 2u * ((cc >> 1) & 3u);
@@ -549,8 +663,8 @@ struct Fmt<KF_Q6_K> {
                                                      const Ctx&) {
         const uint32_t off = ph + (c >> 4) * S, cc = c & 14u, gi = cc >> 3, h = c & 1u;
         const float d = h2f(lds_2<PH>(in, off + 208u));
-        const float ds0 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(in[off + 192u + cc])));
-        const float ds1 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(in[off + 193u + cc])));
+        const float ds0 = __fmul_rn(d, i8_float(in[off + 192u + cc]));
+        const float ds1 = __fmul_rn(d, i8_float(in[off + 193u + cc]));
         const uint32_t lb = off + 64u * gi + 16u * (cc & 3u), hb = off + 128u + 32u * gi;
         const uint2 la = lds_8(in, lb + 8u * h), lbb = lds_8(in, lb + 24u - 8u * h);
         const uint2 ha = lds_8(in, hb + 8u * h), hbb = lds_8(in, hb + 24u - 8u * h);
@@ -582,14 +696,17 @@ struct Fmt<KF_Q4_G64> {
         for (int h = 0; h < 2; ++h) {
             const uint32_t lo = (wv[h] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((wv[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
             float* o = v + 8 * h;
-            o[0] = __fmul_rn(s, byte_minus<0>(lo, bias));
-            o[1] = __fmul_rn(s, byte_minus<0>(hi, bias));
-            o[2] = __fmul_rn(s, byte_minus<1>(lo, bias));
-            o[3] = __fmul_rn(s, byte_minus<1>(hi, bias));
-            o[4] = __fmul_rn(s, byte_minus<2>(lo, bias));
-            o[5] = __fmul_rn(s, byte_minus<2>(hi, bias));
-            o[6] = __fmul_rn(s, byte_minus<3>(lo, bias));
-            o[7] = __fmul_rn(s, byte_minus<3>(hi, bias));
+            const float2 ss = make_float2(s, s);
+            const float2 a = mul2(ss, bytes_minus2<0>(lo, hi, bias)), b = mul2(ss, bytes_minus2<1>(lo, hi, bias));
+            const float2 e = mul2(ss, bytes_minus2<2>(lo, hi, bias)), f = mul2(ss, bytes_minus2<3>(lo, hi, bias));
+            o[0] = a.x;
+            o[1] = a.y;
+            o[2] = b.x;
+            o[3] = b.y;
+            o[4] = e.x;
+            o[5] = e.y;
+            o[6] = f.x;
+            o[7] = f.y;
         }
     }
 };
@@ -614,15 +731,11 @@ struct Fmt<KF_Q4_1> {
         const uint32_t off = ph + (c >> 1) * S;
         const float d = h2f(lds_2<PH>(in, off)), m = h2f(lds_2<PH>(in, off + 2u));
         const uint4 n = nib_plane16(lds_16<false>(in, off + 4u), c & 1u);
-        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
         const float bias = 8388608.0f;  // 2^23
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[4 * q + 0] = __fmaf_rn(d, byte_minus<0>(w[q], bias), m);
-            v[4 * q + 1] = __fmaf_rn(d, byte_minus<1>(w[q], bias), m);
-            v[4 * q + 2] = __fmaf_rn(d, byte_minus<2>(w[q], bias), m);
-            v[4 * q + 3] = __fmaf_rn(d, byte_minus<3>(w[q], bias), m);
-        }
+        fma4(d, n.x, bias, m, v);
+        fma4(d, n.y, bias, m, v + 4);
+        fma4(d, n.z, bias, m, v + 8);
+        fma4(d, n.w, bias, m, v + 12);
     }
 };
 
@@ -643,11 +756,7 @@ struct Q5Impl {
         for (int q = 0; q < 4; ++q) {
             const uint32_t u = w[q] | spread4_b4((hb >> (4 * q)) & 15u);
             if (AFF) {
-                const float bias = 8388608.0f;  // 2^23
-                v[4 * q + 0] = __fmaf_rn(d, byte_minus<0>(u, bias), m);
-                v[4 * q + 1] = __fmaf_rn(d, byte_minus<1>(u, bias), m);
-                v[4 * q + 2] = __fmaf_rn(d, byte_minus<2>(u, bias), m);
-                v[4 * q + 3] = __fmaf_rn(d, byte_minus<3>(u, bias), m);
+                fma4(d, u, 8388608.0f, m, v + 4 * q);  // 2^23
             } else {
                 mul4(d, u, 8388624.0f, v + 4 * q);  // 2^23 + 16
             }
@@ -728,18 +837,14 @@ struct Fmt<KF_Q2_K> {
         const uint32_t off = ph + (c >> 4) * S, cc = c & 15u;
         const uint32_t sc = in[off + cc];
         const float d = h2f(lds_2<PH>(in, off + 80u)), dmin = h2f(lds_2<PH>(in, off + 82u));
-        const float ds = __fmul_rn(d, static_cast<float>(sc & 15u));
-        const float ndm = -__fmul_rn(dmin, static_cast<float>(sc >> 4));
+        const float ds = __fmul_rn(d, small_uint(sc & 15u));
+        const float ndm = -__fmul_rn(dmin, small_uint(sc >> 4));
         const uint4 n = plane2_16(lds_16<false>(in, off + 16u + 32u * (cc >> 3) + 16u * (cc & 1u)), (cc >> 1) & 3u);
-        const uint32_t w[4] = {n.x, n.y, n.z, n.w};
         const float bias = 8388608.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[4 * q + 0] = __fmaf_rn(ds, byte_minus<0>(w[q], bias), ndm);
-            v[4 * q + 1] = __fmaf_rn(ds, byte_minus<1>(w[q], bias), ndm);
-            v[4 * q + 2] = __fmaf_rn(ds, byte_minus<2>(w[q], bias), ndm);
-            v[4 * q + 3] = __fmaf_rn(ds, byte_minus<3>(w[q], bias), ndm);
-        }
+        fma4(ds, n.x, bias, ndm, v);
+        fma4(ds, n.y, bias, ndm, v + 4);
+        fma4(ds, n.z, bias, ndm, v + 8);
+        fma4(ds, n.w, bias, ndm, v + 12);
     }
 };
 
@@ -756,7 +861,7 @@ struct Fmt<KF_Q3_K> {
         const float d = h2f(lds_2<PH>(in, off + 108u));
         const uint32_t l = (in[off + 96u + (cc & 7u)] >> (4u * (cc >> 3))) & 15u;
         const uint32_t a = (in[off + 104u + (cc & 3u)] >> (2u * (cc >> 2))) & 3u;
-        const float ds = __fmul_rn(d, static_cast<float>(static_cast<int32_t>(l + 16u * a) - 32));
+        const float ds = __fmul_rn(d, __fsub_rn(__uint_as_float(0x4B000000u | (l + 16u * a)), 8388640.0f));  // - 32
         const uint4 vq = plane2_16(lds_16<false>(in, off + 32u + 32u * (cc >> 3) + 16u * (cc & 1u)), (cc >> 1) & 3u);
         const uint4 hm = plane1_16(lds_16<false>(in, off + 16u * (cc & 1u)), cc >> 1);
         // v - 4*(1 - h) = (v + 4h) - 4
@@ -783,19 +888,15 @@ struct Fmt<KF_Q5_K> {
         const bool lo = k < 4u;
         const uint32_t sa = lo ? (b0 & 63u) : ((b2 & 15u) | ((b0 >> 6) << 4));
         const uint32_t sm = lo ? (b1 & 63u) : ((b2 >> 4) | ((b1 >> 6) << 4));
-        const float da = __fmul_rn(d, static_cast<float>(sa));
-        const float ndm = -__fmul_rn(dmin, static_cast<float>(sm));
+        const float da = __fmul_rn(d, small_uint(sa));
+        const float ndm = -__fmul_rn(dmin, small_uint(sm));
         const uint4 n = nib_plane16(lds_16<!PH>(in, off + 48u + 32u * (cc >> 2) + 16u * (cc & 1u)), k & 1u);
         const uint4 hb = plane1_16(lds_16<!PH>(in, off + 16u + 16u * (cc & 1u)), k);
-        const uint32_t w[4] = {n.x | (hb.x << 4), n.y | (hb.y << 4), n.z | (hb.z << 4), n.w | (hb.w << 4)};
         const float bias = 8388608.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[4 * q + 0] = __fmaf_rn(da, byte_minus<0>(w[q], bias), ndm);
-            v[4 * q + 1] = __fmaf_rn(da, byte_minus<1>(w[q], bias), ndm);
-            v[4 * q + 2] = __fmaf_rn(da, byte_minus<2>(w[q], bias), ndm);
-            v[4 * q + 3] = __fmaf_rn(da, byte_minus<3>(w[q], bias), ndm);
-        }
+        fma4(da, n.x | (hb.x << 4), bias, ndm, v);
+        fma4(da, n.y | (hb.y << 4), bias, ndm, v + 4);
+        fma4(da, n.z | (hb.z << 4), bias, ndm, v + 8);
+        fma4(da, n.w | (hb.w << 4), bias, ndm, v + 12);
     }
 };
 
@@ -812,8 +913,8 @@ struct Fmt<KF_IQ4_XS> {
         const float d = h2f(lds_2<PH>(in, off));
         const uint32_t high = lds_2<PH>(in, off + 2u);
         const uint32_t lo4 = (in[off + 4u + (k >> 1)] >> (4u * (k & 1u))) & 15u;
-        const int32_t sc = static_cast<int32_t>(lo4 | (((high >> (2u * k)) & 3u) << 4)) - 32;
-        const float ds = __fmul_rn(d, static_cast<float>(sc));
+        const uint32_t sc = lo4 | (((high >> (2u * k)) & 3u) << 4);  // s + 32
+        const float ds = __fmul_rn(d, __fsub_rn(__uint_as_float(0x4B000000u | sc), 8388640.0f));
         const uint4 n = nib_plane16(lds_16<false>(in, off + 8u + 16u * k), cc & 1u);
         const float* T = x.H->lut_iq4;
         lut4(T, ds, n.x, v);
@@ -1503,10 +1604,22 @@ __device__ __forceinline__ void store16_pairs(uint16_t* y, uint64_t e0, const ui
     }
 }
 
-// A 16-byte-aligned nvfp4 stage through the table (row s at L[s]).  One
-// group of 16 outputs per chunk: scale byte g of the block, then 8 code
-// bytes whose low nibbles are outputs 0..7 and high nibbles outputs 8..15
-// (the blocks' 36-byte stride keeps them 4-byte aligned).
+// Chunk c (16 outputs) of a 16-byte-aligned nvfp4 stage through the table
+// (row s at L[s]), as 8 words of output pairs: group g = c & 3 of block
+// c >> 2 is its scale byte, then 8 code bytes whose low nibbles are outputs
+// 0..7 and high nibbles outputs 8..15 (the blocks' 36-byte stride keeps them
+// 4-byte aligned).
+__device__ __forceinline__ void lut16_chunk(const uint8_t* in, const uint4* L, uint32_t c, uint32_t* w) {
+    const uint32_t off = (c >> 2) * 36u, g = c & 3u;
+    const uint32_t s = in[off + g];
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(in + off + 4u + 8u * g);
+    const uint4 r = L[s];
+    lut16_word(qw[0], r, w[0], w[1], w[4], w[5]);
+    lut16_word(qw[1], r, w[2], w[3], w[6], w[7]);
+}
+
+// A 16-byte-aligned nvfp4 stage through the table, every consumer thread
+// storing its chunks itself.
 __device__ __forceinline__ void decode_tile_lut16(const StageInfo& si, const uint8_t* in, const uint4* L, uint32_t tid) {
     uint16_t* y = static_cast<uint16_t*>(si.t.y);
     const bool vec = si.t.yvec != 0;
@@ -1516,19 +1629,97 @@ __device__ __forceinline__ void decode_tile_lut16(const StageInfo& si, const uin
         const uint32_t c = tid + static_cast<uint32_t>(k * kThreads);
         const bool ok = c < nch;
         uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (ok) {
-            const uint32_t off = (c >> 2) * 36u, g = c & 3u;
-            const uint32_t s = in[off + g];
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(in + off + 4u + 8u * g);
-            const uint4 r = L[s];
-            lut16_word(qw[0], r, w[0], w[1], w[4], w[5]);
-            lut16_word(qw[1], r, w[2], w[3], w[6], w[7]);
-        }
+        if (ok) lut16_chunk(in, L, c, w);
         const uint64_t e0 = si.block0 * 64u + 16u * c;
         if (vec)  // (uniform over the warp)
             store16_pairs(y, e0, w, c & 1u, ok, (c | 1u) < nch);
         else if (ok)
             store_words16<8>(y + e0, w, false);
+    }
+}
+
+// Chunk c of a 16-byte-aligned stage as CE/2 words of 16-bit output pairs of
+// type O (LUT: the nvfp4 byte table L).
+template <int F, int O, bool LUT>
+__device__ __forceinline__ void chunk_words(const uint8_t* in, uint32_t c, const Ctx& x, const uint4* L, uint32_t* w) {
+    using Fm = Fmt<F>;
+    if constexpr (LUT) {
+        lut16_chunk(in, L, c, w);
+    } else if constexpr (has_chunk16<F>::value) {
+        Fm::template chunk16<false, O>(in, 0u, c, w, x);
+    } else {
+        float v[Fm::CE];
+        Fm::template chunk<false>(in, 0u, c, v, x);
+#pragma unroll
+        for (int i = 0; i < Fm::CE / 2; ++i)
+            w[i] = (O == KO_BF16) ? pack_bf16(v[2 * i], v[2 * i + 1]) : pack_f16(v[2 * i], v[2 * i + 1]);
+    }
+}
+
+// One consumer warp's share of a full, 16-byte-aligned stage with a 16-bit
+// output: the warp's kWarpOut consecutive outputs (chunks cw0 + 32k +
+// lane), written in output order to the warp's output buffer `ob`, which the
+// caller copies to y with one bulk copy.  Chunk j of the share is bytes
+// [2*CE*j, 2*CE*(j+1)) of the buffer.
+template <int F, int O, bool LUT>
+__device__ __forceinline__ void decode_warp16(const uint8_t* in, const Ctx& x, const uint4* L, uint32_t warp,
+                                              uint32_t lane, uint8_t* ob) {
+    constexpr int CE = LUT ? 16 : Fmt<F>::CE;
+    constexpr int kPer = kWarpOut / CE / 32;  // chunks per lane
+    const uint32_t cw0 = warp * static_cast<uint32_t>(kWarpOut / CE);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const uint32_t j = static_cast<uint32_t>(32 * k) + lane;
+        uint32_t w[CE / 2];
+        chunk_words<F, O, LUT>(in, cw0 + j, x, L, w);
+        uint4* d = reinterpret_cast<uint4*>(ob) + j * static_cast<uint32_t>(CE / 8);
+#pragma unroll
+        for (int q = 0; q < CE / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+}
+
+// Output type dispatch (OSEL < 0: the tensor's own 16-bit type).
+template <int F, int OSEL, bool LUT>
+__device__ __forceinline__ void decode_warp16_o(const StageInfo& si, const uint8_t* in, const Ctx& x, const uint4* L,
+                                                uint32_t warp, uint32_t lane, uint8_t* ob) {
+    if constexpr (OSEL == KO_F16) {
+        decode_warp16<F, KO_F16, LUT>(in, x, L, warp, lane, ob);
+    } else if constexpr (OSEL == KO_BF16) {
+        decode_warp16<F, KO_BF16, LUT>(in, x, L, warp, lane, ob);
+    } else if constexpr (OSEL < 0) {
+        if (si.t.out == KO_F16)
+            decode_warp16<F, KO_F16, false>(in, x, L, warp, lane, ob);
+        else
+            decode_warp16<F, KO_BF16, false>(in, x, L, warp, lane, ob);
+    }
+}
+
+// Format dispatch of a staged warp share (FSEL / OSEL as for k_decode).
+template <int FSEL, int OSEL>
+__device__ __forceinline__ void decode_warp16_fast(const StageInfo& si, const uint8_t* in, const Ctx& x,
+                                                   const uint4* L, uint32_t warp, uint32_t lane, uint8_t* ob) {
+    if constexpr (FSEL >= 0) {
+        decode_warp16_o<FSEL, OSEL, uses_lut16(FSEL, OSEL)>(si, in, x, L, warp, lane, ob);
+    } else if constexpr (FSEL == kFselKQuantMix) {
+        switch (si.t.fmt) {
+            case KF_Q8_0: decode_warp16_o<KF_Q8_0, OSEL, false>(si, in, x, L, warp, lane, ob); break;
+            case KF_Q4_K: decode_warp16_o<KF_Q4_K, OSEL, false>(si, in, x, L, warp, lane, ob); break;
+            default: decode_warp16_o<KF_Q6_K, OSEL, false>(si, in, x, L, warp, lane, ob); break;
+        }
+    } else {
+        switch (si.t.fmt) {
+#define NDQ_W16(K) \
+    case K: decode_warp16_o<K, OSEL, false>(si, in, x, L, warp, lane, ob); break;
+            NDQ_W16(KF_Q8_0) NDQ_W16(KF_Q4_0) NDQ_W16(KF_IQ4_NL) NDQ_W16(KF_Q4_K) NDQ_W16(KF_Q6_K)
+            NDQ_W16(KF_MXFP4) NDQ_W16(KF_GGUF_NVFP4) NDQ_W16(KF_NVFP4) NDQ_W16(KF_Q4_1) NDQ_W16(KF_Q5_0)
+            NDQ_W16(KF_Q5_1) NDQ_W16(KF_Q8_1) NDQ_W16(KF_Q8_K) NDQ_W16(KF_Q2_K) NDQ_W16(KF_Q3_K) NDQ_W16(KF_Q5_K)
+            NDQ_W16(KF_IQ4_XS) NDQ_W16(KF_TQ1_0) NDQ_W16(KF_TQ2_0) NDQ_W16(KF_Q1_0) NDQ_W16(KF_Q2_0)
+            NDQ_W16(KF_IQ2_XXS) NDQ_W16(KF_IQ2_XS) NDQ_W16(KF_IQ2_S) NDQ_W16(KF_IQ3_XXS) NDQ_W16(KF_IQ3_S)
+            NDQ_W16(KF_IQ1_S) NDQ_W16(KF_IQ1_M) NDQ_W16(KF_Q5_G64) NDQ_W16(KF_Q6_G64) NDQ_W16(KF_T2_G128)
+            NDQ_W16(KF_FP8_ROW_BF16) NDQ_W16(KF_FP8_ROW_FP16)
+#undef NDQ_W16
+            default: decode_warp16_o<KF_Q4_G64, OSEL, false>(si, in, x, L, warp, lane, ob); break;
+        }
     }
 }
 
@@ -1747,7 +1938,34 @@ __device__ __forceinline__ void decode_tile_fast(const StageInfo& si, const uint
 // ---------------------------------------------------------------------------
 // Producer warp (lane 0): stages tiles it = 0, 1, ... of this CTA.
 // ---------------------------------------------------------------------------
+// The payload span of a tile: its first block, block count, source and the
+// 16-byte lines holding it (from the line below its first byte to the line
+// above its last; an fp8 row tensor's span stops at the end of its code
+// plane, before the row multipliers).
+struct TileSpan {
+    uint64_t b0;
+    const uint8_t* src;
+    uint32_t nb, phase, bytes;
+};
+__device__ __forceinline__ TileSpan tile_span(const DevTensor& t, uint64_t tile) {
+    TileSpan r;
+    r.b0 = (tile - t.tile_begin) * t.bpt;
+    const uint64_t left = t.nblocks - r.b0;
+    r.nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
+    r.src = t.x + r.b0 * t.S;
+    r.phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(r.src) & 15u);
+    uint32_t span = r.nb * t.S;
+    if (t.fmt == KF_FP8_ROW_BF16 || t.fmt == KF_FP8_ROW_FP16) {
+        const uint64_t plane = reinterpret_cast<uintptr_t>(t.divs) - reinterpret_cast<uintptr_t>(r.src);
+        if (plane < span) span = static_cast<uint32_t>(plane);
+    }
+    r.bytes = (r.phase + span + 15u) & ~15u;
+    return r;
+}
+
+template <int NST>
 __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
+    static_assert(NST <= kStages, "decode stages");
     const uint64_t grid = gridDim.x;
     int32_t di = 0;   // current tensor (tiles of a CTA increase, so it only moves forward)
     int issued = 0;   // tiles staged so far
@@ -1759,9 +1977,9 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
     uint32_t nv_same = 0;
     int withheld = -1;  // staging whose copy was withheld on request (never completes)
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++issued) {
-        const int s = issued % kStages;
-        if (issued >= kStages &&
-            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kStages) - 1) & 1), p.wait_ns)) {
+        const int s = issued % NST;
+        if (issued >= NST &&
+            !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / NST) - 1) & 1), p.wait_ns)) {
             fault = true;
             break;
         }
@@ -1777,18 +1995,10 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
         const DevTensor& t = p.table ? p.table[di] : p.single;
         StageInfo& si = H.info[s];
         si.t = t;
-        const uint64_t b0 = (tile - t.tile_begin) * t.bpt;
-        const uint64_t left = t.nblocks - b0;
-        const uint32_t nb = left < t.bpt ? static_cast<uint32_t>(left) : t.bpt;
-        const uint8_t* src = t.x + b0 * t.S;
-        const uint32_t phase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-        uint32_t span = nb * t.S;
-        if (t.fmt == KF_FP8_ROW_BF16 || t.fmt == KF_FP8_ROW_FP16) {
-            // stop at the end of the code plane (the row multipliers follow it)
-            const uint64_t plane = reinterpret_cast<uintptr_t>(t.divs) - reinterpret_cast<uintptr_t>(src);
-            if (plane < span) span = static_cast<uint32_t>(plane);
-        }
-        const uint32_t bytes = (phase + span + 15u) & ~15u;
+        const TileSpan sp = tile_span(t, tile);
+        const uint64_t b0 = sp.b0;
+        const uint32_t nb = sp.nb, phase = sp.phase, bytes = sp.bytes;
+        const uint8_t* src = sp.src;
         if (t.fmt == KF_FP8_ROW_BF16 || t.fmt == KF_FP8_ROW_FP16) {  // one division per tile
             const uint64_t e0 = b0 * 16u;
             si.row0 = e0 / t.blocks_per_div;
@@ -1814,12 +2024,12 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
     if (fault) atomicOr(p.fault, 1u);
     if (fault || withheld >= 0) {
         // The consumers may have stopped early: wait (bounded) for every copy
-        // still in flight before the CTA can exit.  Only the last kStages
+        // still in flight before the CTA can exit.  Only the last NST
         // stagings can be in flight (an older stage was reused only after the
         // consumers released it); a withheld staging has no copy.
-        for (int j = issued - kStages; j < issued; ++j)
+        for (int j = issued - NST; j < issued; ++j)
             if (j >= 0 && j != withheld)
-                mbar_wait_bounded(&H.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+                mbar_wait_bounded(&H.full[j % NST], static_cast<uint32_t>((j / NST) & 1));
     }
 }
 
@@ -1829,16 +2039,19 @@ __device__ void producer(const KParams& p, SmemHdr& H, uint8_t* inbuf) {
 template <int FSEL, int OSEL>
 __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr bool kStaged = decode_staged(FSEL, OSEL);
+    constexpr int NST = decode_stages(FSEL);
     uint8_t* inbuf = smem;
-    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kStages * kInStride);
-    float* tab = reinterpret_cast<float*>(smem + kStages * kInStride + kHdrBytes);
+    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + NST * kInStride);
+    uint8_t* outbuf = smem + NST * kInStride + kHdrBytes;  // (16-bit outputs only)
+    float* tab = reinterpret_cast<float*>(outbuf + (kStaged ? kOutStageBytes : 0));
     const uint32_t tid = threadIdx.x;
     constexpr bool kLut = uses_lut16(FSEL, OSEL);
 
     // Shared-memory set-up that reads nothing another kernel writes runs
     // before the wait below, overlapping the previous kernel's tail.
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&H.full[s], 1);
             mbar_init(&H.empty[s], kConsumerWarps);
         }
@@ -1847,6 +2060,20 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     if (tid < 16) {
         H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
         H.lut_v[tid] = static_cast<float>(c_v[tid]);
+    }
+
+    // A single-tensor launch knows its tiles from its parameters: the
+    // producer warms L2 with this CTA's first spans while the previous
+    // kernel of the stream may still run.  A prefetch returns no data to the
+    // CTA, so it cannot observe that kernel's unfinished writes (L2 is where
+    // they land); the staging copies read the spans after the wait below.
+    if (p.table == nullptr && tid == kThreads) {
+        for (int j = 0; j < NST; ++j) {
+            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+            if (tile >= p.total_tiles) break;
+            const TileSpan sp = tile_span(p.single, tile);
+            prefetch_l2(sp.src - sp.phase, sp.bytes);
+        }
     }
 
     // Programmatic dependent launch: this grid may have started before the
@@ -1867,7 +2094,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
     __syncthreads();
 
     if (tid >= kThreads) {  // producer warp: starts staging while the consumers build the tables
-        if (tid == kThreads) producer(p, H, inbuf);
+        if (tid == kThreads) producer<NST>(p, H, inbuf);
         return;
     }
 
@@ -1916,14 +2143,19 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
 
     // consumer warps
     const uint64_t grid = gridDim.x;
-    const uint32_t lane = tid & 31u;
+    const uint32_t lane = tid & 31u, warp = tid >> 5;
+    uint8_t* const wbuf = outbuf + warp * (2u * kOutBufBytes);  // this warp's two output buffers
+    uint32_t nstore = 0;  // bulk copies this warp issued (lane 0); buffer nstore & 1 is the next one
     int it = 0;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += grid, ++it) {
-        const int s = it % kStages;
+        const int s = it % NST;
         // (decided by the whole warp: the decoders shuffle between lanes)
         if (!__all_sync(0xffffffffu,
-                        mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / kStages) & 1), p.wait_ns))) {
-            if (lane == 0) atomicOr(p.fault, 2u);
+                        mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((it / NST) & 1), p.wait_ns))) {
+            if (lane == 0) {
+                atomicOr(p.fault, 2u);
+                if (kStaged) bulk_wait_all();  // (the output buffers stay until their copies are read)
+            }
             return;
         }
         const StageInfo& si = H.info[s];
@@ -1937,14 +2169,45 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
                 decode_tile_slow_one<(FSEL >= 0 ? FSEL : 0), OSEL>(si, in, xs, tid);
             else
                 decode_tile_slow(si, in, xs, tid);
-        } else if constexpr (kLut) {
-            decode_tile_lut16(si, in, reinterpret_cast<const uint4*>(tab), tid);
         } else {
-            decode_tile_fast<FSEL, OSEL>(si, in, Ctx{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t), si.row0, si.col0}, tid);
+            const Ctx xf{&H, tab, si.t.divs, si.block0, si.t.blocks_per_div, p.grids, code_count(si.t), si.row0,
+                         si.col0};
+            if constexpr (kStaged) {
+                // A full tile to a 16-byte-aligned 16-bit output: each warp
+                // decodes its 1024 outputs into its own buffer and copies them
+                // to y with one bulk copy (whole lines, no per-lane stores).
+                const bool out16 = OSEL >= 0 || si.t.out == KO_F16 || si.t.out == KO_BF16;
+                const bool kq = FSEL != kFselKQuantMix || si.t.fmt == KF_Q8_0 || si.t.fmt == KF_Q4_K ||
+                                si.t.fmt == KF_Q6_K;
+                const bool full = si.nb == si.t.bpt &&
+                                  (!is_fp8_row(si.t.fmt) || (si.block0 + si.nb) * 16u <= code_count(si.t));
+                if (out16 && kq && full && si.t.yvec) {
+                    uint8_t* ob = wbuf + (nstore & 1u) * kOutBufBytes;
+                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous copy has read it
+                    __syncwarp();
+                    decode_warp16_fast<FSEL, OSEL>(si, in, xf, reinterpret_cast<const uint4*>(tab), warp, lane, ob);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&H.empty[s]);
+                        uint16_t* y = static_cast<uint16_t*>(si.t.y) + si.block0 * si.t.B + warp * kWarpOut;
+                        bulk_store(y, ob, kOutBufBytes);
+                        bulk_commit();
+                    }
+                    ++nstore;
+                    continue;
+                }
+            }
+            if constexpr (kLut) {
+                decode_tile_lut16(si, in, reinterpret_cast<const uint4*>(tab), tid);
+            } else {
+                decode_tile_fast<FSEL, OSEL>(si, in, xf, tid);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&H.empty[s]);
     }
+    if (kStaged && lane == 0) bulk_wait_all();
 }
 
 // Kernel of format F for output type `osel` (launches that mix output types

@@ -16,7 +16,8 @@ KernelFn kernel_generic(int osel) {
 }
 KernelFn kernel_kquant_mix(int osel) { return kernel_row<kFselKQuantMix>(osel); }
 
-size_t decode_smem_bytes(bool tab) {
-    return static_cast<size_t>(kStages * kInStride + kHdrBytes) + (tab ? kTabEntries * sizeof(float) : 0);
+size_t decode_smem_bytes(bool tab, bool lut, bool staged, int stages) {
+    return static_cast<size_t>(stages * kInStride + kHdrBytes) + (staged ? kOutStageBytes : 0) +
+           (tab ? (lut ? static_cast<size_t>(kLutBytes) : kTabEntries * sizeof(float)) : 0);
 }
 }  // namespace ndq

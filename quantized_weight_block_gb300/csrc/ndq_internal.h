@@ -80,6 +80,20 @@ constexpr int kTabEntries = 256 * 16;         // nvfp4 quotient table (floats)
 NDQ_HOST_DEVICE constexpr bool uses_lut16(int fsel, int osel) {
     return fsel == KF_NVFP4 && (osel == KO_F16 || osel == KO_BF16);
 }
+// Decode kernels whose output type is 16-bit (or mixed) stage each warp's
+// share of a full tile in shared memory and write it with one bulk copy
+// (measured faster for most formats), except those measured faster storing
+// from registers: the k-quant mix kernel, gguf:q4_k, gguf:q4_0 and nvfp4.
+NDQ_HOST_DEVICE constexpr bool decode_staged(int fsel, int osel) {
+    return fsel != kFselKQuantMix && fsel != KF_Q4_K && fsel != KF_Q4_0 && fsel != KF_NVFP4 &&
+           (osel < 0 || osel == KO_F16 || osel == KO_BF16);
+}
+// Payload stages in flight per decode CTA: 4 for the kernels that run two
+// CTAs per SM (the launches that mix formats, and the q6_k and fp8 row
+// decoders, whose 16-bit variants need more than 75 registers), else 3.
+NDQ_HOST_DEVICE constexpr int decode_stages(int fsel) {
+    return (fsel < 0 || fsel == KF_Q6_K || fsel == KF_FP8_ROW_BF16 || fsel == KF_FP8_ROW_FP16) ? 4 : 3;
+}
 // Resident CTAs per SM for launches that mix formats (the whole-model decode):
 // measured fastest at 2 even when registers and shared memory allow 3.
 // Single-format launches use every CTA the occupancy calculator allows.
@@ -298,8 +312,10 @@ KernelFn kernel_generic_any();
 KernelFn kernel_generic(int osel);
 KernelFn kernel_kquant_mix(int osel);
 
-// Dynamic shared memory of a decode CTA (with or without the nvfp4 table).
-size_t decode_smem_bytes(bool tab);
+// Dynamic shared memory of a decode CTA: with or without the nvfp4 tables
+// (lut: the 4 KB byte table instead of the 16 KB quotient table), and with
+// or without the 16-bit output buffers.
+size_t decode_smem_bytes(bool tab, bool lut, bool staged, int stages);
 
 // Launch one decode over p.total_tiles tiles on `stream` (a cudaStream_t).
 // Returns 0 or a CUDA error code.

@@ -81,7 +81,6 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 
-size_t smem_bytes(bool tab) { return decode_smem_bytes(tab); }
 
 // Device addresses of the fault word and the IQ codebooks, resolved once per
 // device.
@@ -109,8 +108,10 @@ int launch_decode(const KParams& p, void* stream) {
     if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
     const int fsel = ((p.fsel >= 0 && p.fsel < KF_COUNT) || p.fsel == kFselKQuantMix) ? p.fsel : -1;
     const int osel = (p.osel >= 0 && p.osel <= KO_F64) ? p.osel : -1;
-    const bool tab = p.nv_index >= 0 || uses_lut16(fsel, osel);
-    const size_t smem = smem_bytes(tab);
+    const bool lut = uses_lut16(fsel, osel), staged = decode_staged(fsel, osel);
+    const int stages = decode_stages(fsel);
+    const bool tab = p.nv_index >= 0 || lut;
+    const size_t smem = decode_smem_bytes(tab, lut, staged, stages);
     const KernelFn fn = pick_kernel(fsel, osel);
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     DeviceInfo& di = g_dev[dev];
@@ -123,7 +124,8 @@ int launch_decode(const KParams& p, void* stream) {
     }
     int& cps = di.ctas_per_sm[slot_of(fsel, osel)][tab ? 1 : 0];
     if (cps == 0) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes(true)));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(decode_smem_bytes(true, lut, staged, stages)));
         if (e != cudaSuccess) return static_cast<int>(e);
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
