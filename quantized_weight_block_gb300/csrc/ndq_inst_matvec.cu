@@ -48,9 +48,11 @@ MvKernelFn matvec_for(int kfmt, int variant) {
 }
 
 namespace {
+constexpr int kMvSmemBuckets = static_cast<int>(kMvXBytes / 8192) + 1;  // activation copies in 8 KB steps
 struct MvDeviceInfo {
     int sms = 0;
-    int ctas_per_sm[KF_COUNT][3] = {};  // per decode family and variant; 0 = not yet queried
+    bool attr_set[KF_COUNT][kMvVariants] = {};
+    int ctas_per_sm[KF_COUNT][kMvVariants][kMvSmemBuckets] = {};  // 0 = not yet queried
 };
 MvDeviceInfo g_mv_dev[64];
 }  // namespace
@@ -70,10 +72,29 @@ int launch_matvec(const MvParams& p0, void* stream) {
     // segments of a row are whole tiles, which always do
     const uint64_t unit_rows = static_cast<uint64_t>(p.rows_per_stage);
     const bool aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (unit_rows * p.bpr * p.w.S) % 16u == 0;
-    const int variant = aligned ? (p.m == 1 ? 0 : 1) : 2;
+    // the activations: one row as binary32 or several as bfloat16 in shared
+    // memory when they fit, else read from global memory
+    const uint64_t xf32 = p.K * 4u, xbf16 = static_cast<uint64_t>(p.m) * p.K * 2u;
+    // one row: k_gemv1 (a warp per weight row) when the row fits
+    const bool rows_aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0;
+    int variant = kMvAnyAlign;
+    uint64_t xbytes = 0;
+    if (p.m == 1 && xf32 <= kMvXBytes) {
+        variant = rows_aligned ? kMvOneRowF32 : kMvOneRowF32Any;
+        xbytes = xf32;
+    } else if (aligned && p.m > 1 && p.xvec && xbf16 <= kMvXBytes) {
+        variant = kMvRowsBf16;
+        xbytes = xbf16;
+    } else if (aligned) {
+        variant = kMvRowsGlobal;
+    }
     const MvKernelFn fn = (f >= 0 && f < KF_COUNT) ? matvec_for(f, variant) : nullptr;
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
-    const size_t smem = static_cast<size_t>(kStages * kInStride + kHdrBytes + kMvExtraBytes);
+    const bool one_row = variant == kMvOneRowF32 || variant == kMvOneRowF32Any;
+    const size_t base = one_row ? gemv1_smem_base(p.w.B, p.w.S)
+                                : static_cast<size_t>(kStages * kInStride + kHdrBytes + kMvExtraBytes);
+    const int bucket = static_cast<int>((xbytes + 8191u) / 8192u);
+    const size_t smem = base + static_cast<size_t>(bucket) * 8192u;
     MvDeviceInfo& di = g_mv_dev[dev];
     if (di.sms == 0) {
         int sms = 0;
@@ -81,22 +102,37 @@ int launch_matvec(const MvParams& p0, void* stream) {
         if (e != cudaSuccess) return static_cast<int>(e);
         di.sms = sms;
     }
-    int& cps = di.ctas_per_sm[f][variant];
-    if (cps == 0) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (!di.attr_set[f][variant]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(base + kMvXBytes));
         if (e != cudaSuccess) return static_cast<int>(e);
+        di.attr_set[f][variant] = true;
+    }
+    int& cps = di.ctas_per_sm[f][variant][bucket];
+    if (cps == 0) {
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
         if (e != cudaSuccess) return static_cast<int>(e);
         cps = n > 0 ? n : 1;
     }
-    const uint64_t R = static_cast<uint64_t>(p.rows_per_stage);
-    const uint64_t units = (p.n_rows + R - 1) / R;
+    const uint64_t R = static_cast<uint64_t>(one_row ? kGvRows : p.rows_per_stage);
+    const uint64_t units = (p.n_rows + R - 1) / R;  // (k_gemv1: blocks of 8 rows)
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(units < resident ? units : resident);
     void* args[] = {&p};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kBlockThreads), args, smem,
-                         static_cast<cudaStream_t>(stream));
+    // programmatic stream serialization: the kernel waits on the previous
+    // grid itself (griddepcontrol.wait), after warming L2 with its weights
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kBlockThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
     return static_cast<int>(e);
 }
 

@@ -170,6 +170,23 @@ struct MvParams {
 
 using MvKernelFn = void (*)(MvParams);
 
+// Where a fused kernel reads the activations: a copy in shared memory
+// (binary32 for one row, bfloat16 for several) when it fits in kMvXBytes,
+// else global memory.
+constexpr uint64_t kMvXBytes = 64 * 1024;
+enum MvX : int { kMvXGlobal = 0, kMvXF32 = 1, kMvXBf16 = 2 };
+// Fused kernel variants: 16-byte-aligned payload with one activation row in
+// shared memory (binary32), several rows in shared memory (bfloat16), several
+// rows from global memory; and any payload alignment (rows from global).
+enum MvVariant : int {
+    kMvOneRowF32 = 0,     // one row (k_gemv1), rows 16-byte aligned
+    kMvRowsBf16 = 1,
+    kMvRowsGlobal = 2,
+    kMvAnyAlign = 3,
+    kMvOneRowF32Any = 4,  // one row (k_gemv1), any alignment
+    kMvVariants = 5
+};
+
 // Decode fused into a tensor-core (tcgen05) product (ndq_mma.cuh): tiles of
 // 128 weight rows by bn activation rows, the weights rounded to bfloat16.
 struct MmaParams {

@@ -70,6 +70,33 @@ def test_matmul_against_oracle(orc, fmt, weights):
     _check(_run(fmt, N, K, M, w, x_t, weights=weights), ref, yabs, K, what=f"{fmt} {weights}")
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("weights", ["float32", "bfloat16"])
+def test_matmul_one_row(orc, fmt, weights):
+    # one activation row (a generation step): the activations as binary32 in
+    # shared memory; rows of two segments (8192 + 4096 elements)
+    N, K = 41, 12288
+    w = synth.payload(fmt, (N, K), seed=21)
+    x_t, x_bits = _x_bf16(1, K, 22)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+    _check(_run(fmt, N, K, 1, w, x_t, weights=weights), ref, yabs, K, what=f"{fmt} M=1 {weights}")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q6_k", "gguf:q8_0", "nvfp4", "fp8_e4m3fn_row_bf16"])
+@pytest.mark.parametrize("K,x_off", [(14336, 0), (14336, 1), (20480, 0), (256, 0), (4096, 3)])
+def test_matmul_one_row_activation_sources(orc, fmt, K, x_off):
+    # one row up to K = 16384 is held in shared memory (converted with
+    # 16-byte loads, or element by element when X is not 16-byte aligned);
+    # longer rows are read from global memory
+    B = synth.GEOMETRY[fmt][0]
+    K = K // max(B, 16) * max(B, 16)
+    N = 23
+    w = synth.payload(fmt, (N, K), seed=K + x_off)
+    x_t, x_bits = _x_bf16(1, K, K)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
+    _check(_run(fmt, N, K, 1, w, x_t, x_off=x_off), ref, yabs, K, what=f"{fmt} M=1 K={K} x+{x_off}")
+
+
 @pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q8_0", "gguf:mxfp4", "gguf:iq3_s", "nvfp4", "fp8_e4m3fn_row_fp16"])
 @pytest.mark.parametrize("N,K", [(37, 4096), (13, 2048), (9, 1024), (17, 512), (5, 256), (130, 8192), (3, 12800)])
 def test_matmul_whole_rows_per_stage(orc, fmt, N, K):
