@@ -524,22 +524,25 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
                       ("gguf:q8_0", 128256, 4096)):
         i = next(j for j, s in enumerate(specs) if s.fmt == fmt and s.shape == (N, K))
         w, wb = views[i][1], wviews[i]
-        for M in (1, 8):
+        for M, wdt in ((1, torch.float32), (8, torch.float32), (8, torch.bfloat16)):
             x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
             yf = torch.empty(M, N, device="cuda")
             yb = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
-            tf = timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf))
+            tf = timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf, weight_dtype=wdt))
             tu = timed(lambda: (ndq.dequantize_packed(fmt, (N, K), w, torch.bfloat16, y=wb),
                                 torch.matmul(x, wb.t(), out=yb)))
-            single[f"{fmt.split(':')[-1]}[{N},{K}] M={M}"] = {"fused_us": round(tf * 1e3, 1),
-                                                                "unfused_us": round(tu * 1e3, 1),
-                                                                "speedup": round(tu / tf, 3)}
+            tag = "binary32 weights, CUDA cores" if wdt == torch.float32 else "bfloat16 weights, tensor cores"
+            single[f"{fmt.split(':')[-1]}[{N},{K}] M={M} {tag}"] = {"fused_us": round(tf * 1e3, 1),
+                                                                      "unfused_us": round(tu * 1e3, 1),
+                                                                      "speedup": round(tu / tf, 3)}
     # bfloat16 weights on the tensor cores (tcgen05) for more activation rows
     tensor = {}
-    for fmt, N, K in (("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336)):
-        i = next(j for j, s in enumerate(specs) if s.fmt == fmt and s.shape == (N, K))
+    for fmt, N, K in (("gguf:q4_k", 14336, 4096), ("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336)):
+        i = next(j for j, s in enumerate(specs) if s.shape == (N, K) and (s.fmt == fmt or fmt == "gguf:q4_k"))
         w, wb = views[i][1], wviews[i]
-        for M in (16, 64, 256):
+        if fmt != specs[i].fmt:  # the model has no q4_k FFN tensor: a payload of that shape
+            w = torch.from_numpy(synth.payload(fmt, (N, K), 3)).cuda()
+        for M in (16, 64, 256, 1024):
             x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
             yf = torch.empty(M, N, device="cuda")
             yb = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)

@@ -1,6 +1,7 @@
 // Launcher of the fused decode + product kernels (one per decode family,
 // instantiated beside each family's decode kernels).
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "ndq_matvec.cuh"
 #include "ndq_mma.cuh"
@@ -191,31 +192,45 @@ int launch_mma(const MmaParams& p0, void* stream) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return static_cast<int>(e);
-    // 256 activation rows per tile unless those tiles fill fewer than half of
-    // the SMs; then 128 (twice the decode per activation row, but K can split)
-    if (p.bn > 128 &&
-        2u * ((p.n_rows + kMmaRows - 1) / kMmaRows) * ((p.m_rows + 255u) / 256u) < static_cast<uint64_t>(sms))
-        p.bn = 128;
-    const size_t smem = mma_smem_bytes(p.bn, p.span_bytes);
+    // (bn: the smallest power of two >= M up to 256, so that each weight is
+    // decoded once per 256 activation rows; short grids split K instead)
+    mma_stages(p.bn, p.span_bytes, &p.na, &p.ns);
+    p.aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0 && p.span_bytes % 16u == 0;
+    const size_t smem = mma_smem_bytes(p.bn, p.span_bytes, p.na, p.ns);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
+    // X as a 2-D tensor map: [m_rows, K] bfloat16, boxes of 64 columns (one
+    // 128-byte swizzle span) by bn rows, zero outside X
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;  // (benign race: same value)
+    if (!encode) {
+        void* fp = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fp, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fp) return static_cast<int>(cudaErrorNotSupported);
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fp);
+    }
+    const cuuint64_t gdim[2] = {p.K, p.m_rows};
+    const cuuint64_t gstride[1] = {p.K * 2u};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kMmaK), p.bn};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.x), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return static_cast<int>(cudaErrorInvalidValue);
     const uint64_t tiles_n = (p.n_rows + kMmaRows - 1) / kMmaRows;
     const uint64_t tiles_m = (p.m_rows + p.bn - 1) / p.bn;
-    // Split K over a thread-block cluster of up to 8 CTAs (partial tiles of
-    // 128 x bn <= 128 binary32 fit over the operand stages; every CTA keeps
-    // at least two spans): the largest split whose CTAs number at most one
-    // per SM, or two per SM for tiles of 16 activation rows.  A sweep of
-    // splits 1-8 on GB300 picked these in five of six cases (q4_k
-    // [14336,4096] at 16 rows: 77 -> 59 us with split 2; q6_k [4096,14336]:
-    // 60 us with split 8 at 16 rows, 84 us with split 4 at 64 rows).  Asking
-    // the occupancy calculator for co-resident clusters instead gave
-    // different splits on different boxes (q6_k [4096,14336] at 64 rows:
-    // split 2 and 155 us on one of them).
+    // Split K over a thread-block cluster of up to 8 CTAs (each CTA's partial
+    // tile, 128 x bn binary32, is parked over its operand and span stages;
+    // every CTA keeps at least two spans): the largest split whose CTAs
+    // number at most one per SM (one CTA fills an SM's shared memory).
     const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
     const uint64_t tiles = tiles_n * tiles_m;
-    const uint64_t max_ctas = (p.bn <= 16 ? 2u : 1u) * static_cast<uint64_t>(sms);
+    const uint64_t max_ctas = static_cast<uint64_t>(sms);
+    const bool parks = static_cast<uint64_t>(p.bn) * kMmaRows * 4u <=
+                       static_cast<uint64_t>(p.na) * (kMmaATile + mma_b_tile(p.bn)) +
+                           static_cast<uint64_t>(p.ns) * mma_span_stage(p.span_bytes);
     unsigned split = 1;
-    while (split < kMaxMmaSplit && p.bn <= 128 && spans >= 4u * split && tiles * 2u * split <= max_ctas) split *= 2;
+    while (split < kMaxMmaSplit && parks && spans >= 4u * split && tiles * 2u * split <= max_ctas) split *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m), split);
     cfg.blockDim = dim3(kMmaThreads);

@@ -2,6 +2,8 @@
 // and the decode kernels (ndq_kernels.cu).  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the tensor-core product's activation map)
+
 #include <cstddef>
 #include <cstdint>
 
@@ -201,8 +203,13 @@ struct MmaParams {
     uint32_t span_elems;  // weights per staged span: max(B, 64), whole blocks
     uint32_t span_bytes;  // payload bytes of a full span
     int32_t out_bf16;
+    uint32_t na;          // operand stages (A and B tiles in flight), 2..4 (set by the launcher)
+    uint32_t ns;          // staged payload spans, 2..4 (set by the launcher)
+    uint32_t aligned;     // 1: the payload, its rows and its spans start on 16-byte boundaries
+    uint32_t pad_;
     unsigned int* fault;
     const IqGrids* grids;
+    CUtensorMap xmap;     // X as a 2-D bfloat16 tensor [m_rows, K], boxes of 64 x bn, 128-byte swizzle
 };
 using MmaKernelFn = void (*)(MmaParams);
 MmaKernelFn mma_fp8_row_bf16();

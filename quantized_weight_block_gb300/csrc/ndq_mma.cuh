@@ -8,28 +8,33 @@
 // accumulates in binary32 in TMEM.
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M) by BN activation
-// rows (the MMA's N, 16..256) over its share of K, in k-steps of 64:
-//   * a producer warp copies, for each span of max(B, 64) weights (whole
-//     blocks), the packed bytes of the tile's 128 rows into a two-stage ring
-//     with asynchronous 16-byte copies (rounded out to 16-byte lines that all
-//     hold payload bytes; full/empty mbarriers, each lane's copies counted on
-//     the full barrier as they land);
-//   * 8 consumer warps decode 64-weight slices of the staged span with the
-//     same Fmt<F> decoders, round them to bfloat16 and write them as the A
-//     operand in the 128-byte-swizzled K-major layout, and copy the X slice
-//     [BN x 64] as the B operand in the same layout;
-//   * one thread issues four tcgen05.mma (K = 16 each) and commits them to an
-//     mbarrier; two operand stages let the next slice be decoded while the
-//     tensor core works on the current one;
+// rows (the MMA's N, 16..256) over its share of K, in k-steps of 64, with
+// warp-specialised roles joined only by mbarriers:
+//   * warp 8 (payload producer) copies, for each span of max(B, 64) weights
+//     (whole blocks), the packed bytes of the tile's 128 rows into a
+//     two-stage ring with asynchronous 16-byte copies (rounded out to 16-byte
+//     lines that all hold payload bytes; each lane's copies are counted on
+//     the span's full barrier as they land);
+//   * warps 0-7 (decoders) decode each k-step's 64 weights of the 128 rows
+//     with the same Fmt<F> decoders, round them to bfloat16 and write them as
+//     the A operand of one of NA operand stages (128-byte-swizzled K-major),
+//     then arrive on that stage's A-full barrier;
+//   * warp 9, one thread, loads the X slice [BN x 64] of each k-step into the
+//     stage's B operand with one TMA tensor copy (the 128-byte swizzle is the
+//     operand layout; rows and columns outside X read as zero), NA - 1
+//     k-steps ahead, and issues the four tcgen05.mma (K = 16 each) of a
+//     k-step once its A and B are full, committing them to the stage's free
+//     barrier, which the decoders and the X copies wait on before reusing the
+//     stage;
 //   * the epilogue reads the accumulator back with tcgen05.ld (warp w reads
 //     TMEM lanes 32*(w%4).., half of the columns each).  With split-K
 //     (gridDim.z > 1, one thread-block cluster per tile) each CTA parks its
 //     partial tile in shared memory and the cluster's rank-0 CTA adds them
 //     in rank order through distributed shared memory, so the result does
 //     not depend on timing.
-// Every wait is bounded; a wait that gives up sets the fault word, the
-// consumers leave their loops together, and the CTA still reaches the
-// cluster barriers and frees its TMEM.
+// Every wait is bounded; a wait that gives up sets the fault word and its
+// role stops, so every other role's waits run out in turn; every CTA still
+// reaches the cluster barriers and frees its TMEM.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -40,26 +45,33 @@ namespace ndq {
 namespace cg = cooperative_groups;
 namespace {
 
-constexpr int kMmaConsumers = 256;               // 8 warps: decode, operands, MMA issue, epilogue
-constexpr int kMmaThreads = kMmaConsumers + 32;  // + one bulk-copy producer warp
-constexpr int kMmaRows = 128;                    // weight rows per CTA (MMA M)
-constexpr int kMmaK = 64;                        // weights per k-step (one 128-byte swizzle atom of bf16)
-constexpr int kMmaATile = kMmaRows * kMmaK * 2;  // 16 KB
-constexpr int kMmaStages = 2;                    // operand stages (A, B)
-constexpr int kMmaSpanStages = 2;                // staged packed spans
-constexpr uint32_t kMaxMmaSplit = 8;             // CTAs of a split-K cluster (portable cluster size)
+constexpr int kMmaDecoders = 512;                     // 16 decode warps
+constexpr int kMmaConsumers = 256;                    // the epilogue: warps 0-7
+constexpr int kMmaProducerWarp = kMmaDecoders / 32;   // warp 16 stages the payload
+constexpr int kMmaIssueWarp = kMmaProducerWarp + 1;   // warp 17 issues the MMAs
+constexpr int kMmaXWarp = kMmaProducerWarp + 2;       // warp 18 loads the X slices
+constexpr int kMmaThreads = kMmaDecoders + 96;
+constexpr int kMmaRows = 128;                         // weight rows per CTA (MMA M)
+constexpr int kMmaK = 64;                             // weights per k-step (one 128-byte swizzle atom of bf16)
+constexpr int kMmaATile = kMmaRows * kMmaK * 2;       // 16 KB
+constexpr uint32_t kMmaMaxStages = 4;                 // operand stages (A, B) at most
+constexpr uint32_t kMmaMaxSpans = 4;                  // staged packed spans at most
+constexpr uint32_t kMaxMmaSplit = 8;                  // CTAs of a split-K cluster (portable cluster size)
+constexpr uint32_t kMmaSmemLimit = 227u * 1024u;      // dynamic shared memory of one CTA at most
 
 struct MmaShared {
-    uint64_t full[kMmaSpanStages];   // packed span staged (bulk copies complete)
-    uint64_t empty[kMmaSpanStages];  // every consumer warp is done decoding the span
-    uint64_t mma_bar[kMmaStages];    // the MMAs reading an operand stage are done
+    uint64_t full[kMmaMaxSpans];     // packed span staged (bulk copies complete)
+    uint64_t empty[kMmaMaxSpans];    // every decode warp is done with the span
+    uint64_t afull[kMmaMaxStages];   // the decode warps wrote the stage's A operand
+    uint64_t bfull[kMmaMaxStages];   // the stage's X slice landed (TMA transaction count)
+    uint64_t sfree[kMmaMaxStages];   // the MMAs reading the stage are done (tcgen05.commit)
     uint32_t tmem;
     uint32_t pad[3];
 };
 
-// Dynamic shared memory: [A x2][B x2][packed spans x2][MmaShared], 1024-byte
-// aligned pieces.  After the k-loop the A and B region holds the partial tile
-// (128 x bn binary32) of a split-K reduction.
+// Dynamic shared memory: [A x na][B x na][packed spans x ns][MmaShared],
+// 1024-byte aligned pieces.  After the k-loop the A and B region holds the
+// partial tile (128 x bn binary32) of a split-K reduction.
 __host__ __device__ constexpr uint32_t mma_b_tile(uint32_t bn) { return bn * 128u; }
 // Staged row stride: room for the span, its byte phase and the decoders'
 // over-read, rounded to an odd number of 16-byte units so that the rows a
@@ -71,9 +83,31 @@ __host__ __device__ constexpr uint32_t mma_row_stride(uint32_t span) {
 __host__ __device__ constexpr uint32_t mma_span_stage(uint32_t span) {
     return (kMmaRows * mma_row_stride(span) + 1023u) & ~1023u;
 }
-__host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span) {
-    return 1024u + kMmaStages * kMmaATile + kMmaStages * mma_b_tile(bn) + kMmaSpanStages * mma_span_stage(span) +
-           1024u;
+__host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span, uint32_t na, uint32_t ns) {
+    return 1024u + na * (kMmaATile + mma_b_tile(bn)) + ns * mma_span_stage(span) + 1024u;
+}
+// Operand stages na and span stages ns: the deepest pipeline that fits,
+// operand stages first (4, 3, then 2 of each at least).
+__host__ __device__ inline void mma_stages(uint32_t bn, uint32_t span, uint32_t* na, uint32_t* ns) {
+    *na = 2u;
+    *ns = 2u;
+    for (uint32_t a = 4u; a >= 2u; --a)
+        for (uint32_t s = 4u; s >= 2u; --s)
+            if (mma_smem_bytes(bn, span, a, s) <= kMmaSmemLimit && a * 8u + s > *na * 8u + *ns &&
+                (a >= 3u || s <= 3u)) {
+                *na = a;
+                *ns = s;
+            }
+}
+
+// TMA tile copy of a 2-D tensor-map box at (x, y) into shared memory,
+// completing its bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
 
 // K-major 128-byte swizzle: row r, 16-byte unit u (8 units per 128-byte row).
@@ -104,21 +138,18 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Barrier of the 256 consumer threads (named barrier 1) that also ORs a
-// fault flag across them, so that they all leave a loop together.
-__device__ __forceinline__ bool consumers_sync_or(bool flag) {
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
     uint32_t r;
     asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
-        "bar.red.or.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"(flag ? 1u : 0u), "n"(kMmaConsumers)
-        : "memory");
+        "{\n.reg .b32 rx;\n.reg .pred px;\n"
+        "elect.sync rx|px, 0xffffffff;\nselp.u32 %0, 1, 0, px;\n}\n"
+        : "=r"(r));
     return r != 0;
 }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // TMEM -> registers: 8 consecutive binary32 columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
@@ -136,31 +167,33 @@ __device__ __forceinline__ void mma_span_range(const MmaParams& p, uint64_t& sp0
     sp1 = ns * (blockIdx.z + 1) / gridDim.z;
 }
 
+template <int F>
 __device__ void mma_producer(const MmaParams& p, MmaShared& S, uint8_t* sP, uint32_t rstride, uint32_t stage_bytes) {
+    constexpr uint32_t B = Fmt<F>::B, SB = Fmt<F>::S;
     const DevTensor& t = p.w;
     const uint32_t lane = threadIdx.x & 31u;
+    const int ns = static_cast<int>(p.ns);
     const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
     uint64_t sp0, sp1;
     mma_span_range(p, sp0, sp1);
     int issued = 0;
     bool fault = false;
     for (uint64_t sp = sp0; sp < sp1; ++sp, ++issued) {
-        const int s = issued % kMmaSpanStages;
-        if (issued >= kMmaSpanStages &&
-            !mbar_wait_bounded(&S.empty[s], static_cast<uint32_t>(((issued / kMmaSpanStages) - 1) & 1))) {
+        const int s = issued % ns;
+        if (issued >= ns && !mbar_wait_bounded(&S.empty[s], static_cast<uint32_t>(((issued / ns) - 1) & 1))) {
             fault = true;
             break;
         }
         const uint64_t k0 = sp * p.span_elems;
         const uint64_t kleft = p.K - k0;
-        const uint32_t span = static_cast<uint32_t>((kleft < p.span_elems ? kleft : p.span_elems) / t.B * t.S);
+        const uint32_t span = static_cast<uint32_t>((kleft < p.span_elems ? kleft : p.span_elems) / B * SB);
         // every lane copies the 16-byte lines of rows lane, lane + 32, ...
         // (asynchronous copies; the lines all hold payload bytes), then has
         // the full barrier count its arrival once they have landed
         for (uint32_t r = lane; r < kMmaRows; r += 32) {
             const uint64_t n = n0 + r;
             if (n < p.n_rows) {
-                const uint8_t* src = t.x + (n * p.bpr + k0 / t.B) * t.S;
+                const uint8_t* src = t.x + (n * p.bpr + k0 / B) * SB;
                 const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
                 const uint32_t lines = (ph + span + 15u) >> 4;
                 const uint8_t* g = src - ph;
@@ -174,25 +207,34 @@ __device__ void mma_producer(const MmaParams& p, MmaShared& S, uint8_t* sP, uint
     }
     if (fault) {
         if (lane == 0) atomicOr(p.fault, 1u);
-        for (int j = issued - kMmaSpanStages; j < issued; ++j)
-            if (j >= 0) mbar_wait_bounded(&S.full[j % kMmaSpanStages], static_cast<uint32_t>((j / kMmaSpanStages) & 1));
+        for (int j = issued - ns; j < issued; ++j)
+            if (j >= 0) mbar_wait_bounded(&S.full[j % ns], static_cast<uint32_t>((j / ns) & 1));
     }
 }
 
+// k-steps of this CTA: K in steps of 64 from its first span (every span but
+// a partial last one holds span_elems / 64 k-steps).
+__device__ __forceinline__ uint32_t mma_ksteps(const MmaParams& p, uint64_t sp0, uint64_t sp1) {
+    const uint64_t k0 = sp0 * p.span_elems;
+    const uint64_t k1 = (sp1 * p.span_elems < p.K) ? sp1 * p.span_elems : p.K;
+    return static_cast<uint32_t>((k1 - k0 + kMmaK - 1) / kMmaK);
+}
+
 template <int F>
-__global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
+__global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const __grid_constant__ MmaParams p) {
     using Fm = Fmt<F>;
     constexpr int CE = Fm::CE;
     extern __shared__ __align__(1024) uint8_t mma_smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023u) & ~uintptr_t(1023));
-    const uint32_t bn = p.bn;
+    const uint32_t bn = p.bn, na = p.na;
     uint8_t* sA = base;
-    uint8_t* sB = base + kMmaStages * kMmaATile;
-    uint8_t* sP = sB + kMmaStages * mma_b_tile(bn);
+    uint8_t* sB = base + na * kMmaATile;
+    uint8_t* sP = sB + na * mma_b_tile(bn);
     const uint32_t rstride = mma_row_stride(p.span_bytes);
     const uint32_t stage_bytes = mma_span_stage(p.span_bytes);
-    MmaShared& S = *reinterpret_cast<MmaShared*>(sP + kMmaSpanStages * stage_bytes);
-    __shared__ SmemHdr H;  // the decoders' 16-entry tables
+    MmaShared& S = *reinterpret_cast<MmaShared*>(sP + p.ns * stage_bytes);
+    __shared__ SmemHdr H;       // the decoders' 16-entry tables
+    __shared__ uint32_t s_fault;  // a role of this CTA gave up a wait
 
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
     const uint32_t ncols = bn < 32u ? 32u : bn;  // TMEM columns (a power of two)
@@ -202,85 +244,149 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        for (int s = 0; s < kMmaSpanStages; ++s) {
+        for (uint32_t s = 0; s < p.ns; ++s) {
             mbar_init(&S.full[s], 32);  // one arrival per producer lane (cp.async completion)
-            mbar_init(&S.empty[s], kMmaConsumers / 32);
+            mbar_init(&S.empty[s], kMmaDecoders / 32);
         }
-        for (int s = 0; s < kMmaStages; ++s) mbar_init(&S.mma_bar[s], 1);
+        for (uint32_t s = 0; s < na; ++s) {
+            mbar_init(&S.afull[s], kMmaDecoders / 32);
+            mbar_init(&S.bfull[s], 1);
+            mbar_init(&S.sfree[s], 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid < 16) {
         H.lut_iq4[tid] = static_cast<float>(c_iq4[tid]);
         H.lut_v[tid] = static_cast<float>(c_v[tid]);
     }
+    if (tid == 32) s_fault = 0u;
+    if (tid == kMmaXWarp * 32)  // (the X thread) the X map's descriptor into the cache
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem;
     bool fault = false;
-    bool issued_any = false;  // this CTA issued at least one MMA (its accumulator is defined)
+    uint64_t sp0, sp1;
+    mma_span_range(p, sp0, sp1);
+    const uint32_t nk = mma_ksteps(p, sp0, sp1);
+    const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
+    const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
 
-    if (tid >= kMmaConsumers) {
-        mma_producer(p, S, sP, rstride, stage_bytes);
+    if (warp == kMmaProducerWarp) {
+        mma_producer<F>(p, S, sP, rstride, stage_bytes);
+    } else if (warp == kMmaXWarp) {
+        // the X slice of k-step j into stage j % na once the MMAs that read
+        // the stage na k-steps ago are done (the whole warp waits, one lane
+        // issues the copy)
+        const uint32_t xbytes = bn * 128u;
+        const uint64_t kx = sp0 * p.span_elems;
+        uint32_t b = 0, ph = 0;  // stage and the parity of its previous use
+        for (uint32_t j = 0; j < nk; ++j) {
+            if (j >= na && !__all_sync(0xffffffffu, mbar_wait_bounded(&S.sfree[b], ph))) {
+                if (lane == 0) {
+                    atomicOr(p.fault, 4u);
+                    atomicOr(&s_fault, 1u);
+                }
+                break;
+            }
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&S.bfull[b], xbytes);
+                tma_load_2d(sB + b * mma_b_tile(bn), &p.xmap, static_cast<int32_t>(kx + static_cast<uint64_t>(kMmaK) * j),
+                            static_cast<int32_t>(m0), &S.bfull[b]);
+            }
+            __syncwarp();
+            if (++b == na) {
+                b = 0;
+                if (j + 1 > na) ph ^= 1u;
+            }
+        }
+    } else if (warp == kMmaIssueWarp) {
+        // the MMAs of k-step i once the decoders filled A and the copy filled
+        // B; the whole warp waits and computes the descriptors (warp-uniform
+        // values), one lane issues
+        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) | ((kMmaRows >> 4) << 24);
+        uint32_t issued = 0;  // k-steps whose MMAs were issued
+        uint32_t a = 0, ph = 0;
+        for (uint32_t i = 0; i < nk; ++i) {
+            const bool ok = mbar_wait_bounded(&S.afull[a], ph) && mbar_wait_bounded(&S.bfull[a], ph);
+            if (!__all_sync(0xffffffffu, ok)) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + a * kMmaATile), b0 = smem_addr(sB + a * mma_b_tile(bn));
+            if (elect_one()) {
+#pragma unroll
+                for (uint32_t q = 0; q < kMmaK / 16; ++q)
+                    mma_bf16(tmem, mma_sdesc(a0 + 32u * q), mma_sdesc(b0 + 32u * q), idesc, (i > 0 || q > 0) ? 1u : 0u);
+                mma_commit(&S.sfree[a]);
+            }
+            __syncwarp();
+            ++issued;
+            if (++a == na) {
+                a = 0;
+                ph ^= 1u;
+            }
+        }
+        // the last commit covers every MMA issued (also after a fault: no
+        // MMA may still run when the epilogue reads or frees TMEM)
+        if (issued > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&S.sfree[(issued - 1) % na], ((issued - 1) / na) & 1u)))
+            fault = true;
+        if ((fault || issued < nk) && lane == 0) {
+            atomicOr(p.fault, 4u);
+            atomicOr(&s_fault, 1u);
+        }
     } else {
         const DevTensor& t = p.w;
-        const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
-        const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
-        // two adjacent threads per weight row, so that a warp touches 16 rows
-        // at a time (fewer shared-memory bank conflicts than 32)
-        const uint32_t r = tid >> 1;      // this thread's weight row in the tile
-        const uint32_t half = tid & 1u;   // which half of the row's chunks it decodes
+        // four adjacent threads per weight row (a warp touches 8 rows at a
+        // time, which spread over the shared-memory banks)
+        const uint32_t r = tid >> 2;      // this thread's weight row in the tile
+        const uint32_t quad = tid & 3u;   // which quarter of the row's chunks it decodes
         const uint64_t n = n0 + r;
         const bool row_ok = n < p.n_rows;
-        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) | ((kMmaRows >> 4) << 24);
         Ctx x{&H, nullptr, t.divs, 0, t.blocks_per_div, p.grids, code_count(t), n, 0};
-        uint64_t sp0, sp1;
-        mma_span_range(p, sp0, sp1);
-        uint64_t kbi = 0;  // k-steps issued by this CTA
+        uint32_t kbi = 0;  // k-steps decoded by this CTA
+        uint32_t sa = 0, fph = 1;  // operand stage of k-step kbi, parity of its previous use
         constexpr uint32_t kChunks = kMmaK / CE;
-        const uint32_t xunits = bn * 8u;  // 16-byte units of the X slice
         for (uint64_t sp = sp0; sp < sp1 && !fault; ++sp) {
             const uint64_t i = sp - sp0;
-            const int s = static_cast<int>(i % kMmaSpanStages);
-            const bool ok = mbar_wait_bounded(&S.full[s], static_cast<uint32_t>((i / kMmaSpanStages) & 1u));
-            if (consumers_sync_or(!ok)) {
+            const int s = static_cast<int>(i % p.ns);
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&S.full[s], static_cast<uint32_t>((i / p.ns) & 1u)))) {
                 fault = true;
                 break;
             }
             const uint64_t k0s = sp * p.span_elems;
             const uint64_t kend = (k0s + p.span_elems < p.K) ? k0s + p.span_elems : p.K;
             const uint8_t* row_in = sP + s * stage_bytes + r * rstride;
-            const uint32_t ph = static_cast<uint32_t>(
-                reinterpret_cast<uintptr_t>(t.x + (n * p.bpr + k0s / t.B) * t.S) & 15u);
-            x.block0 = n * p.bpr + k0s / t.B;
+            x.block0 = n * p.bpr + k0s / Fm::B;
+            const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(t.x + x.block0 * Fm::S) & 15u);
             x.col0 = k0s;
             for (uint64_t k0 = k0s; k0 < kend; k0 += kMmaK, ++kbi) {
-                const int b = static_cast<int>(kbi & 1u);
-                bool okb = true;
-                if (kbi >= kMmaStages)  // the MMAs that read operand stage b two k-steps ago are done
-                    okb = mbar_wait_bounded(&S.mma_bar[b], static_cast<uint32_t>(((kbi - kMmaStages) >> 1) & 1u));
-                // the activation slice X[m0 .. m0+bn, k0 .. k0+64) into B[b] by
-                // asynchronous 16-byte copies (zero-filled outside X), which
-                // complete while the weights are decoded
-                uint8_t* bS = sB + b * mma_b_tile(bn);
-                for (uint32_t iu = tid; iu < xunits; iu += kMmaConsumers) {
-                    const uint64_t m = m0 + (iu >> 3), kk = k0 + 8u * (iu & 7u);
-                    const bool in = m < p.m_rows && kk < p.K;
-                    const uint16_t* src = in ? p.x + m * p.K + kk : p.x;
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(bS + sw128(iu >> 3, iu & 7u))),
-                                 "l"(src), "r"(in ? 16u : 0u)
-                                 : "memory");
+                const uint32_t a = sa;
+                // the MMAs that read this stage na k-steps ago are done (fph:
+                // the parity of that use's completion)
+                if (kbi >= na && !__all_sync(0xffffffffu, mbar_wait_bounded(&S.sfree[a], fph))) {
+                    fault = true;
+                    break;
                 }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                // decode this k-step's 64 weights of row r into A[b] (bf16, swizzled)
-                uint8_t* aS = sA + b * kMmaATile;
+                if (++sa == na) {
+                    sa = 0;
+                    fph ^= 1u;
+                }
+                // this k-step's 64 weights of row r into A[a] (bf16, swizzled)
+                uint8_t* aS = sA + a * kMmaATile;
                 const uint32_t c_first = static_cast<uint32_t>((k0 - k0s) / CE);
-                for (uint32_t j = half; j < kChunks; j += 2) {
+                for (uint32_t j = quad; j < kChunks; j += 4) {
                     const uint64_t kc = k0 + static_cast<uint64_t>(j) * CE;
                     uint32_t wb[CE / 2];
                     if (row_ok && kc < p.K) {
                         float v[CE];
-                        Fm::template chunk<true>(row_in, ph, c_first + j, v, x);
+                        if (p.aligned)  // (every staged row starts on a 16-byte boundary)
+                            Fm::template chunk<false>(row_in, 0u, c_first + j, v, x);
+                        else
+                            Fm::template chunk<true>(row_in, ph, c_first + j, v, x);
 #pragma unroll
                         for (int e = 0; e < CE / 2; ++e) wb[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
                     } else {
@@ -292,36 +398,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
                         *reinterpret_cast<uint4*>(aS + sw128(r, j * (CE / 8) + q)) =
                             make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
                 }
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                tc_fence_before();
-                if (consumers_sync_or(!okb)) {
-                    fault = true;
-                    break;
-                }
-                tc_fence_after();
-                if (tid == 0) {
-                    const uint32_t a0 = smem_addr(aS), b0 = smem_addr(bS);
-#pragma unroll
-                    for (uint32_t q = 0; q < kMmaK / 16; ++q)
-                        mma_bf16(tmem, mma_sdesc(a0 + 32u * q), mma_sdesc(b0 + 32u * q), idesc,
-                                 (kbi > 0 || q > 0) ? 1u : 0u);
-                    mma_commit(&S.mma_bar[b]);
-                }
+                fence_proxy_async_smem();  // the tensor core reads A through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.afull[a]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[s]);  // this warp no longer reads the span
         }
-        // the last commit covers every MMA of the CTA
-        if (!fault && kbi > 0) {
-            const uint64_t kl = kbi - 1;
-            const bool ok = mbar_wait_bounded(&S.mma_bar[kl & 1u], static_cast<uint32_t>((kl >> 1) & 1u));
-            fault = consumers_sync_or(!ok);
+        if (fault && lane == 0) {
+            atomicOr(p.fault, 4u);
+            atomicOr(&s_fault, 1u);
         }
-        tc_fence_after();
-        if (fault && lane == 0) atomicOr(p.fault, 4u);
-        issued_any = kbi > 0;
     }
+    // every role is done: the MMA thread has seen its last commit complete
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool issued_any = nk > 0;
+    fault = s_fault != 0u;  // a faulted tile writes zeros (the fault word reports it)
 
     // Epilogue.  Warp w < 8 reads TMEM lanes 32*(w%4).. (weight rows) and half
     // of the columns (activation rows).  With one CTA per tile it stores Y.
@@ -332,8 +426,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const MmaParams p) {
     // order so that the result does not depend on timing.
     const bool split = gridDim.z > 1;
     float* part = reinterpret_cast<float*>(base);  // [bn][128] binary32, over the operand stages
-    const uint64_t n0 = static_cast<uint64_t>(blockIdx.x) * kMmaRows;
-    const uint64_t m0 = static_cast<uint64_t>(blockIdx.y) * bn;
     const uint32_t quarter = warp & 3u, wh = (warp >> 2) & 1u;
     const uint32_t row = 32u * quarter + lane;
     const uint32_t cbeg = wh * (bn / 2u), cend = cbeg + bn / 2u;
