@@ -308,6 +308,29 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
         q.out_bf16 = p.out_bf16;
         return ndq::launch_mma(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
     }
+    // 2 to 8 activation rows with binary32 weights of gguf:q6_k (a group
+    // scale times a small code): the grouped tensor-core product (the tensor
+    // core sums codes times X per group, the epilogue applies the scales),
+    // when X is 16-byte aligned.  (One row stays on the CUDA cores, which
+    // measured faster there, and so does q8_0, whose 34-byte blocks the
+    // tensor-core kernel stages less efficiently.)
+    if (weight_dtype == NDQ_FLOAT && M >= 2 && M <= ndq::kMvMaxRows && p.xvec && p.w.fmt == ndq::KF_Q6_K) {
+        ndq::MmaParams q;
+        std::memset(&q, 0, sizeof(q));
+        q.w = p.w;
+        q.x = x;
+        q.y = y;
+        q.n_rows = p.n_rows;
+        q.K = p.K;
+        q.bpr = p.bpr;
+        q.m_rows = static_cast<uint64_t>(M);
+        q.bn = 1;
+        while (q.bn < static_cast<uint64_t>(M)) q.bn *= 2;
+        q.span_elems = p.w.B > 64 ? p.w.B : 64;
+        q.span_bytes = q.span_elems / p.w.B * p.w.S;
+        q.out_bf16 = p.out_bf16;
+        return ndq::launch_mmag(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    }
     for (int64_t m0 = 0; m0 < M; m0 += ndq::kMvMaxRows) {
         p.x = x + static_cast<uint64_t>(m0) * static_cast<uint64_t>(K);
         p.y = static_cast<uint8_t*>(y) + static_cast<uint64_t>(m0) * static_cast<uint64_t>(N) * osize;

@@ -4,7 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include "ndq_matvec.cuh"
-#include "ndq_mma.cuh"
+#include "ndq_mmag.cuh"
 
 namespace ndq {
 
@@ -54,6 +54,8 @@ struct MvDeviceInfo {
     int sms = 0;
     bool attr_set[KF_COUNT][kMvVariants] = {};
     int ctas_per_sm[KF_COUNT][kMvVariants][kMvSmemBuckets] = {};  // 0 = not yet queried
+    int lean_slot[KF_COUNT][kMvVariants] = {};  // the lean kernel: slot of the last query and its result
+    int lean_cps[KF_COUNT][kMvVariants] = {};
 };
 MvDeviceInfo g_mv_dev[64];
 }  // namespace
@@ -89,13 +91,24 @@ int launch_matvec(const MvParams& p0, void* stream) {
     } else if (aligned) {
         variant = kMvRowsGlobal;
     }
-    const MvKernelFn fn = (f >= 0 && f < KF_COUNT) ? matvec_for(f, variant) : nullptr;
+    // one row of a K-quant format with whole 512-weight iterations: the lean
+    // kernel (activations in registers, CTAs taking row blocks in turn)
+    MvKernelFn fn = nullptr;
+    const uint64_t nit = p.K / kGlIter;
+    if (p.m == 1 && rows_aligned && p.K % kGlIter == 0 && nit <= 4u * kConsumerWarpsPerCta && f >= 0 &&
+        f < KF_COUNT) {
+        const int xr = nit <= 8u ? 0 : nit <= 16u ? 1 : 2;
+        const int lv = kMvLean + 2 * xr + (p.wbf16 ? 1 : 0);
+        fn = matvec_for(f, lv);
+        if (fn) {
+            variant = lv;
+            xbytes = 0;
+        }
+    }
+    if (!fn) fn = (f >= 0 && f < KF_COUNT) ? matvec_for(f, variant) : nullptr;
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    const bool lean = variant >= kMvLean;
     const bool one_row = variant == kMvOneRowF32 || variant == kMvOneRowF32Any;
-    const size_t base = one_row ? gemv1_smem_base(p.w.B, p.w.S)
-                                : static_cast<size_t>(kStages * kInStride + kHdrBytes + kMvExtraBytes);
-    const int bucket = static_cast<int>((xbytes + 8191u) / 8192u);
-    const size_t smem = base + static_cast<size_t>(bucket) * 8192u;
     MvDeviceInfo& di = g_mv_dev[dev];
     if (di.sms == 0) {
         int sms = 0;
@@ -103,13 +116,30 @@ int launch_matvec(const MvParams& p0, void* stream) {
         if (e != cudaSuccess) return static_cast<int>(e);
         di.sms = sms;
     }
+    if (lean) {  // rows per stage (for two resident CTAs per SM) and the slot they take
+        const uint32_t xr = static_cast<uint32_t>(1 << ((variant - kMvLean) / 2));
+        p.rows_per_stage = static_cast<int32_t>(
+            gemvl_rows_per_stage(p.n_rows, p.bpr * p.w.S, xr, 2u * static_cast<uint64_t>(di.sms)));
+        p.slot = static_cast<int32_t>(gl_slot_bytes(p.bpr * p.w.S, static_cast<uint32_t>(p.rows_per_stage)));
+    }
+    const size_t base = lean      ? gemvl_smem_bytes(static_cast<uint32_t>(p.slot))
+                        : one_row ? gemv1_smem_base(p.w.B, p.w.S)
+                                  : static_cast<size_t>(kStages * kInStride + kHdrBytes + kMvExtraBytes);
+    const int bucket = static_cast<int>((xbytes + 8191u) / 8192u);
+    const size_t smem = base + static_cast<size_t>(bucket) * 8192u;
     if (!di.attr_set[f][variant]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(base + kMvXBytes));
+        const size_t most = lean ? gemvl_smem_bytes(kGlSlotMax) : base + kMvXBytes;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(most));
         if (e != cudaSuccess) return static_cast<int>(e);
         di.attr_set[f][variant] = true;
     }
-    int& cps = di.ctas_per_sm[f][variant][bucket];
+    // (the lean kernel's occupancy depends on its slot size: the last query
+    // per kernel is kept)
+    if (lean && di.lean_slot[f][variant] != p.slot) {
+        di.lean_slot[f][variant] = p.slot;
+        di.lean_cps[f][variant] = 0;
+    }
+    int& cps = lean ? di.lean_cps[f][variant] : di.ctas_per_sm[f][variant][bucket];
     if (cps == 0) {
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, smem);
@@ -177,6 +207,43 @@ MmaKernelFn mma_for(int kfmt) {
     }
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;  // (benign race: same value)
+    if (!encode) {
+        void* fp = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fp, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fp) return nullptr;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fp);
+    }
+    return encode;
+}
+
+// The payload as a byte tensor [N, bpr * S] for one tensor copy per staged
+// span (rows 16-byte aligned and a span that fits a box); else wbox = 0 and
+// the producer copies 16-byte lines.
+int payload_map(MmaParams& p) {
+    p.wbox = 0;
+    const uint64_t row_bytes = p.bpr * p.w.S;
+    const uint32_t wbox = mma_wbox(p.span_bytes);
+    if (wbox == 0u || (reinterpret_cast<uintptr_t>(p.w.x) & 15u) != 0u || row_bytes % 16u != 0u) return 0;
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return static_cast<int>(cudaErrorNotSupported);
+    const cuuint64_t gdim[2] = {row_bytes, p.n_rows};
+    const cuuint64_t gstride[1] = {row_bytes};
+    const cuuint32_t box[2] = {wbox, static_cast<cuuint32_t>(kMmaRows)};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.w.x), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return static_cast<int>(cudaErrorInvalidValue);
+    p.wbox = wbox;
+    return 0;
+}
+}  // namespace
+
 int launch_mma(const MmaParams& p0, void* stream) {
     if (p0.n_rows == 0 || p0.m_rows == 0) return 0;
     int dev = 0;
@@ -201,14 +268,10 @@ int launch_mma(const MmaParams& p0, void* stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     // X as a 2-D tensor map: [m_rows, K] bfloat16, boxes of 64 columns (one
     // 128-byte swizzle span) by bn rows, zero outside X
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;  // (benign race: same value)
-    if (!encode) {
-        void* fp = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fp, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fp) return static_cast<int>(cudaErrorNotSupported);
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fp);
-    }
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return static_cast<int>(cudaErrorNotSupported);
+    const int pm = payload_map(p);
+    if (pm != 0) return pm;
     const cuuint64_t gdim[2] = {p.K, p.m_rows};
     const cuuint64_t gstride[1] = {p.K * 2u};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kMmaK), p.bn};
@@ -243,6 +306,69 @@ int launch_mma(const MmaParams& p0, void* stream) {
     attr[0].val.clusterDim.z = split;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    void* args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
+    return static_cast<int>(e);
+}
+
+MmaKernelFn mmag_for(int kfmt, int mp) {
+    switch (kfmt) {
+        case KF_Q6_K: return mmag_q6_k(mp);
+        case KF_Q8_0: return mmag_q8_0(mp);
+        default: return nullptr;
+    }
+}
+
+namespace {
+// Weights per scale group of the grouped families (k_mmag).
+int mmag_group(int kfmt) { return kfmt == KF_Q6_K ? Gc<KF_Q6_K>::G : Gc<KF_Q8_0>::G; }
+}  // namespace
+
+int launch_mmag(const MmaParams& p0, void* stream) {
+    if (p0.n_rows == 0 || p0.m_rows == 0) return 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    MmaParams p = p0;
+    const int se = device_symbols(dev, &p.fault, &p.grids);
+    if (se != 0) return se;
+    const int f = p.w.fmt;
+    const MmaKernelFn fn = (f >= 0 && f < KF_COUNT) ? mmag_for(f, static_cast<int>(p.bn)) : nullptr;
+    if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    const int ng = kMmaK / mmag_group(f);
+    const uint32_t ncol = mg_ncol(ng, p.bn);
+    mmag_stages(ncol, ng, p.span_bytes, &p.na, &p.ns);
+    p.aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0 && p.span_bytes % 16u == 0;
+    const int pm = payload_map(p);
+    if (pm != 0) return pm;
+    const size_t smem = mmag_smem_bytes(ncol, ng, p.span_bytes, p.na, p.ns);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    // Split K over a cluster of up to 8 CTAs while the tiles leave SMs idle
+    // (every CTA keeps at least four spans; the partial rows, MP x 128
+    // binary32, are parked over the operand stages)
+    const uint64_t tiles = (p.n_rows + kMmaRows - 1) / kMmaRows;
+    const uint64_t spans = (p.K + p.span_elems - 1) / p.span_elems;
+    unsigned split = 1;
+    while (split < kMaxMmaSplit && spans >= 8u * split && tiles * 2u * split <= static_cast<uint64_t>(sms)) split *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1u, split);
+    cfg.blockDim = dim3(kMgThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = split;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     void* args[] = {&p};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
     return static_cast<int>(e);

@@ -165,7 +165,7 @@ struct MvParams {
     int32_t rows_per_stage;  // R in {1, 2, 4, 8}: whole rows per staged unit (K <= 8192/R), 1 = segments
     int32_t wbf16;        // 1: round the decoded weights to bfloat16 before the product
     int32_t out_bf16;     // 1: y is bfloat16, else binary32
-    int32_t pad_;
+    int32_t slot;         // k_gemvl: bytes of one staged row slot (set by the launcher)
     unsigned int* fault;  // device fault word (set by the launcher)
     const IqGrids* grids;  // IQ codebooks (set by the launcher)
 };
@@ -186,7 +186,10 @@ enum MvVariant : int {
     kMvRowsGlobal = 2,
     kMvAnyAlign = 3,
     kMvOneRowF32Any = 4,  // one row (k_gemv1), any alignment
-    kMvVariants = 5
+    // one row, lean per-format decoders (k_gemvl, gguf q8_0 / q4_k / q6_k):
+    // kMvLean + 2 * xr + wbf16, xr = 0, 1, 2 for 1, 2, 4 units per lane
+    kMvLean = 5,
+    kMvVariants = 11
 };
 
 // Decode fused into a tensor-core (tcgen05) product (ndq_mma.cuh): tiles of
@@ -206,12 +209,20 @@ struct MmaParams {
     uint32_t na;          // operand stages (A and B tiles in flight), 2..4 (set by the launcher)
     uint32_t ns;          // staged payload spans, 2..4 (set by the launcher)
     uint32_t aligned;     // 1: the payload, its rows and its spans start on 16-byte boundaries
-    uint32_t pad_;
+    uint32_t wbox;        // bytes per row of a payload tensor copy (wmap), 0: 16-byte copies per row
     unsigned int* fault;
     const IqGrids* grids;
     CUtensorMap xmap;     // X as a 2-D bfloat16 tensor [m_rows, K], boxes of 64 x bn, 128-byte swizzle
+    CUtensorMap wmap;     // (wbox > 0) the payload as bytes [N, bpr * S], boxes of wbox x 128 rows
 };
 using MmaKernelFn = void (*)(MmaParams);
+// The grouped tensor-core product with binary32 weights (k_mmag), for the
+// families whose weight is a group scale times a code exact in bfloat16:
+// the kernel for mp = 1, 2, 4 or 8 activation rows, or nullptr.
+MmaKernelFn mmag_q6_k(int mp);
+MmaKernelFn mmag_q8_0(int mp);
+MmaKernelFn mmag_for(int kfmt, int mp);
+int launch_mmag(const MmaParams& p, void* stream);
 MmaKernelFn mma_fp8_row_bf16();
 MmaKernelFn mma_fp8_row_fp16();
 MmaKernelFn mma_gguf_nvfp4();

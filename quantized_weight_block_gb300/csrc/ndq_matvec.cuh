@@ -581,12 +581,362 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemv1(const MvParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// One activation row, lean decoders: k_gemvl.  For the formats of a K-quant
+// model (gguf q8_0, q4_k, q6_k) with K a multiple of 512 and 16-byte-aligned
+// rows.  A stage holds rb consecutive whole weight rows (one bulk copy); the
+// CTAs take row blocks in turn.  A row is cut into lane units of 16 weights,
+// 32 per warp iteration; warp w always takes the same XR iterations of every
+// row, so its lanes keep their activations in registers (binary32, loaded
+// once per CTA) and reuse them for the stage's rb rows, whose sums are
+// independent chains.  A unit is the 16 weights that a lane decodes from a
+// few aligned 32-bit words of one block (for q6_k, 4 runs of 4 from two
+// low-nibble words and one high-bit word), so the decoders do no per-chunk
+// realignment; the lanes of a group of four share their block's scales by
+// shuffles.  A warp reduces its rb row sums together (a reduce-scatter over
+// the lanes, then a butterfly) and stores one partial per row; the last warp
+// of the stage adds each row's partials in warp order and writes y.
+// Products and sums are binary32 (FMA pairs); W is the exact decode (or its
+// bfloat16 rounding), formed exactly as the decode kernels do.
+// ---------------------------------------------------------------------------
+constexpr int kGlStages = 3;
+constexpr uint32_t kGlIter = 512;     // weights per warp iteration (32 lanes x 16)
+constexpr uint32_t kGlMaxRows = 8;    // rows per stage
+constexpr uint32_t kGlSlotMax = 36u * 1024u;
+
+// Bytes of one stage slot of rb rows: the rows and the decoders' over-read
+// (at most 4 bytes past the last row's last byte), in 128-byte units.
+__host__ __device__ constexpr uint32_t gl_slot_bytes(uint64_t row_bytes, uint32_t rb) {
+    return static_cast<uint32_t>((row_bytes * rb + 16u + 127u) / 128u * 128u);
+}
+
+struct GlShared {
+    float red[kGlStages][kGlMaxRows][kConsumerWarps];  // per-warp partial sums of the staged rows
+    uint32_t cnt[kGlStages];                           // warps that stored their partials
+};
+
+inline size_t gemvl_smem_bytes(uint32_t slot) {
+    return static_cast<size_t>(kGlStages) * slot + kHdrBytes + (sizeof(GlShared) + 127u) / 128u * 128u;
+}
+
+// Rows per stage for a launch: the most (up to 8, and 2 when a lane holds 4
+// units) whose slot fits kGlSlotMax while leaving at least two row blocks per
+// resident CTA.
+inline uint32_t gemvl_rows_per_stage(uint64_t n_rows, uint64_t row_bytes, uint32_t xr, uint64_t resident) {
+    uint32_t rb = xr >= 4u ? 2u : kGlMaxRows;
+    while (rb > 1u && (gl_slot_bytes(row_bytes, rb) > kGlSlotMax || (n_rows + rb - 1u) / rb < 2u * resident))
+        rb >>= 1;
+    return rb;
+}
+
+template <bool WBF16>
+__device__ __forceinline__ float2 gl_round(float2 v) {
+    if (!WBF16) return v;
+    const uint32_t u = pack_bf16(v.x, v.y);
+    return make_float2(bf16_lo(u), bf16_hi(u));
+}
+
+// acc += x[0..3] * (the 4 bytes of w minus the code offset, times d), as
+// two FMA pairs.
+template <bool WBF16>
+__device__ __forceinline__ void gl_mul_acc(float d, uint32_t w, float bias, const float* x, float2& acc) {
+    const float2 dd = make_float2(d, d);
+    const float2 p = gl_round<WBF16>(mul2(dd, bytes_minus2<0>(w, bias)));
+    const float2 q = gl_round<WBF16>(mul2(dd, bytes_minus2<2>(w, bias)));
+    acc = fma2(make_float2(x[0], x[1]), p, acc);
+    acc = fma2(make_float2(x[2], x[3]), q, acc);
+}
+
+// acc += x[0..3] * fma(a, the 4 bytes of w minus the offset, c) (only where
+// a times the code is exact, so the FMA rounds the rule's difference once).
+template <bool WBF16>
+__device__ __forceinline__ void gl_fma_acc(float a, uint32_t w, float bias, float c, const float* x, float2& acc) {
+    const float2 aa = make_float2(a, a), cc = make_float2(c, c);
+    const float2 p = gl_round<WBF16>(fma2(aa, bytes_minus2<0>(w, bias), cc));
+    const float2 q = gl_round<WBF16>(fma2(aa, bytes_minus2<2>(w, bias), cc));
+    acc = fma2(make_float2(x[0], x[1]), p, acc);
+    acc = fma2(make_float2(x[2], x[3]), q, acc);
+}
+
+// The aligned 32-bit word holding bytes [off, off + 4) of the stage, for an
+// offset that is a multiple of 2 (two loads and a funnel shift).
+__device__ __forceinline__ uint32_t lds_4h(const uint8_t* base, uint32_t off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+    return __funnelshift_r(w[0], w[1], (off & 2u) * 8u);
+}
+
+template <int F>
+struct Gl {
+    static constexpr bool kLean = false;
+};
+
+// gguf:q8_0: unit u = elements 16u .. 16u + 15 (half u & 1 of block u >> 1).
+template <>
+struct Gl<KF_Q8_0> {
+    static constexpr bool kLean = true;
+    __device__ __forceinline__ static uint32_t col(uint32_t u, int r) { return 16u * u + 4u * r; }
+    template <bool WBF16>
+    __device__ __forceinline__ static void unit(const uint8_t* in, uint32_t u, uint32_t, const float* x,
+                                                float2& acc) {
+        const uint32_t off = (u >> 1) * 34u;
+        const float d = h2f(*reinterpret_cast<const uint16_t*>(in + off));
+        const uint4 q = lds_16<false>(in, off + 2u + 16u * (u & 1u));
+        const float bias = 8388736.0f;  // 2^23 + 128; XOR 0x80 maps signed to offset-128
+        gl_mul_acc<WBF16>(d, q.x ^ 0x80808080u, bias, x, acc);
+        gl_mul_acc<WBF16>(d, q.y ^ 0x80808080u, bias, x + 4, acc);
+        gl_mul_acc<WBF16>(d, q.z ^ 0x80808080u, bias, x + 8, acc);
+        gl_mul_acc<WBF16>(d, q.w ^ 0x80808080u, bias, x + 12, acc);
+    }
+};
+
+// gguf:q4_k: unit u = 16 b + s of block b: i = s >> 2 picks sub-blocks 2i
+// (low nibbles) and 2i + 1 (high nibbles) of code bytes 32i .. 32i + 31,
+// t = s & 3 the words at 4t and 4t + 16; run r holds elements
+// 64i + 4t + 16 (r & 1) + 32 (r >> 1) .. +3.
+template <>
+struct Gl<KF_Q4_K> {
+    static constexpr bool kLean = true;
+    __device__ __forceinline__ static uint32_t col(uint32_t u, int r) {
+        const uint32_t s = u & 15u;
+        return 256u * (u >> 4) + 64u * (s >> 2) + 4u * (s & 3u) + 16u * (r & 1) + 32u * (r >> 1);
+    }
+    template <bool WBF16>
+    __device__ __forceinline__ static void unit(const uint8_t* in, uint32_t u, uint32_t lane, const float* x,
+                                                float2& acc) {
+        const uint32_t s = u & 15u, i = s >> 2, t = s & 3u;
+        const uint8_t* b = in + (u >> 4) * 144u;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(b + 16u + 32u * i + 4u * t);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(b + 32u + 32u * i + 4u * t);
+        // Lane t of the group forms one of M(d, a[2i]), -M(dmin, m[2i]),
+        // M(d, a[2i+1]), -M(dmin, m[2i+1]) (the 6-bit unpack of the 12 scale
+        // bytes s: with j = k mod 4, k < 4 takes s[j] & 63 and s[j+4] & 63;
+        // k >= 4 takes the low / high nibble of s[j+8] with the top bits of
+        // s[j] / s[j+4]); the others arrive by shuffle.
+        const uint32_t hd = *reinterpret_cast<const uint32_t*>(b);
+        const uint32_t k = 2u * i + (t >> 1), j = k & 3u;
+        const uint32_t b0 = b[4u + j], b1 = b[8u + j], b2 = b[12u + j];
+        const bool mn = (t & 1u) != 0u;
+        const uint32_t lo = mn ? b1 : b0;
+        const uint32_t sv = k < 4u ? (lo & 63u) : ((mn ? (b2 >> 4) : (b2 & 15u)) | ((lo >> 6) << 4));
+        const float sc = __fmul_rn(h2f(mn ? (hd >> 16) : (hd & 0xffffu)), small_uint(sv));
+        const float f = mn ? -sc : sc;
+        const uint32_t g = lane & ~3u;
+        const float da0 = __shfl_sync(0xffffffffu, f, g), ndm0 = __shfl_sync(0xffffffffu, f, g | 1u);
+        const float da1 = __shfl_sync(0xffffffffu, f, g | 2u), ndm1 = __shfl_sync(0xffffffffu, f, g | 3u);
+        const float bias = 8388608.0f;  // 2^23
+        gl_fma_acc<WBF16>(da0, w0 & 0x0F0F0F0Fu, bias, ndm0, x, acc);
+        gl_fma_acc<WBF16>(da0, w1 & 0x0F0F0F0Fu, bias, ndm0, x + 4, acc);
+        gl_fma_acc<WBF16>(da1, (w0 >> 4) & 0x0F0F0F0Fu, bias, ndm1, x + 8, acc);
+        gl_fma_acc<WBF16>(da1, (w1 >> 4) & 0x0F0F0F0Fu, bias, ndm1, x + 12, acc);
+    }
+};
+
+// gguf:q6_k: unit u = 16 b + s of block b: half h = s >> 3 and l0 = 4 (s & 7);
+// run r holds elements 128h + l0 + 32r .. +3, whose low nibbles are low
+// bytes 64h + l0 (runs 0, 2: low / high nibble) and 64h + 32 + l0 (runs 1,
+// 3), whose 2-bit high parts are bits 2r of high bytes 32h + l0, and whose
+// scale is scales[8h + 2r + (l0 >= 16)].
+template <>
+struct Gl<KF_Q6_K> {
+    static constexpr bool kLean = true;
+    __device__ __forceinline__ static uint32_t col(uint32_t u, int r) {
+        const uint32_t s = u & 15u;
+        return 256u * (u >> 4) + 128u * (s >> 3) + 4u * (s & 7u) + 32u * r;
+    }
+    template <bool WBF16>
+    __device__ __forceinline__ static void unit(const uint8_t* in, uint32_t u, uint32_t lane, const float* x,
+                                                float2& acc) {
+        const uint32_t s = u & 15u, h = s >> 3, l0 = 4u * (s & 7u);
+        const uint32_t off = (u >> 4) * 210u;  // even: every field below is at an even offset
+        const uint32_t a = lds_4h(in, off + 64u * h + l0), c = lds_4h(in, off + 64u * h + 32u + l0);
+        const uint32_t q = lds_4h(in, off + 128u + 32u * h + l0);
+        // lane s & 3 of the group forms the scale of run s & 3
+        const float d = h2f(*reinterpret_cast<const uint16_t*>(in + off + 208u));
+        const float dl = __fmul_rn(d, i8_float(in[off + 192u + 8u * h + ((s >> 2) & 1u) + 2u * (s & 3u)]));
+        const uint32_t g = lane & ~3u;
+        const float ds0 = __shfl_sync(0xffffffffu, dl, g), ds1 = __shfl_sync(0xffffffffu, dl, g | 1u);
+        const float ds2 = __shfl_sync(0xffffffffu, dl, g | 2u), ds3 = __shfl_sync(0xffffffffu, dl, g | 3u);
+        const float bias = 8388640.0f;  // 2^23 + 32
+        gl_mul_acc<WBF16>(ds0, (a & 0x0F0F0F0Fu) | ((q & 0x03030303u) << 4), bias, x, acc);
+        gl_mul_acc<WBF16>(ds1, (c & 0x0F0F0F0Fu) | ((q & 0x0C0C0C0Cu) << 2), bias, x + 4, acc);
+        gl_mul_acc<WBF16>(ds2, ((a >> 4) & 0x0F0F0F0Fu) | (q & 0x30303030u), bias, x + 8, acc);
+        gl_mul_acc<WBF16>(ds3, ((c >> 4) & 0x0F0F0F0Fu) | ((q >> 2) & 0x30303030u), bias, x + 12, acc);
+    }
+};
+
+// XR: warp iterations (units) per lane per row, 1, 2 or 4 (K <= 4096 XR);
+// at most RBM rows per stage (p.rows_per_stage).
+template <int F, int XR, bool WBF16>
+__global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
+    using G = Gl<F>;
+    constexpr uint32_t RBM = XR >= 4 ? 2u : kGlMaxRows;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t slot = static_cast<uint32_t>(p.slot), rb = static_cast<uint32_t>(p.rows_per_stage);
+    SmemHdr& H = *reinterpret_cast<SmemHdr*>(smem + kGlStages * slot);
+    GlShared& R = *reinterpret_cast<GlShared*>(smem + kGlStages * slot + kHdrBytes);
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
+    const uint32_t cw = (nit + XR - 1) / XR;  // warps with iterations (at most 8)
+    const uint32_t rowb = static_cast<uint32_t>(p.bpr * p.w.S);  // a multiple of 16
+    const uint64_t nblk = (p.n_rows + rb - 1u) / rb;
+    if (tid == 0) {
+        for (int s = 0; s < kGlStages; ++s) {
+            mbar_init(&H.full[s], 1);
+            mbar_init(&H.empty[s], cw);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < kGlStages) R.cnt[tid] = 0u;
+    // warm L2 with this CTA's first row block (the weights are launch
+    // parameters; the activations, which the previous kernel may write, are
+    // read after the wait)
+    if (tid == kThreads && blockIdx.x < nblk) {
+        const uint64_t r0 = blockIdx.x * static_cast<uint64_t>(rb), nr = p.n_rows - r0 < rb ? p.n_rows - r0 : rb;
+        const uint64_t bytes = nr * rowb;
+        prefetch_l2(p.w.x + r0 * rowb, static_cast<uint32_t>(bytes < 32768u ? bytes : 32768u));
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    if (tid >= kThreads) {  // producer: one bulk copy per row block
+        if (tid != kThreads) return;
+        int issued = 0;
+        bool fault = false;
+        for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++issued) {
+            const int s = issued % kGlStages;
+            if (issued >= kGlStages &&
+                !mbar_wait_bounded(&H.empty[s], static_cast<uint32_t>(((issued / kGlStages) - 1) & 1))) {
+                fault = true;
+                break;
+            }
+            const uint64_t r0 = blk * rb, nr = p.n_rows - r0 < rb ? p.n_rows - r0 : rb;
+            const uint32_t bytes = static_cast<uint32_t>(nr * rowb);
+            mbar_arrive_expect_tx(&H.full[s], bytes);
+            bulk_load(smem + static_cast<uint32_t>(s) * slot, p.w.x + r0 * rowb, bytes, &H.full[s]);
+        }
+        if (fault) {
+            atomicOr(p.fault, 1u);
+            for (int j = issued - kGlStages; j < issued; ++j)
+                if (j >= 0) mbar_wait_bounded(&H.full[j % kGlStages], static_cast<uint32_t>((j / kGlStages) & 1));
+        }
+        return;
+    }
+    if (warp >= cw) return;
+
+    // this lane's activations: run r of unit 32 (XR warp + j) + lane
+    float xv[XR][16];
+#pragma unroll
+    for (int j = 0; j < XR; ++j) {
+        const uint32_t it = warp * XR + j;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            uint32_t lo = 0u, hi = 0u;
+            if (it < nit) {
+                const uint16_t* xp = p.x + G::col(32u * it + lane, r);
+                if (p.xvec) {
+                    const uint2 t2 = __ldg(reinterpret_cast<const uint2*>(xp));
+                    lo = t2.x;
+                    hi = t2.y;
+                } else {
+                    lo = static_cast<uint32_t>(__ldg(xp)) | (static_cast<uint32_t>(__ldg(xp + 1)) << 16);
+                    hi = static_cast<uint32_t>(__ldg(xp + 2)) | (static_cast<uint32_t>(__ldg(xp + 3)) << 16);
+                }
+            }
+            xv[j][4 * r] = bf16_lo(lo);
+            xv[j][4 * r + 1] = bf16_hi(lo);
+            xv[j][4 * r + 2] = bf16_lo(hi);
+            xv[j][4 * r + 3] = bf16_hi(hi);
+        }
+    }
+
+    int n = 0;
+    for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++n) {
+        const int s = n % kGlStages;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((n / kGlStages) & 1)))) {
+            if (lane == 0) atomicOr(p.fault, 2u);
+            return;
+        }
+        const uint64_t r0 = blk * rb;
+        const uint32_t nr = static_cast<uint32_t>(p.n_rows - r0 < rb ? p.n_rows - r0 : rb);
+        const uint8_t* in = smem + static_cast<uint32_t>(s) * slot;
+        float2 acc[RBM];
+#pragma unroll
+        for (uint32_t r = 0; r < RBM; ++r) acc[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < XR; ++j) {
+            const uint32_t it = warp * XR + j;
+            if (it < nit) {
+#pragma unroll
+                for (uint32_t r = 0; r < RBM; ++r)
+                    if (r < nr) G::template unit<WBF16>(in + r * rowb, 32u * it + lane, lane, xv[j], acc[r]);
+            }
+        }
+        // the RBM row sums over the warp: halve the rows a lane keeps at lane
+        // offsets 16, 8, 4 (RBM = 8) or 16 (RBM = 2), then add over the rest;
+        // lane 4k (RBM = 8) or lane 16k (RBM = 2) ends with row k
+        float v[RBM];
+#pragma unroll
+        for (uint32_t r = 0; r < RBM; ++r) v[r] = __fadd_rn(acc[r].x, acc[r].y);
+        uint32_t keep = RBM, o = 16u;
+#pragma unroll
+        for (; keep > 1u; keep >>= 1, o >>= 1) {
+            const bool up = (lane & o) != 0u;
+#pragma unroll
+            for (uint32_t i = 0; i < keep / 2u; ++i) {
+                const float mine = up ? v[keep / 2u + i] : v[i], other = up ? v[i] : v[keep / 2u + i];
+                v[i] = __fadd_rn(mine, __shfl_xor_sync(0xffffffffu, other, o));
+            }
+        }
+#pragma unroll
+        for (; o > 0u; o >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+        constexpr uint32_t kStep = 32u / RBM;  // lanes per row after the halving
+        const uint32_t myrow = (RBM == 8u) ? (lane >> 2) : (lane >> 4);
+        if (lane % kStep == 0u && myrow < nr) R.red[s][myrow][warp] = v[0];
+        __syncwarp();
+        bool last = false;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&R.cnt[s], 1u) == cw - 1u;
+        }
+        last = __shfl_sync(0xffffffffu, last ? 1u : 0u, 0) != 0u;
+        if (last) {  // the stage's last warp adds each row's partials in warp order
+            __threadfence_block();
+            if (lane < nr) {
+                float y = R.red[s][lane][0];
+                for (uint32_t w = 1; w < cw; ++w) y = __fadd_rn(y, R.red[s][lane][w]);
+                if (p.out_bf16)
+                    static_cast<__nv_bfloat16*>(p.y)[r0 + lane] = __float2bfloat16_rn(y);
+                else
+                    static_cast<float*>(p.y)[r0 + lane] = y;
+            }
+            __syncwarp();
+            if (lane == 0) R.cnt[s] = 0u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&H.empty[s]);
+    }
+}
+
 }  // namespace
 
 // Fused kernel of decode family F for a launch variant (used by the
 // per-format instantiation files; see MvVariant in ndq_internal.h).
 template <int F>
 MvKernelFn matvec_kernel(int variant) {
+    if (variant >= kMvLean) {
+        if constexpr (Gl<F>::kLean) {
+            switch (variant - kMvLean) {
+                case 0: return k_gemvl<F, 1, false>;
+                case 1: return k_gemvl<F, 1, true>;
+                case 2: return k_gemvl<F, 2, false>;
+                case 3: return k_gemvl<F, 2, true>;
+                case 4: return k_gemvl<F, 4, false>;
+                default: return k_gemvl<F, 4, true>;
+            }
+        }
+        return nullptr;
+    }
     switch (variant) {
         case kMvOneRowF32: return k_gemv1<F, true>;
         case kMvOneRowF32Any: return k_gemv1<F, false>;

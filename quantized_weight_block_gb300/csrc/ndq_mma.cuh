@@ -83,6 +83,14 @@ __host__ __device__ constexpr uint32_t mma_row_stride(uint32_t span) {
 __host__ __device__ constexpr uint32_t mma_span_stage(uint32_t span) {
     return (kMmaRows * mma_row_stride(span) + 1023u) & ~1023u;
 }
+// Row bytes of a payload tensor copy: the span from the 16-byte line below
+// its first byte plus the decoders' over-read, an odd number of 16-byte
+// units (for the banks), at most 256 (a tensor copy's box); 0 if it does
+// not fit.  It never exceeds mma_row_stride(span).
+__host__ __device__ constexpr uint32_t mma_wbox_odd(uint32_t w) { return (w / 16u) % 2u == 1u ? w : w + 16u; }
+__host__ __device__ constexpr uint32_t mma_wbox(uint32_t span) {
+    return mma_wbox_odd((span + 20u + 15u) / 16u * 16u) <= 256u ? mma_wbox_odd((span + 20u + 15u) / 16u * 16u) : 0u;
+}
 __host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span, uint32_t na, uint32_t ns) {
     return 1024u + na * (kMmaATile + mma_b_tile(bn)) + ns * mma_span_stage(span) + 1024u;
 }
@@ -178,6 +186,27 @@ __device__ void mma_producer(const MmaParams& p, MmaShared& S, uint8_t* sP, uint
     mma_span_range(p, sp0, sp1);
     int issued = 0;
     bool fault = false;
+    if (p.wbox) {  // one tensor copy per span: bytes [x0, x0 + wbox) of the tile's 128 rows, zeros past N
+        for (uint64_t sp = sp0; sp < sp1; ++sp, ++issued) {
+            const int s = issued % ns;
+            if (issued >= ns && !mbar_wait_bounded(&S.empty[s], static_cast<uint32_t>(((issued / ns) - 1) & 1))) {
+                fault = true;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&S.full[s], p.wbox * static_cast<uint32_t>(kMmaRows));
+                tma_load_2d(sP + s * stage_bytes, &p.wmap, static_cast<int32_t>((sp * p.span_bytes) & ~15ull),
+                            static_cast<int32_t>(n0), &S.full[s]);
+            }
+            __syncwarp();
+        }
+        if (fault) {
+            if (lane == 0) atomicOr(p.fault, 1u);
+            for (int j = issued - ns; j < issued; ++j)
+                if (j >= 0) mbar_wait_bounded(&S.full[j % ns], static_cast<uint32_t>((j / ns) & 1));
+        }
+        return;
+    }
     for (uint64_t sp = sp0; sp < sp1; ++sp, ++issued) {
         const int s = issued % ns;
         if (issued >= ns && !mbar_wait_bounded(&S.empty[s], static_cast<uint32_t>(((issued / ns) - 1) & 1))) {
@@ -230,7 +259,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const __grid_constant__ 
     uint8_t* sA = base;
     uint8_t* sB = base + na * kMmaATile;
     uint8_t* sP = sB + na * mma_b_tile(bn);
-    const uint32_t rstride = mma_row_stride(p.span_bytes);
+    const uint32_t rstride = p.wbox ? p.wbox : mma_row_stride(p.span_bytes);
     const uint32_t stage_bytes = mma_span_stage(p.span_bytes);
     MmaShared& S = *reinterpret_cast<MmaShared*>(sP + p.ns * stage_bytes);
     __shared__ SmemHdr H;       // the decoders' 16-entry tables
@@ -245,7 +274,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const __grid_constant__ 
     }
     if (tid == 0) {
         for (uint32_t s = 0; s < p.ns; ++s) {
-            mbar_init(&S.full[s], 32);  // one arrival per producer lane (cp.async completion)
+            mbar_init(&S.full[s], p.wbox ? 1 : 32);  // the tensor copy, or each producer lane's cp.async
             mbar_init(&S.empty[s], kMmaDecoders / 32);
         }
         for (uint32_t s = 0; s < na; ++s) {
@@ -262,6 +291,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_mma(const __grid_constant__ 
     if (tid == 32) s_fault = 0u;
     if (tid == kMmaXWarp * 32)  // (the X thread) the X map's descriptor into the cache
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
+    if (tid == kMmaProducerWarp * 32 && p.wbox)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.wmap)) : "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -97,6 +97,37 @@ def test_matmul_one_row_activation_sources(orc, fmt, K, x_off):
     _check(_run(fmt, N, K, 1, w, x_t, x_off=x_off), ref, yabs, K, what=f"{fmt} M=1 K={K} x+{x_off}")
 
 
+@pytest.mark.parametrize("fmt", ["gguf:q8_0", "gguf:q4_k", "gguf:q6_k", "q8_g32_fp16"])
+@pytest.mark.parametrize("N,K", [(1, 512), (300, 4096), (3000, 4096), (77, 8192), (1000, 14336), (5, 16384),
+                                 (64, 1536)])
+@pytest.mark.parametrize("weights,out", [("float32", torch.float32), ("bfloat16", torch.bfloat16)])
+def test_matmul_one_row_lean_kernel(orc, fmt, N, K, weights, out):
+    # the lean one-row kernel (K a multiple of 512, aligned rows): one, two
+    # or four 16-weight units per lane, 1 to 8 warps per row, rows wrapping
+    # the 4-stage ring (3000 rows), both weight operands and output types
+    w = synth.payload(fmt, (N, K), seed=31 + K)
+    x_t, x_bits = _x_bf16(1, K, 32)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+    got = _run(fmt, N, K, 1, w, x_t, out_dtype=out, weights=weights)
+    _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] {weights} {out}")
+
+
+@pytest.mark.parametrize("N,K", [(300, 4096), (77, 256), (1000, 14336), (130, 12288), (4096, 1024)])
+@pytest.mark.parametrize("M", [2, 3, 5, 8])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_grouped_tensor_core_exact_weights(orc, N, K, M, out):
+    # gguf:q6_k with binary32 weights and 2..8 activation rows: the tensor
+    # core sums codes times X per 16-weight group into its own TMEM column,
+    # the epilogue applies the group scales; row tiles partial, split-K
+    # clusters for the short grids (N = 77, 130, 300)
+    fmt = "gguf:q6_k"
+    w = synth.payload(fmt, (N, K), seed=41 + M)
+    x_t, x_bits = _x_bf16(M, K, 42 + M)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
+    got = _run(fmt, N, K, M, w, x_t, out_dtype=out)
+    _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] M={M} {out}")
+
+
 @pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q8_0", "gguf:mxfp4", "gguf:iq3_s", "nvfp4", "fp8_e4m3fn_row_fp16"])
 @pytest.mark.parametrize("N,K", [(37, 4096), (13, 2048), (9, 1024), (17, 512), (5, 256), (130, 8192), (3, 12800)])
 def test_matmul_whole_rows_per_stage(orc, fmt, N, K):
