@@ -357,14 +357,15 @@ def kernel_source_sha() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(profile_name: str):
+def profiled_traffic(profile_name: str, algorithmic_bytes: int):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; otherwise None."""
+    the current kernel source for a launch of these algorithmic bytes;
+    otherwise None."""
     p = os.path.join(ROOT, "profiles", profile_name)
     try:
         with open(p) as f:
             d = json.load(f)
-        if d.get("kernel_src_sha256") == kernel_source_sha():
+        if d.get("kernel_src_sha256") == kernel_source_sha() and d.get("algorithmic_bytes_per_launch") == algorithmic_bytes:
             return d.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -462,7 +463,10 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
     weight tensor, 225 launches replayed as a CUDA graph) against the
     unfused path on the same payloads (the batched decode to bf16, then one
     cuBLAS bf16 product per tensor, also as a graph).  Also single tensors
-    at M = 1 and M = 8.  Weight operand: the exact binary32 decode."""
+    at M = 1 and M = 8 with the exact binary32 weights (M = 1 on the CUDA
+    cores; M = 8 of q6_k and q8_0 on the tensor cores, the group scales
+    applied after the tensor core's per-group sums) and M = 8 with bfloat16
+    weights."""
     specs = work.specs
     ks = sorted({s.shape[1] for s in specs})
     xs = {k: torch.randn(1, k, device="cuda").to(torch.bfloat16) for k in ks}
@@ -481,6 +485,29 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
     def fused():
         for fmt, w, N, K, yf, _ in views:
             ndq.matmul_packed(fmt, w, N, K, xs[K], y=yf)
+
+    # the products of a layer that read the same activations (q, k and v;
+    # gate and up) as one batched call each
+    groups, cur = [], []
+    for i, s in enumerate(specs):
+        key = s.name.rsplit(".", 1)[0] + (".qkv" if s.name.endswith((".q", ".k", ".v")) else
+                                          ".gu" if s.name.endswith((".gate", ".up")) else f".{i}")
+        if cur and cur[0][0] == key:
+            cur.append((key, i))
+        else:
+            if cur:
+                groups.append([j for _, j in cur])
+            cur = [(key, i)]
+    groups.append([j for _, j in cur])
+
+    def fused_grouped():
+        for g in groups:
+            if len(g) == 1:
+                fmt, w, N, K, yf, _ = views[g[0]]
+                ndq.matmul_packed(fmt, w, N, K, xs[K], y=yf)
+            else:
+                K = views[g[0]][3]
+                ndq.matmul_packed_batched([(views[j][0], views[j][1], views[j][2], views[j][4]) for j in g], K, xs[K])
 
     def gemvs():
         for (fmt, w, N, K, _, yu), wb in zip(views, wviews):
@@ -511,13 +538,22 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
 
     g_fused, g_gemv = graph_of(fused), graph_of(gemvs)
     t_f = timed(g_fused.replay)
+    y_single = y_f.clone()
+    g_grouped = graph_of(fused_grouped)
+    t_fg = timed(g_grouped.replay)
+    same = bool(torch.equal(y_f.view(torch.int32), y_single.view(torch.int32)))
     t_g = timed(g_gemv.replay)
     t_d = timed(decode)
     whole = {"fused_ms": round(t_f, 4), "unfused_ms": round(t_d + t_g, 4), "unfused_decode_ms": round(t_d, 4),
              "unfused_cublas_ms": round(t_g, 4), "speedup": round((t_d + t_g) / t_f, 3),
              "launches": len(specs), "payload_GB/s": round(work.bytes_in / (t_f * 1e-3) / 1e9, 1),
              "weights/s": float(f"{work.elements / (t_f * 1e-3):.4g}"),
-             "what": "one generation step (M=1) over all 225 weight tensors, each a CUDA graph of per-tensor launches"}
+             "what": "one generation step (M=1) over all 225 weight tensors, each a CUDA graph of per-tensor launches",
+             "grouped": {"fused_ms": round(t_fg, 4), "launches": len(groups), "speedup": round((t_d + t_g) / t_fg, 3),
+                         "payload_GB/s": round(work.bytes_in / (t_fg * 1e-3) / 1e9, 1),
+                         "outputs_equal_per_tensor_launches": same,
+                         "what": "the same step with the products that share activations (q, k, v; gate, up) as one "
+                                 "ndq_matmul_packed_batched call each: 4 launches per layer"}}
 
     single = {}
     for fmt, N, K in (("gguf:q4_k", 4096, 4096), ("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336),
@@ -531,10 +567,17 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
             tf = timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf, weight_dtype=wdt))
             tu = timed(lambda: (ndq.dequantize_packed(fmt, (N, K), w, torch.bfloat16, y=wb),
                                 torch.matmul(x, wb.t(), out=yb)))
-            tag = "binary32 weights, CUDA cores" if wdt == torch.float32 else "bfloat16 weights, tensor cores"
-            single[f"{fmt.split(':')[-1]}[{N},{K}] M={M} {tag}"] = {"fused_us": round(tf * 1e3, 1),
-                                                                      "unfused_us": round(tu * 1e3, 1),
-                                                                      "speedup": round(tu / tf, 3)}
+            if wdt == torch.bfloat16:
+                tag = "bfloat16 weights, tensor cores (k_mma)"
+            elif M == 1:
+                tag = "binary32 weights, CUDA cores (k_gemvl)"
+            elif fmt in ("gguf:q6_k", "gguf:q8_0"):
+                tag = "binary32 weights, grouped tensor cores (k_mmag)"
+            else:
+                tag = "binary32 weights, CUDA cores (k_matvec)"
+            single[f"{fmt.split(':')[-1]}[{N},{K}] M={M} {tag}"] = {
+                "fused_us": round(tf * 1e3, 1), "unfused_us": round(tu * 1e3, 1), "speedup": round(tu / tf, 3),
+                "payload_GB/s": round(w.numel() / (tf * 1e-3) / 1e9, 1)}
     # bfloat16 weights on the tensor cores (tcgen05) for more activation rows
     tensor = {}
     for fmt, N, K in (("gguf:q4_k", 14336, 4096), ("gguf:q6_k", 14336, 4096), ("gguf:q6_k", 4096, 14336)):
@@ -847,7 +890,8 @@ def run_ours(args, rank, world, local_rank):
                           "sample": f"first 1/{frac1} of every tensor's blocks ({n1} elements), one thread"}}
     pool.shutdown()
 
-    traffic = profiled_traffic("k_decode_whole_model.json")
+    # (the committed traffic record is for the full model's launch only)
+    traffic = profiled_traffic("k_decode_whole_model.json", step_bytes)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -856,7 +900,7 @@ def run_ours(args, rank, world, local_rank):
                    "bytes_in": work.bytes_in, "bytes_out": work.bytes_out, "out_dtype": "bf16",
                    "elements/s": float(f"{world * work.elements / (ms * 1e-3):.4g}"),
                    "frac_of_8TBs": round(value / world / 8000.0, 4),
-                   "l2": "inputs larger than L2 (20.9 GB moved per step)",
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.1f} GB moved per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),

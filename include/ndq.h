@@ -212,15 +212,49 @@ typedef struct ndq_tensor_desc {
  * Products and sums are binary32 in an unspecified but fixed order, so
  * repeated calls give identical bits; each output is within
  * 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then rounded once
- * to out_dtype.  Up to 8 rows of X are processed per pass on the CUDA cores
- * (fused multiply-adds; each pass reads the payload once); with
- * NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte aligned and K % 8 == 0
- * the product runs on the tensor cores (tcgen05, binary32 accumulation in
- * tensor memory) in one pass.  Same ownership, asynchrony and error
+ * to out_dtype.  Kernels: one row of X on the CUDA cores (fused
+ * multiply-adds); 2 to 8 rows of X with NDQ_FLOAT weights of gguf q6_k,
+ * q8_0 or q8_g32_fp16, X 16-byte aligned and K % 8 == 0, on the tensor
+ * cores with the group scales applied to the tensor core's per-group sums;
+ * other formats up to 8 rows per pass on the CUDA cores (each pass reads
+ * the payload once); with NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte
+ * aligned and K % 8 == 0, on the tensor cores (tcgen05, binary32
+ * accumulation in tensor memory) in one pass.  Same ownership, asynchrony and error
  * rules as ndq_dequantize_packed; M, N or K of 0 is valid (K == 0 writes
  * zeros); NDQ_ERR_BAD_DTYPE for other weight or output types. */
 int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t *w, size_t w_len, const void *x_bf16,
                       int64_t M, int weight_dtype, int out_dtype, void *y, void *stream);
+
+/* One product of a batched fused call: weight payload w [n, K] (device,
+ * w_len bytes, same length rule as ndq_matmul_packed) and its output y
+ * [M, n] (device). */
+typedef struct ndq_matmul_desc {
+    int32_t format_id;
+    int32_t reserved; /* ignored; set to 0 */
+    int64_t n;
+    const uint8_t *w;
+    uint64_t w_len;
+    void *y;
+} ndq_matmul_desc;
+
+/* Several fused products that share their activations X [M, K]:
+ * y_i = X * W_i^T for every descriptor, exactly as `count` calls of
+ * ndq_matmul_packed with the same x_bf16, K, M, weight_dtype and out_dtype
+ * (the same bounds; each output is the same as that call's in every bit
+ * when it takes the same kernel).  This is not part of the DequantizePacked
+ * specification: it lets the weights that read one activation row (a
+ * layer's q, k and v projections, or its gate and up projections) run as
+ * ONE kernel launch when M == 1, count <= 8, every product has n > 0 and
+ * the same format, K % 512 == 0, K <= 16384, the format is gguf q8_0 /
+ * q8_g32_fp16 / q4_k / q6_k and every payload row starts on a 16-byte
+ * boundary; otherwise the products are launched one after another.
+ *   descs  host array of `count` descriptors, read during the call only
+ * Every descriptor is validated before anything is launched (the status of
+ * the first invalid one is returned: the codes of ndq_matmul_packed, or
+ * NDQ_ERR_BAD_COUNT for count < 0); count == 0 returns NDQ_OK.  Allocates
+ * nothing; asynchronous on `stream` like ndq_matmul_packed. */
+int ndq_matmul_packed_batched(const ndq_matmul_desc *descs, int count, int64_t K, const void *x_bf16, int64_t M,
+                              int weight_dtype, int out_dtype, void *stream);
 
 /* Device workspace bytes the batched call needs for n tensors (a table of
  * per-tensor launch descriptors), or 0 when n < 0. */

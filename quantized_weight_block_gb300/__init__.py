@@ -53,6 +53,13 @@ class ndq_tensor_desc(ctypes.Structure):
     ]
 
 
+class ndq_matmul_desc(ctypes.Structure):
+    _fields_ = [
+        ("format_id", ctypes.c_int32), ("reserved", ctypes.c_int32), ("n", ctypes.c_int64), ("w", ctypes.c_void_p),
+        ("w_len", ctypes.c_uint64), ("y", ctypes.c_void_p),
+    ]
+
+
 _c = ctypes
 _lib.ndq_format_from_name.argtypes = [_c.c_char_p]
 _lib.ndq_format_from_name.restype = _c.c_int
@@ -75,13 +82,15 @@ _lib.ndq_test_withhold_copy.argtypes = [_c.c_int64, _c.c_uint32]
 _lib.ndq_dequantize_packed_batched_noalloc.argtypes = [_c.POINTER(ndq_tensor_desc), _c.c_int, _c.c_void_p]
 _lib.ndq_matmul_packed.argtypes = [_c.c_int, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_size_t, _c.c_void_p,
                                    _c.c_int64, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p]
+_lib.ndq_matmul_packed_batched.argtypes = [_c.POINTER(ndq_matmul_desc), _c.c_int, _c.c_int64, _c.c_void_p,
+                                           _c.c_int64, _c.c_int, _c.c_int, _c.c_void_p]
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = (
     "ndq_format_from_name", "ndq_format_name", "ndq_format_geometry", "ndq_format_supported",
     "ndq_status_string", "ndq_payload_geometry", "ndq_dequantize_packed", "ndq_batched_workspace_bytes",
     "ndq_dequantize_packed_batched", "ndq_get_device_fault", "ndq_dequantize_packed_batched_noalloc",
-    "ndq_matmul_packed", "ndq_test_withhold_copy",
+    "ndq_matmul_packed", "ndq_test_withhold_copy", "ndq_matmul_packed_batched",
 )
 
 
@@ -153,6 +162,13 @@ def ndq_matmul_packed(format_id: int, N: int, K: int, w_ptr: int, w_len: int, x_
                       weight_dtype: int, out_dtype: int, y_ptr: int, stream: int = 0) -> int:
     """Raw call of the fused decode + product; returns the status code."""
     return _lib.ndq_matmul_packed(format_id, N, K, w_ptr, w_len, x_ptr, M, weight_dtype, out_dtype, y_ptr, stream)
+
+
+def ndq_matmul_packed_batched(descs, K: int, x_ptr: int, M: int, weight_dtype: int, out_dtype: int,
+                              stream: int = 0) -> int:
+    """Raw call over a sequence of ndq_matmul_desc sharing X; returns the status code."""
+    arr = (ndq_matmul_desc * max(1, len(descs)))(*descs)
+    return _lib.ndq_matmul_packed_batched(arr, len(descs), K, x_ptr, M, weight_dtype, out_dtype, stream)
 
 
 def ndq_test_withhold_copy(tile: int, wait_limit_us: int) -> int:
@@ -263,6 +279,29 @@ def matmul_packed(fmt, w, N: int, K: int, x, out_dtype=None, y=None, stream=None
     if rc:
         raise NdqError(rc, str(fmt))
     return y
+
+
+def matmul_packed_batched(items, K: int, x, out_dtype=None, stream=None, weight_dtype=None):
+    """Several products sharing the bfloat16 activations x [M, K]: items is
+    a sequence of (fmt, w, N) or (fmt, w, N, y) with w a CUDA uint8 payload
+    [N, K]; returns the list of outputs Y_i [M, N_i]."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.float32
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[-1] != K:
+        raise ValueError("x must be a contiguous bfloat16 tensor [M, K]")
+    M = x.numel() // K if K else x.shape[0]
+    descs, ys = [], []
+    for it in items:
+        fmt, w, N = it[0], it[1], it[2]
+        y = it[3] if len(it) > 3 and it[3] is not None else torch.empty((M, N), dtype=out_dtype, device=w.device)
+        descs.append(ndq_matmul_desc(format_id(fmt), 0, N, w.data_ptr(), w.numel(), y.data_ptr()))
+        ys.append(y)
+    wcode = out_dtype_code(weight_dtype or torch.float32)
+    odt = out_dtype_code(ys[0].dtype if ys else out_dtype)
+    rc = ndq_matmul_packed_batched(descs, K, x.data_ptr(), M, wcode, odt, _stream_handle(stream))
+    if rc:
+        raise NdqError(rc)
+    return ys
 
 
 def get_device_fault() -> int:

@@ -308,13 +308,12 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
         q.out_bf16 = p.out_bf16;
         return ndq::launch_mma(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
     }
-    // 2 to 8 activation rows with binary32 weights of gguf:q6_k (a group
-    // scale times a small code): the grouped tensor-core product (the tensor
-    // core sums codes times X per group, the epilogue applies the scales),
-    // when X is 16-byte aligned.  (One row stays on the CUDA cores, which
-    // measured faster there, and so does q8_0, whose 34-byte blocks the
-    // tensor-core kernel stages less efficiently.)
-    if (weight_dtype == NDQ_FLOAT && M >= 2 && M <= ndq::kMvMaxRows && p.xvec && p.w.fmt == ndq::KF_Q6_K) {
+    // 2 to 8 activation rows with binary32 weights of gguf:q6_k or q8_0 (a
+    // group scale times a small code): the grouped tensor-core product (the
+    // tensor core sums codes times X per group, the epilogue applies the
+    // scales), when X is 16-byte aligned.  (One row stays on the CUDA cores,
+    // which measured faster there.)
+    if (weight_dtype == NDQ_FLOAT && M >= 2 && M <= ndq::kMvMaxRows && p.xvec && ndq::mmag_for(p.w.fmt, 1) != nullptr) {
         ndq::MmaParams q;
         std::memset(&q, 0, sizeof(q));
         q.w = p.w;
@@ -335,7 +334,71 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
         p.x = x + static_cast<uint64_t>(m0) * static_cast<uint64_t>(K);
         p.y = static_cast<uint8_t*>(y) + static_cast<uint64_t>(m0) * static_cast<uint64_t>(N) * osize;
         p.m = static_cast<int32_t>(M - m0 < ndq::kMvMaxRows ? M - m0 : ndq::kMvMaxRows);
+        p.nt = 1;
+        p.gt[0].x = p.w.x;
+        p.gt[0].y = p.y;
+        p.gt[0].rows = p.n_rows;
         if (ndq::launch_matvec(p, stream) != 0) return NDQ_ERR_CUDA;
+    }
+    return NDQ_OK;
+}
+
+int ndq_matmul_packed_batched(const ndq_matmul_desc* descs, int count, int64_t K, const void* x_bf16, int64_t M,
+                              int weight_dtype, int out_dtype, void* stream) {
+    if (count < 0) return NDQ_ERR_BAD_COUNT;
+    if (count == 0) return NDQ_OK;
+    if (!descs) return NDQ_ERR_NULL;
+    if (K < 0 || M < 0) return NDQ_ERR_NEGATIVE_DIM;
+    if (out_dtype != NDQ_FLOAT && out_dtype != NDQ_BFLOAT16) return NDQ_ERR_BAD_DTYPE;
+    if (weight_dtype != NDQ_FLOAT && weight_dtype != NDQ_BFLOAT16) return NDQ_ERR_BAD_DTYPE;
+    // every product is checked before anything is launched
+    ndq::MvParams p;
+    std::memset(&p, 0, sizeof(p));
+    uint64_t total_rows = 0;
+    bool one_launch = M == 1 && count <= ndq::kGlMaxTensors && K > 0 && x_bf16 != nullptr;
+    for (int i = 0; i < count; ++i) {
+        const ndq_matmul_desc& d = descs[i];
+        if (!valid_id(d.format_id)) return NDQ_ERR_UNKNOWN_FORMAT;
+        if (d.n < 0) return NDQ_ERR_NEGATIVE_DIM;
+        if (fp8_row(d.format_id) && K % 16 != 0) return NDQ_ERR_NOT_BLOCK_ALIGNED;
+        const int64_t shape[2] = {d.n, K};
+        ndq::DevTensor t;
+        Geometry g;
+        const int rc = prepare(d.format_id, shape, 2, NDQ_FLOAT, d.w, d.w_len, const_cast<uint8_t*>(d.w), &t, &g);
+        if (rc != NDQ_OK) return rc;
+        uint64_t mn = 0, ybytes = 0;
+        if (mul_ovf(static_cast<uint64_t>(M), static_cast<uint64_t>(d.n), &mn) ||
+            mul_ovf(mn, out_dtype == NDQ_FLOAT ? 4u : 2u, &ybytes) || ybytes > static_cast<uint64_t>(INT64_MAX))
+            return NDQ_ERR_OVERFLOW;
+        if (mn != 0 && (!d.y || (K > 0 && !x_bf16))) return NDQ_ERR_NULL;
+        if (i == 0) p.w = t;
+        one_launch = one_launch && d.n > 0 && t.fmt == p.w.fmt;
+        if (i < ndq::kGlMaxTensors) {
+            p.gt[i].x = d.w;
+            p.gt[i].y = d.y;
+            p.gt[i].rows = static_cast<uint64_t>(d.n);
+        }
+        total_rows += static_cast<uint64_t>(d.n);
+    }
+    if (one_launch) {  // one k_gemvl launch over all the products, when the lean kernel takes them
+        p.n_rows = total_rows;
+        p.K = static_cast<uint64_t>(K);
+        p.bpr = p.w.nblocks / (p.gt[0].rows > 0 ? p.gt[0].rows : 1u);
+        p.x = static_cast<const uint16_t*>(x_bf16);
+        p.y = descs[0].y;
+        p.m = 1;
+        p.xvec = (reinterpret_cast<uintptr_t>(x_bf16) & 15u) == 0 && K % 8 == 0;
+        p.wbf16 = weight_dtype == NDQ_BFLOAT16;
+        p.out_bf16 = out_dtype == NDQ_BFLOAT16;
+        p.rows_per_stage = 1;
+        p.nt = count;
+        if (ndq::gemvl_takes(p)) return ndq::launch_matvec(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    }
+    for (int i = 0; i < count; ++i) {
+        const ndq_matmul_desc& d = descs[i];
+        const int rc = ndq_matmul_packed(d.format_id, d.n, K, d.w, d.w_len, x_bf16, M, weight_dtype, out_dtype, d.y,
+                                         stream);
+        if (rc != NDQ_OK) return rc;
     }
     return NDQ_OK;
 }

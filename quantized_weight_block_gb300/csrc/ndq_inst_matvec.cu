@@ -60,6 +60,16 @@ struct MvDeviceInfo {
 MvDeviceInfo g_mv_dev[64];
 }  // namespace
 
+bool gemvl_takes(const MvParams& p) {
+    const int f = p.w.fmt;
+    if (p.m != 1 || p.K == 0 || p.K % kGlIter != 0 || p.K / kGlIter > 4u * kConsumerWarpsPerCta || f < 0 ||
+        f >= KF_COUNT || p.nt < 1 || p.nt > kGlMaxTensors || (p.bpr * p.w.S) % 16u != 0)
+        return false;
+    for (int t = 0; t < p.nt; ++t)
+        if ((reinterpret_cast<uintptr_t>(p.gt[t].x) & 15u) != 0) return false;
+    return matvec_for(f, kMvLean) != nullptr;
+}
+
 int launch_matvec(const MvParams& p0, void* stream) {
     if (p0.n_rows == 0 || p0.m <= 0) return 0;
     int dev = 0;
@@ -79,7 +89,8 @@ int launch_matvec(const MvParams& p0, void* stream) {
     // memory when they fit, else read from global memory
     const uint64_t xf32 = p.K * 4u, xbf16 = static_cast<uint64_t>(p.m) * p.K * 2u;
     // one row: k_gemv1 (a warp per weight row) when the row fits
-    const bool rows_aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0;
+    bool rows_aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0;
+    for (int t = 0; t < p.nt; ++t) rows_aligned = rows_aligned && (reinterpret_cast<uintptr_t>(p.gt[t].x) & 15u) == 0;
     int variant = kMvAnyAlign;
     uint64_t xbytes = 0;
     if (p.m == 1 && xf32 <= kMvXBytes) {
@@ -105,6 +116,7 @@ int launch_matvec(const MvParams& p0, void* stream) {
             xbytes = 0;
         }
     }
+    if (!fn && p.nt > 1) return static_cast<int>(cudaErrorInvalidValue);  // (several tensors: the lean kernel only)
     if (!fn) fn = (f >= 0 && f < KF_COUNT) ? matvec_for(f, variant) : nullptr;
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     const bool lean = variant >= kMvLean;
@@ -121,6 +133,12 @@ int launch_matvec(const MvParams& p0, void* stream) {
         p.rows_per_stage = static_cast<int32_t>(
             gemvl_rows_per_stage(p.n_rows, p.bpr * p.w.S, xr, 2u * static_cast<uint64_t>(di.sms)));
         p.slot = static_cast<int32_t>(gl_slot_bytes(p.bpr * p.w.S, static_cast<uint32_t>(p.rows_per_stage)));
+        if (p.nt < 1 || p.nt > kGlMaxTensors) return static_cast<int>(cudaErrorInvalidValue);
+        uint64_t blocks = 0;
+        for (int t = 0; t < p.nt; ++t) {
+            blocks += (p.gt[t].rows + static_cast<uint64_t>(p.rows_per_stage) - 1) / static_cast<uint64_t>(p.rows_per_stage);
+            p.gt[t].blk_end = blocks;
+        }
     }
     const size_t base = lean      ? gemvl_smem_bytes(static_cast<uint32_t>(p.slot))
                         : one_row ? gemv1_smem_base(p.w.B, p.w.S)
@@ -147,7 +165,8 @@ int launch_matvec(const MvParams& p0, void* stream) {
         cps = n > 0 ? n : 1;
     }
     const uint64_t R = static_cast<uint64_t>(one_row ? kGvRows : p.rows_per_stage);
-    const uint64_t units = (p.n_rows + R - 1) / R;  // (k_gemv1: blocks of 8 rows)
+    // (k_gemv1: blocks of 8 rows; k_gemvl: the row blocks of all its tensors)
+    const uint64_t units = lean ? p.gt[p.nt - 1].blk_end : (p.n_rows + R - 1) / R;
     const uint64_t resident = static_cast<uint64_t>(di.sms) * static_cast<uint64_t>(cps);
     const unsigned grid = static_cast<unsigned>(units < resident ? units : resident);
     void* args[] = {&p};
@@ -261,9 +280,11 @@ int launch_mma(const MmaParams& p0, void* stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     // (bn: the smallest power of two >= M up to 256, so that each weight is
     // decoded once per 256 activation rows; short grids split K instead)
-    mma_stages(p.bn, p.span_bytes, &p.na, &p.ns);
+    // (k_mma's B stages are its A stages: a deeper B ring measured slower)
+    mma_stages(p.bn, p.span_bytes, &p.na, &p.ns, &p.nb);
+    p.nb = p.na;
     p.aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0 && p.span_bytes % 16u == 0;
-    const size_t smem = mma_smem_bytes(p.bn, p.span_bytes, p.na, p.ns);
+    const size_t smem = mma_smem_bytes(p.bn, p.span_bytes, p.na, p.ns, p.nb);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
     // X as a 2-D tensor map: [m_rows, K] bfloat16, boxes of 64 columns (one
@@ -290,7 +311,7 @@ int launch_mma(const MmaParams& p0, void* stream) {
     const uint64_t tiles = tiles_n * tiles_m;
     const uint64_t max_ctas = static_cast<uint64_t>(sms);
     const bool parks = static_cast<uint64_t>(p.bn) * kMmaRows * 4u <=
-                       static_cast<uint64_t>(p.na) * (kMmaATile + mma_b_tile(p.bn)) +
+                       static_cast<uint64_t>(p.na) * kMmaATile + static_cast<uint64_t>(p.nb) * mma_b_tile(p.bn) +
                            static_cast<uint64_t>(p.ns) * mma_span_stage(p.span_bytes);
     unsigned split = 1;
     while (split < kMaxMmaSplit && parks && spans >= 4u * split && tiles * 2u * split <= max_ctas) split *= 2;
@@ -341,11 +362,11 @@ int launch_mmag(const MmaParams& p0, void* stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     const int ng = kMmaK / mmag_group(f);
     const uint32_t ncol = mg_ncol(ng, p.bn);
-    mmag_stages(ncol, ng, p.span_bytes, &p.na, &p.ns);
+    mmag_stages(ncol, ng, p.span_bytes, &p.na, &p.ns, &p.nb);
     p.aligned = (reinterpret_cast<uintptr_t>(p.w.x) & 15u) == 0 && (p.bpr * p.w.S) % 16u == 0 && p.span_bytes % 16u == 0;
     const int pm = payload_map(p);
     if (pm != 0) return pm;
-    const size_t smem = mmag_smem_bytes(ncol, ng, p.span_bytes, p.na, p.ns);
+    const size_t smem = mmag_smem_bytes(ncol, ng, p.span_bytes, p.na, p.ns, p.nb);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
     // Split K over a cluster of up to 8 CTAs while the tiles leave SMs idle

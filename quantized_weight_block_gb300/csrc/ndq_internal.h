@@ -153,6 +153,16 @@ using KernelFn = void (*)(KParams);
 // Decode fused into a product with few activation rows (ndq_matvec.cuh):
 // Y[m, n] = sum_k X[m, k] * W[n, k] for m < m_rows <= kMvMaxRows.
 constexpr int kMvMaxRows = 8;
+// One weight tensor of a k_gemvl launch: its payload rows, its outputs and
+// the end of its row blocks in the launch's block order.
+constexpr int kGlMaxTensors = 8;
+struct GlTensor {
+    const uint8_t* x;  // payload [rows, K] (16-byte-aligned rows)
+    void* y;           // outputs [rows] (the launch's output type)
+    uint64_t rows;
+    uint64_t blk_end;  // (set by the launcher) row blocks of tensors 0..this one
+};
+
 struct MvParams {
     DevTensor w;          // the weight payload as a decode descriptor (y unused)
     const uint16_t* x;    // bfloat16 activations [m, K], row-major
@@ -168,9 +178,18 @@ struct MvParams {
     int32_t slot;         // k_gemvl: bytes of one staged row slot (set by the launcher)
     unsigned int* fault;  // device fault word (set by the launcher)
     const IqGrids* grids;  // IQ codebooks (set by the launcher)
+    // k_gemvl: the launch's tensors (same format and K; n_rows is their
+    // total); a single product is tensor 0 = (w.x, y, n_rows)
+    int32_t nt;
+    int32_t pad2_;
+    GlTensor gt[kGlMaxTensors];
 };
 
 using MvKernelFn = void (*)(MvParams);
+// True when the lean one-row kernel (k_gemvl) takes the launch p: one row of
+// X, K a multiple of 512 up to 16384, a family with lean decoders, and
+// 16-byte-aligned rows in every tensor of p.gt.
+bool gemvl_takes(const MvParams& p);
 
 // Where a fused kernel reads the activations: a copy in shared memory
 // (binary32 for one row, bfloat16 for several) when it fits in kMvXBytes,
@@ -210,6 +229,8 @@ struct MmaParams {
     uint32_t ns;          // staged payload spans, 2..4 (set by the launcher)
     uint32_t aligned;     // 1: the payload, its rows and its spans start on 16-byte boundaries
     uint32_t wbox;        // bytes per row of a payload tensor copy (wmap), 0: 16-byte copies per row
+    uint32_t nb;          // B operand stages (X slices in flight), 2..8 (set by the launcher)
+    uint32_t pad_;
     unsigned int* fault;
     const IqGrids* grids;
     CUtensorMap xmap;     // X as a 2-D bfloat16 tensor [m_rows, K], boxes of 64 x bn, 128-byte swizzle

@@ -584,8 +584,10 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemv1(const MvParams p) {
 // ---------------------------------------------------------------------------
 // One activation row, lean decoders: k_gemvl.  For the formats of a K-quant
 // model (gguf q8_0, q4_k, q6_k) with K a multiple of 512 and 16-byte-aligned
-// rows.  A stage holds rb consecutive whole weight rows (one bulk copy); the
-// CTAs take row blocks in turn.  A row is cut into lane units of 16 weights,
+// rows, of one tensor or of up to 8 tensors that share X (one launch for,
+// say, the q, k and v projections).  A stage holds rb consecutive whole
+// weight rows of one tensor (one bulk copy); the CTAs take row blocks in
+// turn.  A row is cut into lane units of 16 weights,
 // 32 per warp iteration; warp w always takes the same XR iterations of every
 // row, so its lanes keep their activations in registers (binary32, loaded
 // once per CTA) and reuse them for the stage's rb rows, whose sums are
@@ -778,7 +780,16 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
     const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
     const uint32_t cw = (nit + XR - 1) / XR;  // warps with iterations (at most 8)
     const uint32_t rowb = static_cast<uint32_t>(p.bpr * p.w.S);  // a multiple of 16
-    const uint64_t nblk = (p.n_rows + rb - 1u) / rb;
+    const uint64_t nblk = p.gt[p.nt - 1].blk_end;
+    // row block -> (tensor, first row, rows): tensor t holds blocks
+    // [gt[t-1].blk_end, gt[t].blk_end)
+    auto locate = [&](uint64_t blk, int& t, uint64_t& r0, uint32_t& nr) {
+        t = 0;
+        while (t + 1 < p.nt && blk >= p.gt[t].blk_end) ++t;
+        r0 = (blk - (t > 0 ? p.gt[t - 1].blk_end : 0u)) * rb;
+        const uint64_t left = p.gt[t].rows - r0;
+        nr = static_cast<uint32_t>(left < rb ? left : rb);
+    };
     if (tid == 0) {
         for (int s = 0; s < kGlStages; ++s) {
             mbar_init(&H.full[s], 1);
@@ -791,9 +802,12 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
     // parameters; the activations, which the previous kernel may write, are
     // read after the wait)
     if (tid == kThreads && blockIdx.x < nblk) {
-        const uint64_t r0 = blockIdx.x * static_cast<uint64_t>(rb), nr = p.n_rows - r0 < rb ? p.n_rows - r0 : rb;
-        const uint64_t bytes = nr * rowb;
-        prefetch_l2(p.w.x + r0 * rowb, static_cast<uint32_t>(bytes < 32768u ? bytes : 32768u));
+        int t;
+        uint64_t r0;
+        uint32_t nr;
+        locate(blockIdx.x, t, r0, nr);
+        const uint32_t bytes = nr * rowb;
+        prefetch_l2(p.gt[t].x + r0 * rowb, bytes < 32768u ? bytes : 32768u);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -810,10 +824,13 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
                 fault = true;
                 break;
             }
-            const uint64_t r0 = blk * rb, nr = p.n_rows - r0 < rb ? p.n_rows - r0 : rb;
-            const uint32_t bytes = static_cast<uint32_t>(nr * rowb);
+            int t;
+            uint64_t r0;
+            uint32_t nr;
+            locate(blk, t, r0, nr);
+            const uint32_t bytes = nr * rowb;
             mbar_arrive_expect_tx(&H.full[s], bytes);
-            bulk_load(smem + static_cast<uint32_t>(s) * slot, p.w.x + r0 * rowb, bytes, &H.full[s]);
+            bulk_load(smem + static_cast<uint32_t>(s) * slot, p.gt[t].x + r0 * rowb, bytes, &H.full[s]);
         }
         if (fault) {
             atomicOr(p.fault, 1u);
@@ -857,8 +874,10 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
             if (lane == 0) atomicOr(p.fault, 2u);
             return;
         }
-        const uint64_t r0 = blk * rb;
-        const uint32_t nr = static_cast<uint32_t>(p.n_rows - r0 < rb ? p.n_rows - r0 : rb);
+        int t;
+        uint64_t r0;
+        uint32_t nr;
+        locate(blk, t, r0, nr);
         const uint8_t* in = smem + static_cast<uint32_t>(s) * slot;
         float2 acc[RBM];
 #pragma unroll
@@ -906,9 +925,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
                 float y = R.red[s][lane][0];
                 for (uint32_t w = 1; w < cw; ++w) y = __fadd_rn(y, R.red[s][lane][w]);
                 if (p.out_bf16)
-                    static_cast<__nv_bfloat16*>(p.y)[r0 + lane] = __float2bfloat16_rn(y);
+                    static_cast<__nv_bfloat16*>(p.gt[t].y)[r0 + lane] = __float2bfloat16_rn(y);
                 else
-                    static_cast<float*>(p.y)[r0 + lane] = y;
+                    static_cast<float*>(p.gt[t].y)[r0 + lane] = y;
             }
             __syncwarp();
             if (lane == 0) R.cnt[s] = 0u;

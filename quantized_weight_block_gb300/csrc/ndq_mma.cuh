@@ -54,22 +54,24 @@ constexpr int kMmaThreads = kMmaDecoders + 96;
 constexpr int kMmaRows = 128;                         // weight rows per CTA (MMA M)
 constexpr int kMmaK = 64;                             // weights per k-step (one 128-byte swizzle atom of bf16)
 constexpr int kMmaATile = kMmaRows * kMmaK * 2;       // 16 KB
-constexpr uint32_t kMmaMaxStages = 4;                 // operand stages (A, B) at most
+constexpr uint32_t kMmaMaxStages = 4;                 // A operand stages at most
+constexpr uint32_t kMmaMaxB = 8;                      // B operand stages (X slices) at most
 constexpr uint32_t kMmaMaxSpans = 4;                  // staged packed spans at most
 constexpr uint32_t kMaxMmaSplit = 8;                  // CTAs of a split-K cluster (portable cluster size)
-constexpr uint32_t kMmaSmemLimit = 227u * 1024u;      // dynamic shared memory of one CTA at most
+constexpr uint32_t kMmaSmemLimit = 223u * 1024u;      // dynamic shared memory of one CTA at most (227 KB less the static part)
 
 struct MmaShared {
     uint64_t full[kMmaMaxSpans];     // packed span staged (bulk copies complete)
     uint64_t empty[kMmaMaxSpans];    // every decode warp is done with the span
     uint64_t afull[kMmaMaxStages];   // the decode warps wrote the stage's A operand
-    uint64_t bfull[kMmaMaxStages];   // the stage's X slice landed (TMA transaction count)
-    uint64_t sfree[kMmaMaxStages];   // the MMAs reading the stage are done (tcgen05.commit)
+    uint64_t sfree[kMmaMaxStages];   // the MMAs reading the A stage are done (tcgen05.commit)
+    uint64_t bfull[kMmaMaxB];        // the B stage's X slice landed
+    uint64_t bfree[kMmaMaxB];        // the MMAs reading the B stage are done (tcgen05.commit)
     uint32_t tmem;
     uint32_t pad[3];
 };
 
-// Dynamic shared memory: [A x na][B x na][packed spans x ns][MmaShared],
+// Dynamic shared memory: [A x na][B x nb][packed spans x ns][MmaShared],
 // 1024-byte aligned pieces.  After the k-loop the A and B region holds the
 // partial tile (128 x bn binary32) of a split-K reduction.
 __host__ __device__ constexpr uint32_t mma_b_tile(uint32_t bn) { return bn * 128u; }
@@ -91,21 +93,26 @@ __host__ __device__ constexpr uint32_t mma_wbox_odd(uint32_t w) { return (w / 16
 __host__ __device__ constexpr uint32_t mma_wbox(uint32_t span) {
     return mma_wbox_odd((span + 20u + 15u) / 16u * 16u) <= 256u ? mma_wbox_odd((span + 20u + 15u) / 16u * 16u) : 0u;
 }
-__host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span, uint32_t na, uint32_t ns) {
-    return 1024u + na * (kMmaATile + mma_b_tile(bn)) + ns * mma_span_stage(span) + 1024u;
+__host__ __device__ constexpr uint32_t mma_smem_bytes(uint32_t bn, uint32_t span, uint32_t na, uint32_t ns,
+                                                      uint32_t nb) {
+    return 1024u + na * kMmaATile + nb * mma_b_tile(bn) + ns * mma_span_stage(span) + 1024u;
 }
-// Operand stages na and span stages ns: the deepest pipeline that fits,
-// operand stages first (4, 3, then 2 of each at least).
-__host__ __device__ inline void mma_stages(uint32_t bn, uint32_t span, uint32_t* na, uint32_t* ns) {
+// A stages na, span stages ns and B stages nb: the deepest A and span
+// pipeline that fits with at least na B stages (4, 3, then 2 of each at
+// least), then as many B stages as fit, up to 8: the X slices come from L2
+// and a deep B ring keeps their latency off the MMA issue.
+__host__ __device__ inline void mma_stages(uint32_t bn, uint32_t span, uint32_t* na, uint32_t* ns, uint32_t* nb) {
     *na = 2u;
     *ns = 2u;
     for (uint32_t a = 4u; a >= 2u; --a)
         for (uint32_t s = 4u; s >= 2u; --s)
-            if (mma_smem_bytes(bn, span, a, s) <= kMmaSmemLimit && a * 8u + s > *na * 8u + *ns &&
+            if (mma_smem_bytes(bn, span, a, s, a) <= kMmaSmemLimit && a * 8u + s > *na * 8u + *ns &&
                 (a >= 3u || s <= 3u)) {
                 *na = a;
                 *ns = s;
             }
+    *nb = *na;
+    while (*nb < kMmaMaxB && mma_smem_bytes(bn, span, *na, *ns, *nb + 1u) <= kMmaSmemLimit) ++*nb;
 }
 
 // TMA tile copy of a 2-D tensor-map box at (x, y) into shared memory,

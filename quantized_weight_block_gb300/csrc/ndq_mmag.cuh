@@ -65,6 +65,48 @@ __device__ __forceinline__ uint32_t bf16_codes(uint32_t w, uint32_t bias2) {
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// Lean codes decoder for gguf:q6_k (one span = one block): the four threads
+// of a weight row take the two k-steps 2h, 2h+1 of half h of the block as
+// runs of 4 codes that come from aligned 32-bit words: thread t takes l0 =
+// 4t and 4t + 16 (low bytes 64h + l0 and 64h + 32 + l0, high bytes 32h +
+// l0); runs 0 and 1 (K offsets l0, l0 + 32 of k-step 2h) use the low
+// nibbles and high-bit pairs 0, 1, runs 2 and 3 (the same offsets of k-step
+// 2h + 1) the high nibbles and pairs 2, 3.  Each run is stored as 8 bytes of
+// the A operand (the codes exact in bfloat16); thread t also forms the
+// scales 8h + t and 8h + 4 + t, group t of each k-step.  `in` is the row's
+// staged span, ph the block's byte phase in it; ok = false (a row past N)
+// stores zeros.
+// ---------------------------------------------------------------------------
+struct TlQ6K {
+    static constexpr int KS = 2;  // k-steps per call
+    template <bool PH>
+    __device__ __forceinline__ static void run(const uint8_t* in, uint32_t ph, uint32_t ks, uint32_t t,
+                                               uint8_t* const* aS, float* const* sc, uint32_t r, bool ok) {
+        const uint32_t h = ks >> 1;
+        const float d = h2f(lds_2<PH>(in, ph + 208u));
+        sc[0][4u * r + t] = ok ? __fmul_rn(d, i8_float(in[ph + 192u + 8u * h + t])) : 0.0f;
+        sc[1][4u * r + t] = ok ? __fmul_rn(d, i8_float(in[ph + 196u + 8u * h + t])) : 0.0f;
+#pragma unroll
+        for (uint32_t jj = 0; jj < 2; ++jj) {
+            const uint32_t l0 = 4u * t + 16u * jj;
+            const uint32_t A = lds_4(in, ph + 64u * h + l0), C = lds_4(in, ph + 64u * h + 32u + l0);
+            const uint32_t Q = lds_4(in, ph + 128u + 32u * h + l0);
+            const uint32_t c[4] = {(A & 0x0F0F0F0Fu) | ((Q & 0x03030303u) << 4),
+                                   (C & 0x0F0F0F0Fu) | ((Q & 0x0C0C0C0Cu) << 2),
+                                   ((A >> 4) & 0x0F0F0F0Fu) | (Q & 0x30303030u),
+                                   ((C >> 4) & 0x0F0F0F0Fu) | ((Q >> 2) & 0x30303030u)};
+#pragma unroll
+            for (uint32_t q = 0; q < 4; ++q) {
+                const uint32_t k = l0 + 32u * (q & 1u);
+                const uint2 v = ok ? make_uint2(bf16_codes<0>(c[q], 0x43204320u), bf16_codes<2>(c[q], 0x43204320u))
+                                   : make_uint2(0u, 0u);  // (128 + code) - 160
+                *reinterpret_cast<uint2*>(aS[q >> 1] + sw128(r, k >> 3) + 8u * ((k >> 2) & 1u)) = v;
+            }
+        }
+    }
+};
+
 template <>
 struct Gc<KF_Q6_K> {
     static constexpr bool kOk = true;
@@ -121,21 +163,23 @@ __host__ __device__ constexpr uint32_t mg_ncol(int ng, uint32_t mp) {
     return static_cast<uint32_t>(ng) * mp < 16u ? 16u : static_cast<uint32_t>(ng) * mp;
 }
 __host__ __device__ constexpr uint32_t mg_scale_bytes(int ng) { return kMmaRows * 4u * static_cast<uint32_t>(ng); }
-// Dynamic shared memory: [A x na][B x na][scales x na][spans x ns][MmaShared][MgShared].
+// Dynamic shared memory: [A x na][B x nb][scales x na][spans x ns][MmaShared][MgShared].
 __host__ __device__ constexpr uint32_t mmag_smem_bytes(uint32_t ncol, int ng, uint32_t span, uint32_t na,
-                                                       uint32_t ns) {
-    return 1024u + na * (kMmaATile + mma_b_tile(ncol) + mg_scale_bytes(ng)) + ns * mma_span_stage(span) + 1024u;
+                                                       uint32_t ns, uint32_t nb) {
+    return 1024u + na * (kMmaATile + mg_scale_bytes(ng)) + nb * mma_b_tile(ncol) + ns * mma_span_stage(span) + 1024u;
 }
-__host__ __device__ inline void mmag_stages(uint32_t ncol, int ng, uint32_t span, uint32_t* na, uint32_t* ns) {
+__host__ __device__ inline void mmag_stages(uint32_t ncol, int ng, uint32_t span, uint32_t* na, uint32_t* ns,
+                                            uint32_t* nb) {
     *na = 2u;
     *ns = 2u;
     for (uint32_t a = 4u; a >= 2u; --a)
         for (uint32_t s = 4u; s >= 2u; --s)
-            if (mmag_smem_bytes(ncol, ng, span, a, s) <= kMmaSmemLimit && a * 8u + s > *na * 8u + *ns &&
+            if (mmag_smem_bytes(ncol, ng, span, a, s, kMmaMaxB) <= kMmaSmemLimit && a * 8u + s > *na * 8u + *ns &&
                 (a >= 3u || s <= 3u)) {
                 *na = a;
                 *ns = s;
             }
+    *nb = kMmaMaxB;
 }
 
 // TMEM -> registers: N consecutive binary32 columns of this thread's lane.
@@ -172,10 +216,10 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_mmag(const __grid_constant__ 
     constexpr uint32_t kTmemCols = kMgRegions * NCOL < 32u ? 32u : kMgRegions * NCOL;
     extern __shared__ __align__(1024) uint8_t mg_smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mg_smem_raw) + 1023u) & ~uintptr_t(1023));
-    const uint32_t na = p.na;
+    const uint32_t na = p.na, nb = p.nb;
     uint8_t* sA = base;
     uint8_t* sB = base + na * kMmaATile;
-    float* sS = reinterpret_cast<float*>(sB + na * mma_b_tile(NCOL));
+    float* sS = reinterpret_cast<float*>(sB + nb * mma_b_tile(NCOL));
     uint8_t* sP = reinterpret_cast<uint8_t*>(sS) + na * mg_scale_bytes(NG);
     const uint32_t rstride = p.wbox ? p.wbox : mma_row_stride(p.span_bytes);
     const uint32_t stage_bytes = mma_span_stage(p.span_bytes);
@@ -196,9 +240,12 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_mmag(const __grid_constant__ 
         }
         for (uint32_t s = 0; s < na; ++s) {
             mbar_init(&S.afull[s], kMmaDecoders / 32);
-            mbar_init(&S.bfull[s], 1);
             mbar_init(&S.sfree[s], 1);
             mbar_init(&Q.efree[s], 4);
+        }
+        for (uint32_t s = 0; s < nb; ++s) {
+            mbar_init(&S.bfull[s], 32);  // one arrival per B-warp lane (cp.async completion)
+            mbar_init(&S.bfree[s], 1);
         }
         for (uint32_t r = 0; r < kMgRegions; ++r) {
             mbar_init(&Q.dfull[r], 1);
@@ -243,13 +290,16 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_mmag(const __grid_constant__ 
         mma_producer<F>(p, S, sP, rstride, stage_bytes);
     } else if (warp == kMgBWarp) {
         // zeros everywhere once, then per k-step the X slices of the
-        // staircase: row g * MP + m, 16-byte units of group g
-        for (uint32_t i = lane; i < na * mma_b_tile(NCOL) / 16u; i += 32u)
+        // staircase (row g * MP + m, the 16-byte units of group g) by
+        // asynchronous copies that every lane has counted on the stage's
+        // full barrier when they land (a unit past X reads no bytes and
+        // lands as zeros); nb stages ahead of the MMAs
+        for (uint32_t i = lane; i < nb * mma_b_tile(NCOL) / 16u; i += 32u)
             reinterpret_cast<uint4*>(sB)[i] = make_uint4(0u, 0u, 0u, 0u);
         const uint64_t kx = sp0 * p.span_elems;
-        uint32_t b = 0, ph = 0;
         for (uint32_t j = 0; j < nk; ++j) {
-            if (j >= na && !__all_sync(0xffffffffu, mbar_wait_bounded(&S.sfree[b], ph))) {
+            const uint32_t b = j % nb;
+            if (j >= nb && !__all_sync(0xffffffffu, mbar_wait_bounded(&S.bfree[b], ((j / nb) - 1u) & 1u))) {
                 if (lane == 0) {
                     atomicOr(p.fault, 4u);
                     atomicOr(&s_fault, 1u);
@@ -257,40 +307,40 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_mmag(const __grid_constant__ 
                 break;
             }
             const uint64_t k0 = kx + static_cast<uint64_t>(kMmaK) * j;
-            uint8_t* bS = sB + b * mma_b_tile(NCOL);
+            const uint32_t bS = smem_addr(sB + b * mma_b_tile(NCOL));
             for (uint32_t e = lane; e < static_cast<uint32_t>(MP) * 8u; e += 32u) {
                 const uint32_t m = e >> 3, u = e & 7u, g = (8u * u) / static_cast<uint32_t>(G);
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (m < p.m_rows && k0 + 8u * u < p.K)
-                    v = __ldg(reinterpret_cast<const uint4*>(p.x + m * p.K + k0 + 8u * u));
-                *reinterpret_cast<uint4*>(bS + sw128(g * MP + m, u)) = v;
+                const bool in_x = m < p.m_rows && k0 + 8u * u < p.K;
+                const uint16_t* src = in_x ? p.x + m * p.K + k0 + 8u * u : p.x;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(bS + sw128(g * MP + m, u)), "l"(src),
+                             "r"(in_x ? 16u : 0u)
+                             : "memory");
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.bfull[b]);
-            if (++b == na) {
-                b = 0;
-                if (j + 1 > na) ph ^= 1u;
-            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&S.bfull[b])) : "memory");
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // (no copy of this lane outlives the role)
     } else if (warp == kMgIssueWarp) {
         const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((NCOL >> 3) << 17) | ((kMmaRows >> 4) << 24);
         uint32_t issued = 0;
         for (uint32_t i = 0; i < nk; ++i) {
-            const uint32_t a = i % na, ap = (i / na) & 1u, r = i % kMgRegions;
-            bool ok = mbar_wait_bounded(&S.afull[a], ap) && mbar_wait_bounded(&S.bfull[a], ap);
+            const uint32_t a = i % na, ap = (i / na) & 1u, b = i % nb, r = i % kMgRegions;
+            bool ok = mbar_wait_bounded(&S.afull[a], ap) && mbar_wait_bounded(&S.bfull[b], (i / nb) & 1u);
             if (ok && i >= kMgRegions) ok = mbar_wait_bounded(&Q.dfree[r], ((i / kMgRegions) - 1u) & 1u);
             if (!__all_sync(0xffffffffu, ok)) {
                 fault = true;
                 break;
             }
+            // (the B stage was written by asynchronous copies of the generic
+            // proxy: order them before the tensor core's reads)
+            fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t a0 = smem_addr(sA + a * kMmaATile), b0 = smem_addr(sB + a * mma_b_tile(NCOL));
+            const uint32_t a0 = smem_addr(sA + a * kMmaATile), b0 = smem_addr(sB + b * mma_b_tile(NCOL));
             if (elect_one()) {
 #pragma unroll
                 for (uint32_t q = 0; q < kMmaK / 16; ++q)
                     mma_bf16(tmem + r * NCOL, mma_sdesc(a0 + 32u * q), mma_sdesc(b0 + 32u * q), idesc, q > 0 ? 1u : 0u);
                 mma_commit(&S.sfree[a]);
+                mma_commit(&S.bfree[b]);
                 mma_commit(&Q.dfull[r]);
             }
             __syncwarp();
@@ -353,37 +403,71 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_mmag(const __grid_constant__ 
             const uint8_t* row_in = sP + s * stage_bytes + r * rstride;
             const uint64_t block0 = n * p.bpr + k0s / static_cast<uint64_t>(Fmt<F>::B);
             const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(t.x + block0 * Fmt<F>::S) & 15u);
-            for (uint64_t k0 = k0s; k0 < kend; k0 += kMmaK, ++kbi) {
-                const uint32_t a = kbi % na;
-                if (kbi >= na) {  // the MMAs and the epilogue are done with this stage's previous use
-                    const uint32_t pp = ((kbi / na) - 1u) & 1u;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_bounded(&S.sfree[a], pp) && mbar_wait_bounded(&Q.efree[a], pp))) {
+            if constexpr (F == KF_Q6_K) {  // two k-steps at a time from aligned code words
+                constexpr int KS = TlQ6K::KS;
+                for (uint64_t k0 = k0s; k0 < kend; k0 += KS * kMmaK, kbi += KS) {
+                    uint8_t* aS[KS];
+                    float* scs[KS];
+                    bool ok = true;
+#pragma unroll
+                    for (int e = 0; e < KS; ++e) {  // the MMAs and the epilogue are done with the stage's previous use
+                        const uint32_t kb = kbi + e, a = kb % na;
+                        if (kb >= na) {
+                            const uint32_t pp = ((kb / na) - 1u) & 1u;
+                            ok = ok && mbar_wait_bounded(&S.sfree[a], pp) && mbar_wait_bounded(&Q.efree[a], pp);
+                        }
+                        aS[e] = sA + a * kMmaATile;
+                        scs[e] = sS + a * (kMmaRows * NG);
+                    }
+                    if (!__all_sync(0xffffffffu, ok)) {
                         fault = true;
                         break;
                     }
-                }
-                uint8_t* aS = sA + a * kMmaATile;
-                const uint32_t c = static_cast<uint32_t>((k0 - k0s) / 16u) + quad;
-                const uint64_t kc = k0 + 16u * quad;
-                uint32_t wb[8];
-                float sc = 0.0f;
-                if (row_ok && kc < p.K) {
+                    const uint32_t ks = static_cast<uint32_t>((k0 - k0s) / kMmaK);
                     if (p.aligned)
-                        Gd::template chunk<false>(row_in, 0u, c, wb, sc);
+                        TlQ6K::run<false>(row_in, 0u, ks, quad, aS, scs, r, row_ok);
                     else
-                        Gd::template chunk<true>(row_in, ph, c, wb, sc);
-                } else {
+                        TlQ6K::run<true>(row_in, ph, ks, quad, aS, scs, r, row_ok);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) wb[e] = 0u;
+                        for (int e = 0; e < KS; ++e) mbar_arrive(&S.afull[(kbi + e) % na]);
+                    }
                 }
-                *reinterpret_cast<uint4*>(aS + sw128(r, 2u * quad)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-                *reinterpret_cast<uint4*>(aS + sw128(r, 2u * quad + 1u)) = make_uint4(wb[4], wb[5], wb[6], wb[7]);
-                if (quad % static_cast<uint32_t>(G / 16) == 0u)
-                    sS[a * (kMmaRows * NG) + r * NG + quad / static_cast<uint32_t>(G / 16)] = sc;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.afull[a]);
+            } else {
+                for (uint64_t k0 = k0s; k0 < kend; k0 += kMmaK, ++kbi) {
+                    const uint32_t a = kbi % na;
+                    if (kbi >= na) {  // the MMAs and the epilogue are done with this stage's previous use
+                        const uint32_t pp = ((kbi / na) - 1u) & 1u;
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait_bounded(&S.sfree[a], pp) && mbar_wait_bounded(&Q.efree[a], pp))) {
+                            fault = true;
+                            break;
+                        }
+                    }
+                    uint8_t* aS = sA + a * kMmaATile;
+                    const uint32_t c = static_cast<uint32_t>((k0 - k0s) / 16u) + quad;
+                    const uint64_t kc = k0 + 16u * quad;
+                    uint32_t wb[8];
+                    float sc = 0.0f;
+                    if (row_ok && kc < p.K) {
+                        if (p.aligned)
+                            Gd::template chunk<false>(row_in, 0u, c, wb, sc);
+                        else
+                            Gd::template chunk<true>(row_in, ph, c, wb, sc);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) wb[e] = 0u;
+                    }
+                    *reinterpret_cast<uint4*>(aS + sw128(r, 2u * quad)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+                    *reinterpret_cast<uint4*>(aS + sw128(r, 2u * quad + 1u)) = make_uint4(wb[4], wb[5], wb[6], wb[7]);
+                    if (quad % static_cast<uint32_t>(G / 16) == 0u)
+                        sS[a * (kMmaRows * NG) + r * NG + quad / static_cast<uint32_t>(G / 16)] = sc;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.afull[a]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[s]);

@@ -160,6 +160,38 @@ def test_batched_validation():
     assert ndq.ndq_dequantize_packed_batched([desc(q40, (0, 32), 0, 0, 0)], 0, 0) == 0  # all empty
 
 
+def test_batched_matmul_validation():
+    # every product of a batched fused call is checked before any launch, so
+    # these run without a GPU (one invalid descriptor rejects the call)
+    q4k = ndq.format_id("gguf:q4_k")
+    F, BF = ndq.NDQ_FLOAT, ndq.NDQ_BFLOAT16
+
+    def desc(fmt, n, w_len, w=16, y=16):
+        return ndq.ndq_matmul_desc(fmt, 0, n, w, w_len, y)
+
+    K = 512
+    row = K // 256 * 144
+    good = desc(q4k, 3, 3 * row)
+    assert ndq.ndq_matmul_packed_batched([], K, 16, 1, F, F) == 0
+    assert ndq._lib.ndq_matmul_packed_batched(None, -1, K, None, 1, F, F, None) == 13
+    assert ndq._lib.ndq_matmul_packed_batched(None, 2, K, None, 1, F, F, None) == 1
+    assert ndq.ndq_matmul_packed_batched([good, desc(99, 3, 3 * row)], K, 16, 1, F, F) == 2
+    assert ndq.ndq_matmul_packed_batched([good, desc(q4k, -1, 0)], K, 16, 1, F, F) == 5
+    assert ndq.ndq_matmul_packed_batched([good], K + 32, 16, 1, F, F) == 6     # K not a multiple of 256
+    assert ndq.ndq_matmul_packed_batched([good, desc(q4k, 3, 3 * row + 1)], K, 16, 1, F, F) == 7
+    assert ndq.ndq_matmul_packed_batched([good, desc(q4k, 3, 3 * row, y=0)], K, 16, 1, F, F) == 1
+    assert ndq.ndq_matmul_packed_batched([good], K, 0, 1, F, F) == 1           # no activations
+    assert ndq.ndq_matmul_packed_batched([good], K, 16, -1, F, F) == 5
+    assert ndq.ndq_matmul_packed_batched([good], K, 16, 1, 7, F) == 9          # weight type
+    assert ndq.ndq_matmul_packed_batched([good], K, 16, 1, F, 10) == 9         # output type
+    assert ndq.ndq_matmul_packed_batched([good], K, 16, 1, BF, ndq.NDQ_DOUBLE) == 9
+    fp8 = ndq.format_id("fp8_e4m3fn_row_bf16")
+    assert ndq.ndq_matmul_packed_batched([desc(fp8, 2, 2 * 40 + 4)], 40, 16, 1, F, F) == 6  # fp8 rows: K % 16
+    # empty products (n = 0 or M = 0) are valid and launch nothing
+    assert ndq.ndq_matmul_packed_batched([desc(q4k, 0, 0, 0, 0)], K, 16, 1, F, F) == 0
+    assert ndq.ndq_matmul_packed_batched([good], K, 0, 0, F, F) == 0
+
+
 def test_status_strings():
     for code in ndq.STATUS:
         assert ndq.ndq_status_string(code)

@@ -112,15 +112,15 @@ def test_matmul_one_row_lean_kernel(orc, fmt, N, K, weights, out):
     _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] {weights} {out}")
 
 
+@pytest.mark.parametrize("fmt", ["gguf:q6_k", "gguf:q8_0", "q8_g32_fp16"])
 @pytest.mark.parametrize("N,K", [(300, 4096), (77, 256), (1000, 14336), (130, 12288), (4096, 1024)])
 @pytest.mark.parametrize("M", [2, 3, 5, 8])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-def test_grouped_tensor_core_exact_weights(orc, N, K, M, out):
-    # gguf:q6_k with binary32 weights and 2..8 activation rows: the tensor
-    # core sums codes times X per 16-weight group into its own TMEM column,
-    # the epilogue applies the group scales; row tiles partial, split-K
-    # clusters for the short grids (N = 77, 130, 300)
-    fmt = "gguf:q6_k"
+def test_grouped_tensor_core_exact_weights(orc, fmt, N, K, M, out):
+    # gguf:q6_k and q8_0 with binary32 weights and 2..8 activation rows: the
+    # tensor core sums codes times X per 16- or 32-weight group into its own
+    # TMEM column, the epilogue applies the group scales; row tiles partial,
+    # split-K clusters for the short grids (N = 77, 130, 300)
     w = synth.payload(fmt, (N, K), seed=41 + M)
     x_t, x_bits = _x_bf16(M, K, 42 + M)
     ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
@@ -251,3 +251,52 @@ def test_tensor_core_split_k_16_rows(orc, fmt, N, K):
     a = _run(fmt, N, K, M, w, x_t, weights="bfloat16")
     _check(a, ref, yabs, K, what=f"{fmt} [{N},{K}] M=16")
     assert np.array_equal(a, _run(fmt, N, K, M, w, x_t, weights="bfloat16"))
+
+
+def _batched(items, K, M, weights="float32", out=torch.float32, seed=51):
+    # items: (fmt, N); returns outputs of the batched call and of single calls
+    x_t, x_bits = _x_bf16(M, K, seed)
+    x = x_t.to(DEV)
+    ws = [(fmt, N, synth.payload(fmt, (N, K), seed=seed + 7 * i)) for i, (fmt, N) in enumerate(items)]
+    wd = [torch.from_numpy(w).to(DEV) for _, _, w in ws]
+    wdt = torch.float32 if weights == "float32" else torch.bfloat16
+    got = ndq.matmul_packed_batched([(fmt, w, N) for (fmt, N, _), w in zip(ws, wd)], K, x, out_dtype=out,
+                                    weight_dtype=wdt)
+    single = [ndq.matmul_packed(fmt, w, N, K, x, out_dtype=out, weight_dtype=wdt) for (fmt, N, _), w in zip(ws, wd)]
+    torch.cuda.synchronize()
+    return ws, x_bits, got, single
+
+
+@pytest.mark.parametrize("items,K", [
+    ([("gguf:q4_k", 512), ("gguf:q4_k", 128), ("gguf:q4_k", 128)], 4096),        # q, k, v of a layer
+    ([("gguf:q6_k", 1000), ("gguf:q6_k", 1000)], 4096),                          # gate and up
+    ([("gguf:q8_0", n) for n in (1, 7, 130, 3, 64, 9, 300, 2)], 14336),          # 8 tensors, 4 units per lane
+    ([("q8_g32_fp16", 33), ("gguf:q8_0", 17)], 8192),                            # one family, two identifiers
+])
+@pytest.mark.parametrize("weights,out", [("float32", torch.float32), ("bfloat16", torch.bfloat16)])
+def test_batched_products_one_launch(orc, items, K, weights, out):
+    # one k_gemvl launch over all the products: each output equals the
+    # single call's bit for bit (the same per-row summation) and the oracle
+    ws, x_bits, got, single = _batched(items, K, 1, weights, out)
+    for (fmt, N, w), g, s1 in zip(ws, got, single):
+        assert torch.equal(g.view(torch.int32 if out == torch.float32 else torch.int16),
+                           s1.view(torch.int32 if out == torch.float32 else torch.int16)), f"{fmt} [{N},{K}]"
+        ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+        _check(g.float().cpu().numpy().astype(np.float64), ref, yabs, K, bf16_out=out == torch.bfloat16,
+               what=f"batched {fmt} [{N},{K}]")
+
+
+@pytest.mark.parametrize("items,K,M", [
+    ([("gguf:q4_k", 300), ("gguf:q6_k", 200), ("gguf:iq4_nl", 50)], 4096, 1),     # formats differ
+    ([("gguf:q6_k", 300), ("gguf:q8_0", 77)], 4096, 3),                          # three rows of X
+    ([("gguf:q4_k", 100)] * 9, 4096, 1),                                          # more than 8 products
+    ([("gguf:q4_k", 100), ("gguf:q4_k", 0)], 4096, 1),                            # an empty product
+])
+def test_batched_products_one_after_another(orc, items, K, M):
+    ws, x_bits, got, single = _batched(items, K, M)
+    for (fmt, N, w), g, s1 in zip(ws, got, single):
+        assert torch.equal(g.view(torch.int32), s1.view(torch.int32)), f"{fmt} [{N},{K}]"
+        if N == 0:
+            continue
+        ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
+        _check(g.cpu().numpy().astype(np.float64), ref, yabs, K, what=f"batched {fmt} [{N},{K}] M={M}")
