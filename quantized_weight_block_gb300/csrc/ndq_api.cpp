@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "ndq.h"
+#include "ndq_fused.h"
 #include "ndq_internal.h"
 
 static_assert(NDQ_NOALLOC_MAX_TENSORS == ndq::kNoAllocMaxTensors, "no-allocation table size");

@@ -22,6 +22,7 @@
 #pragma once
 
 #include "ndq_device.cuh"
+#include "ndq_fused.h"
 
 namespace ndq {
 namespace {

@@ -40,6 +40,7 @@
 #include <cooperative_groups.h>
 
 #include "ndq_device.cuh"
+#include "ndq_fused.h"
 
 namespace ndq {
 namespace cg = cooperative_groups;
