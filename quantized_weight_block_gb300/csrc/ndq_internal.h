@@ -91,9 +91,13 @@ NDQ_HOST_DEVICE constexpr bool decode_staged(int fsel, int osel) {
 }
 // Payload stages in flight per decode CTA: 4 for the kernels that run two
 // CTAs per SM (the launches that mix formats, and the q6_k and fp8 row
-// decoders, whose 16-bit variants need more than 75 registers), else 3.
+// decoders, whose 16-bit variants need more than 75 registers) and for
+// gguf:q4_0 (no output staging, so 4 stages still fit three CTAs per SM:
+// [4096,4096] -> bf16 measured 9.3 us with 3 and 8.6 us with 4), else 3
+// (q4_g64, q4_k and the others measured 2-7 % slower with 4).
 NDQ_HOST_DEVICE constexpr int decode_stages(int fsel) {
-    return (fsel < 0 || fsel == KF_Q6_K || fsel == KF_FP8_ROW_BF16 || fsel == KF_FP8_ROW_FP16) ? 4 : 3;
+    return (fsel < 0 || fsel == KF_Q6_K || fsel == KF_FP8_ROW_BF16 || fsel == KF_FP8_ROW_FP16 || fsel == KF_Q4_0) ? 4
+                                                                                                                    : 3;
 }
 // Resident CTAs per SM for launches that mix formats (the whole-model decode):
 // measured fastest at 2 even when registers and shared memory allow 3.
