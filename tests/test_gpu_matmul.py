@@ -104,7 +104,7 @@ def test_matmul_one_row_activation_sources(orc, fmt, K, x_off):
 def test_matmul_one_row_lean_kernel(orc, fmt, N, K, weights, out):
     # the lean one-row kernel (K a multiple of 512, aligned rows): one, two
     # or four 16-weight units per lane, 1 to 8 warps per row, rows wrapping
-    # the 4-stage ring (3000 rows), both weight operands and output types
+    # the 3-stage ring (3000 rows), both weight operands and output types
     w = synth.payload(fmt, (N, K), seed=31 + K)
     x_t, x_bits = _x_bf16(1, K, 32)
     ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
@@ -126,6 +126,21 @@ def test_grouped_tensor_core_exact_weights(orc, fmt, N, K, M, out):
     ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
     got = _run(fmt, N, K, M, w, x_t, out_dtype=out)
     _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] M={M} {out}")
+
+
+@pytest.mark.parametrize("fmt", ["gguf:q6_k", "gguf:q8_0"])
+@pytest.mark.parametrize("w_off,M,weights", [(1, 4, "float32"), (6, 3, "float32"), (8, 8, "float32"),
+                                             (2, 16, "bfloat16"), (12, 40, "bfloat16")])
+def test_tensor_core_products_unaligned_payload(orc, fmt, w_off, M, weights):
+    # a payload that starts off a 16-byte boundary: the tensor-core kernels
+    # stage its rows by 16-byte lines (no tensor copy) and decode every
+    # block at its own byte phase
+    N, K = 150, 2048
+    w = synth.payload(fmt, (N, K), seed=60 + w_off)
+    x_t, x_bits = _x_bf16(M, K, 61)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+    _check(_run(fmt, N, K, M, w, x_t, w_off=w_off, weights=weights), ref, yabs, K,
+           what=f"{fmt} +{w_off} M={M} {weights}")
 
 
 @pytest.mark.parametrize("fmt", ["gguf:q4_k", "gguf:q8_0", "gguf:mxfp4", "gguf:iq3_s", "nvfp4", "fp8_e4m3fn_row_fp16"])
