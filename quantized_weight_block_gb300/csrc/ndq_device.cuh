@@ -2189,8 +2189,10 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_decode(const KParams p) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&H.empty[s]);
+                        // (the destination comes from the stage header, which
+                        // the producer rewrites once the stage is released)
                         uint16_t* y = static_cast<uint16_t*>(si.t.y) + si.block0 * si.t.B + warp * kWarpOut;
+                        mbar_arrive(&H.empty[s]);
                         bulk_store(y, ob, kOutBufBytes);
                         bulk_commit();
                     }
