@@ -10,10 +10,13 @@
 // fusion, reduction order and intermediate precision).  The result is
 // deterministic: every output is summed in a fixed order.
 //
-// The CTA layout is the decode kernel's: one producer warp stages payload
-// units into the shared-memory ring with bulk copies; 8 consumer warps
-// decode 16-element chunks with the same Fmt<F> decoders and accumulate
-// against X.  A unit is R = rows_per_stage whole weight rows (K <= 8192/R),
+// Three kernels: k_gemvl (one row of X, the formats of a K-quant model,
+// lean per-format decoders and X in registers; below), k_gemv1 (one row of
+// X, any format; below) and k_matvec (up to 8 rows of X).  k_matvec's CTA
+// layout is the decode kernel's: one producer warp stages payload units
+// into the shared-memory ring with bulk copies; 8 consumer warps decode
+// 16-element chunks with the same Fmt<F> decoders and accumulate against X.
+// A unit is R = rows_per_stage whole weight rows (K <= 8192/R),
 // or, when K > 4096, a segment of up to 8192 elements of one row.  Each CTA
 // owns whole units, so a row's partial sums meet in the CTA: the 256/R
 // threads of a row group take its chunks in turn; warp shuffles, then one

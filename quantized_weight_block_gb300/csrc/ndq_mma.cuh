@@ -10,28 +10,30 @@
 // One CTA computes a tile of 128 weight rows (the MMA's M) by BN activation
 // rows (the MMA's N, 16..256) over its share of K, in k-steps of 64, with
 // warp-specialised roles joined only by mbarriers:
-//   * warp 8 (payload producer) copies, for each span of max(B, 64) weights
-//     (whole blocks), the packed bytes of the tile's 128 rows into a
-//     two-stage ring with asynchronous 16-byte copies (rounded out to 16-byte
-//     lines that all hold payload bytes; each lane's copies are counted on
-//     the span's full barrier as they land);
-//   * warps 0-7 (decoders) decode each k-step's 64 weights of the 128 rows
-//     with the same Fmt<F> decoders, round them to bfloat16 and write them as
-//     the A operand of one of NA operand stages (128-byte-swizzled K-major),
-//     then arrive on that stage's A-full barrier;
-//   * warp 9, one thread, loads the X slice [BN x 64] of each k-step into the
-//     stage's B operand with one TMA tensor copy (the 128-byte swizzle is the
-//     operand layout; rows and columns outside X read as zero), NA - 1
-//     k-steps ahead, and issues the four tcgen05.mma (K = 16 each) of a
-//     k-step once its A and B are full, committing them to the stage's free
-//     barrier, which the decoders and the X copies wait on before reusing the
-//     stage;
-//   * the epilogue reads the accumulator back with tcgen05.ld (warp w reads
-//     TMEM lanes 32*(w%4).., half of the columns each).  With split-K
-//     (gridDim.z > 1, one thread-block cluster per tile) each CTA parks its
-//     partial tile in shared memory and the cluster's rank-0 CTA adds them
-//     in rank order through distributed shared memory, so the result does
-//     not depend on timing.
+//   * warp 16 (payload producer) stages, for each span of whole blocks (64
+//     to 256 weights), the packed bytes of the tile's 128 rows into a ring
+//     of up to 4 span stages: one 2-D tensor copy per span from a byte
+//     tensor map of the payload when the rows are 16-byte aligned, else
+//     asynchronous 16-byte copies of each row's lines (each lane's copies are
+//     counted on the span's full barrier as they land);
+//   * warps 0-15 (decoders, four threads per weight row) decode each k-step's
+//     64 weights of the 128 rows with the Fmt<F> decoders, round them to
+//     bfloat16 and write them as the A operand of one of NA operand stages
+//     (128-byte-swizzled K-major), then arrive on that stage's A-full
+//     barrier;
+//   * warp 18 loads the X slice [BN x 64] of each k-step into the stage's B
+//     operand with one TMA tensor copy (the 128-byte swizzle is the operand
+//     layout; rows and columns outside X read as zero) once the MMAs that
+//     last read the stage are done;
+//   * warp 17 issues the four tcgen05.mma (K = 16 each) of a k-step once its
+//     A and B are full, committing them to the stage's free barrier, which
+//     the decoders and the X copies wait on before reusing the stage;
+//   * after the k-loop, warps 0-7 read the accumulator back with tcgen05.ld
+//     (warp w reads TMEM lanes 32*(w%4).., half of the columns each).  With
+//     split-K (gridDim.z > 1, one thread-block cluster per tile) each CTA
+//     parks its partial tile in shared memory and rank r adds its share of
+//     the columns over every rank's partial in rank order through
+//     distributed shared memory, so the result does not depend on timing.
 // Every wait is bounded; a wait that gives up sets the fault word and its
 // role stops, so every other role's waits run out in turn; every CTA still
 // reaches the cluster barriers and frees its TMEM.
