@@ -463,10 +463,10 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
     weight tensor, 225 launches replayed as a CUDA graph) against the
     unfused path on the same payloads (the batched decode to bf16, then one
     cuBLAS bf16 product per tensor, also as a graph).  Also single tensors
-    at M = 1 and M = 8 with the exact binary32 weights (M = 1 on the CUDA
-    cores; M = 8 of q6_k and q8_0 on the tensor cores, the group scales
-    applied after the tensor core's per-group sums) and M = 8 with bfloat16
-    weights."""
+    at M = 1, 4 and 8 with the exact binary32 weights (the lean CUDA-core
+    kernels where K <= 4096; the [4096,14336] q6_k down projection at M > 1
+    on the tensor cores, the group scales applied after the tensor core's
+    per-group sums) and M = 8 with bfloat16 weights."""
     specs = work.specs
     ks = sorted({s.shape[1] for s in specs})
     xs = {k: torch.randn(1, k, device="cuda").to(torch.bfloat16) for k in ks}
@@ -571,17 +571,20 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
                       ("gguf:q8_0", 128256, 4096)):
         i = next(j for j, s in enumerate(specs) if s.fmt == fmt and s.shape == (N, K))
         w, wb = views[i][1], wviews[i]
-        for M, wdt in ((1, torch.float32), (8, torch.float32), (8, torch.bfloat16)):
+        for M, wdt in ((1, torch.float32), (4, torch.float32), (8, torch.float32), (8, torch.bfloat16)):
             x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
             yf = torch.empty(M, N, device="cuda")
             yb = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
             tf = graph_timed(lambda: ndq.matmul_packed(fmt, w, N, K, x, y=yf, weight_dtype=wdt))
             tu = graph_timed(lambda: (ndq.dequantize_packed(fmt, (N, K), w, torch.bfloat16, y=wb),
                                 torch.matmul(x, wb.t(), out=yb)))
-            if wdt == torch.bfloat16:
-                tag = "bfloat16 weights, tensor cores (k_mma)"
-            elif M == 1:
+            wname = "bfloat16" if wdt == torch.bfloat16 else "binary32"
+            if M == 1:
                 tag = "binary32 weights, CUDA cores (k_gemvl)"
+            elif K % 512 == 0 and K <= 4096:  # (every format here has lean decoders)
+                tag = f"{wname} weights, CUDA cores (k_gemvm)"
+            elif wdt == torch.bfloat16:
+                tag = "bfloat16 weights, tensor cores (k_mma)"
             elif fmt in ("gguf:q6_k", "gguf:q8_0"):
                 tag = "binary32 weights, grouped tensor cores (k_mmag)"
             else:

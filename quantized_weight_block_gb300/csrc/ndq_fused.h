@@ -68,8 +68,16 @@ enum MvVariant : int {
     // one row, lean per-format decoders (k_gemvl, gguf q8_0 / q4_k / q6_k):
     // kMvLean + 2 * xr + wbf16, xr = 0, 1, 2 for 1, 2, 4 units per lane
     kMvLean = 5,
-    kMvVariants = 11
+    // 2 to 8 rows, lean decoders (k_gemvm): kMvMulti + 2 * mpi + wbf16,
+    // mpi = 0, 1, 2 for kernels of 2, 4, 8 activation rows
+    kMvMulti = 11,
+    kMvVariants = 17
 };
+// True when the lean kernel for several activation rows (k_gemvm) takes the
+// launch p: 2 <= m <= 8, K a multiple of 512 up to 4096, a family with lean
+// decoders, one tensor (p.w) with 16-byte-aligned rows.
+bool gemvm_takes(const MvParams& p);
+int launch_gemvm(const MvParams& p, void* stream);
 
 // Decode fused into a tensor-core (tcgen05) product (ndq_mma.cuh): tiles of
 // 128 weight rows by bn activation rows, the weights rounded to bfloat16.

@@ -186,6 +186,78 @@ int launch_matvec(const MvParams& p0, void* stream) {
     return static_cast<int>(e);
 }
 
+bool gemvm_takes(const MvParams& p) {
+    const int f = p.w.fmt;
+    if (p.m < 2 || p.m > kMvMaxRows || p.K == 0 || p.K % kGlIter != 0 || p.K > 8u * kGlIter || f < 0 ||
+        f >= KF_COUNT || (p.bpr * p.w.S) % 16u != 0 || (reinterpret_cast<uintptr_t>(p.w.x) & 15u) != 0)
+        return false;
+    return matvec_for(f, kMvMulti) != nullptr;
+}
+
+int launch_gemvm(const MvParams& p0, void* stream) {
+    if (p0.n_rows == 0) return 0;
+    if (!gemvm_takes(p0)) return static_cast<int>(cudaErrorInvalidValue);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    MvParams p = p0;
+    const int se = device_symbols(dev, &p.fault, &p.grids);
+    if (se != 0) return se;
+    const int f = p.w.fmt;
+    const uint32_t mp = p.m <= 2 ? 2u : p.m <= 4 ? 4u : 8u;
+    const int variant = kMvMulti + 2 * (mp == 2u ? 0 : mp == 4u ? 1 : 2) + (p.wbf16 ? 1 : 0);
+    const MvKernelFn fn = matvec_for(f, variant);
+    if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
+    MvDeviceInfo& di = g_mv_dev[dev];
+    if (di.sms == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        di.sms = sms;
+    }
+    // rows per stage: 4 rg pp (every row group takes pp quads), the most
+    // (pp <= 4) that fit one CTA per SM and leave at least two row blocks
+    // per CTA
+    const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
+    const uint32_t rg = gm_row_groups(nit, mp);
+    const uint64_t rowb = p.bpr * p.w.S;
+    const uint64_t sms = static_cast<uint64_t>(di.sms);
+    auto smem_of = [&](uint32_t pp) {
+        const uint32_t rb = kGmQuad * rg * pp;
+        return gm_smem_bytes(gl_slot_bytes(rowb, rb), mp, p.K, rb);
+    };
+    uint32_t pp = 4;
+    while (pp > 1u && (smem_of(pp) > kGmSmemMax ||
+                       (p.n_rows + kGmQuad * rg * pp - 1u) / (kGmQuad * rg * pp) < 2u * sms))
+        pp >>= 1;
+    const size_t smem = smem_of(pp);
+    if (smem > kGmSmemMax) return static_cast<int>(cudaErrorInvalidValue);
+    const uint32_t rb = kGmQuad * rg * pp;
+    p.rows_per_stage = static_cast<int32_t>(rb);
+    p.slot = static_cast<int32_t>(gl_slot_bytes(rowb, rb));
+    if (!di.attr_set[f][variant]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGmSmemMax));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        di.attr_set[f][variant] = true;
+    }
+    const uint64_t nblk = (p.n_rows + rb - 1u) / rb;
+    const unsigned grid = static_cast<unsigned>(nblk < sms ? nblk : sms);
+    void* args[] = {&p};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
+    return static_cast<int>(e);
+}
+
 MmaKernelFn mma_for(int kfmt) {
     switch (kfmt) {
         case KF_FP8_ROW_BF16: return mma_fp8_row_bf16();

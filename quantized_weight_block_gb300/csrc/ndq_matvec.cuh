@@ -693,6 +693,27 @@ struct Gl<KF_Q8_0> {
         gl_mul_acc<WBF16>(d, q.z ^ 0x80808080u, bias, x + 8, acc);
         gl_mul_acc<WBF16>(d, q.w ^ 0x80808080u, bias, x + 12, acc);
     }
+    // The same unit in two steps for k_gemvm: its fields (prep), then the 4
+    // weights of run r (run), bit-identical to unit()'s.
+    struct U {
+        float d;
+        uint4 q;
+    };
+    __device__ __forceinline__ static U prep(const uint8_t* in, uint32_t u, uint32_t) {
+        const uint32_t off = (u >> 1) * 34u;
+        U s;
+        s.d = h2f(*reinterpret_cast<const uint16_t*>(in + off));
+        s.q = lds_16<false>(in, off + 2u + 16u * (u & 1u));
+        return s;
+    }
+    template <bool WBF16>
+    __device__ __forceinline__ static void run(const U& s, int r, float2& w01, float2& w23) {
+        const uint32_t q = (r == 0 ? s.q.x : r == 1 ? s.q.y : r == 2 ? s.q.z : s.q.w) ^ 0x80808080u;
+        const float2 dd = make_float2(s.d, s.d);
+        const float bias = 8388736.0f;
+        w01 = gl_round<WBF16>(mul2(dd, bytes_minus2<0>(q, bias)));
+        w23 = gl_round<WBF16>(mul2(dd, bytes_minus2<2>(q, bias)));
+    }
 };
 
 // gguf:q4_k: unit u = 16 b + s of block b: i = s >> 2 picks sub-blocks 2i
@@ -735,6 +756,39 @@ struct Gl<KF_Q4_K> {
         gl_fma_acc<WBF16>(da1, (w0 >> 4) & 0x0F0F0F0Fu, bias, ndm1, x + 8, acc);
         gl_fma_acc<WBF16>(da1, (w1 >> 4) & 0x0F0F0F0Fu, bias, ndm1, x + 12, acc);
     }
+    struct U {
+        uint32_t w0, w1;
+        float da0, ndm0, da1, ndm1;
+    };
+    __device__ __forceinline__ static U prep(const uint8_t* in, uint32_t u, uint32_t lane) {
+        const uint32_t s = u & 15u, i = s >> 2, t = s & 3u;
+        const uint8_t* b = in + (u >> 4) * 144u;
+        U v;
+        v.w0 = *reinterpret_cast<const uint32_t*>(b + 16u + 32u * i + 4u * t);
+        v.w1 = *reinterpret_cast<const uint32_t*>(b + 32u + 32u * i + 4u * t);
+        const uint32_t hd = *reinterpret_cast<const uint32_t*>(b);
+        const uint32_t k = 2u * i + (t >> 1), j = k & 3u;
+        const uint32_t b0 = b[4u + j], b1 = b[8u + j], b2 = b[12u + j];
+        const bool mn = (t & 1u) != 0u;
+        const uint32_t lo = mn ? b1 : b0;
+        const uint32_t sv = k < 4u ? (lo & 63u) : ((mn ? (b2 >> 4) : (b2 & 15u)) | ((lo >> 6) << 4));
+        const float sc = __fmul_rn(h2f(mn ? (hd >> 16) : (hd & 0xffffu)), small_uint(sv));
+        const float f = mn ? -sc : sc;
+        const uint32_t g = lane & ~3u;
+        v.da0 = __shfl_sync(0xffffffffu, f, g);
+        v.ndm0 = __shfl_sync(0xffffffffu, f, g | 1u);
+        v.da1 = __shfl_sync(0xffffffffu, f, g | 2u);
+        v.ndm1 = __shfl_sync(0xffffffffu, f, g | 3u);
+        return v;
+    }
+    template <bool WBF16>
+    __device__ __forceinline__ static void run(const U& s, int r, float2& w01, float2& w23) {
+        const uint32_t c = ((r & 1) ? s.w1 : s.w0) >> ((r & 2) ? 4 : 0) & 0x0F0F0F0Fu;
+        const float a = r < 2 ? s.da0 : s.da1, m = r < 2 ? s.ndm0 : s.ndm1;
+        const float2 aa = make_float2(a, a), cc = make_float2(m, m);
+        w01 = gl_round<WBF16>(fma2(aa, bytes_minus2<0>(c, 8388608.0f), cc));
+        w23 = gl_round<WBF16>(fma2(aa, bytes_minus2<2>(c, 8388608.0f), cc));
+    }
 };
 
 // gguf:q6_k: unit u = 16 b + s of block b: half h = s >> 3 and l0 = 4 (s & 7);
@@ -767,6 +821,48 @@ struct Gl<KF_Q6_K> {
         gl_mul_acc<WBF16>(ds1, (c & 0x0F0F0F0Fu) | ((q & 0x0C0C0C0Cu) << 2), bias, x + 4, acc);
         gl_mul_acc<WBF16>(ds2, ((a >> 4) & 0x0F0F0F0Fu) | (q & 0x30303030u), bias, x + 8, acc);
         gl_mul_acc<WBF16>(ds3, ((c >> 4) & 0x0F0F0F0Fu) | ((q >> 2) & 0x30303030u), bias, x + 12, acc);
+    }
+    struct U {
+        uint32_t a, c, q;
+        float ds0, ds1, ds2, ds3;
+    };
+    __device__ __forceinline__ static U prep(const uint8_t* in, uint32_t u, uint32_t lane) {
+        const uint32_t s = u & 15u, h = s >> 3, l0 = 4u * (s & 7u);
+        const uint32_t off = (u >> 4) * 210u;
+        U v;
+        v.a = lds_4h(in, off + 64u * h + l0);
+        v.c = lds_4h(in, off + 64u * h + 32u + l0);
+        v.q = lds_4h(in, off + 128u + 32u * h + l0);
+        const float d = h2f(*reinterpret_cast<const uint16_t*>(in + off + 208u));
+        const float dl = __fmul_rn(d, i8_float(in[off + 192u + 8u * h + ((s >> 2) & 1u) + 2u * (s & 3u)]));
+        const uint32_t g = lane & ~3u;
+        v.ds0 = __shfl_sync(0xffffffffu, dl, g);
+        v.ds1 = __shfl_sync(0xffffffffu, dl, g | 1u);
+        v.ds2 = __shfl_sync(0xffffffffu, dl, g | 2u);
+        v.ds3 = __shfl_sync(0xffffffffu, dl, g | 3u);
+        return v;
+    }
+    template <bool WBF16>
+    __device__ __forceinline__ static void run(const U& s, int r, float2& w01, float2& w23) {
+        uint32_t code;
+        float d;
+        if (r == 0) {
+            code = (s.a & 0x0F0F0F0Fu) | ((s.q & 0x03030303u) << 4);
+            d = s.ds0;
+        } else if (r == 1) {
+            code = (s.c & 0x0F0F0F0Fu) | ((s.q & 0x0C0C0C0Cu) << 2);
+            d = s.ds1;
+        } else if (r == 2) {
+            code = ((s.a >> 4) & 0x0F0F0F0Fu) | (s.q & 0x30303030u);
+            d = s.ds2;
+        } else {
+            code = ((s.c >> 4) & 0x0F0F0F0Fu) | ((s.q >> 2) & 0x30303030u);
+            d = s.ds3;
+        }
+        const float2 dd = make_float2(d, d);
+        const float bias = 8388640.0f;  // 2^23 + 32
+        w01 = gl_round<WBF16>(mul2(dd, bytes_minus2<0>(code, bias)));
+        w23 = gl_round<WBF16>(mul2(dd, bytes_minus2<2>(code, bias)));
     }
 };
 
@@ -941,12 +1037,257 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Two to eight activation rows, lean decoders: k_gemvm.  For the formats of
+// k_gemvl, K a multiple of 512 up to 4096 and 16-byte-aligned rows.  One CTA
+// of 16 warps per SM; a ring of 3 slots, each holding rb whole weight rows
+// staged by one bulk copy, which the last warp to finish a slot issues for
+// the slot's next row block (no producer warp: four warps per SM
+// sub-partition leave 128 registers a thread).  The warps first convert X
+// to binary32 in shared memory, in lane-unit order (activation row m,
+// iteration it, run r, lane: 4 floats), so that a warp reads the 4
+// activations of one run of its 32 units with one 16-byte load per lane,
+// without bank conflicts.  Warp (it, mh, g) takes the units of iteration it
+// (32 it + lane) of every row, the activation rows MS mh .. MS mh + MS - 1
+// (MS = min(MP, 4)) and the row quads g, g + rg, ... of each stage: it
+// decodes one unit of 4 weight rows at a time (the unit's fields first,
+// then run by run the 4 x 4 weights) and adds them times the MS activation
+// runs into 4 MS independent FMA-pair chains.  Per weight that is M
+// multiply-adds (the FMA pipe) and, 4 rows sharing each activation load,
+// 2 M bytes of X read from shared memory, which keep those two units about
+// equally busy.  A warp reduces its 4 MS sums together (reduce-scatter, then
+// a butterfly) and stores one partial per (row, activation row, iteration);
+// the last warp of the stage adds each output's partials in iteration order.
+// Products and sums are binary32; W is the exact decode (or its bfloat16
+// rounding), formed exactly as the decode kernels do.
+// ---------------------------------------------------------------------------
+constexpr int kGmWarps = 16;
+constexpr int kGmThreads = kGmWarps * 32;
+constexpr int kGmStages = 3;
+constexpr uint32_t kGmQuad = 4;                  // weight rows per warp pass
+constexpr uint32_t kGmSmemMax = 227u * 1024u;    // dynamic shared memory of one CTA per SM
+constexpr uint32_t kGmHdrBytes = 128;
+
+struct GmHdr {
+    uint64_t full[kGmStages];
+    uint32_t cnt[kGmStages];  // warps that stored their partials of the stage
+};
+static_assert(sizeof(GmHdr) <= kGmHdrBytes, "GmHdr layout");
+
+// Activation rows per warp: all MP up to 4, else half of them.
+__host__ __device__ constexpr uint32_t gm_ms(uint32_t mp) { return mp < 4u ? mp : 4u; }
+
+// Row groups of a launch: warps per row quad are the iterations times the
+// activation-row halves.
+__host__ __device__ constexpr uint32_t gm_row_groups(uint32_t nit, uint32_t mp) {
+    return static_cast<uint32_t>(kGmWarps) / (nit * (mp / gm_ms(mp)));
+}
+
+// Dynamic shared memory: the stage slots, X as binary32, the header, and
+// the partial sums (stage, row, activation row, iteration).
+__host__ __device__ constexpr size_t gm_smem_bytes(uint32_t slot, uint32_t mp, uint64_t K, uint32_t rb) {
+    return static_cast<size_t>(kGmStages) * slot + static_cast<size_t>(mp) * K * 4u + kGmHdrBytes +
+           static_cast<size_t>(kGmStages) * rb * mp * (K / kGlIter) * 4u;
+}
+
+template <int F, int MP, bool WBF16>
+__global__ void __launch_bounds__(kGmThreads, 1) k_gemvm(const MvParams p) {
+    using G = Gl<F>;
+    constexpr uint32_t MS = gm_ms(MP), NH = MP / MS, NV = kGmQuad * MS;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t slot = static_cast<uint32_t>(p.slot), rb = static_cast<uint32_t>(p.rows_per_stage);
+    const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
+    const uint32_t rg = gm_row_groups(nit, MP), wu = rg * nit * NH;
+    const uint32_t xbytes = static_cast<uint32_t>(MP * p.K * 4u);
+    float4* xs = reinterpret_cast<float4*>(smem + kGmStages * slot);
+    GmHdr& H = *reinterpret_cast<GmHdr*>(smem + kGmStages * slot + xbytes);
+    float* red = reinterpret_cast<float*>(smem + kGmStages * slot + xbytes + kGmHdrBytes);
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t rowb = static_cast<uint32_t>(p.bpr * p.w.S);  // a multiple of 16
+    const uint64_t N = p.n_rows, nblk = (N + rb - 1u) / rb;
+    // row block b (first row b rb) into stage s
+    auto stage_in = [&](uint64_t b, int s) {
+        const uint64_t r0 = b * rb;
+        const uint32_t bytes = static_cast<uint32_t>(N - r0 < rb ? N - r0 : rb) * rowb;
+        mbar_arrive_expect_tx(&H.full[s], bytes);
+        bulk_load(smem + static_cast<uint32_t>(s) * slot, p.w.x + r0 * rowb, bytes, &H.full[s]);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kGmStages; ++s) {
+            mbar_init(&H.full[s], 1);
+            H.cnt[s] = 0u;
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // warm L2 with this CTA's first row block (the weights are launch
+        // parameters; the activations, which the previous kernel may write,
+        // are read after the wait)
+        if (blockIdx.x < nblk) {
+            const uint64_t r0 = static_cast<uint64_t>(blockIdx.x) * rb;
+            const uint32_t bytes = static_cast<uint32_t>(N - r0 < rb ? N - r0 : rb) * rowb;
+            prefetch_l2(p.w.x + r0 * rowb, bytes < 32768u ? bytes : 32768u);
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < kGmStages; ++s)
+            if (blockIdx.x + static_cast<uint64_t>(s) * gridDim.x < nblk)
+                stage_in(blockIdx.x + static_cast<uint64_t>(s) * gridDim.x, s);
+
+    // X as binary32 in lane-unit order: entry e = ((m nit + it) 4 + r) 32 + l
+    // holds activations col(32 it + l, r) .. +3 of row m (zeros for m >= M)
+    const uint32_t nx = MP * nit * 128u;
+    for (uint32_t e = tid; e < nx; e += kGmThreads) {
+        const uint32_t l = e & 31u, r = (e >> 5) & 3u, q = e >> 7, it = q % nit, m = q / nit;
+        uint32_t lo = 0u, hi = 0u;
+        if (m < static_cast<uint32_t>(p.m)) {
+            const uint16_t* xp = p.x + static_cast<uint64_t>(m) * p.K + G::col(32u * it + l, static_cast<int>(r));
+            if (p.xvec) {
+                const uint2 t2 = __ldg(reinterpret_cast<const uint2*>(xp));
+                lo = t2.x;
+                hi = t2.y;
+            } else {
+                lo = static_cast<uint32_t>(__ldg(xp)) | (static_cast<uint32_t>(__ldg(xp + 1)) << 16);
+                hi = static_cast<uint32_t>(__ldg(xp + 2)) | (static_cast<uint32_t>(__ldg(xp + 3)) << 16);
+            }
+        }
+        xs[e] = make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));
+    }
+    __syncthreads();
+    if (warp >= wu) return;
+
+    const uint32_t it = warp % nit, mh = (warp / nit) % NH, g = warp / (nit * NH);
+    const float4* xw = xs + (mh * MS * nit + it) * 128u + lane;  // row mh MS + mm, run r: + (mm nit) 128 + 32 r
+    const uint32_t u = 32u * it + lane;
+    int n = 0;
+    for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++n) {
+        const int s = n % kGmStages;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&H.full[s], static_cast<uint32_t>((n / kGmStages) & 1)))) {
+            // give copies already issued to the next slots time to land
+            // before the CTA's shared memory is released
+            if (lane == 0) {
+                atomicOr(p.fault, 2u);
+                for (int j = n + 1; j < n + kGmStages; ++j)
+                    if (blockIdx.x + static_cast<uint64_t>(j) * gridDim.x < nblk)
+                        mbar_wait_bounded(&H.full[j % kGmStages], static_cast<uint32_t>((j / kGmStages) & 1));
+            }
+            __syncwarp();
+            return;
+        }
+        const uint64_t r0 = blk * rb;
+        const uint32_t nr = static_cast<uint32_t>(N - r0 < rb ? N - r0 : rb);
+        const uint8_t* in = smem + static_cast<uint32_t>(s) * slot;
+        // row quads of this warp (rows past nr decode stale slot bytes;
+        // their sums are never read)
+        for (uint32_t qb = kGmQuad * g; qb < rb; qb += kGmQuad * rg) {
+            typename G::U su[kGmQuad];
+#pragma unroll
+            for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
+            float2 acc[kGmQuad][MS];
+#pragma unroll
+            for (uint32_t k = 0; k < kGmQuad; ++k)
+#pragma unroll
+                for (uint32_t mm = 0; mm < MS; ++mm) acc[k][mm] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float2 wv[kGmQuad][2];
+#pragma unroll
+                for (uint32_t k = 0; k < kGmQuad; ++k) G::template run<WBF16>(su[k], r, wv[k][0], wv[k][1]);
+#pragma unroll
+                for (uint32_t mm = 0; mm < MS; ++mm) {
+                    const float4 xv = xw[mm * nit * 128u + 32u * static_cast<uint32_t>(r)];
+                    const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
+#pragma unroll
+                    for (uint32_t k = 0; k < kGmQuad; ++k) {
+                        acc[k][mm] = fma2(x01, wv[k][0], acc[k][mm]);
+                        acc[k][mm] = fma2(x23, wv[k][1], acc[k][mm]);
+                    }
+                }
+            }
+            // the NV sums over the warp: halve the values a lane keeps at
+            // lane offsets 16, 8, ... then add over the rest; lane
+            // (32 / NV) i ends with value i = k MS + mm
+            float v[NV];
+#pragma unroll
+            for (uint32_t k = 0; k < kGmQuad; ++k)
+#pragma unroll
+                for (uint32_t mm = 0; mm < MS; ++mm) v[k * MS + mm] = __fadd_rn(acc[k][mm].x, acc[k][mm].y);
+            uint32_t keep = NV, o = 16u;
+#pragma unroll
+            for (; keep > 1u; keep >>= 1, o >>= 1) {
+                const bool up = (lane & o) != 0u;
+#pragma unroll
+                for (uint32_t i = 0; i < keep / 2u; ++i) {
+                    const float mine = up ? v[keep / 2u + i] : v[i], other = up ? v[i] : v[keep / 2u + i];
+                    v[i] = __fadd_rn(mine, __shfl_xor_sync(0xffffffffu, other, o));
+                }
+            }
+#pragma unroll
+            for (; o > 0u; o >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+            constexpr uint32_t kStep = 32u / NV;
+            if (lane % kStep == 0u) {
+                const uint32_t vi = lane / kStep, k = vi / MS, mm = vi % MS;
+                red[((static_cast<uint32_t>(s) * rb + qb + k) * MP + mh * MS + mm) * nit + it] = v[0];
+            }
+        }
+        __syncwarp();
+        bool last = false;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&H.cnt[s], 1u) == wu - 1u;
+        }
+        last = __shfl_sync(0xffffffffu, last ? 1u : 0u, 0) != 0u;
+        if (last) {
+            // the stage's last warp: every warp is done with the slot and its
+            // partials; add each output's partials in iteration order, then
+            // stage the slot's next row block
+            __threadfence_block();
+            const uint32_t no = nr * static_cast<uint32_t>(p.m);
+            for (uint32_t o2 = lane; o2 < no; o2 += 32u) {
+                const uint32_t row = o2 % nr, m = o2 / nr;
+                const float* pr = red + ((static_cast<uint32_t>(s) * rb + row) * MP + m) * nit;
+                float y = pr[0];
+                for (uint32_t w = 1; w < nit; ++w) y = __fadd_rn(y, pr[w]);
+                const uint64_t yi = static_cast<uint64_t>(m) * N + r0 + row;
+                if (p.out_bf16)
+                    static_cast<__nv_bfloat16*>(p.y)[yi] = __float2bfloat16_rn(y);
+                else
+                    static_cast<float*>(p.y)[yi] = y;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                H.cnt[s] = 0u;
+                const uint64_t nb = blk + static_cast<uint64_t>(kGmStages) * gridDim.x;
+                if (nb < nblk) {
+                    fence_proxy_async_smem();  // the slot's reads before the copy that overwrites it
+                    stage_in(nb, s);
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
 }  // namespace
 
 // Fused kernel of decode family F for a launch variant (used by the
 // per-format instantiation files; see MvVariant in ndq_internal.h).
 template <int F>
 MvKernelFn matvec_kernel(int variant) {
+    if (variant >= kMvMulti) {
+        if constexpr (Gl<F>::kLean) {
+            switch (variant - kMvMulti) {
+                case 0: return k_gemvm<F, 2, false>;
+                case 1: return k_gemvm<F, 2, true>;
+                case 2: return k_gemvm<F, 4, false>;
+                case 3: return k_gemvm<F, 4, true>;
+                case 4: return k_gemvm<F, 8, false>;
+                default: return k_gemvm<F, 8, true>;
+            }
+        }
+        return nullptr;
+    }
     if (variant >= kMvLean) {
         if constexpr (Gl<F>::kLean) {
             switch (variant - kMvLean) {

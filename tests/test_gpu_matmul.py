@@ -112,15 +112,32 @@ def test_matmul_one_row_lean_kernel(orc, fmt, N, K, weights, out):
     _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] {weights} {out}")
 
 
+@pytest.mark.parametrize("fmt", ["gguf:q8_0", "gguf:q4_k", "gguf:q6_k", "q8_g32_fp16"])
+@pytest.mark.parametrize("N,K", [(300, 4096), (4099, 3072), (1000, 512), (77, 1024), (5, 2048), (2000, 2560)])
+@pytest.mark.parametrize("M", [2, 3, 5, 8])
+@pytest.mark.parametrize("weights,out", [("float32", torch.float32), ("bfloat16", torch.bfloat16)])
+def test_matmul_several_rows_lean_kernel(orc, fmt, N, K, M, weights, out):
+    # 2..8 activation rows, K a multiple of 512 up to 4096 (the lean kernel
+    # for several rows): X padded to 2, 4 or 8 rows, the rows split over
+    # warp halves at 8; 1 to 8 iterations per row (5 and 6 leave warps
+    # idle), rows wrapping the 3-slot ring with a partial last block (4099)
+    w = synth.payload(fmt, (N, K), seed=71 + M)
+    x_t, x_bits = _x_bf16(M, K, 72 + M)
+    ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
+    got = _run(fmt, N, K, M, w, x_t, out_dtype=out, weights=weights)
+    _check(got, ref, yabs, K, bf16_out=out == torch.bfloat16, what=f"{fmt} [{N},{K}] M={M} {weights} {out}")
+
+
 @pytest.mark.parametrize("fmt", ["gguf:q6_k", "gguf:q8_0", "q8_g32_fp16"])
-@pytest.mark.parametrize("N,K", [(300, 4096), (77, 256), (1000, 14336), (130, 12288), (4096, 1024)])
+@pytest.mark.parametrize("N,K", [(300, 4608), (77, 256), (1000, 14336), (130, 12288), (4096, 1280)])
 @pytest.mark.parametrize("M", [2, 3, 5, 8])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_grouped_tensor_core_exact_weights(orc, fmt, N, K, M, out):
-    # gguf:q6_k and q8_0 with binary32 weights and 2..8 activation rows: the
-    # tensor core sums codes times X per 16- or 32-weight group into its own
-    # TMEM column, the epilogue applies the group scales; row tiles partial,
-    # split-K clusters for the short grids (N = 77, 130, 300)
+    # gguf:q6_k and q8_0 with binary32 weights and 2..8 activation rows where
+    # the lean kernel does not take them (K not a multiple of 512, or above
+    # 4096): the tensor core sums codes times X per 16- or 32-weight group
+    # into its own TMEM column, the epilogue applies the group scales; row
+    # tiles partial, split-K clusters for the short grids (N = 77, 130, 300)
     w = synth.payload(fmt, (N, K), seed=41 + M)
     x_t, x_bits = _x_bf16(M, K, 42 + M)
     ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, "float32")
