@@ -299,16 +299,6 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
            static_cast<int64_t>(p.rows_per_stage) * 2 * K <= ndq::kTileElems)
         p.rows_per_stage *= 2;
     p.out_bf16 = out_dtype == NDQ_BFLOAT16;
-    // 2 to 8 activation rows of gguf q8_0 / q4_k / q6_k with K a multiple of
-    // 512 up to 4096 and 16-byte-aligned rows, either weight type: the lean
-    // CUDA-core kernel (k_gemvm; X in shared memory as binary32, each
-    // weight decoded once for all the rows)
-    if (M >= 2 && M <= ndq::kMvMaxRows) {
-        p.x = x;
-        p.y = y;
-        p.m = static_cast<int32_t>(M);
-        if (ndq::gemvm_takes(p)) return ndq::launch_gemvm(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
-    }
     // Six or more activation rows with bfloat16 weights: the tensor-core
     // (tcgen05) product (measured faster than the CUDA-core passes from M = 6
     // on), when X is 16-byte aligned and K % 8 == 0.
@@ -330,6 +320,16 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
         q.span_bytes = q.span_elems / p.w.B * p.w.S;
         q.out_bf16 = p.out_bf16;
         return ndq::launch_mma(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
+    }
+    // 2 to 8 activation rows of gguf q8_0 / q4_k / q6_k with K a multiple of
+    // 512 up to 4096 and 16-byte-aligned rows (bfloat16 weights: up to 5
+    // rows): the lean CUDA-core kernel (k_gemvm; X in shared memory as
+    // binary32, each weight decoded once per 4 activation rows)
+    if (M >= 2 && M <= ndq::kMvMaxRows) {
+        p.x = x;
+        p.y = y;
+        p.m = static_cast<int32_t>(M);
+        if (ndq::gemvm_takes(p)) return ndq::launch_gemvm(p, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
     }
     // 2 to 8 activation rows with binary32 weights of gguf:q6_k or q8_0 (a
     // group scale times a small code): the grouped tensor-core product (the

@@ -246,7 +246,7 @@ int launch_gemvm(const MvParams& p0, void* stream) {
     void* args[] = {&p};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGmThreads);
+    cfg.blockDim = dim3(gm_warps(mp) * 32u);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];

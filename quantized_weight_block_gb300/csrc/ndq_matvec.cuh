@@ -671,6 +671,21 @@ __device__ __forceinline__ uint32_t lds_4h(const uint8_t* base, uint32_t off) {
     return __funnelshift_r(w[0], w[1], (off & 2u) * 8u);
 }
 
+// Pair operations through the compiler's float2 builtins (the same
+// correctly rounded lane results as sub2 / mul2 / fma2, which the compiler
+// can schedule and place in register pairs itself): used by k_gemvm's
+// decoders and products.
+__device__ __forceinline__ float2 gm_fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 gm_mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// Bytes I and I+1 of w as the floats 2^23 + byte, minus `bias` (adding
+// -bias rounds as subtracting bias does; both are exact here).
+template <int I>
+__device__ __forceinline__ float2 gm_bytes_minus2(uint32_t w, float bias) {
+    return __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | I)),
+                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (I + 1)))),
+                      make_float2(-bias, -bias));
+}
+
 template <int F>
 struct Gl {
     static constexpr bool kLean = false;
@@ -711,8 +726,8 @@ struct Gl<KF_Q8_0> {
         const uint32_t q = (r == 0 ? s.q.x : r == 1 ? s.q.y : r == 2 ? s.q.z : s.q.w) ^ 0x80808080u;
         const float2 dd = make_float2(s.d, s.d);
         const float bias = 8388736.0f;
-        w01 = gl_round<WBF16>(mul2(dd, bytes_minus2<0>(q, bias)));
-        w23 = gl_round<WBF16>(mul2(dd, bytes_minus2<2>(q, bias)));
+        w01 = gl_round<WBF16>(gm_mul2(dd, gm_bytes_minus2<0>(q, bias)));
+        w23 = gl_round<WBF16>(gm_mul2(dd, gm_bytes_minus2<2>(q, bias)));
     }
 };
 
@@ -786,8 +801,8 @@ struct Gl<KF_Q4_K> {
         const uint32_t c = ((r & 1) ? s.w1 : s.w0) >> ((r & 2) ? 4 : 0) & 0x0F0F0F0Fu;
         const float a = r < 2 ? s.da0 : s.da1, m = r < 2 ? s.ndm0 : s.ndm1;
         const float2 aa = make_float2(a, a), cc = make_float2(m, m);
-        w01 = gl_round<WBF16>(fma2(aa, bytes_minus2<0>(c, 8388608.0f), cc));
-        w23 = gl_round<WBF16>(fma2(aa, bytes_minus2<2>(c, 8388608.0f), cc));
+        w01 = gl_round<WBF16>(gm_fma2(aa, gm_bytes_minus2<0>(c, 8388608.0f), cc));
+        w23 = gl_round<WBF16>(gm_fma2(aa, gm_bytes_minus2<2>(c, 8388608.0f), cc));
     }
 };
 
@@ -861,8 +876,8 @@ struct Gl<KF_Q6_K> {
         }
         const float2 dd = make_float2(d, d);
         const float bias = 8388640.0f;  // 2^23 + 32
-        w01 = gl_round<WBF16>(mul2(dd, bytes_minus2<0>(code, bias)));
-        w23 = gl_round<WBF16>(mul2(dd, bytes_minus2<2>(code, bias)));
+        w01 = gl_round<WBF16>(gm_mul2(dd, gm_bytes_minus2<0>(code, bias)));
+        w23 = gl_round<WBF16>(gm_mul2(dd, gm_bytes_minus2<2>(code, bias)));
     }
 };
 
@@ -1040,29 +1055,28 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
 // ---------------------------------------------------------------------------
 // Two to eight activation rows, lean decoders: k_gemvm.  For the formats of
 // k_gemvl, K a multiple of 512 up to 4096 and 16-byte-aligned rows.  One CTA
-// of 16 warps per SM; a ring of 3 slots, each holding rb whole weight rows
+// per SM (16 warps; 8 for 5 to 8 activation rows, whose accumulators take
+// more registers); a ring of 3 slots, each holding rb whole weight rows
 // staged by one bulk copy, which the last warp to finish a slot issues for
-// the slot's next row block (no producer warp: four warps per SM
-// sub-partition leave 128 registers a thread).  The warps first convert X
-// to binary32 in shared memory, in lane-unit order (activation row m,
-// iteration it, run r, lane: 4 floats), so that a warp reads the 4
+// the slot's next row block (no producer warp).  The warps first convert X
+// to binary32 in shared memory, in lane-unit order (iteration it,
+// activation row m, run r, lane: 4 floats), so that a warp reads the 4
 // activations of one run of its 32 units with one 16-byte load per lane,
-// without bank conflicts.  Warp (it, mh, g) takes the units of iteration it
-// (32 it + lane) of every row, the activation rows MS mh .. MS mh + MS - 1
-// (MS = min(MP, 4)) and the row quads g, g + rg, ... of each stage: it
-// decodes one unit of 4 weight rows at a time (the unit's fields first,
-// then run by run the 4 x 4 weights) and adds them times the MS activation
-// runs into 4 MS independent FMA-pair chains.  Per weight that is M
-// multiply-adds (the FMA pipe) and, 4 rows sharing each activation load,
-// 2 M bytes of X read from shared memory, which keep those two units about
-// equally busy.  A warp reduces its 4 MS sums together (reduce-scatter, then
-// a butterfly) and stores one partial per (row, activation row, iteration);
-// the last warp of the stage adds each output's partials in iteration order.
-// Products and sums are binary32; W is the exact decode (or its bfloat16
-// rounding), formed exactly as the decode kernels do.
+// without bank conflicts.  Warp (it, g) takes the units of iteration it
+// (32 it + lane) of every row, for all the activation rows, and the row
+// quads g, g + rg, ... of each stage: it decodes one unit of 4 weight rows
+// at a time (the unit's fields first, then run by run the 4 x 4 weights)
+// and adds them times the MP activation runs into 4 MP independent FMA-pair
+// chains.  Per weight that is one decode, M multiply-adds (the FMA pipe)
+// and, 4 rows sharing each activation load, M bytes of X read from shared
+// memory.  A warp reduces its 4 MP sums together (reduce-scatter, then a
+// butterfly) and stores one partial per (row, activation row, iteration);
+// the last warp of the stage adds each output's partials in iteration
+// order.  Products and sums are binary32; W is the exact decode (or its
+// bfloat16 rounding), formed exactly as the decode kernels do.
 // ---------------------------------------------------------------------------
-constexpr int kGmWarps = 16;
-constexpr int kGmThreads = kGmWarps * 32;
+// Warps of a CTA for a kernel of mp activation rows.
+__host__ __device__ constexpr uint32_t gm_warps(uint32_t mp) { return mp > 4u ? 8u : 16u; }
 constexpr int kGmStages = 3;
 constexpr uint32_t kGmQuad = 4;                  // weight rows per warp pass
 constexpr uint32_t kGmSmemMax = 227u * 1024u;    // dynamic shared memory of one CTA per SM
@@ -1074,14 +1088,8 @@ struct GmHdr {
 };
 static_assert(sizeof(GmHdr) <= kGmHdrBytes, "GmHdr layout");
 
-// Activation rows per warp: all MP up to 4, else half of them.
-__host__ __device__ constexpr uint32_t gm_ms(uint32_t mp) { return mp < 4u ? mp : 4u; }
-
-// Row groups of a launch: warps per row quad are the iterations times the
-// activation-row halves.
-__host__ __device__ constexpr uint32_t gm_row_groups(uint32_t nit, uint32_t mp) {
-    return static_cast<uint32_t>(kGmWarps) / (nit * (mp / gm_ms(mp)));
-}
+// Row groups of a launch: each row quad takes one warp per iteration.
+__host__ __device__ constexpr uint32_t gm_row_groups(uint32_t nit, uint32_t mp) { return gm_warps(mp) / nit; }
 
 // Dynamic shared memory: the stage slots, X as binary32, the header, and
 // the partial sums (stage, row, activation row, iteration).
@@ -1091,13 +1099,13 @@ __host__ __device__ constexpr size_t gm_smem_bytes(uint32_t slot, uint32_t mp, u
 }
 
 template <int F, int MP, bool WBF16>
-__global__ void __launch_bounds__(kGmThreads, 1) k_gemvm(const MvParams p) {
+__global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p) {
     using G = Gl<F>;
-    constexpr uint32_t MS = gm_ms(MP), NH = MP / MS, NV = kGmQuad * MS;
+    constexpr uint32_t NT = gm_warps(MP) * 32u, NV = kGmQuad * MP;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t slot = static_cast<uint32_t>(p.slot), rb = static_cast<uint32_t>(p.rows_per_stage);
     const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
-    const uint32_t rg = gm_row_groups(nit, MP), wu = rg * nit * NH;
+    const uint32_t rg = gm_row_groups(nit, MP), wu = rg * nit;
     const uint32_t xbytes = static_cast<uint32_t>(MP * p.K * 4u);
     float4* xs = reinterpret_cast<float4*>(smem + kGmStages * slot);
     GmHdr& H = *reinterpret_cast<GmHdr*>(smem + kGmStages * slot + xbytes);
@@ -1135,30 +1143,41 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_gemvm(const MvParams p) {
             if (blockIdx.x + static_cast<uint64_t>(s) * gridDim.x < nblk)
                 stage_in(blockIdx.x + static_cast<uint64_t>(s) * gridDim.x, s);
 
-    // X as binary32 in lane-unit order: entry e = ((m nit + it) 4 + r) 32 + l
-    // holds activations col(32 it + l, r) .. +3 of row m (zeros for m >= M)
+    // X as binary32 in lane-unit order: entry e = ((it MP + m) 4 + r) 32 + l
+    // holds activations col(32 it + l, r) .. +3 of row m (zeros for m >= M);
+    // kGmXIn entries per thread are loaded before any is stored, so that
+    // their global reads overlap
     const uint32_t nx = MP * nit * 128u;
-    for (uint32_t e = tid; e < nx; e += kGmThreads) {
-        const uint32_t l = e & 31u, r = (e >> 5) & 3u, q = e >> 7, it = q % nit, m = q / nit;
-        uint32_t lo = 0u, hi = 0u;
-        if (m < static_cast<uint32_t>(p.m)) {
-            const uint16_t* xp = p.x + static_cast<uint64_t>(m) * p.K + G::col(32u * it + l, static_cast<int>(r));
-            if (p.xvec) {
-                const uint2 t2 = __ldg(reinterpret_cast<const uint2*>(xp));
-                lo = t2.x;
-                hi = t2.y;
-            } else {
-                lo = static_cast<uint32_t>(__ldg(xp)) | (static_cast<uint32_t>(__ldg(xp + 1)) << 16);
-                hi = static_cast<uint32_t>(__ldg(xp + 2)) | (static_cast<uint32_t>(__ldg(xp + 3)) << 16);
+    constexpr uint32_t kGmXIn = 8;
+    for (uint32_t e0 = tid; e0 < nx; e0 += NT * kGmXIn) {
+        uint2 xv[kGmXIn];
+#pragma unroll
+        for (uint32_t j = 0; j < kGmXIn; ++j) {
+            const uint32_t e = e0 + j * NT;
+            const uint32_t l = e & 31u, r = (e >> 5) & 3u, q = e >> 7, it = q / MP, m = q % MP;
+            xv[j] = make_uint2(0u, 0u);
+            if (e < nx && m < static_cast<uint32_t>(p.m)) {
+                const uint16_t* xp =
+                    p.x + static_cast<uint64_t>(m) * p.K + G::col(32u * it + l, static_cast<int>(r));
+                if (p.xvec) {
+                    xv[j] = __ldg(reinterpret_cast<const uint2*>(xp));
+                } else {
+                    xv[j].x = static_cast<uint32_t>(__ldg(xp)) | (static_cast<uint32_t>(__ldg(xp + 1)) << 16);
+                    xv[j].y = static_cast<uint32_t>(__ldg(xp + 2)) | (static_cast<uint32_t>(__ldg(xp + 3)) << 16);
+                }
             }
         }
-        xs[e] = make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));
+#pragma unroll
+        for (uint32_t j = 0; j < kGmXIn; ++j) {
+            const uint32_t e = e0 + j * NT;
+            if (e < nx) xs[e] = make_float4(bf16_lo(xv[j].x), bf16_hi(xv[j].x), bf16_lo(xv[j].y), bf16_hi(xv[j].y));
+        }
     }
     __syncthreads();
     if (warp >= wu) return;
 
-    const uint32_t it = warp % nit, mh = (warp / nit) % NH, g = warp / (nit * NH);
-    const float4* xw = xs + (mh * MS * nit + it) * 128u + lane;  // row mh MS + mm, run r: + (mm nit) 128 + 32 r
+    const uint32_t it = warp % nit, g = warp / nit;
+    const float4* xw = xs + it * MP * 128u + lane;  // activation row m, run r: + 128 m + 32 r
     const uint32_t u = 32u * it + lane;
     int n = 0;
     for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++n) {
@@ -1184,35 +1203,35 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_gemvm(const MvParams p) {
             typename G::U su[kGmQuad];
 #pragma unroll
             for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
-            float2 acc[kGmQuad][MS];
+            float2 acc[kGmQuad][MP];
 #pragma unroll
             for (uint32_t k = 0; k < kGmQuad; ++k)
 #pragma unroll
-                for (uint32_t mm = 0; mm < MS; ++mm) acc[k][mm] = make_float2(0.0f, 0.0f);
+                for (uint32_t mm = 0; mm < MP; ++mm) acc[k][mm] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 float2 wv[kGmQuad][2];
 #pragma unroll
                 for (uint32_t k = 0; k < kGmQuad; ++k) G::template run<WBF16>(su[k], r, wv[k][0], wv[k][1]);
 #pragma unroll
-                for (uint32_t mm = 0; mm < MS; ++mm) {
-                    const float4 xv = xw[mm * nit * 128u + 32u * static_cast<uint32_t>(r)];
+                for (uint32_t mm = 0; mm < MP; ++mm) {
+                    const float4 xv = xw[128u * mm + 32u * static_cast<uint32_t>(r)];
                     const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
 #pragma unroll
                     for (uint32_t k = 0; k < kGmQuad; ++k) {
-                        acc[k][mm] = fma2(x01, wv[k][0], acc[k][mm]);
-                        acc[k][mm] = fma2(x23, wv[k][1], acc[k][mm]);
+                        acc[k][mm] = gm_fma2(x01, wv[k][0], acc[k][mm]);
+                        acc[k][mm] = gm_fma2(x23, wv[k][1], acc[k][mm]);
                     }
                 }
             }
             // the NV sums over the warp: halve the values a lane keeps at
             // lane offsets 16, 8, ... then add over the rest; lane
-            // (32 / NV) i ends with value i = k MS + mm
+            // (32 / NV) i ends with value i = k MP + mm
             float v[NV];
 #pragma unroll
             for (uint32_t k = 0; k < kGmQuad; ++k)
 #pragma unroll
-                for (uint32_t mm = 0; mm < MS; ++mm) v[k * MS + mm] = __fadd_rn(acc[k][mm].x, acc[k][mm].y);
+                for (uint32_t mm = 0; mm < MP; ++mm) v[k * MP + mm] = __fadd_rn(acc[k][mm].x, acc[k][mm].y);
             uint32_t keep = NV, o = 16u;
 #pragma unroll
             for (; keep > 1u; keep >>= 1, o >>= 1) {
@@ -1227,8 +1246,8 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_gemvm(const MvParams p) {
             for (; o > 0u; o >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
             constexpr uint32_t kStep = 32u / NV;
             if (lane % kStep == 0u) {
-                const uint32_t vi = lane / kStep, k = vi / MS, mm = vi % MS;
-                red[((static_cast<uint32_t>(s) * rb + qb + k) * MP + mh * MS + mm) * nit + it] = v[0];
+                const uint32_t vi = lane / kStep, k = vi / MP, mm = vi % MP;
+                red[((static_cast<uint32_t>(s) * rb + qb + k) * MP + mm) * nit + it] = v[0];
             }
         }
         __syncwarp();
