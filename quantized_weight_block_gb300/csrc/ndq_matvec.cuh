@@ -1148,7 +1148,7 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
     // kGmXIn entries per thread are loaded before any is stored, so that
     // their global reads overlap
     const uint32_t nx = MP * nit * 128u;
-    constexpr uint32_t kGmXIn = 4u * MP;  // (one pass for K <= 4096)
+    constexpr uint32_t kGmXIn = 8;
     for (uint32_t e0 = tid; e0 < nx; e0 += NT * kGmXIn) {
         uint2 xv[kGmXIn];
 #pragma unroll
@@ -1199,28 +1199,10 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
         const uint8_t* in = smem + static_cast<uint32_t>(s) * slot;
         // row quads of this warp (rows past nr decode stale slot bytes;
         // their sums are never read)
-        // (with 8 warps a CTA, the next quad's fields are read while this
-        // quad's products run)
-        constexpr bool kAhead = MP == 8;
-        const uint32_t qstep = kGmQuad * rg;
-        typename G::U nx4[kGmQuad];
-        if (kAhead) {
-#pragma unroll
-            for (uint32_t k = 0; k < kGmQuad; ++k) nx4[k] = G::prep(in + (kGmQuad * g + k) * rowb, u, lane);
-        }
-        for (uint32_t qb = kGmQuad * g; qb < rb; qb += qstep) {
+        for (uint32_t qb = kGmQuad * g; qb < rb; qb += kGmQuad * rg) {
             typename G::U su[kGmQuad];
-            if (kAhead) {
 #pragma unroll
-                for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = nx4[k];
-                if (qb + qstep < rb) {
-#pragma unroll
-                    for (uint32_t k = 0; k < kGmQuad; ++k) nx4[k] = G::prep(in + (qb + qstep + k) * rowb, u, lane);
-                }
-            } else {
-#pragma unroll
-                for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
-            }
+            for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
             float2 acc[kGmQuad][MP];
 #pragma unroll
             for (uint32_t k = 0; k < kGmQuad; ++k)
