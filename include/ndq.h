@@ -213,13 +213,16 @@ typedef struct ndq_tensor_desc {
  * repeated calls give identical bits; each output is within
  * 2*(K+16)*2^-24 * sum_k |X[m,k] W[n,k]| of the exact sum, then rounded once
  * to out_dtype.  Kernels: one row of X on the CUDA cores (fused
- * multiply-adds); 2 to 8 rows of X with NDQ_FLOAT weights of gguf q6_k,
- * q8_0 or q8_g32_fp16, X 16-byte aligned and K % 8 == 0, on the tensor
- * cores with the group scales applied to the tensor core's per-group sums;
- * other formats up to 8 rows per pass on the CUDA cores (each pass reads
- * the payload once); with NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte
+ * multiply-adds); with NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte
  * aligned and K % 8 == 0, on the tensor cores (tcgen05, binary32
- * accumulation in tensor memory) in one pass.  Same ownership, asynchrony and error
+ * accumulation in tensor memory) in one pass; otherwise 2 to 8 rows of
+ * gguf q8_0, q8_g32_fp16, q4_k or q6_k with K % 512 == 0, K <= 4096 and
+ * 16-byte-aligned payload rows on the CUDA cores with X held in shared
+ * memory (each weight decoded once for all the rows); 2 to 8 rows with
+ * NDQ_FLOAT weights of gguf q6_k, q8_0 or q8_g32_fp16, X 16-byte aligned
+ * and K % 8 == 0, on the tensor cores with the group scales applied to the
+ * tensor core's per-group sums; other cases up to 8 rows per pass on the
+ * CUDA cores (each pass reads the payload once).  Same ownership, asynchrony and error
  * rules as ndq_dequantize_packed; M, N or K of 0 is valid (K == 0 writes
  * zeros); NDQ_ERR_BAD_DTYPE for other weight or output types. */
 int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t *w, size_t w_len, const void *x_bf16,

@@ -10,8 +10,9 @@
 // fusion, reduction order and intermediate precision).  The result is
 // deterministic: every output is summed in a fixed order.
 //
-// Three kernels: k_gemvl (one row of X, the formats of a K-quant model,
-// lean per-format decoders and X in registers; below), k_gemv1 (one row of
+// Four kernels: k_gemvl (one row of X, the formats of a K-quant model,
+// lean per-format decoders and X in registers; below), k_gemvm (2 to 8 rows
+// of X, the same decoders, X in shared memory; below), k_gemv1 (one row of
 // X, any format; below) and k_matvec (up to 8 rows of X).  k_matvec's CTA
 // layout is the decode kernel's: one producer warp stages payload units
 // into the shared-memory ring with bulk copies; 8 consumer warps decode
