@@ -581,10 +581,10 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
             wname = "bfloat16" if wdt == torch.bfloat16 else "binary32"
             if M == 1:
                 tag = "binary32 weights, CUDA cores (k_gemvl)"
+            elif wdt == torch.bfloat16 and M >= 6:
+                tag = "bfloat16 weights, tensor cores (k_mma)"
             elif K % 512 == 0 and K <= 4096:  # (every format here has lean decoders)
                 tag = f"{wname} weights, CUDA cores (k_gemvm)"
-            elif wdt == torch.bfloat16:
-                tag = "bfloat16 weights, tensor cores (k_mma)"
             elif fmt in ("gguf:q6_k", "gguf:q8_0"):
                 tag = "binary32 weights, grouped tensor cores (k_mmag)"
             else:
