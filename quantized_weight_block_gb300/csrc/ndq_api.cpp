@@ -321,11 +321,12 @@ int ndq_matmul_packed(int format_id, int64_t N, int64_t K, const uint8_t* w, siz
         q.out_bf16 = p.out_bf16;
         return ndq::launch_mma(q, stream) == 0 ? NDQ_OK : NDQ_ERR_CUDA;
     }
-    // 2 to 8 activation rows of gguf q8_0 / q4_k / q6_k with K a multiple of
-    // 512 up to 4096 and 16-byte-aligned rows (bfloat16 weights: up to 5
-    // rows): the lean CUDA-core kernel (k_gemvm; X in shared memory as
-    // binary32, each weight decoded once per 4 activation rows)
-    if (M >= 2 && M <= ndq::kMvMaxRows) {
+    // Up to 8 activation rows of gguf q8_0 / q4_k / q6_k with K a multiple
+    // of 512 and 16-byte-aligned rows, X as binary32 fitting shared memory
+    // beside the weight slots (bfloat16 weights: up to 5 rows; one row only
+    // for K > 4096): the lean CUDA-core kernel (k_gemvm; X in shared memory,
+    // each weight decoded once for all the rows)
+    if (M >= 1 && M <= ndq::kMvMaxRows) {
         p.x = x;
         p.y = y;
         p.m = static_cast<int32_t>(M);

@@ -68,13 +68,15 @@ enum MvVariant : int {
     // one row, lean per-format decoders (k_gemvl, gguf q8_0 / q4_k / q6_k):
     // kMvLean + 2 * xr + wbf16, xr = 0, 1, 2 for 1, 2, 4 units per lane
     kMvLean = 5,
-    // 2 to 8 rows, lean decoders (k_gemvm): kMvMulti + 2 * mpi + wbf16,
-    // mpi = 0, 1, 2 for kernels of 2, 4, 8 activation rows
+    // X in shared memory, lean decoders (k_gemvm): kMvMulti + 2 * mpi +
+    // wbf16, mpi = 0, 1, 2, 3 for kernels of 1, 2, 4, 8 activation rows
     kMvMulti = 11,
-    kMvVariants = 17
+    kMvVariants = 19
 };
-// True when the lean kernel for several activation rows (k_gemvm) takes the
-// launch p: 2 <= m <= 8, K a multiple of 512 up to 4096, a family with lean
+// True when the lean kernel with X in shared memory (k_gemvm) takes the
+// launch p: 1 <= m <= 8 (m == 1 only for K > 4096, where it measured
+// faster than k_gemvl), K a multiple of 512 up to 16384, X as binary32 and
+// three slots of 4 rows fitting one CTA's shared memory, a family with lean
 // decoders, one tensor (p.w) with 16-byte-aligned rows.
 bool gemvm_takes(const MvParams& p);
 int launch_gemvm(const MvParams& p, void* stream);

@@ -186,11 +186,22 @@ int launch_matvec(const MvParams& p0, void* stream) {
     return static_cast<int>(e);
 }
 
+// Activation rows of the k_gemvm kernel for m rows.
+static uint32_t gm_mp(int32_t m) { return m <= 1 ? 1u : m <= 2 ? 2u : m <= 4 ? 4u : 8u; }
+
+// Shared memory of a k_gemvm launch with rb rows per stage.
+static size_t gm_smem_of(const MvParams& p, uint32_t rb) {
+    return gm_smem_bytes(gl_slot_bytes(p.bpr * p.w.S, rb), gm_mp(p.m), p.K, rb);
+}
+
 bool gemvm_takes(const MvParams& p) {
     const int f = p.w.fmt;
-    if (p.m < 2 || p.m > kMvMaxRows || p.K == 0 || p.K % kGlIter != 0 || p.K > 8u * kGlIter || f < 0 ||
-        f >= KF_COUNT || (p.bpr * p.w.S) % 16u != 0 || (reinterpret_cast<uintptr_t>(p.w.x) & 15u) != 0)
+    if (p.m < 1 || p.m > kMvMaxRows || p.K == 0 || p.K % kGlIter != 0 || p.K > 32u * kGlIter ||
+        (p.m == 1 && p.K <= 8u * kGlIter) || f < 0 || f >= KF_COUNT || (p.bpr * p.w.S) % 16u != 0 ||
+        (reinterpret_cast<uintptr_t>(p.w.x) & 15u) != 0)
         return false;
+    const uint32_t mp = gm_mp(p.m);
+    if (gm_smem_of(p, kGmQuad * gm_row_groups(static_cast<uint32_t>(p.K / kGlIter), mp)) > kGmSmemMax) return false;
     return matvec_for(f, kMvMulti) != nullptr;
 }
 
@@ -205,8 +216,8 @@ int launch_gemvm(const MvParams& p0, void* stream) {
     const int se = device_symbols(dev, &p.fault, &p.grids);
     if (se != 0) return se;
     const int f = p.w.fmt;
-    const uint32_t mp = p.m <= 2 ? 2u : p.m <= 4 ? 4u : 8u;
-    const int variant = kMvMulti + 2 * (mp == 2u ? 0 : mp == 4u ? 1 : 2) + (p.wbf16 ? 1 : 0);
+    const uint32_t mp = gm_mp(p.m);
+    const int variant = kMvMulti + 2 * (mp == 1u ? 0 : mp == 2u ? 1 : mp == 4u ? 2 : 3) + (p.wbf16 ? 1 : 0);
     const MvKernelFn fn = matvec_for(f, variant);
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     MvDeviceInfo& di = g_mv_dev[dev];
@@ -223,10 +234,7 @@ int launch_gemvm(const MvParams& p0, void* stream) {
     const uint32_t rg = gm_row_groups(nit, mp);
     const uint64_t rowb = p.bpr * p.w.S;
     const uint64_t sms = static_cast<uint64_t>(di.sms);
-    auto smem_of = [&](uint32_t pp) {
-        const uint32_t rb = kGmQuad * rg * pp;
-        return gm_smem_bytes(gl_slot_bytes(rowb, rb), mp, p.K, rb);
-    };
+    auto smem_of = [&](uint32_t pp) { return gm_smem_of(p, kGmQuad * rg * pp); };
     uint32_t pp = 4;
     while (pp > 1u && (smem_of(pp) > kGmSmemMax ||
                        (p.n_rows + kGmQuad * rg * pp - 1u) / (kGmQuad * rg * pp) < 2u * sms))

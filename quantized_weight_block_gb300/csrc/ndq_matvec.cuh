@@ -1089,14 +1089,24 @@ struct GmHdr {
 };
 static_assert(sizeof(GmHdr) <= kGmHdrBytes, "GmHdr layout");
 
-// Row groups of a launch: each row quad takes one warp per iteration.
-__host__ __device__ constexpr uint32_t gm_row_groups(uint32_t nit, uint32_t mp) { return gm_warps(mp) / nit; }
+// Warps along a row: one per iteration, or, when there are more iterations
+// than warps, the largest divisor nwi of nit that is at most the warp count
+// (each such warp takes iterations i0, i0 + nwi, ...: nit / nwi of them).
+__host__ __device__ constexpr uint32_t gm_row_warps(uint32_t nit, uint32_t mp) {
+    uint32_t d = nit < gm_warps(mp) ? nit : gm_warps(mp);
+    while (d > 1u && nit % d != 0u) --d;
+    return d;
+}
+// Row groups of a launch: each row quad takes gm_row_warps warps.
+__host__ __device__ constexpr uint32_t gm_row_groups(uint32_t nit, uint32_t mp) {
+    return gm_warps(mp) / gm_row_warps(nit, mp);
+}
 
 // Dynamic shared memory: the stage slots, X as binary32, the header, and
-// the partial sums (stage, row, activation row, iteration).
+// the partial sums (stage, row, activation row, warp along the row).
 __host__ __device__ constexpr size_t gm_smem_bytes(uint32_t slot, uint32_t mp, uint64_t K, uint32_t rb) {
     return static_cast<size_t>(kGmStages) * slot + static_cast<size_t>(mp) * K * 4u + kGmHdrBytes +
-           static_cast<size_t>(kGmStages) * rb * mp * (K / kGlIter) * 4u;
+           static_cast<size_t>(kGmStages) * rb * mp * gm_row_warps(static_cast<uint32_t>(K / kGlIter), mp) * 4u;
 }
 
 template <int F, int MP, bool WBF16>
@@ -1106,7 +1116,7 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t slot = static_cast<uint32_t>(p.slot), rb = static_cast<uint32_t>(p.rows_per_stage);
     const uint32_t nit = static_cast<uint32_t>(p.K / kGlIter);
-    const uint32_t rg = gm_row_groups(nit, MP), wu = rg * nit;
+    const uint32_t nwi = gm_row_warps(nit, MP), rg = gm_row_groups(nit, MP), wu = rg * nwi;
     const uint32_t xbytes = static_cast<uint32_t>(MP * p.K * 4u);
     float4* xs = reinterpret_cast<float4*>(smem + kGmStages * slot);
     GmHdr& H = *reinterpret_cast<GmHdr*>(smem + kGmStages * slot + xbytes);
@@ -1177,9 +1187,7 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
     __syncthreads();
     if (warp >= wu) return;
 
-    const uint32_t it = warp % nit, g = warp / nit;
-    const float4* xw = xs + it * MP * 128u + lane;  // activation row m, run r: + 128 m + 32 r
-    const uint32_t u = 32u * it + lane;
+    const uint32_t i0 = warp % nwi, g = warp / nwi;
     int n = 0;
     for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++n) {
         const int s = n % kGmStages;
@@ -1201,27 +1209,32 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
         // row quads of this warp (rows past nr decode stale slot bytes;
         // their sums are never read)
         for (uint32_t qb = kGmQuad * g; qb < rb; qb += kGmQuad * rg) {
-            typename G::U su[kGmQuad];
-#pragma unroll
-            for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
             float2 acc[kGmQuad][MP];
 #pragma unroll
             for (uint32_t k = 0; k < kGmQuad; ++k)
 #pragma unroll
                 for (uint32_t mm = 0; mm < MP; ++mm) acc[k][mm] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
+            for (uint32_t it = i0; it < nit; it += nwi) {
+                const float4* xw = xs + it * MP * 128u + lane;  // activation row m, run r: + 128 m + 32 r
+                const uint32_t u = 32u * it + lane;
+                typename G::U su[kGmQuad];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                float2 wv[kGmQuad][2];
+                for (uint32_t k = 0; k < kGmQuad; ++k) su[k] = G::prep(in + (qb + k) * rowb, u, lane);
 #pragma unroll
-                for (uint32_t k = 0; k < kGmQuad; ++k) G::template run<WBF16>(su[k], r, wv[k][0], wv[k][1]);
+                for (int r = 0; r < 4; ++r) {
+                    float2 wv[kGmQuad][2];
 #pragma unroll
-                for (uint32_t mm = 0; mm < MP; ++mm) {
-                    const float4 xv = xw[128u * mm + 32u * static_cast<uint32_t>(r)];
-                    const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
+                    for (uint32_t k = 0; k < kGmQuad; ++k) G::template run<WBF16>(su[k], r, wv[k][0], wv[k][1]);
 #pragma unroll
-                    for (uint32_t k = 0; k < kGmQuad; ++k) {
-                        acc[k][mm] = gm_fma2(x01, wv[k][0], acc[k][mm]);
-                        acc[k][mm] = gm_fma2(x23, wv[k][1], acc[k][mm]);
+                    for (uint32_t mm = 0; mm < MP; ++mm) {
+                        const float4 xv = xw[128u * mm + 32u * static_cast<uint32_t>(r)];
+                        const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
+#pragma unroll
+                        for (uint32_t k = 0; k < kGmQuad; ++k) {
+                            acc[k][mm] = gm_fma2(x01, wv[k][0], acc[k][mm]);
+                            acc[k][mm] = gm_fma2(x23, wv[k][1], acc[k][mm]);
+                        }
                     }
                 }
             }
@@ -1248,7 +1261,7 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
             constexpr uint32_t kStep = 32u / NV;
             if (lane % kStep == 0u) {
                 const uint32_t vi = lane / kStep, k = vi / MP, mm = vi % MP;
-                red[((static_cast<uint32_t>(s) * rb + qb + k) * MP + mm) * nit + it] = v[0];
+                red[((static_cast<uint32_t>(s) * rb + qb + k) * MP + mm) * nwi + i0] = v[0];
             }
         }
         __syncwarp();
@@ -1266,9 +1279,9 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
             const uint32_t no = nr * static_cast<uint32_t>(p.m);
             for (uint32_t o2 = lane; o2 < no; o2 += 32u) {
                 const uint32_t row = o2 % nr, m = o2 / nr;
-                const float* pr = red + ((static_cast<uint32_t>(s) * rb + row) * MP + m) * nit;
+                const float* pr = red + ((static_cast<uint32_t>(s) * rb + row) * MP + m) * nwi;
                 float y = pr[0];
-                for (uint32_t w = 1; w < nit; ++w) y = __fadd_rn(y, pr[w]);
+                for (uint32_t w = 1; w < nwi; ++w) y = __fadd_rn(y, pr[w]);
                 const uint64_t yi = static_cast<uint64_t>(m) * N + r0 + row;
                 if (p.out_bf16)
                     static_cast<__nv_bfloat16*>(p.y)[yi] = __float2bfloat16_rn(y);
@@ -1298,11 +1311,13 @@ MvKernelFn matvec_kernel(int variant) {
     if (variant >= kMvMulti) {
         if constexpr (Gl<F>::kLean) {
             switch (variant - kMvMulti) {
-                case 0: return k_gemvm<F, 2, false>;
-                case 1: return k_gemvm<F, 2, true>;
-                case 2: return k_gemvm<F, 4, false>;
-                case 3: return k_gemvm<F, 4, true>;
-                case 4: return k_gemvm<F, 8, false>;
+                case 0: return k_gemvm<F, 1, false>;
+                case 1: return k_gemvm<F, 1, true>;
+                case 2: return k_gemvm<F, 2, false>;
+                case 3: return k_gemvm<F, 2, true>;
+                case 4: return k_gemvm<F, 4, false>;
+                case 5: return k_gemvm<F, 4, true>;
+                case 6: return k_gemvm<F, 8, false>;
                 default: return k_gemvm<F, 8, true>;
             }
         }
