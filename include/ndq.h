@@ -248,7 +248,7 @@ typedef struct ndq_matmul_desc {
  * specification: it lets the weights that read one activation row (a
  * layer's q, k and v projections, or its gate and up projections) run as
  * ONE kernel launch when M == 1, count <= 8, every product has n > 0 and
- * the same format, K % 512 == 0, K <= 16384, the format is gguf q8_0 /
+ * the same format, K % 512 == 0, K <= 4096, the format is gguf q8_0 /
  * q8_g32_fp16 / q4_k / q6_k and every payload row starts on a 16-byte
  * boundary; otherwise the products are launched one after another.
  *   descs  host array of `count` descriptors, read during the call only

@@ -379,7 +379,9 @@ int ndq_matmul_packed_batched(const ndq_matmul_desc* descs, int count, int64_t K
     ndq::MvParams p;
     std::memset(&p, 0, sizeof(p));
     uint64_t total_rows = 0;
-    bool one_launch = M == 1 && count <= ndq::kGlMaxTensors && K > 0 && x_bf16 != nullptr;
+    // (one row with K > 4096 takes k_gemvm in a single call; the batch then
+    // runs those calls, so that every output keeps the single call's bits)
+    bool one_launch = M == 1 && count <= ndq::kGlMaxTensors && K > 0 && K <= 4096 && x_bf16 != nullptr;
     for (int i = 0; i < count; ++i) {
         const ndq_matmul_desc& d = descs[i];
         if (!valid_id(d.format_id)) return NDQ_ERR_UNKNOWN_FORMAT;

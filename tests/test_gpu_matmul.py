@@ -302,8 +302,9 @@ def _batched(items, K, M, weights="float32", out=torch.float32, seed=51):
 @pytest.mark.parametrize("items,K", [
     ([("gguf:q4_k", 512), ("gguf:q4_k", 128), ("gguf:q4_k", 128)], 4096),        # q, k, v of a layer
     ([("gguf:q6_k", 1000), ("gguf:q6_k", 1000)], 4096),                          # gate and up
-    ([("gguf:q8_0", n) for n in (1, 7, 130, 3, 64, 9, 300, 2)], 14336),          # 8 tensors, 4 units per lane
-    ([("q8_g32_fp16", 33), ("gguf:q8_0", 17)], 8192),                            # one family, two identifiers
+    ([("gguf:q8_0", n) for n in (1, 7, 130, 3, 64, 9, 300, 2)], 4096),           # 8 tensors
+    ([("q8_g32_fp16", 33), ("gguf:q8_0", 17)], 2048),                            # one family, two identifiers
+    ([("gguf:q8_0", n) for n in (1, 7, 130)], 14336),                            # K > 4096: one call each
 ])
 @pytest.mark.parametrize("weights,out", [("float32", torch.float32), ("bfloat16", torch.bfloat16)])
 def test_batched_products_one_launch(orc, items, K, weights, out):
