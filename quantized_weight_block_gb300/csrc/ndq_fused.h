@@ -68,10 +68,11 @@ enum MvVariant : int {
     // one row, lean per-format decoders (k_gemvl, gguf q8_0 / q4_k / q6_k):
     // kMvLean + 2 * xr + wbf16, xr = 0, 1, 2 for 1, 2, 4 units per lane
     kMvLean = 5,
-    // X in shared memory, lean decoders (k_gemvm): kMvMulti + 2 * mpi +
-    // wbf16, mpi = 0, 1, 2, 3 for kernels of 1, 2, 4, 8 activation rows
+    // X in shared memory, lean decoders (k_gemvm): kMvMulti + 4 * mpi +
+    // 2 * mi + wbf16, mpi = 0, 1, 2, 3 for kernels of 1, 2, 4, 8 activation
+    // rows, mi = 1 when a warp takes several iterations of a row
     kMvMulti = 11,
-    kMvVariants = 19
+    kMvVariants = 27
 };
 // True when the lean kernel with X in shared memory (k_gemvm) takes the
 // launch p: 1 <= m <= 8 (m == 1 only for K > 4096, where it measured

@@ -217,7 +217,9 @@ int launch_gemvm(const MvParams& p0, void* stream) {
     if (se != 0) return se;
     const int f = p.w.fmt;
     const uint32_t mp = gm_mp(p.m);
-    const int variant = kMvMulti + 2 * (mp == 1u ? 0 : mp == 2u ? 1 : mp == 4u ? 2 : 3) + (p.wbf16 ? 1 : 0);
+    const bool mi = p.K / kGlIter > gm_warps(mp);
+    const int variant =
+        kMvMulti + 4 * (mp == 1u ? 0 : mp == 2u ? 1 : mp == 4u ? 2 : 3) + (mi ? 2 : 0) + (p.wbf16 ? 1 : 0);
     const MvKernelFn fn = matvec_for(f, variant);
     if (!fn) return static_cast<int>(cudaErrorInvalidDeviceFunction);
     MvDeviceInfo& di = g_mv_dev[dev];

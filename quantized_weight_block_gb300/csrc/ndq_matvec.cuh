@@ -1109,7 +1109,9 @@ __host__ __device__ constexpr size_t gm_smem_bytes(uint32_t slot, uint32_t mp, u
            static_cast<size_t>(kGmStages) * rb * mp * gm_row_warps(static_cast<uint32_t>(K / kGlIter), mp) * 4u;
 }
 
-template <int F, int MP, bool WBF16>
+// MI: a warp may take several iterations (K / 512 above the warp count);
+// without it every warp takes exactly one.
+template <int F, int MP, bool MI, bool WBF16>
 __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p) {
     using G = Gl<F>;
     constexpr uint32_t NT = gm_warps(MP) * 32u, NV = kGmQuad * MP;
@@ -1214,8 +1216,8 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
             for (uint32_t k = 0; k < kGmQuad; ++k)
 #pragma unroll
                 for (uint32_t mm = 0; mm < MP; ++mm) acc[k][mm] = make_float2(0.0f, 0.0f);
-#pragma unroll 1
-            for (uint32_t it = i0; it < nit; it += nwi) {
+            // the quad's units of iteration it, times the activation runs
+            auto one_it = [&](uint32_t it) {
                 const float4* xw = xs + it * MP * 128u + lane;  // activation row m, run r: + 128 m + 32 r
                 const uint32_t u = 32u * it + lane;
                 typename G::U su[kGmQuad];
@@ -1237,6 +1239,12 @@ __global__ void __launch_bounds__(gm_warps(MP) * 32, 1) k_gemvm(const MvParams p
                         }
                     }
                 }
+            };
+            if constexpr (MI) {
+#pragma unroll 1
+                for (uint32_t it = i0; it < nit; it += nwi) one_it(it);
+            } else {
+                one_it(i0);
             }
             // the NV sums over the warp: halve the values a lane keeps at
             // lane offsets 16, 8, ... then add over the rest; lane
@@ -1311,14 +1319,22 @@ MvKernelFn matvec_kernel(int variant) {
     if (variant >= kMvMulti) {
         if constexpr (Gl<F>::kLean) {
             switch (variant - kMvMulti) {
-                case 0: return k_gemvm<F, 1, false>;
-                case 1: return k_gemvm<F, 1, true>;
-                case 2: return k_gemvm<F, 2, false>;
-                case 3: return k_gemvm<F, 2, true>;
-                case 4: return k_gemvm<F, 4, false>;
-                case 5: return k_gemvm<F, 4, true>;
-                case 6: return k_gemvm<F, 8, false>;
-                default: return k_gemvm<F, 8, true>;
+                case 0: return k_gemvm<F, 1, false, false>;
+                case 1: return k_gemvm<F, 1, false, true>;
+                case 2: return k_gemvm<F, 1, true, false>;
+                case 3: return k_gemvm<F, 1, true, true>;
+                case 4: return k_gemvm<F, 2, false, false>;
+                case 5: return k_gemvm<F, 2, false, true>;
+                case 6: return k_gemvm<F, 2, true, false>;
+                case 7: return k_gemvm<F, 2, true, true>;
+                case 8: return k_gemvm<F, 4, false, false>;
+                case 9: return k_gemvm<F, 4, false, true>;
+                case 10: return k_gemvm<F, 4, true, false>;
+                case 11: return k_gemvm<F, 4, true, true>;
+                case 12: return k_gemvm<F, 8, false, false>;
+                case 13: return k_gemvm<F, 8, false, true>;
+                case 14: return k_gemvm<F, 8, true, false>;
+                default: return k_gemvm<F, 8, true, true>;
             }
         }
         return nullptr;
