@@ -580,7 +580,7 @@ def time_fused_matmul(torch, ndq, stream, work, x_dev, y_dev, reps=20):
                                 torch.matmul(x, wb.t(), out=yb)))
             wname = "bfloat16" if wdt == torch.bfloat16 else "binary32"
             if M == 1:
-                tag = "binary32 weights, CUDA cores (k_gemvl)"
+                tag = f"binary32 weights, CUDA cores ({'k_gemvl' if K <= 4096 else 'k_gemvm'})"
             elif wdt == torch.bfloat16 and M >= 6:
                 tag = "bfloat16 weights, tensor cores (k_mma)"
             elif K % 512 == 0 and K <= 4096:  # (every format here has lean decoders)

@@ -215,10 +215,11 @@ typedef struct ndq_tensor_desc {
  * to out_dtype.  Kernels: one row of X on the CUDA cores (fused
  * multiply-adds); with NDQ_BFLOAT16 weights, 6 or more rows, X 16-byte
  * aligned and K % 8 == 0, on the tensor cores (tcgen05, binary32
- * accumulation in tensor memory) in one pass; otherwise 2 to 8 rows of
- * gguf q8_0, q8_g32_fp16, q4_k or q6_k with K % 512 == 0, K <= 4096 and
- * 16-byte-aligned payload rows on the CUDA cores with X held in shared
- * memory (each weight decoded once for all the rows); 2 to 8 rows with
+ * accumulation in tensor memory) in one pass; otherwise up to 8 rows of
+ * gguf q8_0, q8_g32_fp16, q4_k or q6_k with K % 512 == 0 and 16-byte-aligned
+ * payload rows on the CUDA cores with X held in shared memory when it fits
+ * (each weight decoded once for all the rows; for one row only when
+ * K > 4096, shorter rows keeping X in registers); 2 to 8 rows with
  * NDQ_FLOAT weights of gguf q6_k, q8_0 or q8_g32_fp16, X 16-byte aligned
  * and K % 8 == 0, on the tensor cores with the group scales applied to the
  * tensor core's per-group sums; other cases up to 8 rows per pass on the

@@ -11,7 +11,7 @@
 // deterministic: every output is summed in a fixed order.
 //
 // Four kernels: k_gemvl (one row of X, the formats of a K-quant model,
-// lean per-format decoders and X in registers; below), k_gemvm (2 to 8 rows
+// lean per-format decoders and X in registers; below), k_gemvm (1 to 8 rows
 // of X, the same decoders, X in shared memory; below), k_gemv1 (one row of
 // X, any format; below) and k_matvec (up to 8 rows of X).  k_matvec's CTA
 // layout is the decode kernel's: one producer warp stages payload units
@@ -1054,8 +1054,10 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Two to eight activation rows, lean decoders: k_gemvm.  For the formats of
-// k_gemvl, K a multiple of 512 up to 4096 and 16-byte-aligned rows.  One CTA
+// Activations in shared memory, lean decoders: k_gemvm.  For the formats of
+// k_gemvl, 1 to 8 activation rows, K a multiple of 512 up to 16384 with X
+// and three slots of 4 rows fitting shared memory, 16-byte-aligned rows (the
+// host takes it for 2 to 8 rows, and for one row when K > 4096).  One CTA
 // per SM (16 warps; 8 for 5 to 8 activation rows, whose accumulators take
 // more registers); a ring of 3 slots, each holding rb whole weight rows
 // staged by one bulk copy, which the last warp to finish a slot issues for
@@ -1065,14 +1067,16 @@ __global__ void __launch_bounds__(kBlockThreads, 2) k_gemvl(const MvParams p) {
 // activations of one run of its 32 units with one 16-byte load per lane,
 // without bank conflicts.  Warp (it, g) takes the units of iteration it
 // (32 it + lane) of every row, for all the activation rows, and the row
-// quads g, g + rg, ... of each stage: it decodes one unit of 4 weight rows
-// at a time (the unit's fields first, then run by run the 4 x 4 weights)
+// quads g, g + rg, ... of each stage (with more iterations than warps,
+// every nwi-th iteration of the row from it): it decodes one unit of 4
+// weight rows at a time (the unit's fields first, then run by run the 4 x 4
+// weights)
 // and adds them times the MP activation runs into 4 MP independent FMA-pair
 // chains.  Per weight that is one decode, M multiply-adds (the FMA pipe)
 // and, 4 rows sharing each activation load, M bytes of X read from shared
 // memory.  A warp reduces its 4 MP sums together (reduce-scatter, then a
-// butterfly) and stores one partial per (row, activation row, iteration);
-// the last warp of the stage adds each output's partials in iteration
+// butterfly) and stores one partial per (row, activation row, warp along
+// the row); the last warp of the stage adds each output's partials in
 // order.  Products and sums are binary32; W is the exact decode (or its
 // bfloat16 rounding), formed exactly as the decode kernels do.
 // ---------------------------------------------------------------------------
