@@ -102,9 +102,12 @@ def test_matmul_one_row_activation_sources(orc, fmt, K, x_off):
                                  (64, 1536)])
 @pytest.mark.parametrize("weights,out", [("float32", torch.float32), ("bfloat16", torch.bfloat16)])
 def test_matmul_one_row_lean_kernel(orc, fmt, N, K, weights, out):
-    # the lean one-row kernel (K a multiple of 512, aligned rows): one, two
-    # or four 16-weight units per lane, 1 to 8 warps per row, rows wrapping
-    # the 3-stage ring (3000 rows), both weight operands and output types
+    # the lean one-row kernels (K a multiple of 512, aligned rows): X in
+    # registers up to K = 4096 and for q8_0 rows too long for the other
+    # (one, two or four 16-weight units per lane, 1 to 8 warps per row), X
+    # in shared memory above K = 4096 (several iterations per warp); rows
+    # wrapping the 3-stage ring (3000 rows), both weight operands and output
+    # types
     w = synth.payload(fmt, (N, K), seed=31 + K)
     x_t, x_bits = _x_bf16(1, K, 32)
     ref, yabs = orc.matmul_packed(fmt, N, K, w, x_bits, weights)
